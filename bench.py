@@ -1,0 +1,501 @@
+#!/usr/bin/env python3
+"""Benchmark of split Shared / Non-Shared beam-search decode attention on one GB300.
+
+One step = one pass of the whole hot path over one batch:
+  xattn_beam_update (the beams' newest token into the Non-Shared pool, ancestry rewrite)
+  + xattn_decode (Shared stage on tensor cores, Non-Shared stage, log-sum-exp Merge).
+Default workload: 8 requests x beam width 128, GQA 32/8, head_dim 128, shared prefix 2048,
+3 Non-Shared tokens per beam with random ancestry, bf16 N(0,1) (synthetic, seeded).
+
+Timing: CUDA graphs of one step per input set, replayed back to back between CUDA events;
+the input sets rotate and together exceed twice the L2 size, so no step finds its inputs
+in L2. Clocks are sampled with nvidia-smi during the timed region. One JSON line is printed
+by rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload NAME]
+
+--impl reference times the fp64 CPU oracle (the plain definition) on the host cores, on a
+bounded sample of the same workload per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn beams/s and µs/step; achieved HBM GB/s as % of GB300 roofline"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gr_r8_bw128_h32x8_d128_L2048_t3")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="wall budget of the CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------------------
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            out = {}
+            for k in FALLBACK:
+                v = d.get(k)
+                if isinstance(v, dict):
+                    v = v.get("value")
+                if v is not None:
+                    out[k] = float(v)
+            if "hbm_gbs" in out and "bf16_tflops" in out:
+                out.setdefault("bf16_tflops_sustained", out["bf16_tflops"])
+                return out, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, max clock, throttle reasons) while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[2:6]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------------------
+def unique_bytes(w, idx_np, shared_lens):
+    """Bytes the step must move at least once: prefix K/V over valid tokens (once per
+    request), the distinct Non-Shared pool rows the ancestry references, q, out, lse and the
+    ancestry entries read."""
+    import numpy as np
+
+    d, Hkv = w.head_dim, w.num_kv_heads
+    prefix = int(sum(shared_lens)) * Hkv * d * 2 * 2
+    T = w.steps
+    distinct = sum(len(np.unique(idx_np[r, :, :T])) for r in range(w.num_requests)) if T > 0 else 0
+    ns = distinct * Hkv * d * 2 * 2
+    rows = w.num_requests * w.beam_width * w.num_q_heads
+    q = rows * d * 2
+    out = rows * d * 2 + rows * 4
+    idx = w.num_requests * w.beam_width * T * 4
+    return prefix + ns + q + out + idx, {"prefix_kv": prefix, "ns_kv": ns, "q": q, "out_lse": out, "idx": idx}
+
+
+def shared_stage_flops(w):
+    """Algorithmic FLOPs of the Shared stage: two matmuls of M x L x d per (request, KV head)."""
+    M = w.beam_width * w.group_size
+    return sum(4.0 * M * L * w.head_dim * w.num_kv_heads for L in w.shared_lens)
+
+
+def shared_stage_bytes(w, plan):
+    M = w.beam_width * w.group_size
+    kv = sum(w.shared_lens) * w.num_kv_heads * w.head_dim * 2 * 2
+    q = w.num_requests * w.beam_width * w.num_q_heads * w.head_dim * 2
+    parts = w.num_requests * w.num_kv_heads * plan.num_splits * M * (w.head_dim + 1) * 4
+    return kv + q + parts
+
+
+def profile_traffic(kernel_file: str, workload: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken on the
+    current source of the kernel; else None."""
+    path = os.path.join(ROOT, "profiles", f"{os.path.splitext(os.path.basename(kernel_file))[0]}__{workload}.md")
+    if not os.path.exists(path):
+        return None
+    src = os.path.join(ROOT, "decode_attention_xattention_gb300", "csrc", kernel_file)
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    traffic, src_sha = None, None
+    for line in open(path):
+        if line.startswith("traffic_bytes_per_launch:"):
+            traffic = float(line.split(":", 1)[1].strip())
+        if line.startswith("kernel_source_sha256_16:"):
+            src_sha = line.split(":", 1)[1].strip()
+    return traffic if (traffic is not None and src_sha == sha) else None
+
+
+# ----------------------------------------------------------------------------------------
+def cpu_oracle_sample(w, inp, budget_s, rows_override=None):
+    """Times the fp64 oracle (as it stands, all host cores) on whole beams of request 0
+    until about budget_s of wall time. Returns (beams/s, cores, description)."""
+    import numpy as np
+
+    import oracle
+
+    orc = oracle.load()
+    pk, pv, idx = oracle.build_cache(orc, inp)
+    D = oracle.dims_of(w)
+    Hq = w.num_q_heads
+    cores = orc.max_threads()
+
+    def run(nbeams, offset=0):
+        b0 = offset % w.num_beams
+        beams = [(b0 + i) % w.num_beams for i in range(nbeams)]
+        rows = np.asarray([b * Hq + h for b in beams for h in range(Hq)], np.int64)
+        t0 = time.perf_counter()
+        orc.decode(D, inp.q, inp.shared_k, inp.shared_v, inp.shared_len, pk, pv, idx, w.steps, rows=rows)
+        return time.perf_counter() - t0
+
+    t = run(1)
+    n = 1
+    while t < 0.2 and n < w.num_beams:
+        n = min(w.num_beams, n * 4)
+        t = run(n)
+    rate = n / t
+    nb = max(1, min(w.num_beams, int(rate * budget_s)))
+    t = run(nb)
+    return nb / t, cores, f"{nb} of {w.num_beams} beams (all {Hq} query heads each), one decode step, " \
+                          f"{cores} OpenMP threads"
+
+
+def run_reference(args, w):
+    """The oracle as the reference arm: each step decodes a bounded sample of beams."""
+    import numpy as np
+
+    import oracle
+    from decode_attention_xattention_gb300 import workloads as wl
+
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    inp = wl.make_inputs(w).as_bf16()
+    orc = oracle.load()
+    pk, pv, idx = oracle.build_cache(orc, inp)
+    D = oracle.dims_of(w)
+    Hq = w.num_q_heads
+    cores = orc.max_threads()
+
+    def step(nb, k):
+        b0 = (k * nb) % w.num_beams
+        rows = np.asarray([((b0 + i) % w.num_beams) * Hq + h for i in range(nb) for h in range(Hq)], np.int64)
+        orc.decode(D, inp.q, inp.shared_k, inp.shared_v, inp.shared_len, pk, pv, idx, w.steps, rows=rows)
+
+    t0 = time.perf_counter()
+    step(1, 0)
+    per_beam = max(time.perf_counter() - t0, 1e-6)
+    total_budget = 120.0
+    nb = int(max(1, min(w.num_beams, total_budget / max(1, args.steps + args.warmup) / per_beam)))
+    for k in range(args.warmup):
+        step(nb, k)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        step(nb, k)
+    el = time.perf_counter() - t0
+    value = nb * args.steps / el
+    ms = el / args.steps * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "beams/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": "beams/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{nb} of {w.num_beams} beams per step (all {Hq} query heads each), "
+                                   f"fp64 C oracle, {cores} OpenMP threads"},
+        "e2e": {"value": value, "unit": "beams/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, extra=None):
+    c = {"workload": w.name, "requests": w.num_requests, "beam_width": w.beam_width, "q_heads": w.num_q_heads,
+         "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "shared_prefix": list(w.shared_lens),
+         "ns_tokens_per_beam": w.steps}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ----------------------------------------------------------------------------------------
+def main():
+    args = parse_args()
+    from decode_attention_xattention_gb300 import workloads as wl
+
+    if args.workload not in wl.ALL:
+        sys.exit(f"unknown workload {args.workload}; choose from {sorted(wl.ALL)}")
+    w = wl.ALL[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from decode_attention_xattention_gb300 import build as xbuild, xattn
+    from decode_attention_xattention_gb300.runner import DeviceBatch
+
+    rank, world, local = dist_info()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    xbuild.build()
+    xattn.load()
+    T = w.steps
+    peaks, peak_src = load_peaks()
+
+    # -- input sets: enough copies that rotating through them defeats the L2 ------------
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size if hasattr(
+        torch.cuda.get_device_properties(local), "L2_cache_size") else 128 << 20
+    stream = torch.cuda.Stream()
+    sets, inputs = [], []
+    set_bytes = None
+    while True:
+        seed = 1000 * rank + len(sets)
+        inp = wl.make_inputs(w, seed=seed).as_bf16()
+        db = DeviceBatch(inp, device=f"cuda:{local}", stream=stream)
+        with torch.cuda.stream(stream):
+            db.build_cache(steps=T - 1)  # the timed step writes token T-1 itself
+        sets.append(db)
+        inputs.append(inp)
+        if set_bytes is None:
+            set_bytes = sum(t.numel() * t.element_size() for t in
+                            (db.q, db.shared_k, db.shared_v, db.pool_k, db.pool_v, db.out, db.lse, db.workspace)
+                            if t is not None)
+        if len(sets) >= 2 and len(sets) * set_bytes >= 2 * l2:
+            break
+    nsets = len(sets)
+    plan = sets[0].plan()
+
+    def step(db):
+        xattn.check(db.beam_update(T - 1))
+        xattn.check(db.decode())
+
+    # eager warm-up of every call (also sets kernel attributes before capture)
+    with torch.cuda.stream(stream):
+        for db in sets:
+            step(db)
+            xattn.check(db.decode_shared())
+            xattn.check(db.decode_merge())
+            xattn.check(db.beam_update(T - 1))
+    stream.synchronize()
+    for db in sets:
+        assert db.read_status() == 0
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    g_step = [capture(lambda db=db: step(db)) for db in sets]
+    g_shared = [capture(lambda db=db: xattn.check(db.decode_shared())) for db in sets]
+    g_merge = [capture(lambda db=db: xattn.check(db.decode_merge())) for db in sets]
+    g_bu = [capture(lambda db=db: xattn.check(db.beam_update(T - 1))) for db in sets]
+
+    def timed(graphs, K, W):
+        with torch.cuda.stream(stream):
+            for k in range(W):
+                graphs[k % nsets].replay()
+        stream.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for k in range(K):
+                graphs[k % nsets].replay()
+            e1.record(stream)
+        e1.synchronize()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=f"cuda:{local}")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    K, W = args.steps, max(3, args.warmup)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    total_ms = timed(g_step, K, W)
+    clocks = sampler.stop()
+    ms_step = total_ms / K
+
+    # per-kernel average launch durations (each stage alone, same rotation)
+    Kk = max(200, min(K, 5000))
+    ms_shared = timed(g_shared, Kk, W) / Kk
+    ms_merge = timed(g_merge, Kk, W) / Kk
+    ms_bu = timed(g_bu, Kk, W) / Kk
+    for db in sets:
+        assert db.read_status() == 0, "device status set during the bench"
+
+    # -- end to end through the C ABI with host buffers ----------------------------------
+    db = sets[0]
+    inp = inputs[0]
+    from decode_attention_xattention_gb300.runner import to_bf16_tensor
+
+    h_q = to_bf16_tensor(inp.q, "cpu").pin_memory()
+    h_nk = to_bf16_tensor(inp.new_k[T - 1], "cpu").pin_memory()
+    h_nv = to_bf16_tensor(inp.new_v[T - 1], "cpu").pin_memory()
+    h_par = torch.from_numpy(inp.parents[T - 1].astype(np.int32)).pin_memory()
+    h_out = torch.empty(db.out.shape, dtype=db.out.dtype).pin_memory()
+    h_lse = torch.empty(db.lse.shape, dtype=db.lse.dtype).pin_memory()
+    d_nk, d_nv, d_par = db.new_k[T - 1], db.new_v[T - 1], db.parents[T - 1]
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_nk, h_nv, h_par))
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+
+    def e2e_step():
+        db.q.copy_(h_q, non_blocking=True)
+        d_nk.copy_(h_nk, non_blocking=True)
+        d_nv.copy_(h_nv, non_blocking=True)
+        d_par.copy_(h_par, non_blocking=True)
+        xattn.check(db.beam_update(T - 1))
+        xattn.check(db.decode())
+        h_out.copy_(db.out, non_blocking=True)
+        h_lse.copy_(db.lse, non_blocking=True)
+
+    Ke = max(50, min(K, 2000))
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            e2e_step()
+    stream.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        e1.record(stream)
+    e1.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / Ke
+    if world > 1:
+        t = torch.tensor([ms_e2e], device=f"cuda:{local}")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+
+    # -- derived figures ------------------------------------------------------------------
+    beams = w.num_beams * world
+    ub, ub_parts = unique_bytes(w, db.idx.cpu().numpy(), inp.shared_len)
+    flops = shared_stage_flops(w)
+    sbytes = shared_stage_bytes(w, plan)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = sbytes / (peaks["hbm_gbs"] * 1e9)
+    bound = "tensor" if t_tc >= t_hbm else "hbm"
+    s_shared = ms_shared * 1e-3
+    if bound == "tensor":
+        achieved, peak, unit = flops / s_shared / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = sbytes / s_shared / 1e9, peaks["hbm_gbs"], "GB/s"
+    kernel_file = "shared_stage_tc.cu" if plan.shared_kernel == 1 else "shared_stage_simt.cu"
+    traffic = profile_traffic(kernel_file, w.name)
+    step_s = ms_step * 1e-3
+    hbm_gbs = ub / step_s / 1e9
+    line = {
+        "metric": METRIC,
+        "value": beams / step_s,
+        "unit": "beams/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": config_of(w, {"l2": f"{nsets} rotating input sets of {set_bytes / 1e6:.0f} MB "
+                                      f"(> 2x the {l2 / 1e6:.0f} MB L2)", "timing": "CUDA graph replays, CUDA events",
+                                "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                                "shared_splits": plan.num_splits, "split_tokens": plan.split_tokens,
+                                "shared_kernel": "tcgen05" if plan.shared_kernel == 1 else "cuda-core"}),
+        "us_per_step": ms_step * 1e3,
+        "attention_us_per_step": (ms_shared + ms_merge) * 1e3,
+        "stage_us": {"beam_update": ms_bu * 1e3, "shared_stage": ms_shared * 1e3, "ns_merge": ms_merge * 1e3},
+        "hbm": {"unique_bytes_per_step": ub, "parts": ub_parts, "achieved_gbs": hbm_gbs,
+                "frac_of_8tbs": hbm_gbs / NOMINAL_HBM_GBS, "frac_of_measured": hbm_gbs / peaks["hbm_gbs"]},
+        "tensor": {"shared_stage_flops": flops, "achieved_tflops": flops / s_shared / 1e12,
+                   "frac_of_peak": flops / s_shared / 1e12 / peaks["bf16_tflops"]},
+        "binding_roofline_frac": max(ub / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12)) / step_s,
+        "roofline": {"kernel": kernel_file.replace(".cu", ""), "bound": bound, "achieved": achieved, "peak": peak,
+                     "unit": unit, "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} (burst; kernel timed alone)",
+                     "algorithmic_per_launch": flops if bound == "tensor" else sbytes},
+        "e2e": {"value": beams / (ms_e2e * 1e-3), "unit": "beams/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, sample = cpu_oracle_sample(w, inputs[0], args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "beams/s", "cores": cores, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,88 @@
+// In-place bookkeeping of one beam-search step for the Non-Shared part.
+//
+// xGR: Efficient Generative Recommendation Serving at Scale, section 2.1 (xAttention):
+// the Non-Shared cache is managed per token, so forking beams copies no physical block;
+// the update is done in place without read-before-write hazards.
+//
+// Reading used here: the token a beam emits at step s is written once, to the fresh slot
+// s*BW + b (for a request the BW new tokens fill one contiguous run of slots, so the K/V
+// write is a straight copy). Only the small ancestry table changes otherwise:
+// row b becomes its parent's row followed by the new slot. Rows are rewritten in place by
+// one CTA per request that stages a band of table columns in shared memory (all reads,
+// barrier, all writes), so no entry is read after it has been overwritten. Column i of
+// the new table depends only on column i of the old one, which is what makes banding safe.
+#include "xattn_internal.cuh"
+
+namespace xattn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTableInts = 8192;  // shared-memory band: 32 KB
+
+__global__ void __launch_bounds__(kThreads) beam_update_kernel(
+    int BW, int HkvD, int S, int Tmax, int step, const int32_t* __restrict__ parent,
+    const __nv_bfloat16* __restrict__ new_k, const __nv_bfloat16* __restrict__ new_v,
+    __nv_bfloat16* __restrict__ pool_k, __nv_bfloat16* __restrict__ pool_v,
+    int32_t* __restrict__ idx, int32_t* status) {
+    const int r = blockIdx.x;
+    // 1. K/V of the new tokens: [BW, Hkv, d] of request r -> slots step*BW .. step*BW+BW-1.
+    {
+        const size_t n16 = (size_t)BW * HkvD / 8;  // 16-byte vectors (HkvD is a multiple of 8)
+        const uint4* sk = reinterpret_cast<const uint4*>(new_k + (size_t)r * BW * HkvD);
+        const uint4* sv = reinterpret_cast<const uint4*>(new_v + (size_t)r * BW * HkvD);
+        uint4* dk = reinterpret_cast<uint4*>(pool_k + ((size_t)r * S + (size_t)step * BW) * HkvD);
+        uint4* dv = reinterpret_cast<uint4*>(pool_v + ((size_t)r * S + (size_t)step * BW) * HkvD);
+        for (size_t i = (size_t)blockIdx.y * kThreads + threadIdx.x; i < n16; i += (size_t)gridDim.y * kThreads) {
+            dk[i] = __ldg(sk + i);
+            dv[i] = __ldg(sv + i);
+        }
+    }
+    if (blockIdx.y != 0) return;
+
+    // 2. Ancestry table of request r, in place.
+    __shared__ int32_t band[kTableInts];
+    int32_t* tab = idx + (size_t)r * BW * Tmax;
+    const int32_t* par = parent ? parent + (size_t)r * BW : nullptr;
+    for (int b = threadIdx.x; b < BW; b += kThreads) {
+        tab[(size_t)b * Tmax + step] = step * BW + b;  // column `step` is never read below
+        if (step > 0) {
+            const int p = par[b];
+            if (p < 0 || p >= BW) set_status(status, XATTN_STATUS_BAD_PARENT);
+        }
+    }
+    if (step == 0) return;
+    const int cols = max(1, min(step, kTableInts / BW));
+    for (int c0 = 0; c0 < step; c0 += cols) {
+        const int cc = min(cols, step - c0);
+        __syncthreads();  // previous band fully written before it is reused
+        for (int i = threadIdx.x; i < BW * cc; i += kThreads) {
+            const int b = i / cc, c = i - b * cc;
+            band[i] = tab[(size_t)b * Tmax + c0 + c];
+        }
+        __syncthreads();  // every old entry of the band read before any is overwritten
+        for (int i = threadIdx.x; i < BW * cc; i += kThreads) {
+            const int b = i / cc, c = i - b * cc;
+            const int p = par[b];
+            tab[(size_t)b * Tmax + c0 + c] = (p >= 0 && p < BW) ? band[p * cc + c] : -1;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_beam_update(int R, int BW, int Hkv, int d, int S, int Tmax, int step,
+                               const int32_t* parent, const __nv_bfloat16* new_k,
+                               const __nv_bfloat16* new_v, __nv_bfloat16* pool_k,
+                               __nv_bfloat16* pool_v, int32_t* idx, int32_t* status,
+                               cudaStream_t stream) {
+    if (BW > kTableInts) return cudaErrorInvalidValue;
+    const size_t n16 = (size_t)BW * Hkv * d / 8;
+    int ybl = (int)((n16 + kThreads * 4 - 1) / (kThreads * 4));
+    ybl = max(1, min(ybl, 64));
+    dim3 grid(R, ybl);
+    beam_update_kernel<<<grid, kThreads, 0, stream>>>(BW, Hkv * d, S, Tmax, step, parent, new_k, new_v,
+                                                      pool_k, pool_v, idx, status);
+    return cudaGetLastError();
+}
+
+}  // namespace xattn

@@ -1,0 +1,334 @@
+// Host entry points of libxattn.so (see include/xattn.h): argument validation, the split
+// plan of the Shared stage, TMA descriptors, and the launches. Nothing here allocates
+// device memory or synchronises (except xattn_read_status).
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "xattn_internal.cuh"
+
+namespace xattn {
+namespace {
+
+constexpr int kSimtMaxRows = 16;  // stacked rows at or below which the CUDA-core stage runs
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int device_sms() {
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult qr;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
+                cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Shape checks shared by every entry point. Returns XATTN_OK or an error code.
+int check_desc(const xattn_desc* d) {
+    if (!d) return XATTN_ERR_INVALID_ARG;
+    if (d->num_requests <= 0 || d->beam_width <= 0 || d->num_q_heads <= 0 || d->num_kv_heads <= 0)
+        return XATTN_ERR_INVALID_ARG;
+    if (d->num_q_heads % d->num_kv_heads != 0) return XATTN_ERR_INVALID_ARG;
+    if (d->max_shared_len < 0 || d->ns_slots < 0 || d->max_steps < 0) return XATTN_ERR_INVALID_ARG;
+    if (!(d->softmax_scale >= 0.f) || !std::isfinite(d->softmax_scale)) return XATTN_ERR_INVALID_ARG;
+    if (d->split_tokens < 0 || d->split_tokens % kTileKeys != 0) return XATTN_ERR_INVALID_ARG;
+    if (d->shared_kernel < 0 || d->shared_kernel > 2) return XATTN_ERR_INVALID_ARG;
+    if (d->dtype != XATTN_DTYPE_BF16) return XATTN_ERR_UNSUPPORTED;
+    if (d->head_dim != 64 && d->head_dim != 128) return XATTN_ERR_UNSUPPORTED;
+    const int G = d->num_q_heads / d->num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return XATTN_ERR_UNSUPPORTED;
+    // Index arithmetic inside the kernels uses 32-bit products of these.
+    const int64_t rows = (int64_t)d->num_requests * d->beam_width * d->num_q_heads;
+    if (rows > (1ll << 30) || (int64_t)d->beam_width * G > (1ll << 24)) return XATTN_ERR_UNSUPPORTED;
+    if ((int64_t)d->beam_width * d->max_steps > (1ll << 30)) return XATTN_ERR_UNSUPPORTED;
+    if (d->max_shared_len > (1 << 30) || d->ns_slots > (1 << 30)) return XATTN_ERR_UNSUPPORTED;
+    return XATTN_OK;
+}
+
+int cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+// Split plan of the Shared stage. A piece is a run of whole 128-token tiles. The automatic
+// choice minimises (waves of CTAs) x (tiles per CTA + one tile of fixed cost per CTA), so
+// that short units are split until they fill the GPU but not beyond.
+void plan(const xattn_desc* d, int step, Geometry* g, int* kernel) {
+    g->R = d->num_requests;
+    g->BW = d->beam_width;
+    g->Hq = d->num_q_heads;
+    g->Hkv = d->num_kv_heads;
+    g->G = g->Hq / g->Hkv;
+    g->d = d->head_dim;
+    g->Lmax = d->max_shared_len;
+    g->S = d->ns_slots;
+    g->Tmax = d->max_steps;
+    g->step = step;
+    g->M = g->BW * g->G;
+    g->row_tiles = cdiv(g->M, kTileRows);
+    const float scale = d->softmax_scale > 0.f ? d->softmax_scale : 1.0f / std::sqrt((float)g->d);
+    g->scale_log2 = scale * 1.4426950408889634f;
+
+    int k = 0;
+    if (g->Lmax > 0) k = d->shared_kernel ? d->shared_kernel : (g->M <= kSimtMaxRows ? 2 : 1);
+    *kernel = k;
+    const int tiles = g->Lmax > 0 ? cdiv(g->Lmax, kTileKeys) : 1;
+    if (d->split_tokens > 0) {
+        g->split_tokens = d->split_tokens;
+    } else if (k == 0) {
+        g->split_tokens = kTileKeys;
+    } else {
+        const int64_t units = (int64_t)g->R * g->Hkv * (k == 1 ? g->row_tiles : cdiv(g->M, 4));
+        const int64_t slots = (int64_t)device_sms() * (k == 1 ? 1 : 8);
+        int best_n = 1;
+        double best = 1e30;
+        for (int n = 1; n <= tiles; ++n) {
+            const int per = cdiv(tiles, n);
+            if (n > 1 && cdiv(tiles, per) != n) continue;  // same pieces as a smaller n
+            const double waves = (double)cdiv(units * n, slots);
+            const double cost = waves * (per + 1.0) + 0.02 * n;  // small charge for merge traffic
+            if (cost < best) { best = cost; best_n = n; }
+        }
+        g->split_tokens = cdiv(tiles, best_n) * kTileKeys;
+    }
+    g->nsplit = g->Lmax > 0 ? cdiv(g->Lmax, g->split_tokens) : 0;
+}
+
+size_t workspace_bytes_for(const Geometry& g) {
+    const size_t rows = part_rows(g);
+    return kStatusBytes + rows * (size_t)g.d * sizeof(float) + ((rows * sizeof(float) + 255) / 256) * 256;
+}
+
+CUresult make_kv_map(CUtensorMap* map, const void* base, const Geometry& g) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return CUDA_ERROR_NOT_FOUND;
+    // [R, Lmax, Hkv, d] viewed innermost-first as {d, Hkv, Lmax, R}; box = 64 x 1 x 128 x 1.
+    cuuint64_t dims[4] = {(cuuint64_t)g.d, (cuuint64_t)g.Hkv, (cuuint64_t)g.Lmax, (cuuint64_t)g.R};
+    cuuint64_t strides[3] = {(cuuint64_t)g.d * 2, (cuuint64_t)g.Hkv * g.d * 2, (cuuint64_t)g.Lmax * g.Hkv * g.d * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)kTileKeys, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace
+}  // namespace xattn
+
+using namespace xattn;
+
+extern "C" {
+
+size_t xattn_decode_workspace_size(const xattn_desc* desc) {
+    if (check_desc(desc) != XATTN_OK) return 0;
+    Geometry g;
+    int k;
+    plan(desc, 0, &g, &k);
+    return workspace_bytes_for(g);
+}
+
+int xattn_query_plan(const xattn_desc* desc, int32_t step, xattn_plan* out) {
+    int rc = check_desc(desc);
+    if (rc != XATTN_OK) return rc;
+    if (!out || step < 0 || step > desc->max_steps) return XATTN_ERR_INVALID_ARG;
+    Geometry g;
+    int k;
+    plan(desc, step, &g, &k);
+    *out = xattn_plan{};
+    out->shared_kernel = k;
+    out->num_splits = g.nsplit;
+    out->split_tokens = g.split_tokens;
+    out->rows_per_unit = g.M;
+    out->row_tiles = g.row_tiles;
+    out->shared_ctas = k == 0 ? 0 : (k == 1 ? shared_tc_ctas_for(g) : g.R * g.Hkv * ((g.M + 3) / 4) * g.nsplit);
+    out->merge_ctas = merge_ctas_for(g);
+    return XATTN_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+int check_common(const xattn_desc* desc, const void* q, void* workspace) {
+    int rc = check_desc(desc);
+    if (rc != XATTN_OK) return rc;
+    if (!q || !workspace) return XATTN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(workspace, 256)) return XATTN_ERR_MISALIGNED;
+    return XATTN_OK;
+}
+
+int check_shared_args(const xattn_desc* desc, const void* shared_k, const void* shared_v,
+                      const int32_t* shared_len) {
+    if (desc->max_shared_len == 0) return XATTN_OK;
+    if (!shared_k || !shared_v || !shared_len) return XATTN_ERR_INVALID_ARG;
+    if (!aligned(shared_k, 16) || !aligned(shared_v, 16) || !aligned(shared_len, 4)) return XATTN_ERR_MISALIGNED;
+    return XATTN_OK;
+}
+
+int check_merge_args(const xattn_desc* desc, const void* ns_k_pool, const void* ns_v_pool,
+                     const int32_t* beam_tok_idx, int32_t step, const void* out, const float* lse) {
+    if (step < 0 || step > desc->max_steps) return XATTN_ERR_INVALID_ARG;
+    if (step == 0 && desc->max_shared_len == 0) return XATTN_ERR_INVALID_ARG;
+    if (step > 0 && (int64_t)step * desc->beam_width > desc->ns_slots) return XATTN_ERR_INVALID_ARG;
+    if (!out || !lse) return XATTN_ERR_INVALID_ARG;
+    if (step > 0 && (!ns_k_pool || !ns_v_pool || !beam_tok_idx)) return XATTN_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(lse, 4)) return XATTN_ERR_MISALIGNED;
+    if (step > 0 && (!aligned(ns_k_pool, 16) || !aligned(ns_v_pool, 16) || !aligned(beam_tok_idx, 4)))
+        return XATTN_ERR_MISALIGNED;
+    return XATTN_OK;
+}
+
+struct WsView {
+    int32_t* status;
+    float* part_o;
+    float* part_lse;
+};
+
+WsView ws_view(void* workspace, const Geometry& g) {
+    WsView v;
+    v.status = reinterpret_cast<int32_t*>(workspace);
+    v.part_o = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + kStatusBytes);
+    v.part_lse = v.part_o + part_rows(g) * g.d;
+    return v;
+}
+
+int run_shared(const Geometry& g, int kernel, const void* q, const void* shared_k, const void* shared_v,
+               const int32_t* shared_len, const WsView& ws, cudaStream_t st) {
+    auto qb = reinterpret_cast<const __nv_bfloat16*>(q);
+    cudaError_t e = cudaSuccess;
+    if (kernel == 1) {
+        CUtensorMap mk, mv;
+        if (make_kv_map(&mk, shared_k, g) != CUDA_SUCCESS || make_kv_map(&mv, shared_v, g) != CUDA_SUCCESS)
+            return XATTN_ERR_CUDA;
+        e = launch_shared_stage_tc(g, mk, mv, qb, shared_len, ws.part_o, ws.part_lse, ws.status, st);
+    } else if (kernel == 2) {
+        e = launch_shared_stage_simt(g, qb, reinterpret_cast<const __nv_bfloat16*>(shared_k),
+                                     reinterpret_cast<const __nv_bfloat16*>(shared_v), shared_len, ws.part_o,
+                                     ws.part_lse, ws.status, st);
+    }
+    return e == cudaSuccess ? XATTN_OK : XATTN_ERR_CUDA;
+}
+
+int run_merge(const Geometry& g, const xattn_desc* desc, const void* q, const int32_t* shared_len,
+              const void* ns_k_pool, const void* ns_v_pool, const int32_t* beam_tok_idx, void* out, float* lse,
+              const WsView& ws, cudaStream_t st) {
+    cudaError_t e = launch_ns_merge(g, reinterpret_cast<const __nv_bfloat16*>(q),
+                                    reinterpret_cast<const __nv_bfloat16*>(ns_k_pool),
+                                    reinterpret_cast<const __nv_bfloat16*>(ns_v_pool), beam_tok_idx,
+                                    desc->max_shared_len > 0 ? shared_len : nullptr, ws.part_o, ws.part_lse,
+                                    reinterpret_cast<__nv_bfloat16*>(out), lse, ws.status, st);
+    return e == cudaSuccess ? XATTN_OK : XATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int xattn_decode(const xattn_desc* desc, const void* q, const void* shared_k, const void* shared_v,
+                 const int32_t* shared_len, const void* ns_k_pool, const void* ns_v_pool,
+                 const int32_t* beam_tok_idx, int32_t step, void* out, float* lse, void* workspace,
+                 size_t workspace_bytes, xattn_stream_t stream) {
+    int rc = check_common(desc, q, workspace);
+    if (rc == XATTN_OK) rc = check_shared_args(desc, shared_k, shared_v, shared_len);
+    if (rc == XATTN_OK) rc = check_merge_args(desc, ns_k_pool, ns_v_pool, beam_tok_idx, step, out, lse);
+    if (rc != XATTN_OK) return rc;
+    Geometry g;
+    int kernel;
+    plan(desc, step, &g, &kernel);
+    if (workspace_bytes < workspace_bytes_for(g)) return XATTN_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const WsView ws = ws_view(workspace, g);
+    rc = run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st);
+    if (rc != XATTN_OK) return rc;
+    return run_merge(g, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws, st);
+}
+
+int xattn_decode_shared(const xattn_desc* desc, const void* q, const void* shared_k, const void* shared_v,
+                        const int32_t* shared_len, void* workspace, size_t workspace_bytes,
+                        xattn_stream_t stream) {
+    int rc = check_common(desc, q, workspace);
+    if (rc == XATTN_OK && desc->max_shared_len == 0) rc = XATTN_ERR_INVALID_ARG;
+    if (rc == XATTN_OK) rc = check_shared_args(desc, shared_k, shared_v, shared_len);
+    if (rc != XATTN_OK) return rc;
+    Geometry g;
+    int kernel;
+    plan(desc, 0, &g, &kernel);
+    if (workspace_bytes < workspace_bytes_for(g)) return XATTN_ERR_WORKSPACE_TOO_SMALL;
+    return run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws_view(workspace, g),
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+int xattn_decode_merge(const xattn_desc* desc, const void* q, const int32_t* shared_len, const void* ns_k_pool,
+                       const void* ns_v_pool, const int32_t* beam_tok_idx, int32_t step, void* out, float* lse,
+                       void* workspace, size_t workspace_bytes, xattn_stream_t stream) {
+    int rc = check_common(desc, q, workspace);
+    if (rc == XATTN_OK && desc->max_shared_len > 0 && !shared_len) rc = XATTN_ERR_INVALID_ARG;
+    if (rc == XATTN_OK && shared_len && !aligned(shared_len, 4)) rc = XATTN_ERR_MISALIGNED;
+    if (rc == XATTN_OK) rc = check_merge_args(desc, ns_k_pool, ns_v_pool, beam_tok_idx, step, out, lse);
+    if (rc != XATTN_OK) return rc;
+    Geometry g;
+    int kernel;
+    plan(desc, step, &g, &kernel);
+    if (workspace_bytes < workspace_bytes_for(g)) return XATTN_ERR_WORKSPACE_TOO_SMALL;
+    return run_merge(g, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws_view(workspace, g),
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+int xattn_beam_update(const xattn_desc* desc, const int32_t* parent, const void* new_k, const void* new_v,
+                      void* ns_k_pool, void* ns_v_pool, int32_t* beam_tok_idx, int32_t step, int32_t* status,
+                      xattn_stream_t stream) {
+    int rc = check_desc(desc);
+    if (rc != XATTN_OK) return rc;
+    if (step < 0 || step >= desc->max_steps) return XATTN_ERR_INVALID_ARG;
+    if ((int64_t)(step + 1) * desc->beam_width > desc->ns_slots) return XATTN_ERR_INVALID_ARG;
+    if (desc->beam_width > 8192) return XATTN_ERR_UNSUPPORTED;
+    if (!new_k || !new_v || !ns_k_pool || !ns_v_pool || !beam_tok_idx || (step > 0 && !parent))
+        return XATTN_ERR_INVALID_ARG;
+    if (!aligned(new_k, 16) || !aligned(new_v, 16) || !aligned(ns_k_pool, 16) || !aligned(ns_v_pool, 16) ||
+        !aligned(beam_tok_idx, 4) || (parent && !aligned(parent, 4)) || (status && !aligned(status, 4)))
+        return XATTN_ERR_MISALIGNED;
+    cudaError_t e = launch_beam_update(
+        desc->num_requests, desc->beam_width, desc->num_kv_heads, desc->head_dim, desc->ns_slots, desc->max_steps,
+        step, parent, reinterpret_cast<const __nv_bfloat16*>(new_k), reinterpret_cast<const __nv_bfloat16*>(new_v),
+        reinterpret_cast<__nv_bfloat16*>(ns_k_pool), reinterpret_cast<__nv_bfloat16*>(ns_v_pool), beam_tok_idx,
+        status, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? XATTN_OK : XATTN_ERR_CUDA;
+}
+
+int xattn_read_status(void* workspace, int32_t* status_out, int32_t clear, xattn_stream_t stream) {
+    if (!workspace || !status_out) return XATTN_ERR_INVALID_ARG;
+    if (!aligned(workspace, 4)) return XATTN_ERR_MISALIGNED;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(status_out, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return XATTN_ERR_CUDA;
+    if (clear && cudaMemsetAsync(workspace, 0, sizeof(int32_t), st) != cudaSuccess) return XATTN_ERR_CUDA;
+    return cudaStreamSynchronize(st) == cudaSuccess ? XATTN_OK : XATTN_ERR_CUDA;
+}
+
+const char* xattn_status_string(int code) {
+    switch (code) {
+        case XATTN_OK: return "ok";
+        case XATTN_ERR_INVALID_ARG: return "invalid argument";
+        case XATTN_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case XATTN_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case XATTN_ERR_MISALIGNED: return "tensor not 16-byte aligned";
+        case XATTN_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// Internal declarations shared by the kernels and the host entry points of libxattn.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/xattn.h"
+
+namespace xattn {
+
+constexpr int kTileRows = 128;   // rows of one tensor-core M tile (stacked beam x head rows)
+constexpr int kTileKeys = 128;   // prefix tokens per K/V tile
+constexpr int kStatusBytes = 256;
+
+// Device status word helpers ----------------------------------------------------------
+__device__ __forceinline__ void set_status(int32_t* status, int32_t bits) {
+    if (status) atomicOr(status, bits);
+}
+
+// Geometry of one decode call, precomputed on the host.
+struct Geometry {
+    int R, BW, Hq, Hkv, G, d;
+    int Lmax, S, Tmax, step;
+    int M;            // BW * G stacked rows per (request, KV head)
+    int row_tiles;    // ceil(M / 128)
+    int nsplit;       // prefix pieces
+    int split_tokens; // tokens per piece (multiple of 128)
+    float scale_log2; // softmax scale * log2(e)
+};
+
+// Workspace layout: [status (256 B)] [part_o: R*Hkv*nsplit*M*d fp32] [part_lse: R*Hkv*nsplit*M fp32]
+inline size_t part_rows(const Geometry& g) { return (size_t)g.R * g.Hkv * g.nsplit * g.M; }
+
+// Launchers (each returns cudaGetLastError()).
+cudaError_t launch_shared_stage_tc(const Geometry& g, const CUtensorMap& tmap_k,
+                                   const CUtensorMap& tmap_v, const __nv_bfloat16* q,
+                                   const int32_t* shared_len, float* part_o, float* part_lse,
+                                   int32_t* status, cudaStream_t stream);
+cudaError_t launch_shared_stage_simt(const Geometry& g, const __nv_bfloat16* q,
+                                     const __nv_bfloat16* shared_k, const __nv_bfloat16* shared_v,
+                                     const int32_t* shared_len, float* part_o, float* part_lse,
+                                     int32_t* status, cudaStream_t stream);
+cudaError_t launch_ns_merge(const Geometry& g, const __nv_bfloat16* q,
+                            const __nv_bfloat16* pool_k, const __nv_bfloat16* pool_v,
+                            const int32_t* beam_tok_idx, const int32_t* shared_len,
+                            const float* part_o, const float* part_lse, __nv_bfloat16* out,
+                            float* lse, int32_t* status, cudaStream_t stream);
+cudaError_t launch_beam_update(int R, int BW, int Hkv, int d, int S, int Tmax, int step,
+                               const int32_t* parent, const __nv_bfloat16* new_k,
+                               const __nv_bfloat16* new_v, __nv_bfloat16* pool_k,
+                               __nv_bfloat16* pool_v, int32_t* idx, int32_t* status,
+                               cudaStream_t stream);
+
+int merge_ctas_for(const Geometry& g);
+int shared_tc_ctas_for(const Geometry& g);
+
+}  // namespace xattn

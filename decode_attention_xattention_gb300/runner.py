@@ -1,0 +1,109 @@
+"""Device buffers for one workload and the calls that drive them through the C ABI.
+
+torch is used only to hold device memory and streams; every step of the method runs in
+libxattn.so's kernels (xattn_beam_update builds the Non-Shared pool and ancestry table,
+xattn_decode runs the Shared stage, the Non-Shared stage and the Merge).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import workloads as wl
+from . import xattn
+
+
+def to_bf16_tensor(x: np.ndarray, device) -> torch.Tensor:
+    """float32 array of exact bf16 values -> bf16 tensor with the same bits."""
+    bits = wl.bf16_bits(x)
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def bf16_tensor_to_f32(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy()
+
+
+class DeviceBatch:
+    """All device tensors of one decode batch (inputs resident in HBM)."""
+
+    def __init__(self, inp: wl.Inputs, device="cuda", shared_kernel=0, split_tokens=0, stream=None,
+                 extra_steps=0):
+        inp = inp.as_bf16()
+        w = inp.w
+        self.w = w
+        self.device = device
+        self.stream = stream
+        R, BW, Hq, Hkv, d = w.num_requests, w.beam_width, w.num_q_heads, w.num_kv_heads, w.head_dim
+        self.Tmax = w.max_steps + extra_steps
+        self.S = BW * self.Tmax
+        self.desc = xattn.make_desc(R, BW, Hq, Hkv, d, w.max_shared_len, self.S, self.Tmax, w.softmax_scale,
+                                    shared_kernel, split_tokens)
+        self.q = to_bf16_tensor(inp.q, device)
+        if w.max_shared_len > 0:
+            self.shared_k = to_bf16_tensor(inp.shared_k, device)
+            self.shared_v = to_bf16_tensor(inp.shared_v, device)
+        else:
+            self.shared_k = self.shared_v = None
+        self.shared_len = torch.from_numpy(inp.shared_len.astype(np.int32)).to(device)
+        self.new_k = to_bf16_tensor(inp.new_k, device) if w.steps > 0 else None
+        self.new_v = to_bf16_tensor(inp.new_v, device) if w.steps > 0 else None
+        self.parents = torch.from_numpy(inp.parents.astype(np.int32)).to(device)
+        self.pool_k = torch.zeros((R, self.S, Hkv, d), dtype=torch.bfloat16, device=device)
+        self.pool_v = torch.zeros_like(self.pool_k)
+        self.idx = torch.zeros((R, BW, max(self.Tmax, 1)), dtype=torch.int32, device=device)
+        self.out = torch.empty((R, BW, Hq, d), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((R, BW, Hq), dtype=torch.float32, device=device)
+        self.ws_bytes = xattn.xattn_decode_workspace_size(self.desc)
+        if self.ws_bytes == 0:
+            raise xattn.XAttnError("descriptor rejected")
+        self.workspace = torch.zeros((self.ws_bytes + 255) // 256 * 64, dtype=torch.int32, device=device)
+        self.status = torch.zeros((1,), dtype=torch.int32, device=device)
+
+    # -- the method's calls --------------------------------------------------------------
+    def beam_update(self, s: int) -> int:
+        return xattn.xattn_beam_update(self.desc, self.parents[s] if s > 0 else None, self.new_k[s], self.new_v[s],
+                                       self.pool_k, self.pool_v, self.idx, s, self.status, self.stream)
+
+    def build_cache(self, steps=None) -> None:
+        for s in range(self.w.steps if steps is None else steps):
+            xattn.check(self.beam_update(s))
+
+    def decode(self, step=None, out=None, lse=None) -> int:
+        step = self.w.steps if step is None else step
+        return xattn.xattn_decode(self.desc, self.q, self.shared_k, self.shared_v, self.shared_len, self.pool_k,
+                                  self.pool_v, self.idx if step > 0 else None, step,
+                                  self.out if out is None else out, self.lse if lse is None else lse,
+                                  self.workspace, self.ws_bytes, self.stream)
+
+    def decode_shared(self) -> int:
+        return xattn.xattn_decode_shared(self.desc, self.q, self.shared_k, self.shared_v, self.shared_len,
+                                         self.workspace, self.ws_bytes, self.stream)
+
+    def decode_merge(self, step=None) -> int:
+        step = self.w.steps if step is None else step
+        return xattn.xattn_decode_merge(self.desc, self.q, self.shared_len, self.pool_k, self.pool_v,
+                                        self.idx if step > 0 else None, step, self.out, self.lse, self.workspace,
+                                        self.ws_bytes, self.stream)
+
+    def partials(self):
+        """(part_o [R, Hkv, nsplit, M, d], part_lse [R, Hkv, nsplit, M]) views of the workspace."""
+        p = self.plan()
+        w = self.w
+        rows = w.num_requests * w.num_kv_heads * p.num_splits * p.rows_per_unit
+        f = self.workspace.view(torch.float32)
+        po = f[64:64 + rows * w.head_dim].view(w.num_requests, w.num_kv_heads, p.num_splits, p.rows_per_unit,
+                                                w.head_dim)
+        pl = f[64 + rows * w.head_dim:64 + rows * w.head_dim + rows].view(w.num_requests, w.num_kv_heads,
+                                                                             p.num_splits, p.rows_per_unit)
+        return po, pl
+
+    def read_status(self, clear=True) -> int:
+        rc, st = xattn.xattn_read_status(self.workspace, clear, self.stream)
+        xattn.check(rc)
+        return st
+
+    def plan(self, step=None):
+        rc, p = xattn.xattn_query_plan(self.desc, self.w.steps if step is None else step)
+        xattn.check(rc)
+        return p

@@ -43,10 +43,11 @@ class Workload:
     outlier_scale: float = 8.0
     seed: int = 0
     description: str = field(default="", compare=False)
+    lmax: int = 0  # prefix storage per request; 0 = the longest prefix
 
     @property
     def max_shared_len(self) -> int:
-        return max(self.shared_lens) if self.shared_lens else 0
+        return max(self.lmax, max(self.shared_lens) if self.shared_lens else 0)
 
     @property
     def ns_slots(self) -> int:
@@ -107,12 +108,12 @@ ALL = {w.name: w for w in (TINY, GR, WIDE, LONG, FEATHER_1, FEATHER_8, FEATHER_6
 
 
 def custom(R=1, BW=4, Hq=2, Hkv=1, d=64, lens=64, T=2, parent_range=None, seed=0,
-           input_dtype="bf16", outlier_frac=0.0) -> Workload:
+           input_dtype="bf16", outlier_frac=0.0, lmax=0) -> Workload:
     """A small workload of arbitrary shape (tests)."""
     if parent_range is None:
         parent_range = BW
     return _w(f"custom_r{R}_bw{BW}_h{Hq}x{Hkv}_d{d}_t{T}_s{seed}", R, BW, Hq, Hkv, d, lens, T,
-              parent_range, seed=seed, input_dtype=input_dtype, outlier_frac=outlier_frac)
+              parent_range, seed=seed, input_dtype=input_dtype, outlier_frac=outlier_frac, lmax=lmax)
 
 
 # --------------------------------------------------------------------------------------

@@ -1,0 +1,162 @@
+"""ctypes binding of libxattn.so (argument marshalling only).
+
+Every function here has the name and argument order of its C entry point in
+include/xattn.h and returns the C return code. Tensor arguments may be torch tensors (their
+data_ptr() is passed), plain integer addresses, or None (NULL). All compute runs in the
+library's CUDA kernels; if the library is missing this module raises instead of falling
+back to anything else.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libxattn.so")
+
+XATTN_OK = 0
+XATTN_ERR_INVALID_ARG = -1
+XATTN_ERR_UNSUPPORTED = -2
+XATTN_ERR_WORKSPACE_TOO_SMALL = -3
+XATTN_ERR_MISALIGNED = -4
+XATTN_ERR_CUDA = -5
+
+XATTN_STATUS_BAD_SHARED_LEN = 1
+XATTN_STATUS_BAD_SLOT = 2
+XATTN_STATUS_BAD_PARENT = 4
+XATTN_STATUS_EMPTY_ROW = 8
+XATTN_STATUS_TIMEOUT = 16
+
+XATTN_DTYPE_BF16 = 0
+
+# Every symbol include/xattn.h declares.
+EXPORTS = ("xattn_decode_workspace_size", "xattn_decode", "xattn_decode_shared", "xattn_decode_merge",
+           "xattn_beam_update", "xattn_read_status", "xattn_query_plan", "xattn_status_string")
+
+
+class XAttnError(RuntimeError):
+    pass
+
+
+class xattn_desc(ctypes.Structure):
+    _fields_ = [("num_requests", ctypes.c_int32), ("beam_width", ctypes.c_int32),
+                ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("max_shared_len", ctypes.c_int32),
+                ("ns_slots", ctypes.c_int32), ("max_steps", ctypes.c_int32),
+                ("softmax_scale", ctypes.c_float), ("dtype", ctypes.c_int32),
+                ("shared_kernel", ctypes.c_int32), ("split_tokens", ctypes.c_int32)]
+
+
+class xattn_plan(ctypes.Structure):
+    _fields_ = [("shared_kernel", ctypes.c_int32), ("num_splits", ctypes.c_int32),
+                ("split_tokens", ctypes.c_int32), ("rows_per_unit", ctypes.c_int32),
+                ("row_tiles", ctypes.c_int32), ("shared_ctas", ctypes.c_int32),
+                ("merge_ctas", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libxattn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise XAttnError(f"libxattn.so not built at {path}: run decode_attention_xattention_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    pdesc = ctypes.POINTER(xattn_desc)
+    lib.xattn_decode_workspace_size.argtypes = [pdesc]
+    lib.xattn_decode_workspace_size.restype = sz
+    lib.xattn_decode.argtypes = [pdesc, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+    lib.xattn_decode.restype = ctypes.c_int
+    lib.xattn_decode_shared.argtypes = [pdesc, vp, vp, vp, vp, vp, sz, vp]
+    lib.xattn_decode_shared.restype = ctypes.c_int
+    lib.xattn_decode_merge.argtypes = [pdesc, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+    lib.xattn_decode_merge.restype = ctypes.c_int
+    lib.xattn_beam_update.argtypes = [pdesc, vp, vp, vp, vp, vp, vp, i32, vp, vp]
+    lib.xattn_beam_update.restype = ctypes.c_int
+    lib.xattn_read_status.argtypes = [vp, ctypes.POINTER(i32), i32, vp]
+    lib.xattn_read_status.restype = ctypes.c_int
+    lib.xattn_query_plan.argtypes = [pdesc, i32, ctypes.POINTER(xattn_plan)]
+    lib.xattn_query_plan.restype = ctypes.c_int
+    lib.xattn_status_string.argtypes = [ctypes.c_int]
+    lib.xattn_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream  # torch.cuda.Stream
+
+
+def make_desc(R, BW, Hq, Hkv, d, Lmax, S, Tmax, scale=0.0, shared_kernel=0, split_tokens=0) -> xattn_desc:
+    return xattn_desc(R, BW, Hq, Hkv, d, Lmax, S, Tmax, float(scale), XATTN_DTYPE_BF16,
+                      shared_kernel, split_tokens)
+
+
+def xattn_decode_workspace_size(desc: xattn_desc) -> int:
+    return int(load().xattn_decode_workspace_size(ctypes.byref(desc)))
+
+
+def xattn_decode(desc, q, shared_k, shared_v, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, step,
+                 out, lse, workspace, workspace_bytes, stream=None) -> int:
+    return int(load().xattn_decode(ctypes.byref(desc), _ptr(q), _ptr(shared_k), _ptr(shared_v),
+                                   _ptr(shared_len), _ptr(ns_k_pool), _ptr(ns_v_pool), _ptr(beam_tok_idx),
+                                   int(step), _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
+                                   _stream(stream)))
+
+
+def xattn_decode_shared(desc, q, shared_k, shared_v, shared_len, workspace, workspace_bytes, stream=None) -> int:
+    return int(load().xattn_decode_shared(ctypes.byref(desc), _ptr(q), _ptr(shared_k), _ptr(shared_v),
+                                          _ptr(shared_len), _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def xattn_decode_merge(desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, step, out, lse, workspace,
+                       workspace_bytes, stream=None) -> int:
+    return int(load().xattn_decode_merge(ctypes.byref(desc), _ptr(q), _ptr(shared_len), _ptr(ns_k_pool),
+                                         _ptr(ns_v_pool), _ptr(beam_tok_idx), int(step), _ptr(out), _ptr(lse),
+                                         _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def xattn_beam_update(desc, parent, new_k, new_v, ns_k_pool, ns_v_pool, beam_tok_idx, step, status=None,
+                      stream=None) -> int:
+    return int(load().xattn_beam_update(ctypes.byref(desc), _ptr(parent), _ptr(new_k), _ptr(new_v),
+                                        _ptr(ns_k_pool), _ptr(ns_v_pool), _ptr(beam_tok_idx), int(step),
+                                        _ptr(status), _stream(stream)))
+
+
+def xattn_read_status(workspace, clear: bool = True, stream=None) -> tuple[int, int]:
+    """Returns (return code, status word)."""
+    st = ctypes.c_int32(0)
+    rc = load().xattn_read_status(_ptr(workspace), ctypes.byref(st), 1 if clear else 0, _stream(stream))
+    return int(rc), int(st.value)
+
+
+def xattn_query_plan(desc, step) -> tuple[int, xattn_plan]:
+    p = xattn_plan()
+    rc = load().xattn_query_plan(ctypes.byref(desc), int(step), ctypes.byref(p))
+    return int(rc), p
+
+
+def xattn_status_string(code: int) -> str:
+    return load().xattn_status_string(int(code)).decode()
+
+
+def check(rc: int) -> None:
+    if rc != XATTN_OK:
+        raise XAttnError(f"xattn call failed: {rc} ({xattn_status_string(rc)})")

@@ -1,0 +1,116 @@
+"""The C-ABI library builds, loads without a GPU, exports every declared symbol, and rejects
+bad arguments on the host before anything reaches the device (CPU only)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from decode_attention_xattention_gb300 import build, xattn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "xattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return xattn.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(xattn_\w+)\s*\(", text)))
+
+
+def test_header_declares_binding_exports():
+    assert declared_functions() == sorted(xattn.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_desc_layout_matches_header():
+    # 12 four-byte fields
+    assert ctypes.sizeof(xattn.xattn_desc) == 48
+    assert ctypes.sizeof(xattn.xattn_plan) == 44
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert xattn.xattn_status_string(code)
+    assert xattn.xattn_status_string(-99) == "unknown status"
+
+
+def _desc(**kw):
+    base = dict(R=2, BW=4, Hq=8, Hkv=2, d=128, Lmax=256, S=16, Tmax=4)
+    base.update(kw)
+    return xattn.make_desc(base["R"], base["BW"], base["Hq"], base["Hkv"], base["d"], base["Lmax"], base["S"],
+                           base["Tmax"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(R=0), xattn.XATTN_ERR_INVALID_ARG),
+    (dict(BW=0), xattn.XATTN_ERR_INVALID_ARG),
+    (dict(Hq=6, Hkv=4), xattn.XATTN_ERR_INVALID_ARG),
+    (dict(Lmax=-1), xattn.XATTN_ERR_INVALID_ARG),
+    (dict(d=96), xattn.XATTN_ERR_UNSUPPORTED),
+    (dict(Hq=6, Hkv=2), xattn.XATTN_ERR_UNSUPPORTED),
+])
+def test_bad_descriptor_rejected_on_host(lib, kw, code):
+    d = _desc(**kw)
+    assert xattn.xattn_decode_workspace_size(d) == 0
+    rc = xattn.xattn_decode(d, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 1, 0x1000, 0x1000, 0x1000,
+                            1 << 20)
+    assert rc == code
+    rc, _ = xattn.xattn_query_plan(d, 1)
+    assert rc == code
+
+
+def test_bad_calls_rejected_on_host(lib):
+    d = _desc()
+    ws = xattn.xattn_decode_workspace_size(d)
+    assert ws >= 256
+    A = 0x10000  # aligned dummy address; never dereferenced: every case fails validation first
+    args = [A, A, A, A, A, A, A]
+    # step out of range
+    assert xattn.xattn_decode(d, *args, 5, A, A, A, ws) == xattn.XATTN_ERR_INVALID_ARG
+    assert xattn.xattn_decode(d, *args, -1, A, A, A, ws) == xattn.XATTN_ERR_INVALID_ARG
+    # no keys at all
+    d0 = _desc(Lmax=0)
+    assert xattn.xattn_decode(d0, A, None, None, None, A, A, A, 0, A, A, A, ws) == xattn.XATTN_ERR_INVALID_ARG
+    # missing pointers
+    assert xattn.xattn_decode(d, A, None, A, A, A, A, A, 1, A, A, A, ws) == xattn.XATTN_ERR_INVALID_ARG
+    assert xattn.xattn_decode(d, A, A, A, A, None, A, A, 1, A, A, A, ws) == xattn.XATTN_ERR_INVALID_ARG
+    # misaligned tensors / workspace
+    assert xattn.xattn_decode(d, A + 2, A, A, A, A, A, A, 1, A, A, A, ws) == xattn.XATTN_ERR_MISALIGNED
+    assert xattn.xattn_decode(d, A, A, A, A, A, A, A, 1, A, A, A + 16, ws) == xattn.XATTN_ERR_MISALIGNED
+    # workspace too small
+    assert xattn.xattn_decode(d, *args, 1, A, A, A, ws - 1) == xattn.XATTN_ERR_WORKSPACE_TOO_SMALL
+    # beam update: step range, slots, pointers
+    assert xattn.xattn_beam_update(d, A, A, A, A, A, A, 4) == xattn.XATTN_ERR_INVALID_ARG
+    assert xattn.xattn_beam_update(_desc(S=8), A, A, A, A, A, A, 2) == xattn.XATTN_ERR_INVALID_ARG
+    assert xattn.xattn_beam_update(d, None, A, A, A, A, A, 1) == xattn.XATTN_ERR_INVALID_ARG
+    assert xattn.xattn_beam_update(d, A, A + 8, A, A, A, A, 1) == xattn.XATTN_ERR_MISALIGNED
+
+
+def test_split_plan_covers_prefix(lib):
+    for Lmax in (128, 300, 2048, 32768):
+        for split in (0, 128, 1024):
+            d = xattn.make_desc(8, 128, 32, 8, 128, Lmax, 384, 3, 0.0, 0, split)
+            rc, p = xattn.xattn_query_plan(d, 3)
+            assert rc == 0
+            assert p.split_tokens % 128 == 0 and p.split_tokens > 0
+            assert (p.num_splits - 1) * p.split_tokens < Lmax <= p.num_splits * p.split_tokens
+            assert p.rows_per_unit == 512 and p.row_tiles == 4
+            assert p.shared_kernel == 1
+
+
+def test_small_row_units_use_cuda_cores(lib):
+    d = xattn.make_desc(64, 1, 32, 8, 128, 8192, 512, 512)
+    rc, p = xattn.xattn_query_plan(d, 512)
+    assert rc == 0 and p.shared_kernel == 2 and p.rows_per_unit == 4

@@ -1,0 +1,200 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded
+inputs. Small shapes compare every output; the full-size workloads compare sampled rows."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from decode_attention_xattention_gb300 import build, workloads as wl, xattn
+from decode_attention_xattention_gb300.runner import DeviceBatch, bf16_tensor_to_f32
+from gpu_helpers import compare, run_and_check
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    xattn.load()
+
+
+# -- small shapes: every output row, both Shared-stage kernels ---------------------------
+SMALL = [
+    # (R, BW, Hq, Hkv, d, lens, T): several tiles with ragged tails, ragged requests
+    (1, 4, 2, 1, 64, (256,), 3),
+    (2, 5, 8, 2, 128, (300, 129), 3),
+    (3, 40, 16, 4, 128, (1000, 1, 517), 2),     # M = 160 rows: two row tiles, ragged
+    (2, 16, 8, 8, 64, (640, 383), 4),           # G = 1
+    (1, 3, 16, 2, 128, (2049,), 5),             # G = 8
+    (2, 2, 16, 1, 64, (130, 255), 1),           # G = 16
+    (1, 64, 8, 2, 128, (4096,), 6),             # M = 256
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: f"R{s[0]}_BW{s[1]}_H{s[2]}x{s[3]}_d{s[4]}_L{'-'.join(map(str, s[5]))}_t{s[6]}")
+@pytest.mark.parametrize("kernel", [1, 2], ids=["tensor_core", "cuda_core"])
+def test_small_all_rows(shape, kernel):
+    R, BW, Hq, Hkv, d, lens, T = shape
+    w = wl.custom(R=R, BW=BW, Hq=Hq, Hkv=Hkv, d=d, lens=lens, T=T, seed=7)
+    run_and_check(w, shared_kernel=kernel)
+
+
+@pytest.mark.parametrize("split", [128, 256, 384, 1024])
+def test_forced_splits_merge(split):
+    w = wl.custom(R=2, BW=8, Hq=8, Hkv=2, d=128, lens=(1100, 700), T=3, seed=3)
+    run_and_check(w, split_tokens=split)
+
+
+def test_tiny_config_both_kernels():
+    for k in (0, 1, 2):
+        stats, _, _ = run_and_check(wl.TINY, shared_kernel=k)
+
+
+def test_shared_only_and_ns_only():
+    w = wl.custom(R=2, BW=6, Hq=8, Hkv=2, d=128, lens=(777, 300), T=3, seed=5)
+    run_and_check(w, step=0)  # Shared stage alone
+    w0 = wl.custom(R=2, BW=6, Hq=8, Hkv=2, d=128, lens=(0, 0), T=3, seed=5, lmax=256)
+    run_and_check(w0)  # Non-Shared stage alone (prefix length 0, storage present)
+    wn = wl.custom(R=2, BW=6, Hq=8, Hkv=2, d=64, lens=(0, 0), T=3, seed=5)
+    assert wn.max_shared_len == 0
+    run_and_check(wn)  # no prefix storage at all (max_shared_len 0)
+
+
+@pytest.mark.parametrize("kernel", [1, 2], ids=["tensor_core", "cuda_core"])
+def test_shared_stage_pieces_match_oracle_partials(kernel):
+    """xattn_decode_shared alone: every prefix piece's (normalised output, lse) against the
+    oracle's attention restricted to that piece's tokens."""
+    w = wl.custom(R=2, BW=8, Hq=8, Hkv=2, d=128, lens=(1100, 300), T=3, seed=3)
+    inp = wl.make_inputs(w)
+    db = DeviceBatch(inp, shared_kernel=kernel, split_tokens=256)
+    xattn.check(db.decode_shared())
+    torch.cuda.synchronize()
+    p = db.plan()
+    assert p.num_splits == 5 and p.split_tokens == 256
+    po, pl = (t.cpu().numpy() for t in db.partials())
+    orc = oracle.load()
+    D = oracle.dims_of(w)
+    R, BW, Hkv, G, d = w.num_requests, w.beam_width, w.num_kv_heads, w.group_size, w.head_dim
+    for c in range(p.num_splits):
+        ro, rl = orc.partial(D, inp.q, inp.shared_k, inp.shared_v, inp.shared_len, inp.shared_k[:, :1] * 0,
+                             inp.shared_v[:, :1] * 0, np.zeros((R, BW, w.max_steps), np.int32), c * 256,
+                             (c + 1) * 256, 0, 0)
+        ro = ro.reshape(R, BW, Hkv, G, d).transpose(0, 2, 1, 3, 4).reshape(R, Hkv, BW * G, d)
+        rl = rl.reshape(R, BW, Hkv, G).transpose(0, 2, 1, 3).reshape(R, Hkv, BW * G)
+        for r in range(R):
+            if np.isneginf(rl[r]).all():  # piece past this request's prefix
+                assert np.isneginf(pl[r, :, c]).all() and not po[r, :, c].any()
+                continue
+            compare(po[r, :, c], pl[r, :, c], ro[r], rl[r], f"piece {c} of request {r}")
+
+
+def test_equal_ancestry_equal_output_bitwise():
+    w = wl.custom(R=1, BW=8, Hq=8, Hkv=2, d=128, lens=(900,), T=3, seed=11)
+    inp = wl.make_inputs(w)
+    par = inp.parents.copy()
+    par[1:, 0, :] = 3
+    q = inp.q.copy()
+    q[0, 5] = q[0, 2]
+    inp = wl.Inputs(w, q, inp.shared_k, inp.shared_v, inp.shared_len, inp.new_k, inp.new_v, par)
+    db = DeviceBatch(inp)
+    db.build_cache()
+    idx = db.idx.clone()
+    idx[0, 5] = idx[0, 2]
+    db.idx.copy_(idx)
+    xattn.check(db.decode())
+    torch.cuda.synchronize()
+    o = db.out.float().cpu().numpy()
+    l = db.lse.cpu().numpy()
+    np.testing.assert_array_equal(o[0, 5], o[0, 2])
+    np.testing.assert_array_equal(l[0, 5], l[0, 2])
+
+
+def test_repeated_calls_deterministic():
+    w = wl.custom(R=2, BW=16, Hq=8, Hkv=2, d=128, lens=(1500, 900), T=3, seed=13)
+    db = DeviceBatch(wl.make_inputs(w))
+    db.build_cache()
+    xattn.check(db.decode())
+    a = db.out.clone()
+    for _ in range(3):
+        xattn.check(db.decode())
+    torch.cuda.synchronize()
+    assert torch.equal(a, db.out)
+
+
+def test_cuda_graph_capture_replay():
+    w = wl.custom(R=2, BW=16, Hq=8, Hkv=2, d=128, lens=(1500, 900), T=3, seed=17)
+    inp = wl.make_inputs(w)
+    s = torch.cuda.Stream()
+    db = DeviceBatch(inp, stream=s)
+    with torch.cuda.stream(s):
+        db.build_cache()
+        xattn.check(db.decode())
+    s.synchronize()
+    ref = db.out.clone()
+    db.out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        xattn.check(db.decode())
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(ref, db.out)
+
+
+# -- device-detected data errors: status word + NaN rows, no trap --------------------------
+def test_bad_slot_sets_status_and_nan_row():
+    w = wl.custom(R=1, BW=4, Hq=4, Hkv=2, d=128, lens=(200,), T=2, seed=1)
+    db = DeviceBatch(wl.make_inputs(w))
+    db.build_cache()
+    db.idx[0, 1, 0] = 10_000
+    xattn.check(db.decode())
+    st = db.read_status()
+    assert st & xattn.XATTN_STATUS_BAD_SLOT
+    o = db.out.float().cpu()
+    assert torch.isnan(o[0, 1]).all() and torch.isfinite(o[0, 0]).all()
+    assert db.read_status() == 0  # cleared by the previous read
+
+
+def test_bad_shared_len_sets_status():
+    w = wl.custom(R=2, BW=4, Hq=4, Hkv=2, d=128, lens=(200, 100), T=2, seed=1)
+    db = DeviceBatch(wl.make_inputs(w))
+    db.build_cache()
+    db.shared_len[1] = 5000
+    xattn.check(db.decode())
+    st = db.read_status()
+    assert st & xattn.XATTN_STATUS_BAD_SHARED_LEN
+    o = db.out.float().cpu()
+    assert torch.isnan(o[1]).all() and torch.isfinite(o[0]).all()
+
+
+def test_bad_parent_sets_status():
+    w = wl.custom(R=1, BW=4, Hq=4, Hkv=2, d=128, lens=(64,), T=3, seed=1)
+    db = DeviceBatch(wl.make_inputs(w))
+    xattn.check(db.beam_update(0))
+    db.parents[1, 0, 2] = 9
+    xattn.check(db.beam_update(1))
+    torch.cuda.synchronize()
+    assert int(db.status.item()) & xattn.XATTN_STATUS_BAD_PARENT
+    assert int(db.idx[0, 2, 0].item()) == -1
+
+
+def test_empty_row_status():
+    w = wl.custom(R=1, BW=2, Hq=2, Hkv=1, d=64, lens=(0,), T=1, seed=1, lmax=64)
+    db = DeviceBatch(wl.make_inputs(w))
+    xattn.check(db.decode(0))
+    assert db.read_status() & xattn.XATTN_STATUS_EMPTY_ROW
+
+
+# -- the full-size workloads: sampled rows vs the oracle ---------------------------------
+FULL = [wl.GR, wl.WIDE, wl.LONG, wl.FEATHER_1, wl.FEATHER_8, wl.FEATHER_64]
+
+
+@pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
+def test_full_size_sampled_rows(w):
+    rows = wl.sample_rows(w, 384, seed=2)
+    stats, db, _ = run_and_check(w, rows=rows)
+    # every output row is finite and every lse is finite
+    assert torch.isfinite(db.out.float()).all()
+    assert torch.isfinite(db.lse).all()
