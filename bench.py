@@ -345,9 +345,13 @@ def main():
         return g
 
     g_step = [capture(lambda db=db: step(db)) for db in sets]
-    g_shared = [capture(lambda db=db: xattn.check(db.decode_shared())) for db in sets]
-    g_merge = [capture(lambda db=db: xattn.check(db.decode_merge())) for db in sets]
     g_bu = [capture(lambda db=db: xattn.check(db.beam_update(T - 1))) for db in sets]
+    if plan.fused:  # xattn_decode is one kernel: Shared stage + Non-Shared + Merge
+        g_dominant = [capture(lambda db=db: xattn.check(db.decode())) for db in sets]
+        g_merge = None
+    else:
+        g_dominant = [capture(lambda db=db: xattn.check(db.decode_shared())) for db in sets]
+        g_merge = [capture(lambda db=db: xattn.check(db.decode_merge())) for db in sets]
 
     def timed(graphs, K, W):
         with torch.cuda.stream(stream):
@@ -382,10 +386,10 @@ def main():
     clocks = sampler.stop()
     ms_step = total_ms / K
 
-    # per-kernel average launch durations (each stage alone, same rotation)
+    # per-kernel average launch durations (each alone, same rotation of input sets)
     Kk = max(200, min(K, 5000))
-    ms_shared = timed(g_shared, Kk, W) / Kk
-    ms_merge = timed(g_merge, Kk, W) / Kk
+    ms_dom = timed(g_dominant, Kk, W) / Kk
+    ms_merge = timed(g_merge, Kk, W) / Kk if g_merge else 0.0
     ms_bu = timed(g_bu, Kk, W) / Kk
     for db in sets:
         assert db.read_status() == 0, "device status set during the bench"
@@ -439,11 +443,11 @@ def main():
     beams = w.num_beams * world
     ub, ub_parts = unique_bytes(w, db.idx.cpu().numpy(), inp.shared_len)
     flops = shared_stage_flops(w)
-    sbytes = shared_stage_bytes(w, plan)
+    sbytes = ub if plan.fused else shared_stage_bytes(w, plan)  # fused: the kernel moves the step's unique bytes
     t_tc = flops / (peaks["bf16_tflops"] * 1e12)
     t_hbm = sbytes / (peaks["hbm_gbs"] * 1e9)
     bound = "tensor" if t_tc >= t_hbm else "hbm"
-    s_shared = ms_shared * 1e-3
+    s_shared = ms_dom * 1e-3
     if bound == "tensor":
         achieved, peak, unit = flops / s_shared / 1e12, peaks["bf16_tflops"], "TFLOP/s"
     else:
@@ -469,10 +473,13 @@ def main():
                                       f"(> 2x the {l2 / 1e6:.0f} MB L2)", "timing": "CUDA graph replays, CUDA events",
                                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                                 "shared_splits": plan.num_splits, "split_tokens": plan.split_tokens,
-                                "shared_kernel": "tcgen05" if plan.shared_kernel == 1 else "cuda-core"}),
+                                "shared_kernel": "tcgen05" if plan.shared_kernel == 1 else "cuda-core",
+                                "fused_ns_merge": bool(plan.fused)}),
         "us_per_step": ms_step * 1e3,
-        "attention_us_per_step": (ms_shared + ms_merge) * 1e3,
-        "stage_us": {"beam_update": ms_bu * 1e3, "shared_stage": ms_shared * 1e3, "ns_merge": ms_merge * 1e3},
+        "attention_us_per_step": (ms_dom + ms_merge) * 1e3,
+        "stage_us": {"beam_update": ms_bu * 1e3,
+                     ("decode_fused" if plan.fused else "shared_stage"): ms_dom * 1e3,
+                     "ns_merge": ms_merge * 1e3},
         "hbm": {"unique_bytes_per_step": ub, "parts": ub_parts, "achieved_gbs": hbm_gbs,
                 "frac_of_8tbs": hbm_gbs / NOMINAL_HBM_GBS, "frac_of_measured": hbm_gbs / peaks["hbm_gbs"]},
         "tensor": {"shared_stage_flops": flops, "achieved_tflops": flops / s_shared / 1e12,
@@ -484,7 +491,7 @@ def main():
                      "algorithmic_per_launch": flops if bound == "tensor" else sbytes},
         "e2e": {"value": beams / (ms_e2e * 1e-3), "unit": "beams/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
-        "gpu_launches": 3 * K,
+        "gpu_launches": (2 if plan.fused else 3) * K,
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(256) ns_merge_kernel(
     Geometry g, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ pool_k,
     const __nv_bfloat16* __restrict__ pool_v, const int32_t* __restrict__ idx,
     const int32_t* __restrict__ shared_len, const float* __restrict__ part_o,
-    const float* __restrict__ part_lse, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+    const float* __restrict__ part_lse, void* __restrict__ out, float* __restrict__ lse,
     int32_t* status) {
     constexpr int E = D / 32;
     const int lane = threadIdx.x & 31;
@@ -173,7 +173,16 @@ __global__ void __launch_bounds__(256) ns_merge_kernel(
             for (int e = 0; e < E; ++e) o[e] = acc[gg][e] * inv;
             row_lse = (m[gg] + __log2f(l[gg])) * kLn2;
         }
-        LaneVec<D>::store(out + (qrow0 + gg) * D + lane * E, o);
+        if (g.out_f32) {
+            float* dst = reinterpret_cast<float*>(out) + (qrow0 + gg) * D + lane * E;
+            if constexpr (E == 4) {
+                *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+            } else {
+                *reinterpret_cast<float2*>(dst) = make_float2(o[0], o[1]);
+            }
+        } else {
+            LaneVec<D>::store(reinterpret_cast<__nv_bfloat16*>(out) + (qrow0 + gg) * D + lane * E, o);
+        }
         if (lane == 0) lse[qrow0 + gg] = row_lse;
     }
 }
@@ -181,7 +190,7 @@ __global__ void __launch_bounds__(256) ns_merge_kernel(
 template <int D>
 cudaError_t launch_d(const Geometry& g, dim3 grid, dim3 block, cudaStream_t st, const __nv_bfloat16* q,
                      const __nv_bfloat16* pk, const __nv_bfloat16* pv, const int32_t* idx,
-                     const int32_t* slen, const float* po, const float* pl, __nv_bfloat16* out,
+                     const int32_t* slen, const float* po, const float* pl, void* out,
                      float* lse, int32_t* status) {
     switch (g.G) {
 #define XATTN_G(GV) \
@@ -203,7 +212,7 @@ int merge_ctas_for(const Geometry& g) {
 cudaError_t launch_ns_merge(const Geometry& g, const __nv_bfloat16* q, const __nv_bfloat16* pool_k,
                             const __nv_bfloat16* pool_v, const int32_t* beam_tok_idx,
                             const int32_t* shared_len, const float* part_o, const float* part_lse,
-                            __nv_bfloat16* out, float* lse, int32_t* status, cudaStream_t stream) {
+                            void* out, float* lse, int32_t* status, cudaStream_t stream) {
     dim3 grid(merge_ctas_for(g)), block(256);
     if (g.d == 128)
         return launch_d<128>(g, grid, block, stream, q, pool_k, pool_v, beam_tok_idx, shared_len, part_o,

@@ -1,26 +1,36 @@
-// Shared stage on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), sm_103a.
+// Shared stage on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), sm_103a,
+// optionally fused with the Non-Shared stage and the Merge.
 //
 // xGR: Efficient Generative Recommendation Serving at Scale, section 2.1 (xAttention): the
 // prompt KV is stored once per request, so the Shared stage serves every beam of a
 // request from one copy; it produces local scores and max/sum statistics that the Merge
-// stage later combines with an online softmax. The same section fuses the batched matmul
-// with the softmax and pipelines the stages across hardware units; on GB300 that becomes
-// one warp-specialised CTA: a TMA warp streams K/V tiles, an MMA warp drives the tensor
-// core, and a softmax warpgroup turns scores into probabilities between the two matmuls.
+// stage combines with those of the Non-Shared stage by an online softmax. The section fuses
+// the batched matmul with the softmax and pipelines the stages across hardware units; on
+// GB300 that becomes one warp-specialised CTA: a TMA warp streams K/V tiles, an MMA warp
+// drives the tensor core, and two softmax warpgroups turn scores into probabilities
+// between the two matmuls, each on its own 128-row tile so the tensor core always has the
+// other tile's work while one warpgroup computes exponentials.
 //
 // Work unit: (request r, KV head h). All BW beams x G query heads of that KV head are
 // stacked into M = BW*G rows (row m = b*G + g), so one K/V tile read from HBM feeds every
-// beam. A CTA owns one 128-row tile of those rows and one piece of the prefix:
-//   for each 128-token K/V tile j of the piece:
-//     S_j = Q . K_j^T               (tcgen05, bf16 in, fp32 in TMEM; S double-buffered)
-//     P_j = exp2(S_j*scale*log2e - m) (softmax warpgroup: one thread per row)
-//     O  += P_j . V_j               (tcgen05, P from shared memory, V as MN-major operand)
-// The running max is only raised when it grows by more than 2^8, so O is rescaled rarely;
-// every P stays below 2^8. The piece's normalised output and natural-log LSE are written
-// to the workspace for the Merge stage.
+// beam. A CTA owns two 128-row tiles (rows 256p .. 256p+255) and one piece of the prefix.
+// Per 128-token K/V tile j and row tile i:
+//     S_i = Q_i . K_j^T                 tcgen05 (SS), fp32 in TMEM columns [128 i, 128 i + 128)
+//     P_i = exp2(S_i*scale*log2e - m_i) softmax warpgroup i; P written back over S_i as bf16
+//     O_i += P_i . V_j                  tcgen05 (TS: P read from TMEM), V as MN-major operand
+// The MMA warp issues, per tile j and row tile i: PV_i(j-1) then QK_i(j), then commits
+// s_full[i]; the commit therefore also tells softmax i that O_i is up to date. The running
+// max is raised only when it grows by more than 2^8, so O is rescaled rarely and every P
+// stays below 2^8.
+//
+// Epilogue. When the prefix is not split (one piece) and the beams have at most
+// kMaxFusedSteps Non-Shared tokens, the CTA finishes the job: each softmax thread gathers
+// its beam's ancestry tokens from the pool, folds their scores into its row's (max, sum)
+// and O, and writes the normalised output and LSE. Otherwise it writes the piece's
+// normalised output and LSE to the workspace for the separate Non-Shared + Merge kernel.
 //
 // Every on-chip wait is bounded: on a timeout the CTA records XATTN_STATUS_TIMEOUT, writes
-// NaN partials, waits (bounded) for its own TMA copies and MMAs, frees TMEM and returns.
+// NaN, waits (bounded) for its own TMA copies and MMAs, frees TMEM and returns.
 #include "sm100_ptx.cuh"
 #include "xattn_internal.cuh"
 
@@ -29,26 +39,26 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 192;  // warps 0-3 softmax / epilogue, warp 4 TMA, warp 5 MMA
+constexpr int kThreads = 320;  // warps 0-7: two softmax warpgroups; warp 8: TMA; warp 9: MMA
+constexpr int kWarpTma = 8, kWarpMma = 9;
 constexpr int kMaxStages = 4;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256;
+constexpr uint32_t kTmemCols = 512;  // S0 | S1 | O0 | O1, 128 columns each
+constexpr uint32_t kTmemO = 256;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr uint32_t kNaN = 0x7fc00000u;
 
 // K/V pipeline depth: 2 stages at d = 128, 4 at d = 64. Either way the shared memory
 // admits one CTA per SM, so a CTA never waits for another's 512 TMEM columns.
 template <int D>
 struct Cfg {
     static constexpr int kStages = D == 64 ? 4 : 2;
-    static constexpr int KB = D / 64;            // 128-byte swizzle blocks along d
-    static constexpr int kTileBytes = KB * 16384; // 128 rows (or tokens) x d bf16
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kTileBytes;
+    static constexpr int KB = D / 64;              // 128-byte swizzle blocks along d
+    static constexpr int kTileBytes = KB * 16384;  // 128 rows (or tokens) x d bf16
+    static constexpr int kOffQ = 0;                // two row tiles
+    static constexpr int kOffK = kOffQ + 2 * kTileBytes;
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
-    static constexpr int kOffP = kOffV + kStages * kTileBytes;
-    static constexpr int kPBytes = 2 * 16384;     // 128 rows x 128 tokens bf16
-    static constexpr int kSmemBytes = kOffP + kPBytes + 1024;
+    static constexpr int kSmemBytes = kOffV + kStages * kTileBytes + 1024;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -62,23 +72,48 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
+    return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u));
+}
+
 // Byte offset of 16-byte chunk `ch` (along the contraction dim) of row `row` in a tile
 // stored as [ch/8 block][128 rows][128 B] with the 128-byte swizzle (chunk ^= row % 8).
 __device__ __forceinline__ uint32_t sw128_offset(int row, int ch) {
     return (uint32_t)((ch >> 3) * 16384 + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
 }
 
+__device__ __forceinline__ float max32(const uint32_t (&s)[32], int valid) {
+    float m[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m[i] = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const float x = i < valid ? __uint_as_float(s[i]) : -INFINITY;
+        m[i & 7] = fmaxf(m[i & 7], x);
+    }
+    return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+}
+
 struct Bars {
-    uint64_t k_full[kMaxStages], v_full[kMaxStages], kv_empty[kMaxStages];
-    uint64_t s_full[2], s_free[2];
-    uint64_t p_full, pv_done, q_ready, final_mma;
+    uint64_t k_full[kMaxStages], k_empty[kMaxStages], v_full[kMaxStages], v_empty[kMaxStages];
+    uint64_t s_full[2], p_full[2], q_ready[2];
+    uint64_t o_full, final_mma;
+};
+
+struct FusedArgs {
+    const __nv_bfloat16* pool_k;
+    const __nv_bfloat16* pool_v;
+    const int32_t* idx;
+    void* out;
+    float* lse;
+    int enabled;
 };
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
     Geometry g, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ shared_len,
-    float* __restrict__ part_o, float* __restrict__ part_lse, int32_t* status) {
+    float* __restrict__ part_o, float* __restrict__ part_lse, int32_t* status, FusedArgs fa) {
     using C = Cfg<D>;
     constexpr int kStages = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -86,7 +121,6 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     uint8_t* sQ = smem + C::kOffQ;
     uint8_t* sK = smem + C::kOffK;
     uint8_t* sV = smem + C::kOffV;
-    uint8_t* sP = smem + C::kOffP;
     __shared__ Bars bars;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
@@ -94,37 +128,40 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // Work item: CTAs of one (unit, piece) are adjacent so its K/V tiles are shared in L2.
+    const int row_pairs = (g.row_tiles + 1) >> 1;
     long t = blockIdx.x;
-    const int mt = (int)(t % g.row_tiles);
-    t /= g.row_tiles;
+    const int mp = (int)(t % row_pairs);
+    t /= row_pairs;
     const int c = (int)(t % g.nsplit);
     const long unit = t / g.nsplit;
     const int h = (int)(unit % g.Hkv);
     const int r = (int)(unit / g.Hkv);
-    int L = shared_len[r];
-    if (L < 0 || L > g.Lmax) L = 0;  // reported by the Merge stage
+    const int L_raw = shared_len[r];
+    const bool bad_len = L_raw < 0 || L_raw > g.Lmax;
+    const int L = bad_len ? 0 : L_raw;
     const int t0 = c * g.split_tokens;
     const int t1 = min(t0 + g.split_tokens, L);
     const int ntiles = t1 > t0 ? (t1 - t0 + kTileKeys - 1) / kTileKeys : 0;
+    const int ntile_m = (2 * mp + 1 < g.row_tiles) ? 2 : 1;  // row tiles this CTA owns
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bars.k_full[s], 1);
+            mbar_init(&bars.k_empty[s], 1);
             mbar_init(&bars.v_full[s], 1);
-            mbar_init(&bars.kv_empty[s], 1);
+            mbar_init(&bars.v_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars.s_full[s], 1);
-            mbar_init(&bars.s_free[s], 128);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.s_full[i], 1);
+            mbar_init(&bars.p_full[i], 128);
+            mbar_init(&bars.q_ready[i], 128);
         }
-        mbar_init(&bars.p_full, 128);
-        mbar_init(&bars.pv_done, 1);
-        mbar_init(&bars.q_ready, 128);
+        mbar_init(&bars.o_full, 1);
         mbar_init(&bars.final_mma, 1);
         abort_sh = 0;
         fence_barrier_init();
     }
-    if (warp == 5 && ntiles > 0) {
+    if (warp == kWarpMma && ntiles > 0) {
         tmem_alloc(&tmem_base_sh, kTmemCols);
         tmem_relinquish();
     }
@@ -133,196 +170,324 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
 
-    const size_t prow0 = ((size_t)unit * g.nsplit + c) * g.M;  // first partial row of this piece
-
-    if (warp < 4) {
-        // ------------------------------------------------ softmax warpgroup: thread = row
-        const int row = mt * kTileRows + tid;
-        const bool row_ok = row < g.M;
+    if (warp < 8) {
+        // ============================================ softmax warpgroups: thread = row
+        const int wg = warp >> 2;
+        const int rloc = tid & 127;
+        const int mt = 2 * mp + wg;
+        const bool tile_ok = wg < ntile_m;
+        const int row = mt * kTileRows + rloc;
+        const bool row_ok = tile_ok && row < g.M;
+        const int b = row / g.G, gg = row - (row / g.G) * g.G;
+        uint8_t* sQw = sQ + wg * C::kTileBytes;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
-        if (ntiles > 0) {
+        if (tile_ok && ntiles > 0) {
             {  // Q tile -> shared memory, K-major, 128-byte swizzle; rows past M are zero
-                const __nv_bfloat16* src = nullptr;
-                if (row_ok) {
-                    const int b = row / g.G, gg = row - b * g.G;
-                    src = q + (((size_t)r * g.BW + b) * g.Hq + (size_t)h * g.G + gg) * D;
-                }
+                const __nv_bfloat16* src = row_ok ? q + (((size_t)r * g.BW + b) * g.Hq + (size_t)h * g.G + gg) * D
+                                                  : nullptr;
 #pragma unroll
                 for (int ch = 0; ch < D / 8; ++ch) {
                     uint4 v = make_uint4(0, 0, 0, 0);
                     if (row_ok) v = __ldg(reinterpret_cast<const uint4*>(src) + ch);
-                    *reinterpret_cast<uint4*>(sQ + sw128_offset(tid, ch)) = v;
+                    *reinterpret_cast<uint4*>(sQw + sw128_offset(rloc, ch)) = v;
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(&bars.q_ready);
+                mbar_arrive(&bars.q_ready[wg]);
             }
-            const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+            const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+            const uint32_t tS = tmem + lane_base + wg * 128;
+            const uint32_t tO = tmem + lane_base + kTmemO + wg * 128;
             for (int j = 0; j < ntiles; ++j) {
-                const int sb = j & 1;
-                if (!__all_sync(0xffffffffu, mbar_wait(&bars.s_full[sb], (j >> 1) & 1, &abort_sh))) { ok = false; break; }
+                if (!__all_sync(0xffffffffu, mbar_wait(&bars.s_full[wg], j & 1, &abort_sh))) { ok = false; break; }
                 tc_fence_after();
-                uint32_t sr[4][32];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) tmem_ld32(tmem + lane_base + (sb ? kTmemS1 : kTmemS0) + k * 32, sr[k]);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(&bars.s_free[sb]);  // S buffer may be overwritten now
-
                 const int lim = t1 - (t0 + j * kTileKeys);  // valid columns of this tile (>= 1)
+                // pass 1: row max of the raw scores
                 float mx = -INFINITY;
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        float x = __uint_as_float(sr[k][i]) * g.scale_log2;
-                        x = (k * 32 + i < lim) ? x : -INFINITY;
-                        sr[k][i] = __float_as_uint(x);
-                        mx = fmaxf(mx, x);
-                    }
-                const float m_new = fmaxf(m_run, mx);
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t s[32];
+                    tmem_ld32(tS + k * 32, s);
+                    tmem_wait_ld();
+                    mx = fmaxf(mx, max32(s, lim - k * 32));
+                }
+                const float m_new = fmaxf(m_run, mx * g.scale_log2);
                 const bool resc = m_new > m_run + kRescaleThreshold;
                 const float alpha = resc ? ex2(m_run - m_new) : 1.f;
                 const float m_use = resc ? m_new : m_run;
-                float sum = 0.f;
-                uint32_t pk[4][16];
+                // pass 2: P = exp2(S*scale*log2e - m) as bf16, written over the consumed S columns
+                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t s[32], p[16];
+                    tmem_ld32(tS + k * 32, s);
+                    tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float p0 = ex2(__uint_as_float(sr[k][2 * i]) - m_use);
-                        const float p1 = ex2(__uint_as_float(sr[k][2 * i + 1]) - m_use);
-                        sum += p0 + p1;
-                        pk[k][i] = pack_bf16(p0, p1);
+                        const int col = k * 32 + 2 * i;
+                        const float x0 = col < lim ? fmaf(__uint_as_float(s[2 * i]), g.scale_log2, -m_use) : -INFINITY;
+                        const float x1 = col + 1 < lim ? fmaf(__uint_as_float(s[2 * i + 1]), g.scale_log2, -m_use) : -INFINITY;
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        sum4[i & 3] += p0 + p1;
+                        p[i] = pack_bf16(p0, p1);
                     }
-                l_run = l_run * alpha + sum;
-                m_run = m_use;
-
-                // O and the P buffer are free once the previous P.V has completed.
-                if (j > 0) {
-                    if (!__all_sync(0xffffffffu, mbar_wait(&bars.pv_done, (j - 1) & 1, &abort_sh))) { ok = false; break; }
-                    tc_fence_after();
+                    tmem_st16(tS + k * 16, p);
                 }
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {  // 16-byte chunk = 8 tokens
-                        const int ch = k * 4 + cc;
-                        *reinterpret_cast<uint4*>(sP + sw128_offset(tid, ch)) =
-                            make_uint4(pk[k][cc * 4 + 0], pk[k][cc * 4 + 1], pk[k][cc * 4 + 2], pk[k][cc * 4 + 3]);
-                    }
+                l_run = l_run * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+                m_run = m_use;
                 if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
                     for (int k = 0; k < D / 32; ++k) {
                         uint32_t o[32];
-                        tmem_ld32(tmem + lane_base + kTmemO + k * 32, o);
+                        tmem_ld32(tO + k * 32, o);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st32(tmem + lane_base + kTmemO + k * 32, o);
+                        tmem_st32(tO + k * 32, o);
                     }
-                    tmem_wait_st();
                 }
-                fence_proxy_async_smem();
+                tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&bars.p_full);
+                mbar_arrive(&bars.p_full[wg]);
             }
-            if (ok && !__all_sync(0xffffffffu, mbar_wait(&bars.pv_done, (ntiles - 1) & 1, &abort_sh))) ok = false;
+            if (ok && !__all_sync(0xffffffffu, mbar_wait(&bars.o_full, 0, &abort_sh))) ok = false;
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
             if (!ok) {
                 abort_sh = 1;
                 if (lane == 0) set_status(status, XATTN_STATUS_TIMEOUT);
             }
-            // Epilogue: normalised O row and its LSE.
-            const float inv = ok ? 1.f / l_run : __int_as_float(0x7fc00000);
+        }
+        const uint32_t tO = tmem + ((uint32_t)((warp & 3) * 32) << 16) + kTmemO + wg * 128;
+        const bool have_o = tile_ok && ntiles > 0;  // O_i holds accumulated P.V (TMEM allocated)
+
+        if (fa.enabled) {
+            // ---------------------------------------- fused Non-Shared stage + Merge
+            bool bad = !ok || bad_len;
+            if (tile_ok && rloc == 0 && mt == 0 && h == 0 && bad_len) set_status(status, XATTN_STATUS_BAD_SHARED_LEN);
+            float s2[kMaxFusedSteps];
+            int slots[kMaxFusedSteps];
+            float m_tot = m_run;
+            const size_t qrow = ((size_t)r * g.BW + b) * g.Hq + (size_t)h * g.G + gg;
+            if (row_ok && g.step > 0) {
+                const int32_t* irow = fa.idx + ((size_t)r * g.BW + b) * g.Tmax;
+                // the query row (bf16 pairs); L2-resident, the Q tile was just read
+                uint32_t qv[D / 2];
+#pragma unroll
+                for (int ch = 0; ch < D / 8; ++ch) {
+                    const uint4 u = __ldg(reinterpret_cast<const uint4*>(q + qrow * D) + ch);
+                    qv[4 * ch] = u.x; qv[4 * ch + 1] = u.y; qv[4 * ch + 2] = u.z; qv[4 * ch + 3] = u.w;
+                }
+                bool bad_slot = false;
+#pragma unroll
+                for (int i = 0; i < kMaxFusedSteps; ++i) {
+                    s2[i] = -INFINITY;
+                    slots[i] = -1;
+                    if (i < g.step) {
+                        const int slot = __ldg(irow + i);
+                        if (slot < 0 || slot >= g.S) { bad_slot = true; continue; }
+                        slots[i] = slot;
+                        const uint4* kr = reinterpret_cast<const uint4*>(fa.pool_k + (((size_t)r * g.S + slot) * g.Hkv + h) * D);
+                        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+                        for (int ch = 0; ch < D / 8; ++ch) {
+                            const uint4 u = __ldg(kr + ch);
+                            const uint32_t kw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 qf = unpack_bf16(qv[4 * ch + e]), kf = unpack_bf16(kw[e]);
+                                acc0 = fmaf(qf.x, kf.x, acc0);
+                                acc1 = fmaf(qf.y, kf.y, acc1);
+                            }
+                        }
+                        s2[i] = (acc0 + acc1) * g.scale_log2;
+                        m_tot = fmaxf(m_tot, s2[i]);
+                    }
+                }
+                if (bad_slot) {
+                    bad = true;
+                    set_status(status, XATTN_STATUS_BAD_SLOT);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < kMaxFusedSteps; ++i) { s2[i] = -INFINITY; slots[i] = -1; }
+            }
+            if (row_ok && !bad_len && L == 0 && g.step == 0) {
+                bad = true;
+                set_status(status, XATTN_STATUS_EMPTY_ROW);
+            }
+            const float alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - m_tot);
+            float pw[kMaxFusedSteps];
+            float l_tot = l_run * alpha;
+#pragma unroll
+            for (int i = 0; i < kMaxFusedSteps; ++i) {
+                pw[i] = (s2[i] == -INFINITY) ? 0.f : ex2(s2[i] - m_tot);
+                l_tot += pw[i];
+            }
+            bad = bad || !(l_tot > 0.f);
+            const float inv = bad ? __uint_as_float(kNaN) : 1.f / l_tot;
+            const size_t obase = qrow * D;
 #pragma unroll
             for (int k = 0; k < D / 32; ++k) {
                 uint32_t o[32];
-                tmem_ld32(tmem + lane_base + kTmemO + k * 32, o);
-                tmem_wait_ld();
+                if (have_o) {
+                    tmem_ld32(tO + k * 32, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                }
                 if (row_ok) {
-                    float4* dst = reinterpret_cast<float4*>(part_o + (prow0 + row) * D + k * 32);
+                    float of[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) of[i] = __uint_as_float(o[i]) * alpha;
+#pragma unroll
+                    for (int s = 0; s < kMaxFusedSteps; ++s) {
+                        if (pw[s] == 0.f) continue;
+                        const uint4* vr = reinterpret_cast<const uint4*>(
+                            fa.pool_v + (((size_t)r * g.S + slots[s]) * g.Hkv + h) * D + k * 32);
+#pragma unroll
+                        for (int ch = 0; ch < 4; ++ch) {
+                            const uint4 u = __ldg(vr + ch);
+                            const uint32_t vw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 vf = unpack_bf16(vw[e]);
+                                of[ch * 8 + 2 * e] = fmaf(pw[s], vf.x, of[ch * 8 + 2 * e]);
+                                of[ch * 8 + 2 * e + 1] = fmaf(pw[s], vf.y, of[ch * 8 + 2 * e + 1]);
+                            }
+                        }
+                    }
+                    if (g.out_f32) {
+                        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(fa.out) + obase + k * 32);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(of[4 * i] * inv, of[4 * i + 1] * inv, of[4 * i + 2] * inv,
+                                                 of[4 * i + 3] * inv);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(fa.out) + obase + k * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(pack_bf16(of[8 * i] * inv, of[8 * i + 1] * inv),
+                                                pack_bf16(of[8 * i + 2] * inv, of[8 * i + 3] * inv),
+                                                pack_bf16(of[8 * i + 4] * inv, of[8 * i + 5] * inv),
+                                                pack_bf16(of[8 * i + 6] * inv, of[8 * i + 7] * inv));
+                    }
+                }
+            }
+            if (row_ok) fa.lse[qrow] = bad ? __uint_as_float(kNaN) : (m_tot + __log2f(l_tot)) * kLn2;
+        } else if (tile_ok) {
+            // ---------------------------------------- this piece's partial result
+            const size_t prow = ((size_t)unit * g.nsplit + c) * g.M + row;
+            const float inv = !ok ? __uint_as_float(kNaN) : (ntiles > 0 ? 1.f / l_run : 0.f);
+#pragma unroll
+            for (int k = 0; k < D / 32; ++k) {
+                uint32_t o[32];
+                if (have_o) {
+                    tmem_ld32(tO + k * 32, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                }
+                if (row_ok) {
+                    float4* dst = reinterpret_cast<float4*>(part_o + prow * D + k * 32);
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
                                              __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
                 }
             }
-            if (row_ok) part_lse[prow0 + row] = ok ? (m_run + __log2f(l_run)) * kLn2 : __int_as_float(0x7fc00000);
-        } else if (row_ok) {  // empty piece (past this request's prefix)
-            float4* dst = reinterpret_cast<float4*>(part_o + (prow0 + row) * D);
-#pragma unroll
-            for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            part_lse[prow0 + row] = -INFINITY;
+            if (row_ok)
+                part_lse[prow] = !ok ? __uint_as_float(kNaN)
+                                     : (ntiles > 0 ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY);
         }
-    } else if (warp == 4) {
-        // ------------------------------------------------ TMA producer
+    } else if (warp == kWarpTma) {
+        // ============================================ TMA producer
         if (lane == 0 && ntiles > 0) {
             prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
-            int issued = 0;
+            int issued_k = 0, issued_v = 0;
             for (int j = 0; j < ntiles; ++j) {
                 const int st = j % kStages, u = j / kStages;
-                if (u > 0 && !mbar_wait(&bars.kv_empty[st], (u - 1) & 1, &abort_sh)) break;
                 const int tok = t0 + j * kTileKeys;
+                if (u > 0 && !mbar_wait(&bars.k_empty[st], (u - 1) & 1, &abort_sh)) break;
                 mbar_arrive_expect_tx(&bars.k_full[st], C::kTileBytes);
 #pragma unroll
                 for (int kb = 0; kb < C::KB; ++kb)
                     tma_load_4d(sK + st * C::kTileBytes + kb * 16384, &tmap_k, &bars.k_full[st], kb * 64, h, tok, r);
+                issued_k = j + 1;
+                if (u > 0 && !mbar_wait(&bars.v_empty[st], (u - 1) & 1, &abort_sh)) break;
                 mbar_arrive_expect_tx(&bars.v_full[st], C::kTileBytes);
 #pragma unroll
                 for (int kb = 0; kb < C::KB; ++kb)
                     tma_load_4d(sV + st * C::kTileBytes + kb * 16384, &tmap_v, &bars.v_full[st], kb * 64, h, tok, r);
-                issued = j + 1;
+                issued_v = j + 1;
             }
             if (abort_sh) {  // let the copies still in flight land before the CTA exits
                 volatile int never = 0;
-                for (int j = max(0, issued - kStages); j < issued; ++j) {
+                for (int j = max(0, issued_k - kStages); j < issued_k; ++j)
                     mbar_wait(&bars.k_full[j % kStages], (j / kStages) & 1, &never);
+                for (int j = max(0, issued_v - kStages); j < issued_v; ++j)
                     mbar_wait(&bars.v_full[j % kStages], (j / kStages) & 1, &never);
-                }
             }
         }
     } else {
-        // ------------------------------------------------ MMA issuer
+        // ============================================ MMA issuer
         if (lane == 0 && ntiles > 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kTileKeys, 0, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
-            bool ok = mbar_wait(&bars.q_ready, 0, &abort_sh);
+            bool ok = mbar_wait(&bars.q_ready[0], 0, &abort_sh);
+            if (ok && ntile_m > 1) ok = mbar_wait(&bars.q_ready[1], 0, &abort_sh);
             tc_fence_after();
-            auto issue_pv = [&](int i) -> bool {
-                if (!mbar_wait(&bars.p_full, i & 1, &abort_sh)) return false;
-                const int st = i % kStages;
-                if (!mbar_wait(&bars.v_full[st], (i / kStages) & 1, &abort_sh)) return false;
-                tc_fence_after();
-                const uint32_t pbase = smem_addr(sP), vbase = smem_addr(sV + st * C::kTileBytes);
+            auto issue_pv = [&](int i, int jt, int vs) {
+                const uint32_t vbase = smem_addr(sV + vs * C::kTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < kTileKeys / 16; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(pbase + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
                     const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, 16384, 1024);
-                    mma_ss(tmem + kTmemO, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tmem + kTmemO + i * 128, tmem + i * 128 + kk * 8, bd, idesc_pv, (jt > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(&bars.pv_done);
-                mma_commit(&bars.kv_empty[st]);
-                return true;
             };
             for (int j = 0; ok && j < ntiles; ++j) {
-                const int st = j % kStages, sb = j & 1;
-                if (!mbar_wait(&bars.k_full[st], (j / kStages) & 1, &abort_sh)) { ok = false; break; }
-                if (j >= 2 && !mbar_wait(&bars.s_free[sb], ((j >> 1) - 1) & 1, &abort_sh)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t qbase = smem_addr(sQ), kbase = smem_addr(sK + st * C::kTileBytes);
+                const int ks = j % kStages;
+                if (!mbar_wait(&bars.k_full[ks], (j / kStages) & 1, &abort_sh)) { ok = false; break; }
+                const int vs = (j - 1 + kStages) % kStages;
+                if (j > 0 && !mbar_wait(&bars.v_full[vs], ((j - 1) / kStages) & 1, &abort_sh)) { ok = false; break; }
+                const uint32_t kbase = smem_addr(sK + ks * C::kTileBytes);
+                for (int i = 0; i < ntile_m; ++i) {
+                    if (j > 0) {
+                        if (!mbar_wait(&bars.p_full[i], (j - 1) & 1, &abort_sh)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_pv(i, j - 1, vs);
+                    } else {
+                        tc_fence_after();
+                    }
+                    const uint32_t qbase = smem_addr(sQ + i * C::kTileBytes);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_ss(tmem + (sb ? kTmemS1 : kTmemS0), smem_desc_sw128(qbase + off, 16, 1024),
-                           smem_desc_sw128(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_ss(tmem + i * 128, smem_desc_sw128(qbase + off, 16, 1024),
+                               smem_desc_sw128(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&bars.s_full[i]);
                 }
-                mma_commit(&bars.s_full[sb]);
-                if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
+                if (!ok) break;
+                mma_commit(&bars.k_empty[ks]);
+                if (j > 0) mma_commit(&bars.v_empty[vs]);
             }
-            if (ok && !issue_pv(ntiles - 1)) ok = false;
+            if (ok) {  // P.V of the last tile
+                const int jl = ntiles - 1, vs = jl % kStages;
+                if (!mbar_wait(&bars.v_full[vs], (jl / kStages) & 1, &abort_sh)) ok = false;
+                for (int i = 0; ok && i < ntile_m; ++i) {
+                    if (!mbar_wait(&bars.p_full[i], jl & 1, &abort_sh)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_pv(i, jl, vs);
+                }
+                if (ok) {
+                    mma_commit(&bars.v_empty[vs]);
+                    mma_commit(&bars.o_full);
+                }
+            }
             if (!ok) {
                 abort_sh = 1;
                 set_status(status, XATTN_STATUS_TIMEOUT);
@@ -337,36 +502,40 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 5 && ntiles > 0) tmem_dealloc(tmem, kTmemCols);
+    if (warp == kWarpMma && ntiles > 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int D>
-cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap& tv,
-                     const __nv_bfloat16* q, const int32_t* slen, float* po, float* pl,
-                     int32_t* status, cudaStream_t stream) {
+cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap& tv, const __nv_bfloat16* q,
+                     const int32_t* slen, float* po, float* pl, int32_t* status, const FusedArgs& fa,
+                     cudaStream_t stream) {
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 64 && !attr_done[dev]) {
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
         cudaError_t e = cudaFuncSetAttribute(shared_stage_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Cfg<D>::kSmemBytes);
         if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
-    const long ctas = (long)g.R * g.Hkv * g.nsplit * g.row_tiles;
-    shared_stage_tc_kernel<D><<<(unsigned)ctas, kThreads, Cfg<D>::kSmemBytes, stream>>>(tk, tv, g, q, slen, po, pl, status);
+    const long ctas = shared_tc_ctas_for(g);
+    shared_stage_tc_kernel<D><<<(unsigned)ctas, kThreads, Cfg<D>::kSmemBytes, stream>>>(tk, tv, g, q, slen, po, pl,
+                                                                                         status, fa);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-int shared_tc_ctas_for(const Geometry& g) { return g.R * g.Hkv * g.nsplit * g.row_tiles; }
+int shared_tc_ctas_for(const Geometry& g) { return g.R * g.Hkv * g.nsplit * ((g.row_tiles + 1) / 2); }
 
 cudaError_t launch_shared_stage_tc(const Geometry& g, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                    const __nv_bfloat16* q, const int32_t* shared_len, float* part_o,
-                                   float* part_lse, int32_t* status, cudaStream_t stream) {
-    if (g.d == 128) return launch_d<128>(g, tmap_k, tmap_v, q, shared_len, part_o, part_lse, status, stream);
-    if (g.d == 64) return launch_d<64>(g, tmap_k, tmap_v, q, shared_len, part_o, part_lse, status, stream);
+                                   float* part_lse, int32_t* status, const __nv_bfloat16* pool_k,
+                                   const __nv_bfloat16* pool_v, const int32_t* beam_tok_idx, void* out, float* lse,
+                                   bool fused, cudaStream_t stream) {
+    FusedArgs fa{pool_k, pool_v, beam_tok_idx, out, lse, fused ? 1 : 0};
+    if (g.d == 128) return launch_d<128>(g, tmap_k, tmap_v, q, shared_len, part_o, part_lse, status, fa, stream);
+    if (g.d == 64) return launch_d<64>(g, tmap_k, tmap_v, q, shared_len, part_o, part_lse, status, fa, stream);
     return cudaErrorInvalidValue;
 }
 

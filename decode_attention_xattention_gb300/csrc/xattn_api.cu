@@ -51,6 +51,7 @@ int check_desc(const xattn_desc* d) {
     if (d->split_tokens < 0 || d->split_tokens % kTileKeys != 0) return XATTN_ERR_INVALID_ARG;
     if (d->shared_kernel < 0 || d->shared_kernel > 2) return XATTN_ERR_INVALID_ARG;
     if (d->dtype != XATTN_DTYPE_BF16) return XATTN_ERR_UNSUPPORTED;
+    if (d->out_dtype != XATTN_DTYPE_BF16 && d->out_dtype != XATTN_DTYPE_F32) return XATTN_ERR_UNSUPPORTED;
     if (d->head_dim != 64 && d->head_dim != 128) return XATTN_ERR_UNSUPPORTED;
     const int G = d->num_q_heads / d->num_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return XATTN_ERR_UNSUPPORTED;
@@ -82,6 +83,7 @@ void plan(const xattn_desc* d, int step, Geometry* g, int* kernel) {
     g->row_tiles = cdiv(g->M, kTileRows);
     const float scale = d->softmax_scale > 0.f ? d->softmax_scale : 1.0f / std::sqrt((float)g->d);
     g->scale_log2 = scale * 1.4426950408889634f;
+    g->out_f32 = d->out_dtype == XATTN_DTYPE_F32 ? 1 : 0;
 
     int k = 0;
     if (g->Lmax > 0) k = d->shared_kernel ? d->shared_kernel : (g->M <= kSimtMaxRows ? 2 : 1);
@@ -92,7 +94,8 @@ void plan(const xattn_desc* d, int step, Geometry* g, int* kernel) {
     } else if (k == 0) {
         g->split_tokens = kTileKeys;
     } else {
-        const int64_t units = (int64_t)g->R * g->Hkv * (k == 1 ? g->row_tiles : cdiv(g->M, 4));
+        // tensor-core CTAs own two 128-row tiles; CUDA-core CTAs own four rows
+        const int64_t units = (int64_t)g->R * g->Hkv * (k == 1 ? cdiv(g->row_tiles, 2) : cdiv(g->M, 4));
         const int64_t slots = (int64_t)device_sms() * (k == 1 ? 1 : 8);
         int best_n = 1;
         double best = 1e30;
@@ -155,7 +158,8 @@ int xattn_query_plan(const xattn_desc* desc, int32_t step, xattn_plan* out) {
     out->rows_per_unit = g.M;
     out->row_tiles = g.row_tiles;
     out->shared_ctas = k == 0 ? 0 : (k == 1 ? shared_tc_ctas_for(g) : g.R * g.Hkv * ((g.M + 3) / 4) * g.nsplit);
-    out->merge_ctas = merge_ctas_for(g);
+    out->fused = (k == 1 && g.nsplit == 1 && step <= kMaxFusedSteps) ? 1 : 0;
+    out->merge_ctas = out->fused ? 0 : merge_ctas_for(g);
     return XATTN_OK;
 }
 
@@ -206,15 +210,22 @@ WsView ws_view(void* workspace, const Geometry& g) {
     return v;
 }
 
+// Shared stage; with `fused` (tensor-core kernel only) it also runs the Non-Shared stage and
+// the Merge and writes out / lse.
 int run_shared(const Geometry& g, int kernel, const void* q, const void* shared_k, const void* shared_v,
-               const int32_t* shared_len, const WsView& ws, cudaStream_t st) {
+               const int32_t* shared_len, const WsView& ws, cudaStream_t st, bool fused = false,
+               const void* ns_k_pool = nullptr, const void* ns_v_pool = nullptr,
+               const int32_t* beam_tok_idx = nullptr, void* out = nullptr, float* lse = nullptr) {
     auto qb = reinterpret_cast<const __nv_bfloat16*>(q);
     cudaError_t e = cudaSuccess;
     if (kernel == 1) {
         CUtensorMap mk, mv;
         if (make_kv_map(&mk, shared_k, g) != CUDA_SUCCESS || make_kv_map(&mv, shared_v, g) != CUDA_SUCCESS)
             return XATTN_ERR_CUDA;
-        e = launch_shared_stage_tc(g, mk, mv, qb, shared_len, ws.part_o, ws.part_lse, ws.status, st);
+        e = launch_shared_stage_tc(g, mk, mv, qb, shared_len, ws.part_o, ws.part_lse, ws.status,
+                                   reinterpret_cast<const __nv_bfloat16*>(ns_k_pool),
+                                   reinterpret_cast<const __nv_bfloat16*>(ns_v_pool), beam_tok_idx, out, lse, fused,
+                                   st);
     } else if (kernel == 2) {
         e = launch_shared_stage_simt(g, qb, reinterpret_cast<const __nv_bfloat16*>(shared_k),
                                      reinterpret_cast<const __nv_bfloat16*>(shared_v), shared_len, ws.part_o,
@@ -230,7 +241,7 @@ int run_merge(const Geometry& g, const xattn_desc* desc, const void* q, const in
                                     reinterpret_cast<const __nv_bfloat16*>(ns_k_pool),
                                     reinterpret_cast<const __nv_bfloat16*>(ns_v_pool), beam_tok_idx,
                                     desc->max_shared_len > 0 ? shared_len : nullptr, ws.part_o, ws.part_lse,
-                                    reinterpret_cast<__nv_bfloat16*>(out), lse, ws.status, st);
+                                    out, lse, ws.status, st);
     return e == cudaSuccess ? XATTN_OK : XATTN_ERR_CUDA;
 }
 
@@ -252,6 +263,9 @@ int xattn_decode(const xattn_desc* desc, const void* q, const void* shared_k, co
     if (workspace_bytes < workspace_bytes_for(g)) return XATTN_ERR_WORKSPACE_TOO_SMALL;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const WsView ws = ws_view(workspace, g);
+    if (kernel == 1 && g.nsplit == 1 && step <= kMaxFusedSteps)  // one kernel does all three stages
+        return run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st, true, ns_k_pool, ns_v_pool,
+                          beam_tok_idx, out, lse);
     rc = run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st);
     if (rc != XATTN_OK) return rc;
     return run_merge(g, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws, st);

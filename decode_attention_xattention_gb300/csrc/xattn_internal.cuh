@@ -13,6 +13,7 @@ namespace xattn {
 constexpr int kTileRows = 128;   // rows of one tensor-core M tile (stacked beam x head rows)
 constexpr int kTileKeys = 128;   // prefix tokens per K/V tile
 constexpr int kStatusBytes = 256;
+constexpr int kMaxFusedSteps = 16; // Non-Shared tokens the fused Shared-stage epilogue handles
 
 // Device status word helpers ----------------------------------------------------------
 __device__ __forceinline__ void set_status(int32_t* status, int32_t bits) {
@@ -28,16 +29,22 @@ struct Geometry {
     int nsplit;       // prefix pieces
     int split_tokens; // tokens per piece (multiple of 128)
     float scale_log2; // softmax scale * log2(e)
+    int out_f32;      // output dtype: 0 bf16, 1 fp32
 };
 
 // Workspace layout: [status (256 B)] [part_o: R*Hkv*nsplit*M*d fp32] [part_lse: R*Hkv*nsplit*M fp32]
 inline size_t part_rows(const Geometry& g) { return (size_t)g.R * g.Hkv * g.nsplit * g.M; }
 
 // Launchers (each returns cudaGetLastError()).
+// fused = the CTA also runs the Non-Shared stage and the Merge and writes out / lse
+// (requires a single prefix piece and step <= kMaxFusedSteps); otherwise it writes the
+// piece's partial result into part_o / part_lse.
 cudaError_t launch_shared_stage_tc(const Geometry& g, const CUtensorMap& tmap_k,
                                    const CUtensorMap& tmap_v, const __nv_bfloat16* q,
                                    const int32_t* shared_len, float* part_o, float* part_lse,
-                                   int32_t* status, cudaStream_t stream);
+                                   int32_t* status, const __nv_bfloat16* pool_k,
+                                   const __nv_bfloat16* pool_v, const int32_t* beam_tok_idx,
+                                   void* out, float* lse, bool fused, cudaStream_t stream);
 cudaError_t launch_shared_stage_simt(const Geometry& g, const __nv_bfloat16* q,
                                      const __nv_bfloat16* shared_k, const __nv_bfloat16* shared_v,
                                      const int32_t* shared_len, float* part_o, float* part_lse,
@@ -45,7 +52,7 @@ cudaError_t launch_shared_stage_simt(const Geometry& g, const __nv_bfloat16* q,
 cudaError_t launch_ns_merge(const Geometry& g, const __nv_bfloat16* q,
                             const __nv_bfloat16* pool_k, const __nv_bfloat16* pool_v,
                             const int32_t* beam_tok_idx, const int32_t* shared_len,
-                            const float* part_o, const float* part_lse, __nv_bfloat16* out,
+                            const float* part_o, const float* part_lse, void* out,
                             float* lse, int32_t* status, cudaStream_t stream);
 cudaError_t launch_beam_update(int R, int BW, int Hkv, int d, int S, int Tmax, int step,
                                const int32_t* parent, const __nv_bfloat16* new_k,

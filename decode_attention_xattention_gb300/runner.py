@@ -28,7 +28,7 @@ class DeviceBatch:
     """All device tensors of one decode batch (inputs resident in HBM)."""
 
     def __init__(self, inp: wl.Inputs, device="cuda", shared_kernel=0, split_tokens=0, stream=None,
-                 extra_steps=0):
+                 extra_steps=0, out_fp32=False):
         inp = inp.as_bf16()
         w = inp.w
         self.w = w
@@ -38,7 +38,8 @@ class DeviceBatch:
         self.Tmax = w.max_steps + extra_steps
         self.S = BW * self.Tmax
         self.desc = xattn.make_desc(R, BW, Hq, Hkv, d, w.max_shared_len, self.S, self.Tmax, w.softmax_scale,
-                                    shared_kernel, split_tokens)
+                                    shared_kernel, split_tokens,
+                                    xattn.XATTN_DTYPE_F32 if out_fp32 else xattn.XATTN_DTYPE_BF16)
         self.q = to_bf16_tensor(inp.q, device)
         if w.max_shared_len > 0:
             self.shared_k = to_bf16_tensor(inp.shared_k, device)
@@ -52,7 +53,7 @@ class DeviceBatch:
         self.pool_k = torch.zeros((R, self.S, Hkv, d), dtype=torch.bfloat16, device=device)
         self.pool_v = torch.zeros_like(self.pool_k)
         self.idx = torch.zeros((R, BW, max(self.Tmax, 1)), dtype=torch.int32, device=device)
-        self.out = torch.empty((R, BW, Hq, d), dtype=torch.bfloat16, device=device)
+        self.out = torch.empty((R, BW, Hq, d), dtype=torch.float32 if out_fp32 else torch.bfloat16, device=device)
         self.lse = torch.empty((R, BW, Hq), dtype=torch.float32, device=device)
         self.ws_bytes = xattn.xattn_decode_workspace_size(self.desc)
         if self.ws_bytes == 0:

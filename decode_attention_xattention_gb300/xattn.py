@@ -29,6 +29,7 @@ XATTN_STATUS_EMPTY_ROW = 8
 XATTN_STATUS_TIMEOUT = 16
 
 XATTN_DTYPE_BF16 = 0
+XATTN_DTYPE_F32 = 1
 
 # Every symbol include/xattn.h declares.
 EXPORTS = ("xattn_decode_workspace_size", "xattn_decode", "xattn_decode_shared", "xattn_decode_merge",
@@ -45,14 +46,15 @@ class xattn_desc(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("max_shared_len", ctypes.c_int32),
                 ("ns_slots", ctypes.c_int32), ("max_steps", ctypes.c_int32),
                 ("softmax_scale", ctypes.c_float), ("dtype", ctypes.c_int32),
-                ("shared_kernel", ctypes.c_int32), ("split_tokens", ctypes.c_int32)]
+                ("shared_kernel", ctypes.c_int32), ("split_tokens", ctypes.c_int32),
+                ("out_dtype", ctypes.c_int32)]
 
 
 class xattn_plan(ctypes.Structure):
     _fields_ = [("shared_kernel", ctypes.c_int32), ("num_splits", ctypes.c_int32),
                 ("split_tokens", ctypes.c_int32), ("rows_per_unit", ctypes.c_int32),
                 ("row_tiles", ctypes.c_int32), ("shared_ctas", ctypes.c_int32),
-                ("merge_ctas", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
+                ("merge_ctas", ctypes.c_int32), ("fused", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
 
 _lib = None
@@ -104,9 +106,10 @@ def _stream(s):
     return s.cuda_stream  # torch.cuda.Stream
 
 
-def make_desc(R, BW, Hq, Hkv, d, Lmax, S, Tmax, scale=0.0, shared_kernel=0, split_tokens=0) -> xattn_desc:
+def make_desc(R, BW, Hq, Hkv, d, Lmax, S, Tmax, scale=0.0, shared_kernel=0, split_tokens=0,
+              out_dtype=XATTN_DTYPE_BF16) -> xattn_desc:
     return xattn_desc(R, BW, Hq, Hkv, d, Lmax, S, Tmax, float(scale), XATTN_DTYPE_BF16,
-                      shared_kernel, split_tokens)
+                      shared_kernel, split_tokens, out_dtype)
 
 
 def xattn_decode_workspace_size(desc: xattn_desc) -> int:

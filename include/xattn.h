@@ -75,7 +75,7 @@ enum {
     XATTN_STATUS_TIMEOUT = 16        /* an on-chip wait gave up (internal error)        */
 };
 
-enum { XATTN_DTYPE_BF16 = 0 };
+enum { XATTN_DTYPE_BF16 = 0, XATTN_DTYPE_F32 = 1 };
 
 /* Shapes of one decode batch. */
 typedef struct xattn_desc {
@@ -93,6 +93,7 @@ typedef struct xattn_desc {
                                else tensor cores), 1 tensor cores, 2 CUDA cores            */
     int32_t split_tokens;   /* prefix tokens per Shared-stage piece: 0 automatic, else a
                                multiple of 128                                             */
+    int32_t out_dtype;      /* dtype of `out`: XATTN_DTYPE_BF16 (0) or XATTN_DTYPE_F32      */
 } xattn_desc;
 
 /* Bytes of workspace xattn_decode needs for these shapes (at least 256). The workspace
@@ -109,7 +110,7 @@ XATTN_API size_t xattn_decode_workspace_size(const xattn_desc* desc);
  *   ns_k/v_pool   [R, S, Hkv, d]        bf16   Non-Shared tokens, one slot per token
  *   beam_tok_idx  [R, BW, Tmax]         int32  ancestry: slots of the beam's tokens
  *   step          0 <= step <= Tmax: positions 0 .. step-1 of each ancestry row are used
- *   out           [R, BW, Hq, d]        bf16   normalised attention output
+ *   out           [R, BW, Hq, d]        bf16 (or fp32, desc->out_dtype)  normalised output
  *   lse           [R, BW, Hq]           fp32   natural-log LSE of the scaled scores
  *   workspace     >= xattn_decode_workspace_size(desc) bytes, 256-byte aligned
  * Pointers that a zero-sized part does not touch may be NULL (shared_* when Lmax == 0;
@@ -169,8 +170,11 @@ typedef struct xattn_plan {
     int32_t rows_per_unit;    /* M = BW * G stacked query rows per (request, KV head)    */
     int32_t row_tiles;        /* 128-row tiles per (request, KV head)                    */
     int32_t shared_ctas;      /* CTAs of one Shared-stage launch                         */
-    int32_t merge_ctas;       /* CTAs of one Non-Shared + Merge launch                   */
-    int32_t reserved[4];
+    int32_t merge_ctas;       /* CTAs of one Non-Shared + Merge launch (0 when fused)    */
+    int32_t fused;            /* 1: xattn_decode is one tensor-core kernel that also runs
+                                 the Non-Shared stage and the Merge (single prefix piece,
+                                 step <= 16); 0: Shared stage, then Non-Shared + Merge     */
+    int32_t reserved[3];
 } xattn_plan;
 
 XATTN_API int xattn_query_plan(const xattn_desc* desc, int32_t step, xattn_plan* plan);

@@ -30,12 +30,16 @@ def compare(got_o, got_l, ref_o, ref_l, what=""):
     return stats
 
 
-def run_and_check(w, rows=None, shared_kernel=0, split_tokens=0, check_cache=True, inp=None, step=None):
+def run_and_check(w, rows=None, shared_kernel=0, split_tokens=0, check_cache=True, inp=None, step=None,
+                  out_fp32=True):
     """GPU: beam updates for steps 0..T-1 then one decode. Oracle: its own beam updates
-    then the plain definition. Returns (stats, DeviceBatch, inputs)."""
+    then the plain definition. The kernels compute in fp32; by default they also write fp32
+    output so the comparison measures the computation, not the final bf16 rounding (which
+    test_bf16_output_is_rounded_fp32_output checks exactly). Returns (stats, DeviceBatch,
+    inputs)."""
     orc = oracle.load()
     inp = (wl.make_inputs(w) if inp is None else inp).as_bf16()
-    db = DeviceBatch(inp, shared_kernel=shared_kernel, split_tokens=split_tokens)
+    db = DeviceBatch(inp, shared_kernel=shared_kernel, split_tokens=split_tokens, out_fp32=out_fp32)
     db.build_cache()
     step = w.steps if step is None else step
     xattn.check(db.decode(step))
@@ -48,7 +52,7 @@ def run_and_check(w, rows=None, shared_kernel=0, split_tokens=0, check_cache=Tru
         np.testing.assert_array_equal(bf16_tensor_to_f32(db.pool_v), pv)
     D = oracle.dims_of(w)
     ref_o, ref_l = orc.decode(D, inp.q, inp.shared_k, inp.shared_v, inp.shared_len, pk, pv, idx, step, rows=rows)
-    got_o = bf16_tensor_to_f32(db.out).reshape(-1, w.head_dim)
+    got_o = db.out.float().cpu().numpy().reshape(-1, w.head_dim)
     got_l = db.lse.cpu().numpy().reshape(-1)
     if rows is not None:
         got_o, got_l = got_o[rows], got_l[rows]

@@ -35,8 +35,8 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_desc_layout_matches_header():
-    # 12 four-byte fields
-    assert ctypes.sizeof(xattn.xattn_desc) == 48
+    # 13 four-byte fields
+    assert ctypes.sizeof(xattn.xattn_desc) == 52
     assert ctypes.sizeof(xattn.xattn_plan) == 44
 
 

@@ -42,10 +42,41 @@ def test_small_all_rows(shape, kernel):
     run_and_check(w, shared_kernel=kernel)
 
 
-@pytest.mark.parametrize("split", [128, 256, 384, 1024])
+@pytest.mark.parametrize("split", [128, 256, 384, 1024, 2048])
 def test_forced_splits_merge(split):
     w = wl.custom(R=2, BW=8, Hq=8, Hkv=2, d=128, lens=(1100, 700), T=3, seed=3)
-    run_and_check(w, split_tokens=split)
+    _, db, _ = run_and_check(w, split_tokens=split)
+    assert db.plan().fused == (1 if split >= 1100 else 0)
+
+
+def test_fused_and_split_paths_agree():
+    """The single-kernel path (Shared stage + fused Non-Shared + Merge) and the split path
+    (pieces + Non-Shared/Merge kernel) on the same inputs."""
+    w = wl.custom(R=2, BW=24, Hq=8, Hkv=2, d=128, lens=(1500, 640), T=4, seed=19)
+    _, a, _ = run_and_check(w, split_tokens=2048)
+    _, b, _ = run_and_check(w, split_tokens=256)
+    assert a.plan().fused == 1 and b.plan().fused == 0
+    d = (a.out - b.out).abs().max().item()
+    assert d <= 2e-3, d
+
+
+@pytest.mark.parametrize("w", [wl.GR, wl.LONG, wl.custom(R=2, BW=8, Hq=8, Hkv=2, d=64, lens=(700, 300), T=3, seed=2)],
+                         ids=lambda w: w.name)
+def test_bf16_output_is_rounded_fp32_output(w):
+    """The bf16 output is exactly the round-to-nearest-even of the fp32 output computed by
+    the same kernels on the same inputs (so the precision checks made on the fp32 output
+    carry over, plus at most half a bf16 ulp)."""
+    inp = wl.make_inputs(w)
+    outs = []
+    for fp32 in (True, False):
+        db = DeviceBatch(inp, out_fp32=fp32)
+        db.build_cache()
+        xattn.check(db.decode())
+        torch.cuda.synchronize()
+        outs.append((db.out.clone(), db.lse.clone()))
+    (o32, l32), (o16, l16) = outs
+    assert torch.equal(o32.to(torch.bfloat16), o16)
+    assert torch.equal(l32, l16)
 
 
 def test_tiny_config_both_kernels():
