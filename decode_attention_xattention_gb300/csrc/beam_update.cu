@@ -26,15 +26,26 @@ __global__ void __launch_bounds__(kThreads) beam_update_kernel(
     int32_t* __restrict__ idx, int32_t* status) {
     const int r = blockIdx.x;
     // 1. K/V of the new tokens: [BW, Hkv, d] of request r -> slots step*BW .. step*BW+BW-1.
+    //    All loads of a thread are issued before its stores (independent 16-byte vectors).
     {
         const size_t n16 = (size_t)BW * HkvD / 8;  // 16-byte vectors (HkvD is a multiple of 8)
         const uint4* sk = reinterpret_cast<const uint4*>(new_k + (size_t)r * BW * HkvD);
         const uint4* sv = reinterpret_cast<const uint4*>(new_v + (size_t)r * BW * HkvD);
         uint4* dk = reinterpret_cast<uint4*>(pool_k + ((size_t)r * S + (size_t)step * BW) * HkvD);
         uint4* dv = reinterpret_cast<uint4*>(pool_v + ((size_t)r * S + (size_t)step * BW) * HkvD);
-        for (size_t i = (size_t)blockIdx.y * kThreads + threadIdx.x; i < n16; i += (size_t)gridDim.y * kThreads) {
-            dk[i] = __ldg(sk + i);
-            dv[i] = __ldg(sv + i);
+        const size_t stride = (size_t)gridDim.y * kThreads;
+        size_t i = (size_t)blockIdx.y * kThreads + threadIdx.x;
+        for (; i + 3 * stride < n16; i += 4 * stride) {
+            uint4 a[4], c[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) { a[u] = __ldg(sk + i + u * stride); c[u] = __ldg(sv + i + u * stride); }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) { dk[i + u * stride] = a[u]; dv[i + u * stride] = c[u]; }
+        }
+        for (; i < n16; i += stride) {
+            const uint4 a = __ldg(sk + i), c = __ldg(sv + i);
+            dk[i] = a;
+            dv[i] = c;
         }
     }
     if (blockIdx.y != 0) return;
@@ -77,8 +88,8 @@ cudaError_t launch_beam_update(int R, int BW, int Hkv, int d, int S, int Tmax, i
                                cudaStream_t stream) {
     if (BW > kTableInts) return cudaErrorInvalidValue;
     const size_t n16 = (size_t)BW * Hkv * d / 8;
-    int ybl = (int)((n16 + kThreads * 4 - 1) / (kThreads * 4));
-    ybl = max(1, min(ybl, 64));
+    int ybl = (int)((n16 + kThreads - 1) / kThreads);  // about one vector of K and V per thread
+    ybl = max(1, min(ybl, 1024));
     dim3 grid(R, ybl);
     beam_update_kernel<<<grid, kThreads, 0, stream>>>(BW, Hkv * d, S, Tmax, step, parent, new_k, new_v,
                                                       pool_k, pool_v, idx, status);

@@ -1,14 +1,22 @@
-// Non-Shared stage fused with the Merge stage.
+// Non-Shared stage and Merge stage.
 //
 // xGR: Efficient Generative Recommendation Serving at Scale, section 2.1 (xAttention):
 // the Non-Shared stage computes local scores and max/sum statistics over the tokens a beam
 // generated, reached through its ancestry index (token-granularity management); the Merge
 // stage combines these with the Shared stage's statistics by an online softmax. Here the
 // combine is the log-sum-exp rule: lse = log(sum_i exp(lse_i)), out = sum_i exp(lse_i - lse) o_i,
-// over the Non-Shared part and every prefix piece the Shared stage produced.
+// over every piece of the prefix the Shared stage produced and the Non-Shared part.
 //
-// One warp per (request r, beam b, KV head h) serves the G query heads of that KV head, so
-// each gathered pool row is read once for all G heads. Lanes split the head dimension.
+// Two kernels:
+//   ns_merge_kernel    one warp per (request r, beam b, KV head h) serves the G query heads
+//                      of that KV head (each gathered pool row is read once for all G);
+//                      lanes split the head dimension. It walks the beam's ancestry tokens
+//                      itself when there are few (<= kNsDirectMax), then folds in every
+//                      piece stored in the workspace and writes out / lse.
+//   ns_partial_kernel  for long Non-Shared parts (e.g. a 512-token unshared suffix per
+//                      sequence): CTA = (r, b, h, piece of kNsChunk ancestry positions), four
+//                      warps with four tokens in flight each; writes the piece's normalised
+//                      output and LSE into the workspace after the prefix pieces.
 #include "xattn_internal.cuh"
 
 namespace xattn {
@@ -22,16 +30,16 @@ __device__ __forceinline__ float ex2(float x) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr uint32_t kNaN = 0x7fc00000u;
 
 template <int D>
 struct LaneVec;
 template <>
 struct LaneVec<128> {  // 4 bf16 per lane = 8 bytes
     static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&x)[4]) {
-        uint2 u = *reinterpret_cast<const uint2*>(p);
-        __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&u.x);
-        __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&u.y);
-        float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+        uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+        float2 fa = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u.x));
+        float2 fb = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u.y));
         x[0] = fa.x; x[1] = fa.y; x[2] = fb.x; x[3] = fb.y;
     }
     static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&x)[4]) {
@@ -46,7 +54,7 @@ struct LaneVec<128> {  // 4 bf16 per lane = 8 bytes
 template <>
 struct LaneVec<64> {  // 2 bf16 per lane = 4 bytes
     static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&x)[2]) {
-        float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+        float2 f = __bfloat1622float2(__ldg(reinterpret_cast<const __nv_bfloat162*>(p)));
         x[0] = f.x; x[1] = f.y;
     }
     static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&x)[2]) {
@@ -59,6 +67,31 @@ __device__ __forceinline__ float warp_sum(float v) {
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
+
+// Online-softmax state of G rows, lanes splitting the head dimension (base-2 domain).
+template <int E, int G>
+struct RowState {
+    float acc[G][E], m[G], l[G];
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+            m[gg] = -INFINITY;
+            l[gg] = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[gg][e] = 0.f;
+        }
+    }
+    // fold in one value vector v with log2-weight s2 for row gg
+    __device__ __forceinline__ void add(int gg, float s2, const float (&v)[E]) {
+        const float mn = fmaxf(m[gg], s2);
+        const float alpha = ex2(m[gg] - mn);
+        const float p = ex2(s2 - mn);
+        l[gg] = l[gg] * alpha + p;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[gg][e] = fmaf(p, v[e], acc[gg][e] * alpha);
+        m[gg] = mn;
+    }
+};
 
 template <int D, int G>
 __global__ void __launch_bounds__(256) ns_merge_kernel(
@@ -88,73 +121,59 @@ __global__ void __launch_bounds__(256) ns_merge_kernel(
         if (lane == 0) set_status(status, XATTN_STATUS_EMPTY_ROW);
     }
 
-    // Non-Shared stage: online softmax over the ancestry tokens (base-2 domain).
-    float qv[G][E], acc[G][E], m[G], l[G];
+    RowState<E, G> st;
+    st.init();
+    if (g.ns_pieces == 0 && g.step > 0 && !bad) {
+        // Non-Shared stage: online softmax over the beam's ancestry tokens.
+        float qv[G][E];
 #pragma unroll
-    for (int gg = 0; gg < G; ++gg) {
-        LaneVec<D>::load(q + (qrow0 + gg) * D + lane * E, qv[gg]);
-        m[gg] = -INFINITY;
-        l[gg] = 0.f;
+        for (int gg = 0; gg < G; ++gg) LaneVec<D>::load(q + (qrow0 + gg) * D + lane * E, qv[gg]);
+        const int32_t* row_idx = idx + ((size_t)r * g.BW + b) * g.Tmax;
+        const int my_slot = lane < g.step ? __ldg(row_idx + lane) : 0;  // step <= 32 here
+        for (int i = 0; i < g.step; ++i) {
+            const int slot = __shfl_sync(0xffffffffu, my_slot, i);
+            if (slot < 0 || slot >= g.S) {
+                bad = true;
+                if (lane == 0) set_status(status, XATTN_STATUS_BAD_SLOT);
+                break;
+            }
+            const size_t off = (((size_t)r * g.S + slot) * g.Hkv + h) * D + lane * E;
+            float kv[E], vv[E];
+            LaneVec<D>::load(pool_k + off, kv);
+            LaneVec<D>::load(pool_v + off, vv);
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[gg][e] = 0.f;
-    }
-    const int32_t* row_idx = idx ? idx + ((size_t)r * g.BW + b) * g.Tmax : nullptr;
-    for (int i = 0; i < g.step && !bad; ++i) {
-        const int slot = __ldg(row_idx + i);
-        if (slot < 0 || slot >= g.S) {
-            bad = true;
-            if (lane == 0) set_status(status, XATTN_STATUS_BAD_SLOT);
-            break;
-        }
-        const size_t off = (((size_t)r * g.S + slot) * g.Hkv + h) * D + lane * E;
-        float kv[E], vv[E];
-        LaneVec<D>::load(pool_k + off, kv);
-        LaneVec<D>::load(pool_v + off, vv);
+            for (int gg = 0; gg < G; ++gg) {
+                float s = 0.f;
 #pragma unroll
-        for (int gg = 0; gg < G; ++gg) {
-            float s = 0.f;
-#pragma unroll
-            for (int e = 0; e < E; ++e) s = fmaf(qv[gg][e], kv[e], s);
-            s = warp_sum(s) * g.scale_log2;
-            const float mn = fmaxf(m[gg], s);
-            const float alpha = ex2(m[gg] - mn);
-            const float p = ex2(s - mn);
-            l[gg] = l[gg] * alpha + p;
-#pragma unroll
-            for (int e = 0; e < E; ++e) acc[gg][e] = fmaf(p, vv[e], acc[gg][e] * alpha);
-            m[gg] = mn;
+                for (int e = 0; e < E; ++e) s = fmaf(qv[gg][e], kv[e], s);
+                st.add(gg, warp_sum(s) * g.scale_log2, vv);
+            }
         }
     }
 
-    // Merge: fold every Shared-stage piece into the running (m, l, acc) state. A piece
-    // stores its normalised output o_c and natural-log lse_c; in base 2 it contributes
-    // weight 2^(lse_c * log2 e) times o_c.
-    if (have_prefix && !bad) {
+    // Merge: fold every stored piece (prefix pieces, then Non-Shared pieces) into the
+    // running state. A piece stores its normalised output o_c and natural-log lse_c; in
+    // base 2 it contributes weight 2^(lse_c * log2 e) times o_c.
+    if (!bad) {
         const size_t unit = (size_t)r * g.Hkv + h;
-        for (int c = 0; c < g.nsplit; ++c) {
-            const size_t prow = (unit * g.nsplit + c) * g.M + (size_t)b * G;
+        const int np = g.nsplit + g.ns_pieces;
+        for (int c = 0; c < np; ++c) {
+            const size_t prow = (unit * g.pieces + c) * g.M + (size_t)b * G;
 #pragma unroll
             for (int gg = 0; gg < G; ++gg) {
                 const float lc = __ldg(part_lse + prow + gg);
-                if (lc != lc) bad = true;          // a failed Shared-stage piece poisons the row
+                if (lc != lc) bad = true;          // a failed piece poisons the row
                 if (!(lc > -INFINITY)) continue;  // empty piece (or NaN)
-                const float s2 = lc * kLog2e;
-                const float mn = fmaxf(m[gg], s2);
-                const float alpha = ex2(m[gg] - mn);
-                const float w = ex2(s2 - mn);
-                l[gg] = l[gg] * alpha + w;
-                const float4* po = reinterpret_cast<const float4*>(part_o + (prow + gg) * D + lane * E);
                 float ov[E];
+                const float* po = part_o + (prow + gg) * D + lane * E;
                 if constexpr (E == 4) {
-                    float4 t = __ldg(po);
+                    const float4 t = __ldg(reinterpret_cast<const float4*>(po));
                     ov[0] = t.x; ov[1] = t.y; ov[2] = t.z; ov[3] = t.w;
                 } else {
-                    float2 t = __ldg(reinterpret_cast<const float2*>(po));
+                    const float2 t = __ldg(reinterpret_cast<const float2*>(po));
                     ov[0] = t.x; ov[1] = t.y;
                 }
-#pragma unroll
-                for (int e = 0; e < E; ++e) acc[gg][e] = fmaf(w, ov[e], acc[gg][e] * alpha);
-                m[gg] = mn;
+                st.add(gg, lc * kLog2e, ov);
             }
         }
     }
@@ -163,15 +182,15 @@ __global__ void __launch_bounds__(256) ns_merge_kernel(
     for (int gg = 0; gg < G; ++gg) {
         float o[E];
         float row_lse;
-        if (bad || !(l[gg] > 0.f)) {
+        if (bad || !(st.l[gg] > 0.f)) {
 #pragma unroll
-            for (int e = 0; e < E; ++e) o[e] = __int_as_float(0x7fc00000);
-            row_lse = __int_as_float(0x7fc00000);
+            for (int e = 0; e < E; ++e) o[e] = __uint_as_float(kNaN);
+            row_lse = __uint_as_float(kNaN);
         } else {
-            const float inv = 1.f / l[gg];
+            const float inv = 1.f / st.l[gg];
 #pragma unroll
-            for (int e = 0; e < E; ++e) o[e] = acc[gg][e] * inv;
-            row_lse = (m[gg] + __log2f(l[gg])) * kLn2;
+            for (int e = 0; e < E; ++e) o[e] = st.acc[gg][e] * inv;
+            row_lse = (st.m[gg] + __log2f(st.l[gg])) * kLn2;
         }
         if (g.out_f32) {
             float* dst = reinterpret_cast<float*>(out) + (qrow0 + gg) * D + lane * E;
@@ -187,14 +206,127 @@ __global__ void __launch_bounds__(256) ns_merge_kernel(
     }
 }
 
+// One piece of a long Non-Shared part: ancestry positions [c*kNsChunk, (c+1)*kNsChunk) of
+// beam b. Warp w takes groups of four consecutive positions, w*4, w*4 + 16, ...; the four
+// tokens' K and V rows are loaded before any is used.
+constexpr int kPartWarps = 4;
+constexpr int kUnroll = 4;
+static_assert(kNsChunk == 64, "slots of a piece are held as two 32-lane registers");
+
+template <int D, int G>
+__global__ void __launch_bounds__(kPartWarps * 32) ns_partial_kernel(
+    Geometry g, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ pool_k,
+    const __nv_bfloat16* __restrict__ pool_v, const int32_t* __restrict__ idx, float* __restrict__ part_o,
+    float* __restrict__ part_lse, int32_t* status) {
+    constexpr int E = D / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    long t = blockIdx.x;
+    const int c = (int)(t % g.ns_pieces);
+    t /= g.ns_pieces;
+    const int h = (int)(t % g.Hkv);
+    const int b = (int)((t / g.Hkv) % g.BW);
+    const int r = (int)(t / ((long)g.Hkv * g.BW));
+    const int i0 = c * kNsChunk, i1 = min(i0 + kNsChunk, g.step);
+    const size_t qrow0 = ((size_t)r * g.BW + b) * g.Hq + (size_t)h * G;
+
+    float qv[G][E];
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) LaneVec<D>::load(q + (qrow0 + gg) * D + lane * E, qv[gg]);
+    const int32_t* row_idx = idx + ((size_t)r * g.BW + b) * g.Tmax;
+    // this piece's slots: lane l holds positions i0 + l and i0 + 32 + l
+    const int sl0 = (i0 + lane < i1) ? __ldg(row_idx + i0 + lane) : 0;
+    const int sl1 = (i0 + 32 + lane < i1) ? __ldg(row_idx + i0 + 32 + lane) : 0;
+
+    RowState<E, G> st;
+    st.init();
+    bool bad = false;
+    for (int base = warp * kUnroll; base < kNsChunk; base += kPartWarps * kUnroll) {
+        float kv[kUnroll][E], vv[kUnroll][E];
+        bool use[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int pos = base + u;  // position within the piece, < 64
+            const int s0 = __shfl_sync(0xffffffffu, sl0, pos & 31);
+            const int s1 = __shfl_sync(0xffffffffu, sl1, pos & 31);
+            const int slot = pos < 32 ? s0 : s1;
+            use[u] = i0 + pos < i1;
+            if (use[u] && (slot < 0 || slot >= g.S)) {
+                bad = true;
+                use[u] = false;
+            }
+            if (use[u]) {
+                const size_t off = (((size_t)r * g.S + slot) * g.Hkv + h) * D + lane * E;
+                LaneVec<D>::load(pool_k + off, kv[u]);
+                LaneVec<D>::load(pool_v + off, vv[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            if (!use[u]) continue;
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg) {
+                float s = 0.f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) s = fmaf(qv[gg][e], kv[u][e], s);
+                st.add(gg, warp_sum(s) * g.scale_log2, vv[u]);
+            }
+        }
+    }
+    if (bad && lane == 0) set_status(status, XATTN_STATUS_BAD_SLOT);
+
+    // combine the four warps' states per row and write the piece
+    __shared__ float sm_m[kPartWarps][G], sm_l[kPartWarps][G];
+    __shared__ float sm_acc[kPartWarps][G][D];
+    __shared__ int sm_bad;
+    if (threadIdx.x == 0) sm_bad = 0;
+    __syncthreads();
+    if (bad) sm_bad = 1;
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) {
+        if (lane == 0) {
+            sm_m[warp][gg] = st.m[gg];
+            sm_l[warp][gg] = st.l[gg];
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) sm_acc[warp][gg][lane * E + e] = st.acc[gg][e];
+    }
+    __syncthreads();
+    const size_t prow0 = (((size_t)r * g.Hkv + h) * g.pieces + g.nsplit + c) * g.M + (size_t)b * G;
+    for (int gg = warp; gg < G; gg += kPartWarps) {
+        float M = -INFINITY;
+        for (int w = 0; w < kPartWarps; ++w) M = fmaxf(M, sm_m[w][gg]);
+        float wt[kPartWarps], wsum = 0.f;
+        for (int w = 0; w < kPartWarps; ++w) {
+            wt[w] = (sm_m[w][gg] == -INFINITY) ? 0.f : ex2(sm_m[w][gg] - M);
+            wsum += sm_l[w][gg] * wt[w];
+        }
+        const bool empty = !(wsum > 0.f);
+        const float inv = empty ? 0.f : 1.f / wsum;
+        for (int e = lane; e < D; e += 32) {
+            float o = 0.f;
+            for (int w = 0; w < kPartWarps; ++w) o += sm_acc[w][gg][e] * wt[w];
+            part_o[(prow0 + gg) * D + e] = o * inv;
+        }
+        if (lane == 0)
+            part_lse[prow0 + gg] = sm_bad ? __uint_as_float(kNaN) : (empty ? -INFINITY : (M + __log2f(wsum)) * kLn2);
+    }
+}
+
 template <int D>
-cudaError_t launch_d(const Geometry& g, dim3 grid, dim3 block, cudaStream_t st, const __nv_bfloat16* q,
-                     const __nv_bfloat16* pk, const __nv_bfloat16* pv, const int32_t* idx,
-                     const int32_t* slen, const float* po, const float* pl, void* out,
-                     float* lse, int32_t* status) {
+cudaError_t launch_d(const Geometry& g, cudaStream_t st, const __nv_bfloat16* q, const __nv_bfloat16* pk,
+                     const __nv_bfloat16* pv, const int32_t* idx, const int32_t* slen, float* po, float* pl,
+                     void* out, float* lse, int32_t* status) {
+    const dim3 grid(merge_ctas_for(g)), block(256);
+    const long part_ctas = (long)g.R * g.BW * g.Hkv * g.ns_pieces;
+    if (part_ctas > 0x7fffffffL) return cudaErrorInvalidValue;
     switch (g.G) {
-#define XATTN_G(GV) \
-    case GV: ns_merge_kernel<D, GV><<<grid, block, 0, st>>>(g, q, pk, pv, idx, slen, po, pl, out, lse, status); break;
+#define XATTN_G(GV)                                                                                              \
+    case GV:                                                                                                     \
+        if (g.ns_pieces > 0)                                                                                     \
+            ns_partial_kernel<D, GV><<<(unsigned)part_ctas, kPartWarps * 32, 0, st>>>(g, q, pk, pv, idx, po, pl, \
+                                                                                       status);                 \
+        ns_merge_kernel<D, GV><<<grid, block, 0, st>>>(g, q, pk, pv, idx, slen, po, pl, out, lse, status);     \
+        break;
         XATTN_G(1) XATTN_G(2) XATTN_G(4) XATTN_G(8) XATTN_G(16)
 #undef XATTN_G
         default: return cudaErrorInvalidValue;
@@ -210,16 +342,15 @@ int merge_ctas_for(const Geometry& g) {
 }
 
 cudaError_t launch_ns_merge(const Geometry& g, const __nv_bfloat16* q, const __nv_bfloat16* pool_k,
-                            const __nv_bfloat16* pool_v, const int32_t* beam_tok_idx,
-                            const int32_t* shared_len, const float* part_o, const float* part_lse,
-                            void* out, float* lse, int32_t* status, cudaStream_t stream) {
-    dim3 grid(merge_ctas_for(g)), block(256);
+                            const __nv_bfloat16* pool_v, const int32_t* beam_tok_idx, const int32_t* shared_len,
+                            const float* part_o, const float* part_lse, void* out, float* lse, int32_t* status,
+                            cudaStream_t stream) {
+    float* po = const_cast<float*>(part_o);
+    float* pl = const_cast<float*>(part_lse);
     if (g.d == 128)
-        return launch_d<128>(g, grid, block, stream, q, pool_k, pool_v, beam_tok_idx, shared_len, part_o,
-                             part_lse, out, lse, status);
+        return launch_d<128>(g, stream, q, pool_k, pool_v, beam_tok_idx, shared_len, po, pl, out, lse, status);
     if (g.d == 64)
-        return launch_d<64>(g, grid, block, stream, q, pool_k, pool_v, beam_tok_idx, shared_len, part_o,
-                            part_lse, out, lse, status);
+        return launch_d<64>(g, stream, q, pool_k, pool_v, beam_tok_idx, shared_len, po, pl, out, lse, status);
     return cudaErrorInvalidValue;
 }
 

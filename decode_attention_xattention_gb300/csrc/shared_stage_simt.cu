@@ -7,8 +7,8 @@
 // a 128-row tensor-core tile would be almost all padding; this kernel streams the prefix
 // once per unit on CUDA cores instead (HBM-bound work).
 //
-// CTA = (unit, block of 4 stacked rows, prefix piece). Each of the 4 warps walks every
-// 4th token of the piece with an online softmax; lanes split the head dimension; the
+// CTA = (unit, block of 4 stacked rows, prefix piece). The 4 warps walk interleaved groups
+// of 4 tokens of the piece with an online softmax; lanes split the head dimension; the
 // warps' states are merged in shared memory and the piece's (normalised output, lse) is
 // written for the Merge stage.
 #include "xattn_internal.cuh"
@@ -18,6 +18,7 @@ namespace {
 
 constexpr int kRB = 4;  // stacked rows per CTA
 constexpr int kWarps = 4;
+constexpr int kUnroll = 4;  // tokens in flight per warp
 constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ __forceinline__ float ex2(float x) {
@@ -80,25 +81,36 @@ __global__ void __launch_bounds__(kWarps * 32) shared_stage_simt_kernel(
     const size_t tok_stride = (size_t)g.Hkv * D;
     const __nv_bfloat16* kbase = sk + ((size_t)r * g.Lmax * g.Hkv + h) * D + lane * E;
     const __nv_bfloat16* vbase = sv + ((size_t)r * g.Lmax * g.Hkv + h) * D + lane * E;
-    for (int j = t0 + warp; j < t1; j += kWarps) {
-        float kv[E], vv[E];
-        load_bf16<E>(kbase + (size_t)j * tok_stride, kv);
-        load_bf16<E>(vbase + (size_t)j * tok_stride, vv);
+    // Warp w takes groups of kUnroll consecutive tokens (w*kUnroll, w*kUnroll + 16, ...);
+    // the group's K and V rows are loaded before any is used.
+    for (int j0 = t0 + warp * kUnroll; j0 < t1; j0 += kWarps * kUnroll) {
+        float kv[kUnroll][E], vv[kUnroll][E];
 #pragma unroll
-        for (int i = 0; i < kRB; ++i) {
-            float s = 0.f;
+        for (int u = 0; u < kUnroll; ++u) {
+            if (j0 + u < t1) {
+                load_bf16<E>(kbase + (size_t)(j0 + u) * tok_stride, kv[u]);
+                load_bf16<E>(vbase + (size_t)(j0 + u) * tok_stride, vv[u]);
+            }
+        }
 #pragma unroll
-            for (int e = 0; e < E; ++e) s = fmaf(qv[i][e], kv[e], s);
+        for (int u = 0; u < kUnroll; ++u) {
+            if (j0 + u >= t1) continue;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            s *= g.scale_log2;
-            const float mn = fmaxf(m[i], s);
-            const float alpha = ex2(m[i] - mn);
-            const float p = ex2(s - mn);
-            l[i] = l[i] * alpha + p;
+            for (int i = 0; i < kRB; ++i) {
+                float s = 0.f;
 #pragma unroll
-            for (int e = 0; e < E; ++e) acc[i][e] = fmaf(p, vv[e], acc[i][e] * alpha);
-            m[i] = mn;
+                for (int e = 0; e < E; ++e) s = fmaf(qv[i][e], kv[u][e], s);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                s *= g.scale_log2;
+                const float mn = fmaxf(m[i], s);
+                const float alpha = ex2(m[i] - mn);
+                const float p = ex2(s - mn);
+                l[i] = l[i] * alpha + p;
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[i][e] = fmaf(p, vv[u][e], acc[i][e] * alpha);
+                m[i] = mn;
+            }
         }
     }
 
@@ -117,7 +129,7 @@ __global__ void __launch_bounds__(kWarps * 32) shared_stage_simt_kernel(
     if (i < kRB && row < g.M) {
         float M = -INFINITY;
         for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w][i]);
-        const size_t prow = ((size_t)unit * g.nsplit + c) * g.M + row;
+        const size_t prow = ((size_t)unit * g.pieces + c) * g.M + row;
         if (M == -INFINITY) {  // empty piece
             for (int e = lane; e < D; e += 32) part_o[prow * D + e] = 0.f;
             if (lane == 0) part_lse[prow] = -INFINITY;

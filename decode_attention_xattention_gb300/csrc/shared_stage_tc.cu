@@ -48,17 +48,22 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint32_t kNaN = 0x7fc00000u;
 
-// K/V pipeline depth: 2 stages at d = 128, 4 at d = 64. Either way the shared memory
-// admits one CTA per SM, so a CTA never waits for another's 512 TMEM columns.
+// K/V pipeline depth: K is consumed one tile before V, so K gets the deeper ring
+// (3 + 2 stages at d = 128, 4 + 4 at d = 64). Either way the shared memory admits one CTA
+// per SM, so a CTA never waits for another's 512 TMEM columns. The fused epilogue's
+// per-thread Non-Shared scores reuse the K ring, which is idle by then.
 template <int D>
 struct Cfg {
-    static constexpr int kStages = D == 64 ? 4 : 2;
+    static constexpr int kKStages = D == 64 ? 4 : 3;
+    static constexpr int kVStages = D == 64 ? 4 : 2;
     static constexpr int KB = D / 64;              // 128-byte swizzle blocks along d
     static constexpr int kTileBytes = KB * 16384;  // 128 rows (or tokens) x d bf16
     static constexpr int kOffQ = 0;                // two row tiles
     static constexpr int kOffK = kOffQ + 2 * kTileBytes;
-    static constexpr int kOffV = kOffK + kStages * kTileBytes;
-    static constexpr int kSmemBytes = kOffV + kStages * kTileBytes + 1024;
+    static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+    static constexpr int kOffNS = kOffK;           // fused epilogue: [2][steps][128] fp32
+    static constexpr int kSmemBytes = kOffV + kVStages * kTileBytes + 1024;
+    static_assert(2 * kMaxFusedSteps * kTileRows * 4 <= kKStages * kTileBytes, "NS scores fit the K ring");
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -82,18 +87,6 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int ch) {
     return (uint32_t)((ch >> 3) * 16384 + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
 }
 
-__device__ __forceinline__ float max32(const uint32_t (&s)[32], int valid) {
-    float m[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m[i] = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const float x = i < valid ? __uint_as_float(s[i]) : -INFINITY;
-        m[i & 7] = fmaxf(m[i & 7], x);
-    }
-    return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
-}
-
 struct Bars {
     uint64_t k_full[kMaxStages], k_empty[kMaxStages], v_full[kMaxStages], v_empty[kMaxStages];
     uint64_t s_full[2], p_full[2], q_ready[2];
@@ -115,12 +108,13 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     Geometry g, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ shared_len,
     float* __restrict__ part_o, float* __restrict__ part_lse, int32_t* status, FusedArgs fa) {
     using C = Cfg<D>;
-    constexpr int kStages = C::kStages;
+    constexpr int kKS = C::kKStages, kVS = C::kVStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem + C::kOffQ;
     uint8_t* sK = smem + C::kOffK;
     uint8_t* sV = smem + C::kOffV;
+    float* sNS = reinterpret_cast<float*>(smem + C::kOffNS);
     __shared__ Bars bars;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
@@ -145,9 +139,11 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     const int ntile_m = (2 * mp + 1 < g.row_tiles) ? 2 : 1;  // row tiles this CTA owns
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kKS; ++s) {
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.k_empty[s], 1);
+        }
+        for (int s = 0; s < kVS; ++s) {
             mbar_init(&bars.v_full[s], 1);
             mbar_init(&bars.v_empty[s], 1);
         }
@@ -202,32 +198,47 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 if (!__all_sync(0xffffffffu, mbar_wait(&bars.s_full[wg], j & 1, &abort_sh))) { ok = false; break; }
                 tc_fence_after();
                 const int lim = t1 - (t0 + j * kTileKeys);  // valid columns of this tile (>= 1)
-                // pass 1: row max of the raw scores
-                float mx = -INFINITY;
+                // the whole 128-column row of S in registers: four loads, one wait
+                uint32_t s[4][32];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    uint32_t s[32];
-                    tmem_ld32(tS + k * 32, s);
-                    tmem_wait_ld();
-                    mx = fmaxf(mx, max32(s, lim - k * 32));
+                for (int k = 0; k < 4; ++k) tmem_ld32(tS + k * 32, s[k]);
+                tmem_wait_ld();
+                if (lim < kTileKeys) {  // ragged last tile: columns past the prefix get -inf
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (k * 32 + i >= lim) s[k][i] = 0xff800000u;
+                }
+                float mx;
+                {
+                    float m8[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        m8[i] = fmaxf(fmaxf(__uint_as_float(s[0][i]), __uint_as_float(s[0][i + 8])),
+                                      fmaxf(__uint_as_float(s[0][i + 16]), __uint_as_float(s[0][i + 24])));
+#pragma unroll
+                    for (int k = 1; k < 4; ++k)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            m8[i] = fmaxf(m8[i], fmaxf(fmaxf(__uint_as_float(s[k][i]), __uint_as_float(s[k][i + 8])),
+                                                      fmaxf(__uint_as_float(s[k][i + 16]), __uint_as_float(s[k][i + 24]))));
+                    mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
                 }
                 const float m_new = fmaxf(m_run, mx * g.scale_log2);
                 const bool resc = m_new > m_run + kRescaleThreshold;
                 const float alpha = resc ? ex2(m_run - m_new) : 1.f;
                 const float m_use = resc ? m_new : m_run;
-                // pass 2: P = exp2(S*scale*log2e - m) as bf16, written over the consumed S columns
+                const float neg_m = -m_use;
+                // P = exp2(S*scale*log2e - m) as bf16, written over the consumed S columns
                 float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    uint32_t s[32], p[16];
-                    tmem_ld32(tS + k * 32, s);
-                    tmem_wait_ld();
+                    uint32_t p[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const int col = k * 32 + 2 * i;
-                        const float x0 = col < lim ? fmaf(__uint_as_float(s[2 * i]), g.scale_log2, -m_use) : -INFINITY;
-                        const float x1 = col + 1 < lim ? fmaf(__uint_as_float(s[2 * i + 1]), g.scale_log2, -m_use) : -INFINITY;
-                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        const float p0 = ex2(fmaf(__uint_as_float(s[k][2 * i]), g.scale_log2, neg_m));
+                        const float p1 = ex2(fmaf(__uint_as_float(s[k][2 * i + 1]), g.scale_log2, neg_m));
                         sum4[i & 3] += p0 + p1;
                         p[i] = pack_bf16(p0, p1);
                     }
@@ -236,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 l_run = l_run * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
                 m_run = m_use;
                 if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
+#pragma unroll 1
                     for (int k = 0; k < D / 32; ++k) {
                         uint32_t o[32];
                         tmem_ld32(tO + k * 32, o);
@@ -263,30 +274,28 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
 
         if (fa.enabled) {
             // ---------------------------------------- fused Non-Shared stage + Merge
+            // Scores of the beam's ancestry tokens go to this thread's column of sNS (no
+            // sharing between threads, so no synchronisation); the loops run at run time to
+            // keep the kernel small.
             bool bad = !ok || bad_len;
             if (tile_ok && rloc == 0 && mt == 0 && h == 0 && bad_len) set_status(status, XATTN_STATUS_BAD_SHARED_LEN);
-            float s2[kMaxFusedSteps];
-            int slots[kMaxFusedSteps];
+            float* myNS = sNS + wg * kMaxFusedSteps * kTileRows + rloc;
             float m_tot = m_run;
             const size_t qrow = ((size_t)r * g.BW + b) * g.Hq + (size_t)h * g.G + gg;
+            const int32_t* irow = row_ok && g.step > 0 ? fa.idx + ((size_t)r * g.BW + b) * g.Tmax : nullptr;
             if (row_ok && g.step > 0) {
-                const int32_t* irow = fa.idx + ((size_t)r * g.BW + b) * g.Tmax;
-                // the query row (bf16 pairs); L2-resident, the Q tile was just read
-                uint32_t qv[D / 2];
+                uint32_t qv[D / 2];  // the query row as bf16 pairs (L2-resident: just read)
 #pragma unroll
                 for (int ch = 0; ch < D / 8; ++ch) {
                     const uint4 u = __ldg(reinterpret_cast<const uint4*>(q + qrow * D) + ch);
                     qv[4 * ch] = u.x; qv[4 * ch + 1] = u.y; qv[4 * ch + 2] = u.z; qv[4 * ch + 3] = u.w;
                 }
                 bool bad_slot = false;
-#pragma unroll
-                for (int i = 0; i < kMaxFusedSteps; ++i) {
-                    s2[i] = -INFINITY;
-                    slots[i] = -1;
-                    if (i < g.step) {
-                        const int slot = __ldg(irow + i);
-                        if (slot < 0 || slot >= g.S) { bad_slot = true; continue; }
-                        slots[i] = slot;
+#pragma unroll 1
+                for (int i = 0; i < g.step; ++i) {
+                    const int slot = __ldg(irow + i);
+                    float s2 = -INFINITY;
+                    if (slot >= 0 && slot < g.S) {
                         const uint4* kr = reinterpret_cast<const uint4*>(fa.pool_k + (((size_t)r * g.S + slot) * g.Hkv + h) * D);
                         float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
@@ -300,34 +309,32 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                                 acc1 = fmaf(qf.y, kf.y, acc1);
                             }
                         }
-                        s2[i] = (acc0 + acc1) * g.scale_log2;
-                        m_tot = fmaxf(m_tot, s2[i]);
+                        s2 = (acc0 + acc1) * g.scale_log2;
+                    } else {
+                        bad_slot = true;
                     }
+                    myNS[i * kTileRows] = s2;
+                    m_tot = fmaxf(m_tot, s2);
                 }
                 if (bad_slot) {
                     bad = true;
                     set_status(status, XATTN_STATUS_BAD_SLOT);
                 }
-            } else {
-#pragma unroll
-                for (int i = 0; i < kMaxFusedSteps; ++i) { s2[i] = -INFINITY; slots[i] = -1; }
             }
             if (row_ok && !bad_len && L == 0 && g.step == 0) {
                 bad = true;
                 set_status(status, XATTN_STATUS_EMPTY_ROW);
             }
             const float alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - m_tot);
-            float pw[kMaxFusedSteps];
             float l_tot = l_run * alpha;
-#pragma unroll
-            for (int i = 0; i < kMaxFusedSteps; ++i) {
-                pw[i] = (s2[i] == -INFINITY) ? 0.f : ex2(s2[i] - m_tot);
-                l_tot += pw[i];
+            if (row_ok) {
+#pragma unroll 1
+                for (int i = 0; i < g.step; ++i) l_tot += ex2(myNS[i * kTileRows] - m_tot);
             }
             bad = bad || !(l_tot > 0.f);
             const float inv = bad ? __uint_as_float(kNaN) : 1.f / l_tot;
             const size_t obase = qrow * D;
-#pragma unroll
+#pragma unroll 1
             for (int k = 0; k < D / 32; ++k) {
                 uint32_t o[32];
                 if (have_o) {
@@ -341,11 +348,14 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                     float of[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) of[i] = __uint_as_float(o[i]) * alpha;
-#pragma unroll
-                    for (int s = 0; s < kMaxFusedSteps; ++s) {
-                        if (pw[s] == 0.f) continue;
+#pragma unroll 1
+                    for (int i = 0; i < g.step; ++i) {
+                        const float sc = myNS[i * kTileRows];
+                        if (sc == -INFINITY) continue;
+                        const float pw = ex2(sc - m_tot);
+                        const int slot = __ldg(irow + i);
                         const uint4* vr = reinterpret_cast<const uint4*>(
-                            fa.pool_v + (((size_t)r * g.S + slots[s]) * g.Hkv + h) * D + k * 32);
+                            fa.pool_v + (((size_t)r * g.S + slot) * g.Hkv + h) * D + k * 32);
 #pragma unroll
                         for (int ch = 0; ch < 4; ++ch) {
                             const uint4 u = __ldg(vr + ch);
@@ -353,8 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const float2 vf = unpack_bf16(vw[e]);
-                                of[ch * 8 + 2 * e] = fmaf(pw[s], vf.x, of[ch * 8 + 2 * e]);
-                                of[ch * 8 + 2 * e + 1] = fmaf(pw[s], vf.y, of[ch * 8 + 2 * e + 1]);
+                                of[ch * 8 + 2 * e] = fmaf(pw, vf.x, of[ch * 8 + 2 * e]);
+                                of[ch * 8 + 2 * e + 1] = fmaf(pw, vf.y, of[ch * 8 + 2 * e + 1]);
                             }
                         }
                     }
@@ -378,9 +388,9 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             if (row_ok) fa.lse[qrow] = bad ? __uint_as_float(kNaN) : (m_tot + __log2f(l_tot)) * kLn2;
         } else if (tile_ok) {
             // ---------------------------------------- this piece's partial result
-            const size_t prow = ((size_t)unit * g.nsplit + c) * g.M + row;
+            const size_t prow = ((size_t)unit * g.pieces + c) * g.M + row;
             const float inv = !ok ? __uint_as_float(kNaN) : (ntiles > 0 ? 1.f / l_run : 0.f);
-#pragma unroll
+#pragma unroll 1
             for (int k = 0; k < D / 32; ++k) {
                 uint32_t o[32];
                 if (have_o) {
@@ -409,27 +419,28 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             prefetch_tmap(&tmap_v);
             int issued_k = 0, issued_v = 0;
             for (int j = 0; j < ntiles; ++j) {
-                const int st = j % kStages, u = j / kStages;
                 const int tok = t0 + j * kTileKeys;
-                if (u > 0 && !mbar_wait(&bars.k_empty[st], (u - 1) & 1, &abort_sh)) break;
-                mbar_arrive_expect_tx(&bars.k_full[st], C::kTileBytes);
+                const int ks = j % kKS, ku = j / kKS;
+                if (ku > 0 && !mbar_wait(&bars.k_empty[ks], (ku - 1) & 1, &abort_sh)) break;
+                mbar_arrive_expect_tx(&bars.k_full[ks], C::kTileBytes);
 #pragma unroll
                 for (int kb = 0; kb < C::KB; ++kb)
-                    tma_load_4d(sK + st * C::kTileBytes + kb * 16384, &tmap_k, &bars.k_full[st], kb * 64, h, tok, r);
+                    tma_load_4d(sK + ks * C::kTileBytes + kb * 16384, &tmap_k, &bars.k_full[ks], kb * 64, h, tok, r);
                 issued_k = j + 1;
-                if (u > 0 && !mbar_wait(&bars.v_empty[st], (u - 1) & 1, &abort_sh)) break;
-                mbar_arrive_expect_tx(&bars.v_full[st], C::kTileBytes);
+                const int vs = j % kVS, vu = j / kVS;
+                if (vu > 0 && !mbar_wait(&bars.v_empty[vs], (vu - 1) & 1, &abort_sh)) break;
+                mbar_arrive_expect_tx(&bars.v_full[vs], C::kTileBytes);
 #pragma unroll
                 for (int kb = 0; kb < C::KB; ++kb)
-                    tma_load_4d(sV + st * C::kTileBytes + kb * 16384, &tmap_v, &bars.v_full[st], kb * 64, h, tok, r);
+                    tma_load_4d(sV + vs * C::kTileBytes + kb * 16384, &tmap_v, &bars.v_full[vs], kb * 64, h, tok, r);
                 issued_v = j + 1;
             }
             if (abort_sh) {  // let the copies still in flight land before the CTA exits
                 volatile int never = 0;
-                for (int j = max(0, issued_k - kStages); j < issued_k; ++j)
-                    mbar_wait(&bars.k_full[j % kStages], (j / kStages) & 1, &never);
-                for (int j = max(0, issued_v - kStages); j < issued_v; ++j)
-                    mbar_wait(&bars.v_full[j % kStages], (j / kStages) & 1, &never);
+                for (int j = max(0, issued_k - kKS); j < issued_k; ++j)
+                    mbar_wait(&bars.k_full[j % kKS], (j / kKS) & 1, &never);
+                for (int j = max(0, issued_v - kVS); j < issued_v; ++j)
+                    mbar_wait(&bars.v_full[j % kVS], (j / kVS) & 1, &never);
             }
         }
     } else {
@@ -448,46 +459,41 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                     mma_ts(tmem + kTmemO + i * 128, tmem + i * 128 + kk * 8, bd, idesc_pv, (jt > 0 || kk > 0) ? 1u : 0u);
                 }
             };
-            for (int j = 0; ok && j < ntiles; ++j) {
-                const int ks = j % kStages;
-                if (!mbar_wait(&bars.k_full[ks], (j / kStages) & 1, &abort_sh)) { ok = false; break; }
-                const int vs = (j - 1 + kStages) % kStages;
-                if (j > 0 && !mbar_wait(&bars.v_full[vs], ((j - 1) / kStages) & 1, &abort_sh)) { ok = false; break; }
-                const uint32_t kbase = smem_addr(sK + ks * C::kTileBytes);
+            // Per tile j and row tile i: P.V of tile j-1 first (it needs only V(j-1) and
+            // P_i), then Q.K^T of tile j into the same TMEM columns, then one commit.
+            for (int j = 0; ok && j <= ntiles; ++j) {
+                const int vs = (j - 1) % kVS;  // used only when j > 0
+                if (j > 0 && !mbar_wait(&bars.v_full[vs], ((j - 1) / kVS) & 1, &abort_sh)) { ok = false; break; }
+                const int ks = j % kKS;
+                bool k_ready = false;
                 for (int i = 0; i < ntile_m; ++i) {
                     if (j > 0) {
                         if (!mbar_wait(&bars.p_full[i], (j - 1) & 1, &abort_sh)) { ok = false; break; }
                         tc_fence_after();
                         issue_pv(i, j - 1, vs);
-                    } else {
+                    }
+                    if (j < ntiles) {
+                        if (!k_ready) {
+                            if (!mbar_wait(&bars.k_full[ks], (j / kKS) & 1, &abort_sh)) { ok = false; break; }
+                            k_ready = true;
+                        }
                         tc_fence_after();
-                    }
-                    const uint32_t qbase = smem_addr(sQ + i * C::kTileBytes);
+                        const uint32_t qbase = smem_addr(sQ + i * C::kTileBytes);
+                        const uint32_t kbase = smem_addr(sK + ks * C::kTileBytes);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_ss(tmem + i * 128, smem_desc_sw128(qbase + off, 16, 1024),
-                               smem_desc_sw128(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                            mma_ss(tmem + i * 128, smem_desc_sw128(qbase + off, 16, 1024),
+                                   smem_desc_sw128(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&bars.s_full[i]);
                     }
-                    mma_commit(&bars.s_full[i]);
                 }
                 if (!ok) break;
-                mma_commit(&bars.k_empty[ks]);
+                if (j < ntiles) mma_commit(&bars.k_empty[ks]);
                 if (j > 0) mma_commit(&bars.v_empty[vs]);
             }
-            if (ok) {  // P.V of the last tile
-                const int jl = ntiles - 1, vs = jl % kStages;
-                if (!mbar_wait(&bars.v_full[vs], (jl / kStages) & 1, &abort_sh)) ok = false;
-                for (int i = 0; ok && i < ntile_m; ++i) {
-                    if (!mbar_wait(&bars.p_full[i], jl & 1, &abort_sh)) { ok = false; break; }
-                    tc_fence_after();
-                    issue_pv(i, jl, vs);
-                }
-                if (ok) {
-                    mma_commit(&bars.v_empty[vs]);
-                    mma_commit(&bars.o_full);
-                }
-            }
+            if (ok) mma_commit(&bars.o_full);
             if (!ok) {
                 abort_sh = 1;
                 set_status(status, XATTN_STATUS_TIMEOUT);

@@ -109,6 +109,8 @@ void plan(const xattn_desc* d, int step, Geometry* g, int* kernel) {
         g->split_tokens = cdiv(tiles, best_n) * kTileKeys;
     }
     g->nsplit = g->Lmax > 0 ? cdiv(g->Lmax, g->split_tokens) : 0;
+    g->ns_pieces = step > kNsDirectMax ? cdiv(step, kNsChunk) : 0;
+    g->pieces = g->nsplit + (g->Tmax > kNsDirectMax ? cdiv(g->Tmax, kNsChunk) : 0);
 }
 
 size_t workspace_bytes_for(const Geometry& g) {

@@ -14,6 +14,8 @@ constexpr int kTileRows = 128;   // rows of one tensor-core M tile (stacked beam
 constexpr int kTileKeys = 128;   // prefix tokens per K/V tile
 constexpr int kStatusBytes = 256;
 constexpr int kMaxFusedSteps = 16; // Non-Shared tokens the fused Shared-stage epilogue handles
+constexpr int kNsDirectMax = 32;   // up to this many Non-Shared tokens the merge kernel walks them
+constexpr int kNsChunk = 64;       // beyond it, pieces of this many tokens are computed in parallel
 
 // Device status word helpers ----------------------------------------------------------
 __device__ __forceinline__ void set_status(int32_t* status, int32_t bits) {
@@ -30,10 +32,13 @@ struct Geometry {
     int split_tokens; // tokens per piece (multiple of 128)
     float scale_log2; // softmax scale * log2(e)
     int out_f32;      // output dtype: 0 bf16, 1 fp32
+    int ns_pieces;    // Non-Shared pieces of this call (0: the merge kernel walks the tokens)
+    int pieces;       // piece stride of the workspace: nsplit + Non-Shared pieces for max_steps
 };
 
-// Workspace layout: [status (256 B)] [part_o: R*Hkv*nsplit*M*d fp32] [part_lse: R*Hkv*nsplit*M fp32]
-inline size_t part_rows(const Geometry& g) { return (size_t)g.R * g.Hkv * g.nsplit * g.M; }
+// Workspace layout: [status (256 B)] [part_o: R*Hkv*pieces*M*d fp32] [part_lse: R*Hkv*pieces*M fp32].
+// Pieces 0 .. nsplit-1 are the prefix pieces, nsplit .. nsplit+ns_pieces-1 the Non-Shared ones.
+inline size_t part_rows(const Geometry& g) { return (size_t)g.R * g.Hkv * g.pieces * g.M; }
 
 // Launchers (each returns cudaGetLastError()).
 // fused = the CTA also runs the Non-Shared stage and the Merge and writes out / lse

@@ -79,6 +79,16 @@ def test_bf16_output_is_rounded_fp32_output(w):
     assert torch.equal(l32, l16)
 
 
+@pytest.mark.parametrize("T,d", [(33, 128), (64, 128), (70, 64), (130, 128)])
+def test_long_non_shared_parts(T, d):
+    """More than 32 ancestry tokens per beam: the Non-Shared part is cut into pieces of 64
+    positions computed in parallel (last piece ragged), then merged with the prefix pieces.
+    Request 1 has an empty prefix (Non-Shared only)."""
+    w = wl.custom(R=2, BW=6, Hq=8, Hkv=2, d=d, lens=(300, 0), T=T, seed=T)
+    _, db, _ = run_and_check(w)
+    assert db.plan().fused == 0
+
+
 def test_tiny_config_both_kernels():
     for k in (0, 1, 2):
         stats, _, _ = run_and_check(wl.TINY, shared_kernel=k)
