@@ -33,7 +33,10 @@ XATTN_DTYPE_F32 = 1
 
 # Every symbol include/xattn.h declares.
 EXPORTS = ("xattn_decode_workspace_size", "xattn_decode", "xattn_decode_shared", "xattn_decode_merge",
-           "xattn_beam_update", "xattn_read_status", "xattn_query_plan", "xattn_status_string")
+           "xattn_beam_update", "xattn_read_status", "xattn_query_plan", "xattn_status_string",
+           "xattn_decode_noalloc")
+
+XATTN_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class XAttnError(RuntimeError):
@@ -78,6 +81,8 @@ def load(path: str = LIB_PATH):
     lib.xattn_decode_shared.restype = ctypes.c_int
     lib.xattn_decode_merge.argtypes = [pdesc, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
     lib.xattn_decode_merge.restype = ctypes.c_int
+    lib.xattn_decode_noalloc.argtypes = [pdesc, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp]
+    lib.xattn_decode_noalloc.restype = ctypes.c_int
     lib.xattn_beam_update.argtypes = [pdesc, vp, vp, vp, vp, vp, vp, i32, vp, vp]
     lib.xattn_beam_update.restype = ctypes.c_int
     lib.xattn_read_status.argtypes = [vp, ctypes.POINTER(i32), i32, vp]
@@ -122,6 +127,15 @@ def xattn_decode(desc, q, shared_k, shared_v, shared_len, ns_k_pool, ns_v_pool, 
                                    _ptr(shared_len), _ptr(ns_k_pool), _ptr(ns_v_pool), _ptr(beam_tok_idx),
                                    int(step), _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
                                    _stream(stream)))
+
+
+def xattn_decode_noalloc(desc, q, shared_k, shared_v, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, step,
+                         out, lse, status_out=None, stream=None) -> int:
+    """xattn_decode with the library's own static scratch instead of a caller workspace."""
+    return int(load().xattn_decode_noalloc(ctypes.byref(desc), _ptr(q), _ptr(shared_k), _ptr(shared_v),
+                                           _ptr(shared_len), _ptr(ns_k_pool), _ptr(ns_v_pool),
+                                           _ptr(beam_tok_idx), int(step), _ptr(out), _ptr(lse), _ptr(status_out),
+                                           _stream(stream)))
 
 
 def xattn_decode_shared(desc, q, shared_k, shared_v, shared_len, workspace, workspace_bytes, stream=None) -> int:

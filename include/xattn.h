@@ -158,6 +158,30 @@ XATTN_API int xattn_beam_update(const xattn_desc* desc, const int32_t* parent, c
                       int32_t* beam_tok_idx, int32_t step, int32_t* status,
                       xattn_stream_t stream);
 
+/* Allocation-free decode. The paper has no counterpart to this call; it exists for callers
+ * that cannot allocate device memory or hand the library a workspace (a runtime that owns
+ * every allocation, a latency-critical thread that must not trigger cudaMalloc, a fixed
+ * memory budget). It does exactly what xattn_decode does, with its workspace taken from a
+ * static device array of XATTN_NOALLOC_SCRATCH_BYTES (32 MiB) inside the library; every
+ * device that loads the library holds that array until the process exits.
+ *   - Shapes whose xattn_decode_workspace_size exceeds that limit return
+ *     XATTN_ERR_WORKSPACE_TOO_SMALL before anything is launched; an invalid descriptor
+ *     returns XATTN_ERR_INVALID_ARG.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.
+ *   - All calls share the array: calls whose GPU work overlaps (other streams or threads on
+ *     the same device) race and must be serialised by the caller.
+ *   - The status word is cleared at the start of each call; if `status_out` (a device
+ *     int32, may be NULL) is given, the call's final status word is copied there on `stream`.
+ * No cudaMalloc, cudaFree or allocating library routine is called. Other arguments and
+ * results are those of xattn_decode. */
+#define XATTN_NOALLOC_SCRATCH_BYTES (32u << 20)
+XATTN_API int xattn_decode_noalloc(const xattn_desc* desc, const void* q, const void* shared_k,
+                                   const void* shared_v, const int32_t* shared_len,
+                                   const void* ns_k_pool, const void* ns_v_pool,
+                                   const int32_t* beam_tok_idx, int32_t step, void* out,
+                                   float* lse, int32_t* status_out, xattn_stream_t stream);
+
 /* Copies the status word of `workspace` (device) to *status_out (host), optionally
  * clearing it, and synchronises `stream`. */
 XATTN_API int xattn_read_status(void* workspace, int32_t* status_out, int32_t clear, xattn_stream_t stream);
