@@ -58,7 +58,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             if err.strip():
                 sys.stderr.write(f"--- {os.path.basename(obj)}\n{err}")
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nv, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-lcudart_static", "-ldl", "-lrt", "-lpthread"]
+    cmd = [nv, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-lcudart_static", "-ldl", "-lrt", "-lpthread", "-Xlinker", "--no-undefined"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stderr}")

@@ -97,8 +97,8 @@ template <int D, int G>
 __global__ void __launch_bounds__(256) ns_merge_kernel(
     Geometry g, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ pool_k,
     const __nv_bfloat16* __restrict__ pool_v, const int32_t* __restrict__ idx,
-    const int32_t* __restrict__ shared_len, const float* __restrict__ part_o,
-    const float* __restrict__ part_lse, void* __restrict__ out, float* __restrict__ lse,
+    const int32_t* __restrict__ shared_len, float* __restrict__ part_o,
+    float* __restrict__ part_lse, void* __restrict__ out, float* __restrict__ lse,
     int32_t* status) {
     constexpr int E = D / 32;
     const int lane = threadIdx.x & 31;
@@ -123,6 +123,8 @@ __global__ void __launch_bounds__(256) ns_merge_kernel(
 
     RowState<E, G> st;
     st.init();
+    bool slot_bad = false;
+    if (g.ns_to_piece) bad = false;  // the Shared-stage kernel reports prefix problems
     if (g.ns_pieces == 0 && g.step > 0 && !bad) {
         // Non-Shared stage: online softmax over the beam's ancestry tokens.
         float qv[G][E];
@@ -134,6 +136,7 @@ __global__ void __launch_bounds__(256) ns_merge_kernel(
             const int slot = __shfl_sync(0xffffffffu, my_slot, i);
             if (slot < 0 || slot >= g.S) {
                 bad = true;
+                slot_bad = true;
                 if (lane == 0) set_status(status, XATTN_STATUS_BAD_SLOT);
                 break;
             }
@@ -151,30 +154,92 @@ __global__ void __launch_bounds__(256) ns_merge_kernel(
         }
     }
 
+    if (g.ns_to_piece) {
+        // The Non-Shared part alone, stored as piece `nsplit` for the Shared-stage kernel
+        // to merge (its epilogue also reports prefix-length problems and empty rows).
+        const size_t prow = (((size_t)r * g.Hkv + h) * g.pieces + g.nsplit) * g.M + (size_t)b * G;
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+            const bool empty = !(st.l[gg] > 0.f);
+            const float inv = empty ? 0.f : 1.f / st.l[gg];
+            float* po = part_o + (prow + gg) * D + lane * E;
+            if constexpr (E == 4) {
+                *reinterpret_cast<float4*>(po) =
+                    make_float4(st.acc[gg][0] * inv, st.acc[gg][1] * inv, st.acc[gg][2] * inv, st.acc[gg][3] * inv);
+            } else {
+                *reinterpret_cast<float2*>(po) = make_float2(st.acc[gg][0] * inv, st.acc[gg][1] * inv);
+            }
+            if (lane == 0)
+                part_lse[prow + gg] = slot_bad ? __uint_as_float(kNaN)
+                                               : (empty ? -INFINITY : (st.m[gg] + __log2f(st.l[gg])) * kLn2);
+        }
+        return;
+    }
+
     // Merge: fold every stored piece (prefix pieces, then Non-Shared pieces) into the
     // running state. A piece stores its normalised output o_c and natural-log lse_c; in
-    // base 2 it contributes weight 2^(lse_c * log2 e) times o_c.
+    // base 2 it contributes weight 2^(lse_c * log2 e) times o_c. First pass: the pieces'
+    // LSEs, lane-parallel (lane l holds pieces c = l, l+32, ...), give each row's maximum
+    // and weights; second pass: weighted outputs, four pieces' loads in flight.
     if (!bad) {
         const size_t unit = (size_t)r * g.Hkv + h;
         const int np = g.nsplit + g.ns_pieces;
-        for (int c = 0; c < np; ++c) {
-            const size_t prow = (unit * g.pieces + c) * g.M + (size_t)b * G;
+        const size_t prow_b = unit * g.pieces * g.M + (size_t)b * G;  // piece c row gg: + c*M + gg
 #pragma unroll
-            for (int gg = 0; gg < G; ++gg) {
-                const float lc = __ldg(part_lse + prow + gg);
-                if (lc != lc) bad = true;          // a failed piece poisons the row
-                if (!(lc > -INFINITY)) continue;  // empty piece (or NaN)
-                float ov[E];
-                const float* po = part_o + (prow + gg) * D + lane * E;
-                if constexpr (E == 4) {
-                    const float4 t = __ldg(reinterpret_cast<const float4*>(po));
-                    ov[0] = t.x; ov[1] = t.y; ov[2] = t.z; ov[3] = t.w;
-                } else {
-                    const float2 t = __ldg(reinterpret_cast<const float2*>(po));
-                    ov[0] = t.x; ov[1] = t.y;
-                }
-                st.add(gg, lc * kLog2e, ov);
+        for (int gg = 0; gg < G; ++gg) {
+            float mx = st.m[gg];
+            bool nan_seen = false;
+            for (int c = lane; c < np; c += 32) {
+                const float lc = __ldg(part_lse + prow_b + (size_t)c * g.M + gg);
+                nan_seen |= (lc != lc);
+                mx = fmaxf(mx, lc * kLog2e);
             }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            if (__any_sync(0xffffffffu, nan_seen)) bad = true;  // a failed piece poisons the row
+            if (mx == -INFINITY) continue;                      // nothing at all for this row
+            const float alpha = ex2(st.m[gg] - mx);             // rescale the Non-Shared state
+            float lsum = 0.f;
+            for (int c = lane; c < np; c += 32) {
+                const float lc = __ldg(part_lse + prow_b + (size_t)c * g.M + gg);
+                lsum += (lc > -INFINITY) ? ex2(lc * kLog2e - mx) : 0.f;
+            }
+            lsum = warp_sum(lsum);
+            float acc[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = st.acc[gg][e] * alpha;
+            for (int c0 = 0; c0 < np; c0 += 4) {
+                float ov[4][E], wv[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c = c0 + u;
+                    wv[u] = 0.f;
+                    if (c < np) {
+                        const size_t prow = prow_b + (size_t)c * g.M + gg;
+                        const float lc = __ldg(part_lse + prow);
+                        wv[u] = (lc > -INFINITY) ? ex2(lc * kLog2e - mx) : 0.f;
+                        const float* po = part_o + prow * D + lane * E;
+                        if constexpr (E == 4) {
+                            const float4 t = __ldg(reinterpret_cast<const float4*>(po));
+                            ov[u][0] = t.x; ov[u][1] = t.y; ov[u][2] = t.z; ov[u][3] = t.w;
+                        } else {
+                            const float2 t = __ldg(reinterpret_cast<const float2*>(po));
+                            ov[u][0] = t.x; ov[u][1] = t.y;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < E; ++e) ov[u][e] = 0.f;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc[e] = fmaf(wv[u], wv[u] != 0.f ? ov[u][e] : 0.f, acc[e]);
+            }
+            st.l[gg] = st.l[gg] * alpha + lsum;
+#pragma unroll
+            for (int e = 0; e < E; ++e) st.acc[gg][e] = acc[e];
+            st.m[gg] = mx;
         }
     }
 
@@ -204,6 +269,93 @@ __global__ void __launch_bounds__(256) ns_merge_kernel(
         }
         if (lane == 0) lse[qrow0 + gg] = row_lse;
     }
+}
+
+// Row-parallel merge for calls whose Non-Shared part is already in pieces: one warp per
+// query row (r, b, h) folds every piece. Lanes first take the pieces' LSEs (lane l holds
+// pieces l, l+32, ...) for the row's maximum and total weight, then split the head
+// dimension while eight pieces' outputs are in flight.
+template <int D>
+__global__ void __launch_bounds__(256) merge_rows_kernel(
+    Geometry g, const int32_t* __restrict__ shared_len, const float* __restrict__ part_o,
+    const float* __restrict__ part_lse, void* __restrict__ out, float* __restrict__ lse, int32_t* status) {
+    constexpr int E = D / 32;
+    const int lane = threadIdx.x & 31;
+    const long row = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // (r*BW + b)*Hq + hq
+    if (row >= (long)g.R * g.BW * g.Hq) return;
+    const int hq = (int)(row % g.Hq);
+    const int b = (int)((row / g.Hq) % g.BW);
+    const int r = (int)(row / ((long)g.Hq * g.BW));
+    const int h = hq / g.G, gg = hq - h * g.G;
+    const int L = shared_len ? shared_len[r] : 0;
+    bool bad = (g.Lmax > 0) && (L < 0 || L > g.Lmax);
+    if (bad && lane == 0 && hq == 0 && b == 0) set_status(status, XATTN_STATUS_BAD_SHARED_LEN);
+    const int np = g.nsplit + g.ns_pieces;
+    const size_t prow_b = ((size_t)r * g.Hkv + h) * g.pieces * g.M + (size_t)b * g.G + gg;  // + c*M
+    float mx = -INFINITY;
+    bool nan_seen = false;
+    for (int c = lane; c < np; c += 32) {
+        const float lc = __ldg(part_lse + prow_b + (size_t)c * g.M);
+        nan_seen |= (lc != lc);
+        mx = fmaxf(mx, lc * kLog2e);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    bad = bad || __any_sync(0xffffffffu, nan_seen);
+    float lsum = 0.f;
+    for (int c = lane; c < np; c += 32) {
+        const float lc = __ldg(part_lse + prow_b + (size_t)c * g.M);
+        lsum += (lc > -INFINITY) ? ex2(lc * kLog2e - mx) : 0.f;
+    }
+    lsum = warp_sum(lsum);
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    for (int c0 = 0; c0 < np; c0 += 8) {
+        float ov[8][E], wv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int c = c0 + u;
+            wv[u] = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) ov[u][e] = 0.f;
+            if (c < np) {
+                const size_t prow = prow_b + (size_t)c * g.M;
+                const float lc = __ldg(part_lse + prow);
+                if (lc > -INFINITY) {
+                    wv[u] = ex2(lc * kLog2e - mx);
+                    const float* po = part_o + prow * D + lane * E;
+                    if constexpr (E == 4) {
+                        const float4 t = __ldg(reinterpret_cast<const float4*>(po));
+                        ov[u][0] = t.x; ov[u][1] = t.y; ov[u][2] = t.z; ov[u][3] = t.w;
+                    } else {
+                        const float2 t = __ldg(reinterpret_cast<const float2*>(po));
+                        ov[u][0] = t.x; ov[u][1] = t.y;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = fmaf(wv[u], ov[u][e], acc[e]);
+    }
+    bad = bad || !(lsum > 0.f);
+    const float inv = bad ? __uint_as_float(kNaN) : 1.f / lsum;
+    float o[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[e] = acc[e] * inv;
+    if (g.out_f32) {
+        float* dst = reinterpret_cast<float*>(out) + (size_t)row * D + lane * E;
+        if constexpr (E == 4) {
+            *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+            *reinterpret_cast<float2*>(dst) = make_float2(o[0], o[1]);
+        }
+    } else {
+        LaneVec<D>::store(reinterpret_cast<__nv_bfloat16*>(out) + (size_t)row * D + lane * E, o);
+    }
+    if (lane == 0) lse[row] = bad ? __uint_as_float(kNaN) : (mx + __log2f(lsum)) * kLn2;
 }
 
 // One piece of a long Non-Shared part: ancestry positions [c*kNsChunk, (c+1)*kNsChunk) of
@@ -316,16 +468,20 @@ template <int D>
 cudaError_t launch_d(const Geometry& g, cudaStream_t st, const __nv_bfloat16* q, const __nv_bfloat16* pk,
                      const __nv_bfloat16* pv, const int32_t* idx, const int32_t* slen, float* po, float* pl,
                      void* out, float* lse, int32_t* status) {
-    const dim3 grid(merge_ctas_for(g)), block(256);
+    const dim3 grid((unsigned)(((long)g.R * g.BW * g.Hkv + 7) / 8)), block(256);
     const long part_ctas = (long)g.R * g.BW * g.Hkv * g.ns_pieces;
     if (part_ctas > 0x7fffffffL) return cudaErrorInvalidValue;
+    const unsigned rows_ctas = (unsigned)(((long)g.R * g.BW * g.Hq + 7) / 8);
     switch (g.G) {
 #define XATTN_G(GV)                                                                                              \
     case GV:                                                                                                     \
-        if (g.ns_pieces > 0)                                                                                     \
+        if (g.ns_pieces > 0) {                                                                                   \
             ns_partial_kernel<D, GV><<<(unsigned)part_ctas, kPartWarps * 32, 0, st>>>(g, q, pk, pv, idx, po, pl, \
                                                                                        status);                 \
-        ns_merge_kernel<D, GV><<<grid, block, 0, st>>>(g, q, pk, pv, idx, slen, po, pl, out, lse, status);     \
+            merge_rows_kernel<D><<<rows_ctas, block, 0, st>>>(g, slen, po, pl, out, lse, status);               \
+        } else {                                                                                                 \
+            ns_merge_kernel<D, GV><<<grid, block, 0, st>>>(g, q, pk, pv, idx, slen, po, pl, out, lse, status); \
+        }                                                                                                        \
         break;
         XATTN_G(1) XATTN_G(2) XATTN_G(4) XATTN_G(8) XATTN_G(16)
 #undef XATTN_G
@@ -337,7 +493,8 @@ cudaError_t launch_d(const Geometry& g, cudaStream_t st, const __nv_bfloat16* q,
 }  // namespace
 
 int merge_ctas_for(const Geometry& g) {
-    const long warps = (long)g.R * g.BW * g.Hkv;
+    // warp per (r, b, KV head), or per query row when the Non-Shared part is in pieces
+    const long warps = (long)g.R * g.BW * (g.ns_pieces > 0 ? g.Hq : g.Hkv);
     return (int)((warps + 7) / 8);
 }
 

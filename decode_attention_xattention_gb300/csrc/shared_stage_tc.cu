@@ -23,11 +23,11 @@
 // max is raised only when it grows by more than 2^8, so O is rescaled rarely and every P
 // stays below 2^8.
 //
-// Epilogue. When the prefix is not split (one piece) and the beams have at most
-// kMaxFusedSteps Non-Shared tokens, the CTA finishes the job: each softmax thread gathers
-// its beam's ancestry tokens from the pool, folds their scores into its row's (max, sum)
-// and O, and writes the normalised output and LSE. Otherwise it writes the piece's
-// normalised output and LSE to the workspace for the separate Non-Shared + Merge kernel.
+// Epilogue. When the prefix is one piece and the Non-Shared part is short, xattn_decode
+// first runs the Non-Shared kernel, which leaves each row's Non-Shared (normalised output,
+// LSE) as a piece in the workspace; this kernel's epilogue then merges that piece with its
+// O (log-sum-exp rule) and writes the final output and LSE. Otherwise it writes the
+// prefix piece's normalised output and LSE for the separate Merge kernel.
 //
 // Every on-chip wait is bounded: on a timeout the CTA records XATTN_STATUS_TIMEOUT, writes
 // NaN, waits (bounded) for its own TMA copies and MMAs, frees TMEM and returns.
@@ -39,9 +39,14 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 320;  // warps 0-7: two softmax warpgroups; warp 8: TMA; warp 9: MMA
-constexpr int kWarpTma = 8, kWarpMma = 9;
+// Warp roles: 0-7 two softmax warpgroups; 8 K-tile producer; 9 MMA issuer (and TMEM
+// owner); 10 V-tile producer. Every role that spins on an mbarrier has a warp of its own:
+// divergent lanes of one warp run one path at a time, so a spinning lane would starve its
+// neighbours.
+constexpr int kThreads = 352;
+constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10;
 constexpr int kMaxStages = 4;
+constexpr int kPrefetch = 4;  // K/V tiles prefetched into L2 ahead of their load
 constexpr uint32_t kTmemCols = 512;  // S0 | S1 | O0 | O1, 128 columns each
 constexpr uint32_t kTmemO = 256;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -50,8 +55,8 @@ constexpr uint32_t kNaN = 0x7fc00000u;
 
 // K/V pipeline depth: K is consumed one tile before V, so K gets the deeper ring
 // (3 + 2 stages at d = 128, 4 + 4 at d = 64). Either way the shared memory admits one CTA
-// per SM, so a CTA never waits for another's 512 TMEM columns. The fused epilogue's
-// per-thread Non-Shared scores reuse the K ring, which is idle by then.
+// per SM, so a CTA never waits for another's 512 TMEM columns.
+//
 template <int D>
 struct Cfg {
     static constexpr int kKStages = D == 64 ? 4 : 3;
@@ -61,9 +66,7 @@ struct Cfg {
     static constexpr int kOffQ = 0;                // two row tiles
     static constexpr int kOffK = kOffQ + 2 * kTileBytes;
     static constexpr int kOffV = kOffK + kKStages * kTileBytes;
-    static constexpr int kOffNS = kOffK;           // fused epilogue: [2][steps][128] fp32
     static constexpr int kSmemBytes = kOffV + kVStages * kTileBytes + 1024;
-    static_assert(2 * kMaxFusedSteps * kTileRows * 4 <= kKStages * kTileBytes, "NS scores fit the K ring");
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -75,10 +78,6 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
-    return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u));
 }
 
 // Byte offset of 16-byte chunk `ch` (along the contraction dim) of row `row` in a tile
@@ -93,10 +92,9 @@ struct Bars {
     uint64_t o_full, final_mma;
 };
 
+// Fused epilogue: fold the Non-Shared piece (written into the workspace by the
+// Non-Shared kernel that runs just before, when step > 0) into O and write out / lse.
 struct FusedArgs {
-    const __nv_bfloat16* pool_k;
-    const __nv_bfloat16* pool_v;
-    const int32_t* idx;
     void* out;
     float* lse;
     int enabled;
@@ -114,7 +112,6 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     uint8_t* sQ = smem + C::kOffQ;
     uint8_t* sK = smem + C::kOffK;
     uint8_t* sV = smem + C::kOffV;
-    float* sNS = reinterpret_cast<float*>(smem + C::kOffNS);
     __shared__ Bars bars;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
@@ -154,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         }
         mbar_init(&bars.o_full, 1);
         mbar_init(&bars.final_mma, 1);
+
         abort_sh = 0;
         fence_barrier_init();
     }
@@ -195,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             const uint32_t tS = tmem + lane_base + wg * 128;
             const uint32_t tO = tmem + lane_base + kTmemO + wg * 128;
             for (int j = 0; j < ntiles; ++j) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&bars.s_full[wg], j & 1, &abort_sh))) { ok = false; break; }
+                if (!mbar_wait_warp(&bars.s_full[wg], j & 1, &abort_sh)) { ok = false; break; }
                 tc_fence_after();
                 const int lim = t1 - (t0 + j * kTileKeys);  // valid columns of this tile (>= 1)
                 // the whole 128-column row of S in registers: four loads, one wait
@@ -261,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 tc_fence_before();
                 mbar_arrive(&bars.p_full[wg]);
             }
-            if (ok && !__all_sync(0xffffffffu, mbar_wait(&bars.o_full, 0, &abort_sh))) ok = false;
+            if (ok && !mbar_wait_warp(&bars.o_full, 0, &abort_sh)) ok = false;
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
             if (!ok) {
@@ -273,64 +271,27 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         const bool have_o = tile_ok && ntiles > 0;  // O_i holds accumulated P.V (TMEM allocated)
 
         if (fa.enabled) {
-            // ---------------------------------------- fused Non-Shared stage + Merge
-            // Scores of the beam's ancestry tokens go to this thread's column of sNS (no
-            // sharing between threads, so no synchronisation); the loops run at run time to
-            // keep the kernel small.
+            // ---------------------------------------- Merge with the Non-Shared piece
+            // The Non-Shared kernel ran before this one and left each row's normalised
+            // output o_ns and natural-log lse_ns at piece `nsplit` of the workspace.
             bool bad = !ok || bad_len;
             if (tile_ok && rloc == 0 && mt == 0 && h == 0 && bad_len) set_status(status, XATTN_STATUS_BAD_SHARED_LEN);
-            float* myNS = sNS + wg * kMaxFusedSteps * kTileRows + rloc;
-            float m_tot = m_run;
             const size_t qrow = ((size_t)r * g.BW + b) * g.Hq + (size_t)h * g.G + gg;
-            const int32_t* irow = row_ok && g.step > 0 ? fa.idx + ((size_t)r * g.BW + b) * g.Tmax : nullptr;
+            const size_t nsrow = ((size_t)unit * g.pieces + g.nsplit) * g.M + row;
+            float m_tot = m_run, w_ns = 0.f, alpha = 1.f;
             if (row_ok && g.step > 0) {
-                uint32_t qv[D / 2];  // the query row as bf16 pairs (L2-resident: just read)
-#pragma unroll
-                for (int ch = 0; ch < D / 8; ++ch) {
-                    const uint4 u = __ldg(reinterpret_cast<const uint4*>(q + qrow * D) + ch);
-                    qv[4 * ch] = u.x; qv[4 * ch + 1] = u.y; qv[4 * ch + 2] = u.z; qv[4 * ch + 3] = u.w;
-                }
-                bool bad_slot = false;
-#pragma unroll 1
-                for (int i = 0; i < g.step; ++i) {
-                    const int slot = __ldg(irow + i);
-                    float s2 = -INFINITY;
-                    if (slot >= 0 && slot < g.S) {
-                        const uint4* kr = reinterpret_cast<const uint4*>(fa.pool_k + (((size_t)r * g.S + slot) * g.Hkv + h) * D);
-                        float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-                        for (int ch = 0; ch < D / 8; ++ch) {
-                            const uint4 u = __ldg(kr + ch);
-                            const uint32_t kw[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 qf = unpack_bf16(qv[4 * ch + e]), kf = unpack_bf16(kw[e]);
-                                acc0 = fmaf(qf.x, kf.x, acc0);
-                                acc1 = fmaf(qf.y, kf.y, acc1);
-                            }
-                        }
-                        s2 = (acc0 + acc1) * g.scale_log2;
-                    } else {
-                        bad_slot = true;
-                    }
-                    myNS[i * kTileRows] = s2;
-                    m_tot = fmaxf(m_tot, s2);
-                }
-                if (bad_slot) {
-                    bad = true;
-                    set_status(status, XATTN_STATUS_BAD_SLOT);
-                }
+                const float lns = __ldg(part_lse + nsrow);
+                if (lns != lns) bad = true;  // a bad ancestry slot was reported by the Non-Shared kernel
+                const float s_ns = lns * 1.4426950408889634f;
+                m_tot = fmaxf(m_run, s_ns);
+                alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - m_tot);
+                w_ns = (s_ns > -INFINITY) ? ex2(s_ns - m_tot) : 0.f;
             }
             if (row_ok && !bad_len && L == 0 && g.step == 0) {
                 bad = true;
                 set_status(status, XATTN_STATUS_EMPTY_ROW);
             }
-            const float alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - m_tot);
-            float l_tot = l_run * alpha;
-            if (row_ok) {
-#pragma unroll 1
-                for (int i = 0; i < g.step; ++i) l_tot += ex2(myNS[i * kTileRows] - m_tot);
-            }
+            const float l_tot = l_run * alpha + w_ns;
             bad = bad || !(l_tot > 0.f);
             const float inv = bad ? __uint_as_float(kNaN) : 1.f / l_tot;
             const size_t obase = qrow * D;
@@ -348,24 +309,15 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                     float of[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) of[i] = __uint_as_float(o[i]) * alpha;
-#pragma unroll 1
-                    for (int i = 0; i < g.step; ++i) {
-                        const float sc = myNS[i * kTileRows];
-                        if (sc == -INFINITY) continue;
-                        const float pw = ex2(sc - m_tot);
-                        const int slot = __ldg(irow + i);
-                        const uint4* vr = reinterpret_cast<const uint4*>(
-                            fa.pool_v + (((size_t)r * g.S + slot) * g.Hkv + h) * D + k * 32);
+                    if (w_ns != 0.f) {
+                        const float4* pn = reinterpret_cast<const float4*>(part_o + nsrow * D + k * 32);
 #pragma unroll
-                        for (int ch = 0; ch < 4; ++ch) {
-                            const uint4 u = __ldg(vr + ch);
-                            const uint32_t vw[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 vf = unpack_bf16(vw[e]);
-                                of[ch * 8 + 2 * e] = fmaf(pw, vf.x, of[ch * 8 + 2 * e]);
-                                of[ch * 8 + 2 * e + 1] = fmaf(pw, vf.y, of[ch * 8 + 2 * e + 1]);
-                            }
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 v = __ldg(pn + i);
+                            of[4 * i] = fmaf(w_ns, v.x, of[4 * i]);
+                            of[4 * i + 1] = fmaf(w_ns, v.y, of[4 * i + 1]);
+                            of[4 * i + 2] = fmaf(w_ns, v.z, of[4 * i + 2]);
+                            of[4 * i + 3] = fmaf(w_ns, v.w, of[4 * i + 3]);
                         }
                     }
                     if (g.out_f32) {
@@ -412,35 +364,37 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 part_lse[prow] = !ok ? __uint_as_float(kNaN)
                                      : (ntiles > 0 ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY);
         }
-    } else if (warp == kWarpTma) {
-        // ============================================ TMA producer
+    } else if (warp == kWarpK || warp == kWarpV) {
+        // ============================================ TMA producers
+        // One warp feeds the K ring and another the V ring, each as soon as a slot frees.
+        // Both also prefetch the tile kPrefetch tiles ahead into L2, which hides most of
+        // the HBM latency of the later load.
         if (lane == 0 && ntiles > 0) {
-            prefetch_tmap(&tmap_k);
-            prefetch_tmap(&tmap_v);
-            int issued_k = 0, issued_v = 0;
+            const bool is_k = warp == kWarpK;
+            const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
+            prefetch_tmap(map);
+            const int nst = is_k ? kKS : kVS;
+            uint64_t* full = is_k ? bars.k_full : bars.v_full;
+            uint64_t* empty = is_k ? bars.k_empty : bars.v_empty;
+            uint8_t* ring = is_k ? sK : sV;
+            for (int j = 0; j < min(ntiles, kPrefetch); ++j)
+                for (int kb = 0; kb < C::KB; ++kb) tma_prefetch_4d(map, kb * 64, h, t0 + j * kTileKeys, r);
+            int issued = 0;
             for (int j = 0; j < ntiles; ++j) {
-                const int tok = t0 + j * kTileKeys;
-                const int ks = j % kKS, ku = j / kKS;
-                if (ku > 0 && !mbar_wait(&bars.k_empty[ks], (ku - 1) & 1, &abort_sh)) break;
-                mbar_arrive_expect_tx(&bars.k_full[ks], C::kTileBytes);
-#pragma unroll
+                const int st = j % nst, u = j / nst;
+                if (u > 0 && !mbar_wait(&empty[st], (u - 1) & 1, &abort_sh)) break;
+                if (j + kPrefetch < ntiles)
+                    for (int kb = 0; kb < C::KB; ++kb)
+                        tma_prefetch_4d(map, kb * 64, h, t0 + (j + kPrefetch) * kTileKeys, r);
+                mbar_arrive_expect_tx(&full[st], C::kTileBytes);
                 for (int kb = 0; kb < C::KB; ++kb)
-                    tma_load_4d(sK + ks * C::kTileBytes + kb * 16384, &tmap_k, &bars.k_full[ks], kb * 64, h, tok, r);
-                issued_k = j + 1;
-                const int vs = j % kVS, vu = j / kVS;
-                if (vu > 0 && !mbar_wait(&bars.v_empty[vs], (vu - 1) & 1, &abort_sh)) break;
-                mbar_arrive_expect_tx(&bars.v_full[vs], C::kTileBytes);
-#pragma unroll
-                for (int kb = 0; kb < C::KB; ++kb)
-                    tma_load_4d(sV + vs * C::kTileBytes + kb * 16384, &tmap_v, &bars.v_full[vs], kb * 64, h, tok, r);
-                issued_v = j + 1;
+                    tma_load_4d(ring + st * C::kTileBytes + kb * 16384, map, &full[st], kb * 64, h,
+                                t0 + j * kTileKeys, r);
+                issued = j + 1;
             }
             if (abort_sh) {  // let the copies still in flight land before the CTA exits
                 volatile int never = 0;
-                for (int j = max(0, issued_k - kKS); j < issued_k; ++j)
-                    mbar_wait(&bars.k_full[j % kKS], (j / kKS) & 1, &never);
-                for (int j = max(0, issued_v - kVS); j < issued_v; ++j)
-                    mbar_wait(&bars.v_full[j % kVS], (j / kVS) & 1, &never);
+                for (int j = max(0, issued - nst); j < issued; ++j) mbar_wait(&full[j % nst], (j / nst) & 1, &never);
             }
         }
     } else {
@@ -536,10 +490,9 @@ int shared_tc_ctas_for(const Geometry& g) { return g.R * g.Hkv * g.nsplit * ((g.
 
 cudaError_t launch_shared_stage_tc(const Geometry& g, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                    const __nv_bfloat16* q, const int32_t* shared_len, float* part_o,
-                                   float* part_lse, int32_t* status, const __nv_bfloat16* pool_k,
-                                   const __nv_bfloat16* pool_v, const int32_t* beam_tok_idx, void* out, float* lse,
-                                   bool fused, cudaStream_t stream) {
-    FusedArgs fa{pool_k, pool_v, beam_tok_idx, out, lse, fused ? 1 : 0};
+                                   float* part_lse, int32_t* status, void* out, float* lse, bool fused,
+                                   cudaStream_t stream) {
+    FusedArgs fa{out, lse, fused ? 1 : 0};
     if (g.d == 128) return launch_d<128>(g, tmap_k, tmap_v, q, shared_len, part_o, part_lse, status, fa, stream);
     if (g.d == 64) return launch_d<64>(g, tmap_k, tmap_v, q, shared_len, part_o, part_lse, status, fa, stream);
     return cudaErrorInvalidValue;

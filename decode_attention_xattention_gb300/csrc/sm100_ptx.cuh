@@ -13,12 +13,6 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
-
 // ---- mbarrier ------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
@@ -46,20 +40,48 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait on the phase with the given parity. Returns false when it gave up: after
-// `limit_ns` of waiting, or at once when *abort is already set (another role of the CTA
-// gave up first). Never spins forever.
+// `limit_cycles` SM clock cycles of waiting (about 0.25 s at 2 GHz), or soon after *abort is
+// set (another role of the CTA gave up first). Never spins forever. The timeout uses the
+// SM cycle counter, which is cheap to read, and is checked only every 64 polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint64_t limit_ns = 200ull * 1000 * 1000) {
+                                          long long limit_cycles = 500ll * 1000 * 1000) {
     const uint32_t a = smem_addr(bar);
     if (mbar_try_wait(a, parity)) return true;
-    uint64_t t0 = globaltimer_ns();
+    const long long t0 = clock64();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(a, parity)) return true;
         if ((it & 63u) == 0) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > limit_ns) return false;
+            if (clock64() - t0 > limit_cycles) return false;
         }
     }
+}
+
+// Warp-level bounded wait: lane 0 polls, the others then take the (already complete)
+// phase with one try_wait each, which gives every lane the acquire ordering. Fewer
+// pollers leave the shared-memory pipe to the threads doing work. Warp-uniform result.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) (void)mbar_try_wait(smem_addr(bar), parity);
+    return ok != 0;
+}
+
+// L2 prefetch of `bytes` (multiple of 16) starting at a 16-byte aligned global address.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* gmem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gmem)), "r"(bytes)
+                 : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared through the load/store pipe (for gathers of
+// many small rows, which the bulk-copy engine handles poorly), and its completion wait.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void prefetch_l2(const void* gmem) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(gmem) : "memory");
 }
 
 // ---- TMA -----------------------------------------------------------------------------
@@ -75,6 +97,22 @@ __device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* m
         " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_addr(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
         "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Prefetch of a 4-D tile into L2 (no shared memory, no completion tracking).
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
+// Plain bulk copy global -> shared of `bytes` (multiple of 16, both addresses 16-byte
+// aligned), completion signalled on `bar` (complete_tx bytes).
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_addr(smem_dst)), "l"(reinterpret_cast<uint64_t>(gmem_src)), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
 }
 

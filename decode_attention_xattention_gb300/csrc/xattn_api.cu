@@ -11,8 +11,6 @@
 namespace xattn {
 namespace {
 
-constexpr int kSimtMaxRows = 16;  // stacked rows at or below which the CUDA-core stage runs
-
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int device_sms() {
@@ -85,8 +83,12 @@ void plan(const xattn_desc* d, int step, Geometry* g, int* kernel) {
     g->scale_log2 = scale * 1.4426950408889634f;
     g->out_f32 = d->out_dtype == XATTN_DTYPE_F32 ? 1 : 0;
 
+    // Tensor cores by default, even for few stacked rows: a 128-row tile that is mostly
+    // padding still streams the prefix at HBM speed (the MMA and exp work hide under the
+    // loads), which the CUDA-core kernel does not reach. The CUDA-core kernel stays
+    // selectable (shared_kernel = 2).
     int k = 0;
-    if (g->Lmax > 0) k = d->shared_kernel ? d->shared_kernel : (g->M <= kSimtMaxRows ? 2 : 1);
+    if (g->Lmax > 0) k = d->shared_kernel ? d->shared_kernel : 1;
     *kernel = k;
     const int tiles = g->Lmax > 0 ? cdiv(g->Lmax, kTileKeys) : 1;
     if (d->split_tokens > 0) {
@@ -110,7 +112,8 @@ void plan(const xattn_desc* d, int step, Geometry* g, int* kernel) {
     }
     g->nsplit = g->Lmax > 0 ? cdiv(g->Lmax, g->split_tokens) : 0;
     g->ns_pieces = step > kNsDirectMax ? cdiv(step, kNsChunk) : 0;
-    g->pieces = g->nsplit + (g->Tmax > kNsDirectMax ? cdiv(g->Tmax, kNsChunk) : 0);
+    g->pieces = g->nsplit + (g->Tmax > kNsDirectMax ? cdiv(g->Tmax, kNsChunk) : (g->Tmax > 0 ? 1 : 0));
+    g->ns_to_piece = 0;
 }
 
 size_t workspace_bytes_for(const Geometry& g) {
@@ -160,7 +163,8 @@ int xattn_query_plan(const xattn_desc* desc, int32_t step, xattn_plan* out) {
     out->rows_per_unit = g.M;
     out->row_tiles = g.row_tiles;
     out->shared_ctas = k == 0 ? 0 : (k == 1 ? shared_tc_ctas_for(g) : g.R * g.Hkv * ((g.M + 3) / 4) * g.nsplit);
-    out->fused = (k == 1 && g.nsplit == 1 && step <= kMaxFusedSteps) ? 1 : 0;
+    out->fused = decode_is_fused(g, k, step) ? 1 : 0;
+    out->piece_stride = g.pieces;
     out->merge_ctas = out->fused ? 0 : merge_ctas_for(g);
     return XATTN_OK;
 }
@@ -224,9 +228,7 @@ int run_shared(const Geometry& g, int kernel, const void* q, const void* shared_
         CUtensorMap mk, mv;
         if (make_kv_map(&mk, shared_k, g) != CUDA_SUCCESS || make_kv_map(&mv, shared_v, g) != CUDA_SUCCESS)
             return XATTN_ERR_CUDA;
-        e = launch_shared_stage_tc(g, mk, mv, qb, shared_len, ws.part_o, ws.part_lse, ws.status,
-                                   reinterpret_cast<const __nv_bfloat16*>(ns_k_pool),
-                                   reinterpret_cast<const __nv_bfloat16*>(ns_v_pool), beam_tok_idx, out, lse, fused,
+        e = launch_shared_stage_tc(g, mk, mv, qb, shared_len, ws.part_o, ws.part_lse, ws.status, out, lse, fused,
                                    st);
     } else if (kernel == 2) {
         e = launch_shared_stage_simt(g, qb, reinterpret_cast<const __nv_bfloat16*>(shared_k),
@@ -265,9 +267,18 @@ int xattn_decode(const xattn_desc* desc, const void* q, const void* shared_k, co
     if (workspace_bytes < workspace_bytes_for(g)) return XATTN_ERR_WORKSPACE_TOO_SMALL;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const WsView ws = ws_view(workspace, g);
-    if (kernel == 1 && g.nsplit == 1 && step <= kMaxFusedSteps)  // one kernel does all three stages
-        return run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st, true, ns_k_pool, ns_v_pool,
-                          beam_tok_idx, out, lse);
+    if (decode_is_fused(g, kernel, step)) {
+        // Non-Shared part first, as one piece in the workspace; then the Shared stage, whose
+        // epilogue merges it and writes out / lse.
+        if (step > 0) {
+            Geometry gn = g;
+            gn.ns_to_piece = 1;
+            rc = run_merge(gn, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws, st);
+            if (rc != XATTN_OK) return rc;
+        }
+        return run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st, true, nullptr, nullptr, nullptr, out,
+                          lse);
+    }
     rc = run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st);
     if (rc != XATTN_OK) return rc;
     return run_merge(g, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws, st);

@@ -13,7 +13,6 @@ namespace xattn {
 constexpr int kTileRows = 128;   // rows of one tensor-core M tile (stacked beam x head rows)
 constexpr int kTileKeys = 128;   // prefix tokens per K/V tile
 constexpr int kStatusBytes = 256;
-constexpr int kMaxFusedSteps = 16; // Non-Shared tokens the fused Shared-stage epilogue handles
 constexpr int kNsDirectMax = 32;   // up to this many Non-Shared tokens the merge kernel walks them
 constexpr int kNsChunk = 64;       // beyond it, pieces of this many tokens are computed in parallel
 
@@ -34,22 +33,23 @@ struct Geometry {
     int out_f32;      // output dtype: 0 bf16, 1 fp32
     int ns_pieces;    // Non-Shared pieces of this call (0: the merge kernel walks the tokens)
     int pieces;       // piece stride of the workspace: nsplit + Non-Shared pieces for max_steps
+    int ns_to_piece;  // ns_merge_kernel writes the Non-Shared part as piece `nsplit` (no merge)
 };
 
 // Workspace layout: [status (256 B)] [part_o: R*Hkv*pieces*M*d fp32] [part_lse: R*Hkv*pieces*M fp32].
-// Pieces 0 .. nsplit-1 are the prefix pieces, nsplit .. nsplit+ns_pieces-1 the Non-Shared ones.
+// Pieces 0 .. nsplit-1 are the prefix pieces, nsplit .. the Non-Shared ones (one piece when
+// the Non-Shared part is short, else one per kNsChunk ancestry positions).
 inline size_t part_rows(const Geometry& g) { return (size_t)g.R * g.Hkv * g.pieces * g.M; }
 
 // Launchers (each returns cudaGetLastError()).
-// fused = the CTA also runs the Non-Shared stage and the Merge and writes out / lse
-// (requires a single prefix piece and step <= kMaxFusedSteps); otherwise it writes the
+// fused = the CTA merges its (whole-prefix) result with the Non-Shared piece already in the
+// workspace and writes out / lse (requires a single prefix piece); otherwise it writes the
 // piece's partial result into part_o / part_lse.
 cudaError_t launch_shared_stage_tc(const Geometry& g, const CUtensorMap& tmap_k,
                                    const CUtensorMap& tmap_v, const __nv_bfloat16* q,
                                    const int32_t* shared_len, float* part_o, float* part_lse,
-                                   int32_t* status, const __nv_bfloat16* pool_k,
-                                   const __nv_bfloat16* pool_v, const int32_t* beam_tok_idx,
-                                   void* out, float* lse, bool fused, cudaStream_t stream);
+                                   int32_t* status, void* out, float* lse, bool fused,
+                                   cudaStream_t stream);
 cudaError_t launch_shared_stage_simt(const Geometry& g, const __nv_bfloat16* q,
                                      const __nv_bfloat16* shared_k, const __nv_bfloat16* shared_v,
                                      const int32_t* shared_len, float* part_o, float* part_lse,
@@ -66,6 +66,11 @@ cudaError_t launch_beam_update(int R, int BW, int Hkv, int d, int S, int Tmax, i
                                cudaStream_t stream);
 
 int merge_ctas_for(const Geometry& g);
+// Whether xattn_decode runs the Shared stage and the Merge in one tensor-core kernel (after
+// a short Non-Shared kernel when step > 0): one prefix piece and a short Non-Shared part.
+inline bool decode_is_fused(const Geometry& g, int kernel, int step) {
+    return kernel == 1 && g.nsplit == 1 && step <= kNsDirectMax;
+}
 int shared_tc_ctas_for(const Geometry& g);
 
 }  // namespace xattn

@@ -88,15 +88,16 @@ class DeviceBatch:
                                         self.ws_bytes, self.stream)
 
     def partials(self):
-        """(part_o [R, Hkv, nsplit, M, d], part_lse [R, Hkv, nsplit, M]) views of the workspace."""
+        """(part_o [R, Hkv, pieces, M, d], part_lse [R, Hkv, pieces, M]) views of the workspace;
+        pieces 0 .. num_splits-1 are the prefix pieces."""
         p = self.plan()
         w = self.w
-        rows = w.num_requests * w.num_kv_heads * p.num_splits * p.rows_per_unit
+        rows = w.num_requests * w.num_kv_heads * p.piece_stride * p.rows_per_unit
         f = self.workspace.view(torch.float32)
-        po = f[64:64 + rows * w.head_dim].view(w.num_requests, w.num_kv_heads, p.num_splits, p.rows_per_unit,
+        po = f[64:64 + rows * w.head_dim].view(w.num_requests, w.num_kv_heads, p.piece_stride, p.rows_per_unit,
                                                 w.head_dim)
         pl = f[64 + rows * w.head_dim:64 + rows * w.head_dim + rows].view(w.num_requests, w.num_kv_heads,
-                                                                             p.num_splits, p.rows_per_unit)
+                                                                             p.piece_stride, p.rows_per_unit)
         return po, pl
 
     def read_status(self, clear=True) -> int:

@@ -57,7 +57,8 @@ class xattn_plan(ctypes.Structure):
     _fields_ = [("shared_kernel", ctypes.c_int32), ("num_splits", ctypes.c_int32),
                 ("split_tokens", ctypes.c_int32), ("rows_per_unit", ctypes.c_int32),
                 ("row_tiles", ctypes.c_int32), ("shared_ctas", ctypes.c_int32),
-                ("merge_ctas", ctypes.c_int32), ("fused", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("merge_ctas", ctypes.c_int32), ("fused", ctypes.c_int32), ("piece_stride", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
 
 
 _lib = None

@@ -89,8 +89,8 @@ typedef struct xattn_desc {
     int32_t max_steps;      /* Tmax: row length of beam_tok_idx                            */
     float softmax_scale;    /* 0 selects 1/sqrt(d)                                         */
     int32_t dtype;          /* XATTN_DTYPE_BF16 (q, k, v, out)                             */
-    int32_t shared_kernel;  /* Shared-stage kernel: 0 automatic (CUDA cores when BW*G <= 16,
-                               else tensor cores), 1 tensor cores, 2 CUDA cores            */
+    int32_t shared_kernel;  /* Shared-stage kernel: 0 automatic (tensor cores), 1 tensor
+                               cores, 2 CUDA cores                                         */
     int32_t split_tokens;   /* prefix tokens per Shared-stage piece: 0 automatic, else a
                                multiple of 128                                             */
     int32_t out_dtype;      /* dtype of `out`: XATTN_DTYPE_BF16 (0) or XATTN_DTYPE_F32      */
@@ -128,8 +128,8 @@ XATTN_API int xattn_decode(const xattn_desc* desc, const void* q, const void* sh
  * the BW*G query rows of that KV head (row m = b*G + g) against the prefix, cut into
  * pieces of plan.split_tokens tokens, and writes each piece's normalised output and
  * natural-log LSE into the workspace:
- *   part_o   fp32 [R, Hkv, num_splits, M, d]  at byte offset 256
- *   part_lse fp32 [R, Hkv, num_splits, M]     right after part_o
+ *   part_o   fp32 [R, Hkv, piece_stride, M, d]  at byte offset 256 (pieces 0 .. num_splits-1)
+ *   part_lse fp32 [R, Hkv, piece_stride, M]     right after part_o
  * (a piece past shared_len[r] has lse = -inf and output 0). Requires max_shared_len > 0.
  *
  * xattn_decode_merge: the Non-Shared stage (ancestry-indexed gathers of the first `step`
@@ -195,10 +195,12 @@ typedef struct xattn_plan {
     int32_t row_tiles;        /* 128-row tiles per (request, KV head)                    */
     int32_t shared_ctas;      /* CTAs of one Shared-stage launch                         */
     int32_t merge_ctas;       /* CTAs of one Non-Shared + Merge launch (0 when fused)    */
-    int32_t fused;            /* 1: xattn_decode is one tensor-core kernel that also runs
-                                 the Non-Shared stage and the Merge (single prefix piece,
-                                 step <= 16); 0: Shared stage, then Non-Shared + Merge     */
-    int32_t reserved[3];
+    int32_t fused;            /* 1: xattn_decode runs the Non-Shared part as one piece, then
+                                 the Shared-stage kernel, whose epilogue merges (single
+                                 prefix piece, step <= 32); 0: Shared stage, then the
+                                 Non-Shared + Merge kernel(s)                              */
+    int32_t piece_stride;     /* pieces per (request, KV head) in the workspace layout     */
+    int32_t reserved[2];
 } xattn_plan;
 
 XATTN_API int xattn_query_plan(const xattn_desc* desc, int32_t step, xattn_plan* plan);

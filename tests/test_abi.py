@@ -110,7 +110,15 @@ def test_split_plan_covers_prefix(lib):
             assert p.shared_kernel == 1
 
 
-def test_small_row_units_use_cuda_cores(lib):
+def test_kernel_choice(lib):
+    # tensor cores by default, also for plain per-sequence decode (4 stacked rows)
     d = xattn.make_desc(64, 1, 32, 8, 128, 8192, 512, 512)
     rc, p = xattn.xattn_query_plan(d, 512)
-    assert rc == 0 and p.shared_kernel == 2 and p.rows_per_unit == 4
+    assert rc == 0 and p.shared_kernel == 1 and p.rows_per_unit == 4 and p.fused == 0
+    d = xattn.make_desc(64, 1, 32, 8, 128, 8192, 512, 512, 0.0, 2)
+    rc, p = xattn.xattn_query_plan(d, 512)
+    assert rc == 0 and p.shared_kernel == 2
+    # one prefix piece and few Non-Shared tokens: one fused kernel, no merge launch
+    d = xattn.make_desc(8, 128, 32, 8, 128, 2048, 384, 3)
+    rc, p = xattn.xattn_query_plan(d, 3)
+    assert rc == 0 and p.fused == 1 and p.merge_ctas == 0 and p.num_splits == 1
