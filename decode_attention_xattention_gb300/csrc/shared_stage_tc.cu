@@ -1,15 +1,15 @@
 // Shared stage on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), sm_103a,
-// optionally fused with the Non-Shared stage and the Merge.
+// optionally with the Merge in its epilogue.
 //
 // xGR: Efficient Generative Recommendation Serving at Scale, section 2.1 (xAttention): the
 // prompt KV is stored once per request, so the Shared stage serves every beam of a
 // request from one copy; it produces local scores and max/sum statistics that the Merge
 // stage combines with those of the Non-Shared stage by an online softmax. The section fuses
 // the batched matmul with the softmax and pipelines the stages across hardware units; on
-// GB300 that becomes one warp-specialised CTA: a TMA warp streams K/V tiles, an MMA warp
-// drives the tensor core, and two softmax warpgroups turn scores into probabilities
-// between the two matmuls, each on its own 128-row tile so the tensor core always has the
-// other tile's work while one warpgroup computes exponentials.
+// GB300 that becomes one warp-specialised CTA: producer warps stream K/V tiles with TMA, an
+// MMA warp drives the tensor core, and two softmax warpgroups turn scores into
+// probabilities between the two matmuls, each on its own 128-row tile so the tensor core
+// has the other tile's work while one warpgroup computes exponentials.
 //
 // Work unit: (request r, KV head h). All BW beams x G query heads of that KV head are
 // stacked into M = BW*G rows (row m = b*G + g), so one K/V tile read from HBM feeds every
@@ -56,7 +56,6 @@ constexpr uint32_t kNaN = 0x7fc00000u;
 // K/V pipeline depth: K is consumed one tile before V, so K gets the deeper ring
 // (3 + 2 stages at d = 128, 4 + 4 at d = 64). Either way the shared memory admits one CTA
 // per SM, so a CTA never waits for another's 512 TMEM columns.
-//
 template <int D>
 struct Cfg {
     static constexpr int kKStages = D == 64 ? 4 : 3;
@@ -132,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     const int L = bad_len ? 0 : L_raw;
     const int t0 = c * g.split_tokens;
     const int t1 = min(t0 + g.split_tokens, L);
-    const int ntiles = t1 > t0 ? (t1 - t0 + kTileKeys - 1) / kTileKeys : 0;
+    const int ntiles = t1 > t0 ? (t1 - t0 + kTcTileKeys - 1) / kTcTileKeys : 0;
     const int ntile_m = (2 * mp + 1 < g.row_tiles) ? 2 : 1;  // row tiles this CTA owns
 
     if (tid == 0) {
@@ -151,7 +150,6 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         }
         mbar_init(&bars.o_full, 1);
         mbar_init(&bars.final_mma, 1);
-
         abort_sh = 0;
         fence_barrier_init();
     }
@@ -195,13 +193,13 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             for (int j = 0; j < ntiles; ++j) {
                 if (!mbar_wait_warp(&bars.s_full[wg], j & 1, &abort_sh)) { ok = false; break; }
                 tc_fence_after();
-                const int lim = t1 - (t0 + j * kTileKeys);  // valid columns of this tile (>= 1)
+                const int lim = t1 - (t0 + j * kTcTileKeys);  // valid columns of this tile (>= 1)
                 // the whole 128-column row of S in registers: four loads, one wait
                 uint32_t s[4][32];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) tmem_ld32(tS + k * 32, s[k]);
                 tmem_wait_ld();
-                if (lim < kTileKeys) {  // ragged last tile: columns past the prefix get -inf
+                if (lim < kTcTileKeys) {  // ragged last tile: columns past the prefix get -inf
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
 #pragma unroll
@@ -378,18 +376,18 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             uint64_t* empty = is_k ? bars.k_empty : bars.v_empty;
             uint8_t* ring = is_k ? sK : sV;
             for (int j = 0; j < min(ntiles, kPrefetch); ++j)
-                for (int kb = 0; kb < C::KB; ++kb) tma_prefetch_4d(map, kb * 64, h, t0 + j * kTileKeys, r);
+                for (int kb = 0; kb < C::KB; ++kb) tma_prefetch_4d(map, kb * 64, h, t0 + j * kTcTileKeys, r);
             int issued = 0;
             for (int j = 0; j < ntiles; ++j) {
                 const int st = j % nst, u = j / nst;
                 if (u > 0 && !mbar_wait(&empty[st], (u - 1) & 1, &abort_sh)) break;
                 if (j + kPrefetch < ntiles)
                     for (int kb = 0; kb < C::KB; ++kb)
-                        tma_prefetch_4d(map, kb * 64, h, t0 + (j + kPrefetch) * kTileKeys, r);
+                        tma_prefetch_4d(map, kb * 64, h, t0 + (j + kPrefetch) * kTcTileKeys, r);
                 mbar_arrive_expect_tx(&full[st], C::kTileBytes);
                 for (int kb = 0; kb < C::KB; ++kb)
                     tma_load_4d(ring + st * C::kTileBytes + kb * 16384, map, &full[st], kb * 64, h,
-                                t0 + j * kTileKeys, r);
+                                t0 + j * kTcTileKeys, r);
                 issued = j + 1;
             }
             if (abort_sh) {  // let the copies still in flight land before the CTA exits
@@ -400,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     } else {
         // ============================================ MMA issuer
         if (lane == 0 && ntiles > 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kTileKeys, 0, 0);
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kTcTileKeys, 0, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
             bool ok = mbar_wait(&bars.q_ready[0], 0, &abort_sh);
             if (ok && ntile_m > 1) ok = mbar_wait(&bars.q_ready[1], 0, &abort_sh);
@@ -408,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             auto issue_pv = [&](int i, int jt, int vs) {
                 const uint32_t vbase = smem_addr(sV + vs * C::kTileBytes);
 #pragma unroll
-                for (int kk = 0; kk < kTileKeys / 16; ++kk) {
+                for (int kk = 0; kk < kTcTileKeys / 16; ++kk) {
                     const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, 16384, 1024);
                     mma_ts(tmem + kTmemO + i * 128, tmem + i * 128 + kk * 8, bd, idesc_pv, (jt > 0 || kk > 0) ? 1u : 0u);
                 }

@@ -46,7 +46,7 @@ int check_desc(const xattn_desc* d) {
     if (d->num_q_heads % d->num_kv_heads != 0) return XATTN_ERR_INVALID_ARG;
     if (d->max_shared_len < 0 || d->ns_slots < 0 || d->max_steps < 0) return XATTN_ERR_INVALID_ARG;
     if (!(d->softmax_scale >= 0.f) || !std::isfinite(d->softmax_scale)) return XATTN_ERR_INVALID_ARG;
-    if (d->split_tokens < 0 || d->split_tokens % kTileKeys != 0) return XATTN_ERR_INVALID_ARG;
+    if (d->split_tokens < 0 || d->split_tokens % kPieceGrain != 0) return XATTN_ERR_INVALID_ARG;
     if (d->shared_kernel < 0 || d->shared_kernel > 2) return XATTN_ERR_INVALID_ARG;
     if (d->dtype != XATTN_DTYPE_BF16) return XATTN_ERR_UNSUPPORTED;
     if (d->out_dtype != XATTN_DTYPE_BF16 && d->out_dtype != XATTN_DTYPE_F32) return XATTN_ERR_UNSUPPORTED;
@@ -90,11 +90,11 @@ void plan(const xattn_desc* d, int step, Geometry* g, int* kernel) {
     int k = 0;
     if (g->Lmax > 0) k = d->shared_kernel ? d->shared_kernel : 1;
     *kernel = k;
-    const int tiles = g->Lmax > 0 ? cdiv(g->Lmax, kTileKeys) : 1;
+    const int tiles = g->Lmax > 0 ? cdiv(g->Lmax, kPieceGrain) : 1;
     if (d->split_tokens > 0) {
         g->split_tokens = d->split_tokens;
     } else if (k == 0) {
-        g->split_tokens = kTileKeys;
+        g->split_tokens = kPieceGrain;
     } else {
         // tensor-core CTAs own two 128-row tiles; CUDA-core CTAs own four rows
         const int64_t units = (int64_t)g->R * g->Hkv * (k == 1 ? cdiv(g->row_tiles, 2) : cdiv(g->M, 4));
@@ -108,7 +108,7 @@ void plan(const xattn_desc* d, int step, Geometry* g, int* kernel) {
             const double cost = waves * (per + 1.0) + 0.02 * n;  // small charge for merge traffic
             if (cost < best) { best = cost; best_n = n; }
         }
-        g->split_tokens = cdiv(tiles, best_n) * kTileKeys;
+        g->split_tokens = cdiv(tiles, best_n) * kPieceGrain;
     }
     g->nsplit = g->Lmax > 0 ? cdiv(g->Lmax, g->split_tokens) : 0;
     g->ns_pieces = step > kNsDirectMax ? cdiv(step, kNsChunk) : 0;
@@ -127,7 +127,7 @@ CUresult make_kv_map(CUtensorMap* map, const void* base, const Geometry& g) {
     // [R, Lmax, Hkv, d] viewed innermost-first as {d, Hkv, Lmax, R}; box = 64 x 1 x 128 x 1.
     cuuint64_t dims[4] = {(cuuint64_t)g.d, (cuuint64_t)g.Hkv, (cuuint64_t)g.Lmax, (cuuint64_t)g.R};
     cuuint64_t strides[3] = {(cuuint64_t)g.d * 2, (cuuint64_t)g.Hkv * g.d * 2, (cuuint64_t)g.Lmax * g.Hkv * g.d * 2};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)kTileKeys, 1};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)kTcTileKeys, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

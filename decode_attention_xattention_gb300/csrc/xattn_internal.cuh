@@ -11,7 +11,8 @@
 namespace xattn {
 
 constexpr int kTileRows = 128;   // rows of one tensor-core M tile (stacked beam x head rows)
-constexpr int kTileKeys = 128;   // prefix tokens per K/V tile
+constexpr int kPieceGrain = 128; // prefix pieces are whole multiples of this many tokens
+constexpr int kTcTileKeys = 128; // prefix tokens per K/V tile of the tensor-core kernel (TMA box)
 constexpr int kStatusBytes = 256;
 constexpr int kNsDirectMax = 32;   // up to this many Non-Shared tokens the merge kernel walks them
 constexpr int kNsChunk = 64;       // beyond it, pieces of this many tokens are computed in parallel
