@@ -79,6 +79,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // Byte offset of 16-byte chunk `ch` (along the contraction dim) of row `row` in a tile
 // stored as [ch/8 block][128 rows][128 B] with the 128-byte swizzle (chunk ^= row % 8).
 __device__ __forceinline__ uint32_t sw128_offset(int row, int ch) {
@@ -88,7 +94,7 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int ch) {
 struct Bars {
     uint64_t k_full[kMaxStages], k_empty[kMaxStages], v_full[kMaxStages], v_empty[kMaxStages];
     uint64_t s_full[2], p_full[2], q_ready[2];
-    uint64_t o_full, final_mma;
+    uint64_t o_full[2], final_mma;
 };
 
 // Fused epilogue: fold the Non-Shared piece (written into the workspace by the
@@ -145,10 +151,11 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars.s_full[i], 1);
-            mbar_init(&bars.p_full[i], 128);
+            mbar_init(&bars.p_full[i], 4);
             mbar_init(&bars.q_ready[i], 128);
         }
-        mbar_init(&bars.o_full, 1);
+        mbar_init(&bars.o_full[0], 1);
+        mbar_init(&bars.o_full[1], 1);
         mbar_init(&bars.final_mma, 1);
         abort_sh = 0;
         fence_barrier_init();
@@ -194,53 +201,45 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 if (!mbar_wait_warp(&bars.s_full[wg], j & 1, &abort_sh)) { ok = false; break; }
                 tc_fence_after();
                 const int lim = t1 - (t0 + j * kTcTileKeys);  // valid columns of this tile (>= 1)
-                // the whole 128-column row of S in registers: four loads, one wait
-                uint32_t s[4][32];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) tmem_ld32(tS + k * 32, s[k]);
+                // the whole 128-column row of S in registers with one wide load
+                uint32_t s[kTcTileKeys];
+                tmem_ld128(tS, s);
                 tmem_wait_ld();
                 if (lim < kTcTileKeys) {  // ragged last tile: columns past the prefix get -inf
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (k * 32 + i >= lim) s[k][i] = 0xff800000u;
+                    for (int i = 0; i < kTcTileKeys; ++i)
+                        if (i >= lim) s[i] = 0xff800000u;
                 }
                 float mx;
-                {
+                {  // row max: eight independent chains of three-input max
                     float m8[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        m8[i] = fmaxf(fmaxf(__uint_as_float(s[0][i]), __uint_as_float(s[0][i + 8])),
-                                      fmaxf(__uint_as_float(s[0][i + 16]), __uint_as_float(s[0][i + 24])));
+                    for (int u = 0; u < 8; ++u) m8[u] = fmaxf(__uint_as_float(s[2 * u]), __uint_as_float(s[2 * u + 1]));
 #pragma unroll
-                    for (int k = 1; k < 4; ++k)
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            m8[i] = fmaxf(m8[i], fmaxf(fmaxf(__uint_as_float(s[k][i]), __uint_as_float(s[k][i + 8])),
-                                                      fmaxf(__uint_as_float(s[k][i + 16]), __uint_as_float(s[k][i + 24]))));
-                    mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                    for (int i = 8; i < kTcTileKeys / 2; ++i)
+                        m8[i & 7] = max3(m8[i & 7], __uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
+                    mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
                 }
                 const float m_new = fmaxf(m_run, mx * g.scale_log2);
                 const bool resc = m_new > m_run + kRescaleThreshold;
                 const float alpha = resc ? ex2(m_run - m_new) : 1.f;
                 const float m_use = resc ? m_new : m_run;
-                const float neg_m = -m_use;
                 // P = exp2(S*scale*log2e - m) as bf16, written over the consumed S columns
+                // (columns past the prefix hold -inf, so their P is exactly 0).
+                const float neg_m = -m_use;
                 float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t p[kTcTileKeys / 2];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    uint32_t p[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float p0 = ex2(fmaf(__uint_as_float(s[k][2 * i]), g.scale_log2, neg_m));
-                        const float p1 = ex2(fmaf(__uint_as_float(s[k][2 * i + 1]), g.scale_log2, neg_m));
-                        sum4[i & 3] += p0 + p1;
-                        p[i] = pack_bf16(p0, p1);
-                    }
-                    tmem_st16(tS + k * 16, p);
+                for (int i = 0; i < kTcTileKeys / 2; ++i) {
+                    const float x0 = fmaf(__uint_as_float(s[2 * i]), g.scale_log2, neg_m);
+                    const float x1 = fmaf(__uint_as_float(s[2 * i + 1]), g.scale_log2, neg_m);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    sum4[i & 3] += p0 + p1;
+                    p[i] = pack_bf16(p0, p1);
                 }
-                l_run = l_run * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+                tmem_st64(tS, p);
+                const float tile_sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+                l_run = l_run * alpha + tile_sum;
                 m_run = m_use;
                 if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
@@ -255,9 +254,29 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&bars.p_full[wg]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.p_full[wg]);  // one arrival per warp
             }
-            if (ok && !mbar_wait_warp(&bars.o_full, 0, &abort_sh)) ok = false;
+        }
+        const uint32_t tO = tmem + ((uint32_t)((warp & 3) * 32) << 16) + kTmemO + wg * 128;
+        const bool have_o = tile_ok && ntiles > 0;  // O_i holds accumulated P.V (TMEM allocated)
+
+        // Fused path: the Non-Shared piece of this row (LSE and the first half of its output
+        // row) is loaded before the wait for the last P.V, so the two latencies overlap.
+        const bool fused_ns = fa.enabled && row_ok && g.step > 0;
+        const size_t nsrow = ((size_t)unit * g.pieces + g.nsplit) * g.M + row;
+        const float4* pn = reinterpret_cast<const float4*>(part_o + nsrow * D);
+        float lns = -INFINITY;
+        float4 nq[2][8];
+        if (fused_ns) {
+            lns = __ldg(part_lse + nsrow);
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) nq[u][i] = __ldg(pn + u * 8 + i);
+        }
+        if (have_o) {
+            if (ok && !mbar_wait_warp(&bars.o_full[wg], 0, &abort_sh)) ok = false;
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
             if (!ok) {
@@ -265,8 +284,6 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 if (lane == 0) set_status(status, XATTN_STATUS_TIMEOUT);
             }
         }
-        const uint32_t tO = tmem + ((uint32_t)((warp & 3) * 32) << 16) + kTmemO + wg * 128;
-        const bool have_o = tile_ok && ntiles > 0;  // O_i holds accumulated P.V (TMEM allocated)
 
         if (fa.enabled) {
             // ---------------------------------------- Merge with the Non-Shared piece
@@ -275,10 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             bool bad = !ok || bad_len;
             if (tile_ok && rloc == 0 && mt == 0 && h == 0 && bad_len) set_status(status, XATTN_STATUS_BAD_SHARED_LEN);
             const size_t qrow = ((size_t)r * g.BW + b) * g.Hq + (size_t)h * g.G + gg;
-            const size_t nsrow = ((size_t)unit * g.pieces + g.nsplit) * g.M + row;
             float m_tot = m_run, w_ns = 0.f, alpha = 1.f;
-            if (row_ok && g.step > 0) {
-                const float lns = __ldg(part_lse + nsrow);
+            if (fused_ns) {
                 if (lns != lns) bad = true;  // a bad ancestry slot was reported by the Non-Shared kernel
                 const float s_ns = lns * 1.4426950408889634f;
                 m_tot = fmaxf(m_run, s_ns);
@@ -293,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             bad = bad || !(l_tot > 0.f);
             const float inv = bad ? __uint_as_float(kNaN) : 1.f / l_tot;
             const size_t obase = qrow * D;
-#pragma unroll 1
+#pragma unroll
             for (int k = 0; k < D / 32; ++k) {
                 uint32_t o[32];
                 if (have_o) {
@@ -303,21 +318,24 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = 0u;
                 }
-                if (row_ok) {
-                    float of[32];
+                float of[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) of[i] = __uint_as_float(o[i]) * alpha;
-                    if (w_ns != 0.f) {
-                        const float4* pn = reinterpret_cast<const float4*>(part_o + nsrow * D + k * 32);
+                for (int i = 0; i < 32; ++i) of[i] = __uint_as_float(o[i]) * alpha;
+                if (w_ns != 0.f) {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float4 v = __ldg(pn + i);
-                            of[4 * i] = fmaf(w_ns, v.x, of[4 * i]);
-                            of[4 * i + 1] = fmaf(w_ns, v.y, of[4 * i + 1]);
-                            of[4 * i + 2] = fmaf(w_ns, v.z, of[4 * i + 2]);
-                            of[4 * i + 3] = fmaf(w_ns, v.w, of[4 * i + 3]);
-                        }
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 v = nq[k & 1][i];
+                        of[4 * i] = fmaf(w_ns, v.x, of[4 * i]);
+                        of[4 * i + 1] = fmaf(w_ns, v.y, of[4 * i + 1]);
+                        of[4 * i + 2] = fmaf(w_ns, v.z, of[4 * i + 2]);
+                        of[4 * i + 3] = fmaf(w_ns, v.w, of[4 * i + 3]);
                     }
+                }
+                if (fused_ns && k + 2 < D / 32) {  // refill this buffer with quarter k + 2
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) nq[k & 1][i] = __ldg(pn + (k + 2) * 8 + i);
+                }
+                if (row_ok) {
                     if (g.out_f32) {
                         float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(fa.out) + obase + k * 32);
 #pragma unroll
@@ -403,10 +421,18 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             bool ok = mbar_wait(&bars.q_ready[0], 0, &abort_sh);
             if (ok && ntile_m > 1) ok = mbar_wait(&bars.q_ready[1], 0, &abort_sh);
             tc_fence_after();
+            // The last tile may be ragged: its P columns past the prefix are exact zeros, the
+            // P.V product stops at the 16-token step holding the last valid token, and the
+            // V rows of that step past the prefix are zeroed, so whatever the cache holds
+            // there (even NaN) never reaches O.
+            const int lim_last = t1 - (t0 + (ntiles - 1) * kTcTileKeys);
+            const int pv_steps_last = (lim_last + 15) / 16;
             auto issue_pv = [&](int i, int jt, int vs) {
                 const uint32_t vbase = smem_addr(sV + vs * C::kTileBytes);
+                const int nk = jt == ntiles - 1 ? pv_steps_last : kTcTileKeys / 16;
 #pragma unroll
                 for (int kk = 0; kk < kTcTileKeys / 16; ++kk) {
+                    if (kk >= nk) break;
                     const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, 16384, 1024);
                     mma_ts(tmem + kTmemO + i * 128, tmem + i * 128 + kk * 8, bd, idesc_pv, (jt > 0 || kk > 0) ? 1u : 0u);
                 }
@@ -416,6 +442,18 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             for (int j = 0; ok && j <= ntiles; ++j) {
                 const int vs = (j - 1) % kVS;  // used only when j > 0
                 if (j > 0 && !mbar_wait(&bars.v_full[vs], ((j - 1) / kVS) & 1, &abort_sh)) { ok = false; break; }
+                if (j == ntiles && (lim_last & 15) != 0) {
+                    // zero V rows lim_last .. end of their 16-token step (whole 128-byte rows,
+                    // so the swizzle does not matter), then make them visible to the tensor core
+                    uint8_t* vt = sV + vs * C::kTileBytes;
+                    for (int row = lim_last; row < pv_steps_last * 16; ++row)
+#pragma unroll
+                        for (int kb = 0; kb < C::KB; ++kb)
+#pragma unroll
+                            for (int ch = 0; ch < 8; ++ch)
+                                *reinterpret_cast<uint4*>(vt + kb * 16384 + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+                    fence_proxy_async_smem();
+                }
                 const int ks = j % kKS;
                 bool k_ready = false;
                 for (int i = 0; i < ntile_m; ++i) {
@@ -423,6 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                         if (!mbar_wait(&bars.p_full[i], (j - 1) & 1, &abort_sh)) { ok = false; break; }
                         tc_fence_after();
                         issue_pv(i, j - 1, vs);
+                        if (j == ntiles) mma_commit(&bars.o_full[i]);  // O_i complete
                     }
                     if (j < ntiles) {
                         if (!k_ready) {
@@ -445,7 +484,6 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 if (j < ntiles) mma_commit(&bars.k_empty[ks]);
                 if (j > 0) mma_commit(&bars.v_empty[vs]);
             }
-            if (ok) mma_commit(&bars.o_full);
             if (!ok) {
                 abort_sh = 1;
                 set_status(status, XATTN_STATUS_TIMEOUT);

@@ -105,6 +105,30 @@ def test_shared_only_and_ns_only():
 
 
 @pytest.mark.parametrize("kernel", [1, 2], ids=["tensor_core", "cuda_core"])
+@pytest.mark.parametrize("split", [0, 256])
+def test_cache_past_prefix_is_never_read(kernel, split):
+    """Prefix-cache positions at or past a request's shared length may hold anything (here
+    NaN and inf, in the ragged last tile and beyond): they take no part in the result."""
+    w = wl.custom(R=3, BW=6, Hq=8, Hkv=2, d=128, lens=(1000, 300, 129), T=2, seed=23, lmax=1024)
+    inp = wl.make_inputs(w).as_bf16()
+    orc = oracle.load()
+    db = DeviceBatch(inp, shared_kernel=kernel, split_tokens=split, out_fp32=True)
+    for r, L in enumerate(inp.shared_len):
+        db.shared_k[r, int(L):] = float("nan")
+        db.shared_v[r, int(L):] = float("nan")
+        db.shared_v[r, int(L) + 1::2] = float("inf")
+    db.build_cache()
+    xattn.check(db.decode())
+    torch.cuda.synchronize()
+    assert db.read_status() == 0
+    pk, pv, idx = oracle.build_cache(orc, inp)
+    ref_o, ref_l = orc.decode(oracle.dims_of(w), inp.q, inp.shared_k, inp.shared_v, inp.shared_len, pk, pv, idx,
+                              w.steps)
+    compare(db.out.float().cpu().numpy().reshape(-1, w.head_dim), db.lse.cpu().numpy().reshape(-1), ref_o, ref_l,
+            "poisoned cache tail")
+
+
+@pytest.mark.parametrize("kernel", [1, 2], ids=["tensor_core", "cuda_core"])
 def test_shared_stage_pieces_match_oracle_partials(kernel):
     """xattn_decode_shared alone: every prefix piece's (normalised output, lse) against the
     oracle's attention restricted to that piece's tokens."""
