@@ -29,6 +29,7 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kNsTok = 2;  // Non-Shared tokens per round of the direct walk
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kNaN = 0x7fc00000u;
 
@@ -93,6 +94,121 @@ struct RowState {
     }
 };
 
+// Non-Shared stage of one (request r, beam b, KV head h) warp: online softmax over the
+// beam's ancestry tokens (step <= 32 of them), kNsTok tokens per round: their K/V rows are
+// loaded together, the kNsTok x G partial dot products are reduced across the warp in one
+// interleaved butterfly, and the running state takes one rescale per round. Lanes split the
+// head dimension. Returns false (status BAD_SLOT) when an ancestry slot is out of range.
+template <int D, int G>
+__device__ __forceinline__ bool ns_walk(const Geometry& g, int r, int b, int h, int lane,
+                                        const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ pool_k,
+                                        const __nv_bfloat16* __restrict__ pool_v, const int32_t* __restrict__ idx,
+                                        RowState<D / 32, G>& st, int32_t* status) {
+    constexpr int E = D / 32;
+    const size_t qrow0 = ((size_t)r * g.BW + b) * g.Hq + (size_t)h * G;
+    const int32_t* row_idx = idx + ((size_t)r * g.BW + b) * g.Tmax;
+    const int my_slot = lane < g.step ? __ldg(row_idx + lane) : 0;
+    float qv[G][E];
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) LaneVec<D>::load(q + (qrow0 + gg) * D + lane * E, qv[gg]);
+    if (__any_sync(0xffffffffu, lane < g.step && (my_slot < 0 || my_slot >= g.S))) {
+        if (lane == 0) set_status(status, XATTN_STATUS_BAD_SLOT);
+        return false;
+    }
+    for (int i0 = 0; i0 < g.step; i0 += kNsTok) {
+        float kv[kNsTok][E], vv[kNsTok][E];
+#pragma unroll
+        for (int u = 0; u < kNsTok; ++u) {
+            const int slot = __shfl_sync(0xffffffffu, my_slot, (i0 + u) & 31);
+            if (i0 + u < g.step) {
+                const size_t off = (((size_t)r * g.S + slot) * g.Hkv + h) * D + lane * E;
+                LaneVec<D>::load(pool_k + off, kv[u]);
+                LaneVec<D>::load(pool_v + off, vv[u]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) kv[u][e] = vv[u][e] = 0.f;
+            }
+        }
+        float sc[kNsTok][G];
+#pragma unroll
+        for (int u = 0; u < kNsTok; ++u)
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg) {
+                float t = 0.f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) t = fmaf(qv[gg][e], kv[u][e], t);
+                sc[u][gg] = t;
+            }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int u = 0; u < kNsTok; ++u)
+#pragma unroll
+                for (int gg = 0; gg < G; ++gg) sc[u][gg] += __shfl_xor_sync(0xffffffffu, sc[u][gg], o);
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+            float s2[kNsTok];
+            float mx = st.m[gg];
+#pragma unroll
+            for (int u = 0; u < kNsTok; ++u) {
+                s2[u] = (i0 + u < g.step) ? sc[u][gg] * g.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, s2[u]);
+            }
+            const float alpha = ex2(st.m[gg] - mx);
+            float psum = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) st.acc[gg][e] *= alpha;
+#pragma unroll
+            for (int u = 0; u < kNsTok; ++u) {
+                const float p = ex2(s2[u] - mx);
+                psum += p;
+#pragma unroll
+                for (int e = 0; e < E; ++e) st.acc[gg][e] = fmaf(p, vv[u][e], st.acc[gg][e]);
+            }
+            st.l[gg] = st.l[gg] * alpha + psum;
+            st.m[gg] = mx;
+        }
+    }
+    return true;
+}
+
+// Non-Shared part alone of one (request, beam, KV head), stored as piece `nsplit` of the
+// workspace for the Shared-stage kernel to merge (its epilogue also reports prefix-length
+// problems and empty rows). Kept apart from ns_merge_kernel so that it needs few registers
+// and many warps stay resident to cover the two dependent loads (ancestry slot, then K/V).
+template <int D, int G>
+__global__ void __launch_bounds__(256, G * D <= 256 ? 4 : (G * D <= 512 ? 3 : (G <= 8 ? 2 : 1))) ns_piece_kernel(
+    Geometry g, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ pool_k,
+    const __nv_bfloat16* __restrict__ pool_v, const int32_t* __restrict__ idx, float* __restrict__ part_o,
+    float* __restrict__ part_lse, int32_t* status) {
+    constexpr int E = D / 32;
+    const int lane = threadIdx.x & 31;
+    const long warp_id = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (warp_id >= (long)g.R * g.BW * g.Hkv) return;
+    const int h = (int)(warp_id % g.Hkv);
+    const int b = (int)((warp_id / g.Hkv) % g.BW);
+    const int r = (int)(warp_id / ((long)g.Hkv * g.BW));
+    RowState<E, G> st;
+    st.init();
+    const bool slot_bad = g.step > 0 && !ns_walk<D, G>(g, r, b, h, lane, q, pool_k, pool_v, idx, st, status);
+    const size_t prow = (((size_t)r * g.Hkv + h) * g.pieces + g.nsplit) * g.M + (size_t)b * G;
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) {
+        const bool empty = !(st.l[gg] > 0.f);
+        const float inv = empty ? 0.f : 1.f / st.l[gg];
+        float* po = part_o + (prow + gg) * D + lane * E;
+        if constexpr (E == 4) {
+            *reinterpret_cast<float4*>(po) =
+                make_float4(st.acc[gg][0] * inv, st.acc[gg][1] * inv, st.acc[gg][2] * inv, st.acc[gg][3] * inv);
+        } else {
+            *reinterpret_cast<float2*>(po) = make_float2(st.acc[gg][0] * inv, st.acc[gg][1] * inv);
+        }
+        if (lane == 0)
+            part_lse[prow + gg] = slot_bad ? __uint_as_float(kNaN)
+                                           : (empty ? -INFINITY : (st.m[gg] + __log2f(st.l[gg])) * kLn2);
+    }
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(256) ns_merge_kernel(
     Geometry g, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ pool_k,
@@ -124,56 +240,9 @@ __global__ void __launch_bounds__(256) ns_merge_kernel(
     RowState<E, G> st;
     st.init();
     bool slot_bad = false;
-    if (g.ns_to_piece) bad = false;  // the Shared-stage kernel reports prefix problems
-    if (g.ns_pieces == 0 && g.step > 0 && !bad) {
-        // Non-Shared stage: online softmax over the beam's ancestry tokens.
-        float qv[G][E];
-#pragma unroll
-        for (int gg = 0; gg < G; ++gg) LaneVec<D>::load(q + (qrow0 + gg) * D + lane * E, qv[gg]);
-        const int32_t* row_idx = idx + ((size_t)r * g.BW + b) * g.Tmax;
-        const int my_slot = lane < g.step ? __ldg(row_idx + lane) : 0;  // step <= 32 here
-        for (int i = 0; i < g.step; ++i) {
-            const int slot = __shfl_sync(0xffffffffu, my_slot, i);
-            if (slot < 0 || slot >= g.S) {
-                bad = true;
-                slot_bad = true;
-                if (lane == 0) set_status(status, XATTN_STATUS_BAD_SLOT);
-                break;
-            }
-            const size_t off = (((size_t)r * g.S + slot) * g.Hkv + h) * D + lane * E;
-            float kv[E], vv[E];
-            LaneVec<D>::load(pool_k + off, kv);
-            LaneVec<D>::load(pool_v + off, vv);
-#pragma unroll
-            for (int gg = 0; gg < G; ++gg) {
-                float s = 0.f;
-#pragma unroll
-                for (int e = 0; e < E; ++e) s = fmaf(qv[gg][e], kv[e], s);
-                st.add(gg, warp_sum(s) * g.scale_log2, vv);
-            }
-        }
-    }
-
-    if (g.ns_to_piece) {
-        // The Non-Shared part alone, stored as piece `nsplit` for the Shared-stage kernel
-        // to merge (its epilogue also reports prefix-length problems and empty rows).
-        const size_t prow = (((size_t)r * g.Hkv + h) * g.pieces + g.nsplit) * g.M + (size_t)b * G;
-#pragma unroll
-        for (int gg = 0; gg < G; ++gg) {
-            const bool empty = !(st.l[gg] > 0.f);
-            const float inv = empty ? 0.f : 1.f / st.l[gg];
-            float* po = part_o + (prow + gg) * D + lane * E;
-            if constexpr (E == 4) {
-                *reinterpret_cast<float4*>(po) =
-                    make_float4(st.acc[gg][0] * inv, st.acc[gg][1] * inv, st.acc[gg][2] * inv, st.acc[gg][3] * inv);
-            } else {
-                *reinterpret_cast<float2*>(po) = make_float2(st.acc[gg][0] * inv, st.acc[gg][1] * inv);
-            }
-            if (lane == 0)
-                part_lse[prow + gg] = slot_bad ? __uint_as_float(kNaN)
-                                               : (empty ? -INFINITY : (st.m[gg] + __log2f(st.l[gg])) * kLn2);
-        }
-        return;
+    if (g.ns_pieces == 0 && g.step > 0 && !bad && !ns_walk<D, G>(g, r, b, h, lane, q, pool_k, pool_v, idx, st, status)) {
+        bad = true;
+        slot_bad = true;
     }
 
     // Merge: fold every stored piece (prefix pieces, then Non-Shared pieces) into the
@@ -475,7 +544,9 @@ cudaError_t launch_d(const Geometry& g, cudaStream_t st, const __nv_bfloat16* q,
     switch (g.G) {
 #define XATTN_G(GV)                                                                                              \
     case GV:                                                                                                     \
-        if (g.ns_pieces > 0) {                                                                                   \
+        if (g.ns_to_piece) {                                                                                     \
+            ns_piece_kernel<D, GV><<<grid, block, 0, st>>>(g, q, pk, pv, idx, po, pl, status);                  \
+        } else if (g.ns_pieces > 0) {                                                                            \
             ns_partial_kernel<D, GV><<<(unsigned)part_ctas, kPartWarps * 32, 0, st>>>(g, q, pk, pv, idx, po, pl, \
                                                                                        status);                 \
             merge_rows_kernel<D><<<rows_ctas, block, 0, st>>>(g, slen, po, pl, out, lse, status);               \
