@@ -203,6 +203,19 @@ def profile_traffic(kernel_file: str, workload: str):
     return traffic if (traffic is not None and src_sha == sha) else None
 
 
+def launches_per_step(plan, step):
+    """Kernels of this library launched by one timed step: the beam update, then the
+    decode (Non-Shared piece kernel + Shared stage with merging epilogue when fused; else
+    the Shared stage, if the prefix has storage, and the Non-Shared/Merge kernel, or the
+    Non-Shared piece and row-merge kernels when the Non-Shared part is long)."""
+    n = 1
+    if plan.fused:
+        n += (1 if step > 0 else 0) + 1
+    else:
+        n += (1 if plan.shared_kernel != 0 else 0) + (2 if step > 32 else 1)
+    return n
+
+
 # ----------------------------------------------------------------------------------------
 def cpu_oracle_sample(w, inp, budget_s, rows_override=None):
     """Times the fp64 oracle (as it stands, all host cores) on whole beams of request 0
@@ -495,9 +508,11 @@ def main():
                      "note": ("decode = Non-Shared piece kernel + Shared-stage kernel with merging epilogue"
                               if plan.fused else "decode = Shared-stage kernel + Non-Shared/Merge kernel")},
         "hbm": {"unique_bytes_per_step": ub, "parts": ub_parts, "achieved_gbs": hbm_gbs,
-                "frac_of_8tbs": hbm_gbs / NOMINAL_HBM_GBS, "frac_of_measured": hbm_gbs / peaks["hbm_gbs"]},
+                "frac_of_8tbs": hbm_gbs / NOMINAL_HBM_GBS, "frac_of_peak": hbm_gbs / peaks["hbm_gbs"],
+                "peak_gbs": peaks["hbm_gbs"], "peak_source": peak_src},
         "tensor": {"shared_stage_flops": flops, "achieved_tflops": flops / s_shared / 1e12,
-                   "frac_of_peak": flops / s_shared / 1e12 / peaks["bf16_tflops"]},
+                   "frac_of_peak": flops / s_shared / 1e12 / peaks["bf16_tflops"],
+                   "peak_tflops": peaks["bf16_tflops"], "peak_source": peak_src},
         "binding_roofline_frac": max(ub / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12)) / step_s,
         "roofline": {"kernel": kernel_file.replace(".cu", ""), "bound": bound, "achieved": achieved, "peak": peak,
                      "unit": unit, "frac": achieved / peak, "traffic": traffic,
@@ -506,7 +521,7 @@ def main():
         "e2e": {"value": whole_job_beams_per_s(w.num_beams, world, ms_e2e), "unit": "beams/s",
                 "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
-        "gpu_launches": 3 * K,
+        "gpu_launches": launches_per_step(plan, T) * K,
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

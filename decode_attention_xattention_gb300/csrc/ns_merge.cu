@@ -174,38 +174,119 @@ __device__ __forceinline__ bool ns_walk(const Geometry& g, int r, int b, int h, 
 
 // Non-Shared part alone of one (request, beam, KV head), stored as piece `nsplit` of the
 // workspace for the Shared-stage kernel to merge (its epilogue also reports prefix-length
-// problems and empty rows). Kept apart from ns_merge_kernel so that it needs few registers
-// and many warps stay resident to cover the two dependent loads (ancestry slot, then K/V).
+// problems and empty rows). Lane mapping: lane = (query head within a group of HG heads,
+// slice of EL consecutive elements of d), so a dot product reduces over LP = 32 / HG lanes
+// only, and each lane keeps one head's slice of q and of the output. Groups of more than
+// four heads are done in passes over the same (L1-resident) pool rows. Two tokens per round:
+// their K/V slices are loaded together.
 template <int D, int G>
-__global__ void __launch_bounds__(256, G * D <= 256 ? 4 : (G * D <= 512 ? 3 : (G <= 8 ? 2 : 1))) ns_piece_kernel(
+__global__ void __launch_bounds__(256, D * (G < 4 ? G : 4) / 32 >= 16 ? 3 : 4) ns_piece_kernel(
     Geometry g, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ pool_k,
     const __nv_bfloat16* __restrict__ pool_v, const int32_t* __restrict__ idx, float* __restrict__ part_o,
     float* __restrict__ part_lse, int32_t* status) {
-    constexpr int E = D / 32;
+    constexpr int HG = G < 4 ? G : 4;  // heads per pass
+    constexpr int LP = 32 / HG;        // lanes per head
+    constexpr int EL = D / LP;         // elements of d per lane (2 .. 16)
+    constexpr int NV = EL / 2;         // bf16 pairs per lane
     const int lane = threadIdx.x & 31;
     const long warp_id = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (warp_id >= (long)g.R * g.BW * g.Hkv) return;
     const int h = (int)(warp_id % g.Hkv);
     const int b = (int)((warp_id / g.Hkv) % g.BW);
     const int r = (int)(warp_id / ((long)g.Hkv * g.BW));
-    RowState<E, G> st;
-    st.init();
-    const bool slot_bad = g.step > 0 && !ns_walk<D, G>(g, r, b, h, lane, q, pool_k, pool_v, idx, st, status);
-    const size_t prow = (((size_t)r * g.Hkv + h) * g.pieces + g.nsplit) * g.M + (size_t)b * G;
+    const int hg = lane / LP, sl = lane % LP;
+    const size_t qrow0 = ((size_t)r * g.BW + b) * g.Hq + (size_t)h * G;
+    const size_t prow0 = (((size_t)r * g.Hkv + h) * g.pieces + g.nsplit) * g.M + (size_t)b * G;
+    const int32_t* row_idx = idx + ((size_t)r * g.BW + b) * g.Tmax;
+    const int step = g.step;
+    const int my_slot = lane < step ? __ldg(row_idx + lane) : 0;
+    const bool slot_bad = __any_sync(0xffffffffu, lane < step && (my_slot < 0 || my_slot >= g.S));
+    if (slot_bad && lane == 0) set_status(status, XATTN_STATUS_BAD_SLOT);
+    const size_t kv_head = (size_t)h * D + (size_t)sl * EL;  // offset of this lane's slice in a pool row
+
+    auto load_pairs = [](const __nv_bfloat16* p, uint32_t (&w)[NV]) {
+        if constexpr (NV >= 4) {
 #pragma unroll
-    for (int gg = 0; gg < G; ++gg) {
-        const bool empty = !(st.l[gg] > 0.f);
-        const float inv = empty ? 0.f : 1.f / st.l[gg];
-        float* po = part_o + (prow + gg) * D + lane * E;
-        if constexpr (E == 4) {
-            *reinterpret_cast<float4*>(po) =
-                make_float4(st.acc[gg][0] * inv, st.acc[gg][1] * inv, st.acc[gg][2] * inv, st.acc[gg][3] * inv);
+            for (int c = 0; c < NV / 4; ++c) {
+                const uint4 u = __ldg(reinterpret_cast<const uint4*>(p) + c);
+                w[4 * c] = u.x; w[4 * c + 1] = u.y; w[4 * c + 2] = u.z; w[4 * c + 3] = u.w;
+            }
+        } else if constexpr (NV == 2) {
+            const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+            w[0] = u.x; w[1] = u.y;
         } else {
-            *reinterpret_cast<float2*>(po) = make_float2(st.acc[gg][0] * inv, st.acc[gg][1] * inv);
+            w[0] = __ldg(reinterpret_cast<const uint32_t*>(p));
         }
-        if (lane == 0)
-            part_lse[prow + gg] = slot_bad ? __uint_as_float(kNaN)
-                                           : (empty ? -INFINITY : (st.m[gg] + __log2f(st.l[gg])) * kLn2);
+    };
+    // bf16 pair -> two floats (a bf16 is the top half of its fp32)
+    auto lo = [](uint32_t w) { return __uint_as_float(w << 16); };
+    auto hi = [](uint32_t w) { return __uint_as_float(w & 0xffff0000u); };
+
+#pragma unroll 1
+    for (int pass = 0; pass < G / HG; ++pass) {
+        const int gg = pass * HG + hg;
+        uint32_t qw[NV];
+        load_pairs(q + (qrow0 + gg) * D + sl * EL, qw);
+        float m = -INFINITY, l = 0.f, acc[EL];
+#pragma unroll
+        for (int e = 0; e < EL; ++e) acc[e] = 0.f;
+        if (!slot_bad) {
+            for (int t0 = 0; t0 < step; t0 += 2) {
+                uint32_t kw[2][NV], vw[2][NV];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int slot = __shfl_sync(0xffffffffu, my_slot, (t0 + u) & 31);
+                    if (t0 + u < step) {
+                        const size_t off = ((size_t)r * g.S + slot) * g.Hkv * D + kv_head;
+                        load_pairs(pool_k + off, kw[u]);
+                        load_pairs(pool_v + off, vw[u]);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < NV; ++c) kw[u][c] = vw[u][c] = 0u;
+                    }
+                }
+                float sc[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    float t = 0.f;
+#pragma unroll
+                    for (int c = 0; c < NV; ++c) {
+                        t = fmaf(lo(qw[c]), lo(kw[u][c]), t);
+                        t = fmaf(hi(qw[c]), hi(kw[u][c]), t);
+                    }
+                    sc[u] = t;
+                }
+#pragma unroll
+                for (int o = LP / 2; o > 0; o >>= 1) {
+                    sc[0] += __shfl_xor_sync(0xffffffffu, sc[0], o);
+                    sc[1] += __shfl_xor_sync(0xffffffffu, sc[1], o);
+                }
+                const float s0 = sc[0] * g.scale_log2;
+                const float s1 = t0 + 1 < step ? sc[1] * g.scale_log2 : -INFINITY;
+                const float mn = fmaxf(m, fmaxf(s0, s1));
+                const float alpha = ex2(m - mn), p0 = ex2(s0 - mn), p1 = ex2(s1 - mn);
+                l = l * alpha + (p0 + p1);
+#pragma unroll
+                for (int c = 0; c < NV; ++c) {
+                    acc[2 * c] = fmaf(p1, lo(vw[1][c]), fmaf(p0, lo(vw[0][c]), acc[2 * c] * alpha));
+                    acc[2 * c + 1] = fmaf(p1, hi(vw[1][c]), fmaf(p0, hi(vw[0][c]), acc[2 * c + 1] * alpha));
+                }
+                m = mn;
+            }
+        }
+        const bool empty = !(l > 0.f);
+        const float inv = empty ? 0.f : 1.f / l;
+        float* po = part_o + (prow0 + gg) * D + sl * EL;
+        if constexpr (EL >= 4) {
+#pragma unroll
+            for (int c = 0; c < EL / 4; ++c)
+                reinterpret_cast<float4*>(po)[c] =
+                    make_float4(acc[4 * c] * inv, acc[4 * c + 1] * inv, acc[4 * c + 2] * inv, acc[4 * c + 3] * inv);
+        } else {
+            *reinterpret_cast<float2*>(po) = make_float2(acc[0] * inv, acc[1] * inv);
+        }
+        if (sl == 0)
+            part_lse[prow0 + gg] = slot_bad ? __uint_as_float(kNaN) : (empty ? -INFINITY : (m + __log2f(l)) * kLn2);
     }
 }
 
