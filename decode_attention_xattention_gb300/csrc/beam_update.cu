@@ -20,20 +20,20 @@ constexpr int kThreads = 256;
 constexpr int kTableInts = 8192;  // shared-memory band: 32 KB
 
 __global__ void __launch_bounds__(kThreads) beam_update_kernel(
-    int BW, int HkvD, int S, int Tmax, int step, const int32_t* __restrict__ parent,
+    int BW, int HkvD, int S, int Tmax, int step, int copy_ctas, const int32_t* __restrict__ parent,
     const __nv_bfloat16* __restrict__ new_k, const __nv_bfloat16* __restrict__ new_v,
     __nv_bfloat16* __restrict__ pool_k, __nv_bfloat16* __restrict__ pool_v,
     int32_t* __restrict__ idx, int32_t* status) {
     const int r = blockIdx.x;
-    // 1. K/V of the new tokens: [BW, Hkv, d] of request r -> slots step*BW .. step*BW+BW-1.
-    //    All loads of a thread are issued before its stores (independent 16-byte vectors).
-    {
+    if ((int)blockIdx.y < copy_ctas) {
+        // 1. K/V of the new tokens: [BW, Hkv, d] of request r -> slots step*BW .. step*BW+BW-1.
+        //    All loads of a thread are issued before its stores (independent 16-byte vectors).
         const size_t n16 = (size_t)BW * HkvD / 8;  // 16-byte vectors (HkvD is a multiple of 8)
         const uint4* sk = reinterpret_cast<const uint4*>(new_k + (size_t)r * BW * HkvD);
         const uint4* sv = reinterpret_cast<const uint4*>(new_v + (size_t)r * BW * HkvD);
         uint4* dk = reinterpret_cast<uint4*>(pool_k + ((size_t)r * S + (size_t)step * BW) * HkvD);
         uint4* dv = reinterpret_cast<uint4*>(pool_v + ((size_t)r * S + (size_t)step * BW) * HkvD);
-        const size_t stride = (size_t)gridDim.y * kThreads;
+        const size_t stride = (size_t)copy_ctas * kThreads;
         size_t i = (size_t)blockIdx.y * kThreads + threadIdx.x;
         for (; i + 3 * stride < n16; i += 4 * stride) {
             uint4 a[4], c[4];
@@ -47,13 +47,15 @@ __global__ void __launch_bounds__(kThreads) beam_update_kernel(
             dk[i] = a;
             dv[i] = c;
         }
+        return;
     }
-    if (blockIdx.y != 0) return;
 
-    // 2. Ancestry table of request r, in place.
+    // 2. Ancestry table of request r, in place, by the request's last CTA (which copies
+    //    nothing, so the table's few dependent loads overlap the copies of the others).
     __shared__ int32_t band[kTableInts];
     int32_t* tab = idx + (size_t)r * BW * Tmax;
     const int32_t* par = parent ? parent + (size_t)r * BW : nullptr;
+    const int cols = max(1, min(step, kTableInts / BW));
     for (int b = threadIdx.x; b < BW; b += kThreads) {
         tab[(size_t)b * Tmax + step] = step * BW + b;  // column `step` is never read below
         if (step > 0) {
@@ -62,7 +64,6 @@ __global__ void __launch_bounds__(kThreads) beam_update_kernel(
         }
     }
     if (step == 0) return;
-    const int cols = max(1, min(step, kTableInts / BW));
     for (int c0 = 0; c0 < step; c0 += cols) {
         const int cc = min(cols, step - c0);
         __syncthreads();  // previous band fully written before it is reused
@@ -90,8 +91,8 @@ cudaError_t launch_beam_update(int R, int BW, int Hkv, int d, int S, int Tmax, i
     const size_t n16 = (size_t)BW * Hkv * d / 8;
     int ybl = (int)((n16 + kThreads - 1) / kThreads);  // about one vector of K and V per thread
     ybl = max(1, min(ybl, 1024));
-    dim3 grid(R, ybl);
-    beam_update_kernel<<<grid, kThreads, 0, stream>>>(BW, Hkv * d, S, Tmax, step, parent, new_k, new_v,
+    dim3 grid(R, ybl + 1);  // the last CTA of each request rewrites its ancestry table
+    beam_update_kernel<<<grid, kThreads, 0, stream>>>(BW, Hkv * d, S, Tmax, step, ybl, parent, new_k, new_v,
                                                       pool_k, pool_v, idx, status);
     return cudaGetLastError();
 }

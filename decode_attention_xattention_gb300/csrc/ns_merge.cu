@@ -177,10 +177,12 @@ __device__ __forceinline__ bool ns_walk(const Geometry& g, int r, int b, int h, 
 // problems and empty rows). Lane mapping: lane = (query head within a group of HG heads,
 // slice of EL consecutive elements of d), so a dot product reduces over LP = 32 / HG lanes
 // only, and each lane keeps one head's slice of q and of the output. Groups of more than
-// four heads are done in passes over the same (L1-resident) pool rows. Two tokens per round:
-// their K/V slices are loaded together.
+// four heads are done in passes over the same pool rows. As soon as the ancestry slots are
+// known every pool row the beam needs is prefetched into L1, so of the walk's dependent
+// loads only the first token's waits on memory; the walk then takes one token per step
+// with few registers (many resident warps).
 template <int D, int G>
-__global__ void __launch_bounds__(256, D * (G < 4 ? G : 4) / 32 >= 16 ? 3 : 4) ns_piece_kernel(
+__global__ void __launch_bounds__(256, 4) ns_piece_kernel(
     Geometry g, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ pool_k,
     const __nv_bfloat16* __restrict__ pool_v, const int32_t* __restrict__ idx, float* __restrict__ part_o,
     float* __restrict__ part_lse, int32_t* status) {
@@ -188,6 +190,7 @@ __global__ void __launch_bounds__(256, D * (G < 4 ? G : 4) / 32 >= 16 ? 3 : 4) n
     constexpr int LP = 32 / HG;        // lanes per head
     constexpr int EL = D / LP;         // elements of d per lane (2 .. 16)
     constexpr int NV = EL / 2;         // bf16 pairs per lane
+    constexpr int kLines = D * 2 / 128;  // 128-byte lines per pool row
     const int lane = threadIdx.x & 31;
     const long warp_id = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (warp_id >= (long)g.R * g.BW * g.Hkv) return;
@@ -202,7 +205,22 @@ __global__ void __launch_bounds__(256, D * (G < 4 ? G : 4) / 32 >= 16 ? 3 : 4) n
     const int my_slot = lane < step ? __ldg(row_idx + lane) : 0;
     const bool slot_bad = __any_sync(0xffffffffu, lane < step && (my_slot < 0 || my_slot >= g.S));
     if (slot_bad && lane == 0) set_status(status, XATTN_STATUS_BAD_SLOT);
-    const size_t kv_head = (size_t)h * D + (size_t)sl * EL;  // offset of this lane's slice in a pool row
+    const size_t head_off = (size_t)h * D;
+    if (!slot_bad) {
+        // prefetch every (token, K/V, line) of the walk: 32 lanes per pass
+        constexpr int kPerTok = 2 * kLines;
+        for (int base = 0; base < step * kPerTok; base += 32) {
+            const int e = base + lane;
+            const int t = min(e / kPerTok, 31);
+            const int slot = __shfl_sync(0xffffffffu, my_slot, t);
+            if (e < step * kPerTok) {
+                const int kv = (e / kLines) & 1, line = e % kLines;
+                const __nv_bfloat16* row = (kv ? pool_v : pool_k) + ((size_t)r * g.S + slot) * g.Hkv * D + head_off;
+                asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const char*>(row) + line * 128));
+            }
+        }
+    }
+    const size_t kv_lane = head_off + (size_t)sl * EL;  // offset of this lane's slice in a pool row
 
     auto load_pairs = [](const __nv_bfloat16* p, uint32_t (&w)[NV]) {
         if constexpr (NV >= 4) {
@@ -231,45 +249,28 @@ __global__ void __launch_bounds__(256, D * (G < 4 ? G : 4) / 32 >= 16 ? 3 : 4) n
 #pragma unroll
         for (int e = 0; e < EL; ++e) acc[e] = 0.f;
         if (!slot_bad) {
-            for (int t0 = 0; t0 < step; t0 += 2) {
-                uint32_t kw[2][NV], vw[2][NV];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int slot = __shfl_sync(0xffffffffu, my_slot, (t0 + u) & 31);
-                    if (t0 + u < step) {
-                        const size_t off = ((size_t)r * g.S + slot) * g.Hkv * D + kv_head;
-                        load_pairs(pool_k + off, kw[u]);
-                        load_pairs(pool_v + off, vw[u]);
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < NV; ++c) kw[u][c] = vw[u][c] = 0u;
-                    }
-                }
-                float sc[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    float t = 0.f;
-#pragma unroll
-                    for (int c = 0; c < NV; ++c) {
-                        t = fmaf(lo(qw[c]), lo(kw[u][c]), t);
-                        t = fmaf(hi(qw[c]), hi(kw[u][c]), t);
-                    }
-                    sc[u] = t;
-                }
-#pragma unroll
-                for (int o = LP / 2; o > 0; o >>= 1) {
-                    sc[0] += __shfl_xor_sync(0xffffffffu, sc[0], o);
-                    sc[1] += __shfl_xor_sync(0xffffffffu, sc[1], o);
-                }
-                const float s0 = sc[0] * g.scale_log2;
-                const float s1 = t0 + 1 < step ? sc[1] * g.scale_log2 : -INFINITY;
-                const float mn = fmaxf(m, fmaxf(s0, s1));
-                const float alpha = ex2(m - mn), p0 = ex2(s0 - mn), p1 = ex2(s1 - mn);
-                l = l * alpha + (p0 + p1);
+            for (int t = 0; t < step; ++t) {
+                const int slot = __shfl_sync(0xffffffffu, my_slot, t);
+                const size_t off = ((size_t)r * g.S + slot) * g.Hkv * D + kv_lane;
+                uint32_t kw[NV], vw[NV];
+                load_pairs(pool_k + off, kw);
+                load_pairs(pool_v + off, vw);
+                float sc = 0.f;
 #pragma unroll
                 for (int c = 0; c < NV; ++c) {
-                    acc[2 * c] = fmaf(p1, lo(vw[1][c]), fmaf(p0, lo(vw[0][c]), acc[2 * c] * alpha));
-                    acc[2 * c + 1] = fmaf(p1, hi(vw[1][c]), fmaf(p0, hi(vw[0][c]), acc[2 * c + 1] * alpha));
+                    sc = fmaf(lo(qw[c]), lo(kw[c]), sc);
+                    sc = fmaf(hi(qw[c]), hi(kw[c]), sc);
+                }
+#pragma unroll
+                for (int o = LP / 2; o > 0; o >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, o);
+                const float s2 = sc * g.scale_log2;
+                const float mn = fmaxf(m, s2);
+                const float alpha = ex2(m - mn), p = ex2(s2 - mn);
+                l = l * alpha + p;
+#pragma unroll
+                for (int c = 0; c < NV; ++c) {
+                    acc[2 * c] = fmaf(p, lo(vw[c]), acc[2 * c] * alpha);
+                    acc[2 * c + 1] = fmaf(p, hi(vw[c]), acc[2 * c + 1] * alpha);
                 }
                 m = mn;
             }
