@@ -39,12 +39,11 @@ namespace {
 
 using namespace ptx;
 
-// Warp roles: 0-7 two softmax warpgroups; 8 K-tile producer; 9 MMA issuer (and TMEM
-// owner); 10 V-tile producer. Every role that spins on an mbarrier has a warp of its own:
-// divergent lanes of one warp run one path at a time, so a spinning lane would starve its
-// neighbours.
-constexpr int kThreads = 352;
-constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10;
+// Warp roles: 0-7 two softmax warpgroups; 8 TMA producer; 9 MMA issuer (and TMEM owner).
+// Every role that spins on an mbarrier has a warp of its own: divergent lanes of one warp
+// run one path at a time, so a spinning lane would starve its neighbours.
+constexpr int kThreads = 320;
+constexpr int kWarpLoad = 8, kWarpMma = 9;
 constexpr int kMaxStages = 4;
 constexpr int kPrefetch = 4;  // K/V tiles prefetched into L2 ahead of their load
 constexpr uint32_t kTmemCols = 512;  // S0 | S1 | O0 | O1, 128 columns each
@@ -53,19 +52,20 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint32_t kNaN = 0x7fc00000u;
 
-// K/V pipeline depth: K is consumed one tile before V, so K gets the deeper ring
-// (3 + 2 stages at d = 128, 4 + 4 at d = 64). Either way the shared memory admits one CTA
-// per SM, so a CTA never waits for another's 512 TMEM columns.
+// K/V pipeline. Iteration j of the MMA warp consumes V of tile j-1 (P.V) and K of tile j
+// (Q.K^T), so the producer loads them together as load unit j = {K(j), V(j-1)} under one
+// mbarrier: one data wait per tile on the MMA warp. Two unit slots at d = 128 (four at
+// d = 64), each one K tile and one V tile; the shared memory admits one CTA per SM, so a
+// CTA never waits for another's 512 TMEM columns.
 template <int D>
 struct Cfg {
-    static constexpr int kKStages = D == 64 ? 4 : 3;
-    static constexpr int kVStages = D == 64 ? 4 : 2;
+    static constexpr int kUnits = D == 64 ? 4 : 2;
     static constexpr int KB = D / 64;              // 128-byte swizzle blocks along d
     static constexpr int kTileBytes = KB * 16384;  // 128 rows (or tokens) x d bf16
+    static constexpr int kUnitBytes = 2 * kTileBytes;  // K tile, then V tile
     static constexpr int kOffQ = 0;                // two row tiles
-    static constexpr int kOffK = kOffQ + 2 * kTileBytes;
-    static constexpr int kOffV = kOffK + kKStages * kTileBytes;
-    static constexpr int kSmemBytes = kOffV + kVStages * kTileBytes + 1024;
+    static constexpr int kOffU = kOffQ + 2 * kTileBytes;
+    static constexpr int kSmemBytes = kOffU + kUnits * kUnitBytes + 1024;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -92,7 +92,7 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int ch) {
 }
 
 struct Bars {
-    uint64_t k_full[kMaxStages], k_empty[kMaxStages], v_full[kMaxStages], v_empty[kMaxStages];
+    uint64_t u_full[kMaxStages], u_empty[kMaxStages];
     uint64_t s_full[2], p_full[2], q_ready[2];
     uint64_t o_full[2], final_mma;
 };
@@ -111,12 +111,11 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     Geometry g, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ shared_len,
     float* __restrict__ part_o, float* __restrict__ part_lse, int32_t* status, FusedArgs fa) {
     using C = Cfg<D>;
-    constexpr int kKS = C::kKStages, kVS = C::kVStages;
+    constexpr int kU = C::kUnits;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem + C::kOffQ;
-    uint8_t* sK = smem + C::kOffK;
-    uint8_t* sV = smem + C::kOffV;
+    uint8_t* sU = smem + C::kOffU;  // unit slot u: K tile at sU + u * kUnitBytes, V tile after it
     __shared__ Bars bars;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
@@ -141,13 +140,9 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     const int ntile_m = (2 * mp + 1 < g.row_tiles) ? 2 : 1;  // row tiles this CTA owns
 
     if (tid == 0) {
-        for (int s = 0; s < kKS; ++s) {
-            mbar_init(&bars.k_full[s], 1);
-            mbar_init(&bars.k_empty[s], 1);
-        }
-        for (int s = 0; s < kVS; ++s) {
-            mbar_init(&bars.v_full[s], 1);
-            mbar_init(&bars.v_empty[s], 1);
+        for (int s = 0; s < kU; ++s) {
+            mbar_init(&bars.u_full[s], 1);
+            mbar_init(&bars.u_empty[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars.s_full[i], 1);
@@ -380,37 +375,42 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 part_lse[prow] = !ok ? __uint_as_float(kNaN)
                                      : (ntiles > 0 ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY);
         }
-    } else if (warp == kWarpK || warp == kWarpV) {
-        // ============================================ TMA producers
-        // One warp feeds the K ring and another the V ring, each as soon as a slot frees.
-        // Both also prefetch the tile kPrefetch tiles ahead into L2, which hides most of
-        // the HBM latency of the later load.
+    } else if (warp == kWarpLoad) {
+        // ============================================ TMA producer
+        // Load unit j = {K(j) if j < ntiles, V(j-1) if j >= 1} into slot j % kU as soon as
+        // unit j - kU has been consumed; L2 prefetch kPrefetch units ahead hides most of the
+        // HBM latency of the later load.
         if (lane == 0 && ntiles > 0) {
-            const bool is_k = warp == kWarpK;
-            const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
-            prefetch_tmap(map);
-            const int nst = is_k ? kKS : kVS;
-            uint64_t* full = is_k ? bars.k_full : bars.v_full;
-            uint64_t* empty = is_k ? bars.k_empty : bars.v_empty;
-            uint8_t* ring = is_k ? sK : sV;
-            for (int j = 0; j < min(ntiles, kPrefetch); ++j)
-                for (int kb = 0; kb < C::KB; ++kb) tma_prefetch_4d(map, kb * 64, h, t0 + j * kTcTileKeys, r);
+            prefetch_tmap(&tmap_k);
+            prefetch_tmap(&tmap_v);
+            const int nunits = ntiles + 1;
+            auto prefetch_unit = [&](int j) {
+                for (int kb = 0; kb < C::KB; ++kb) {
+                    if (j < ntiles) tma_prefetch_4d(&tmap_k, kb * 64, h, t0 + j * kTcTileKeys, r);
+                    if (j >= 1) tma_prefetch_4d(&tmap_v, kb * 64, h, t0 + (j - 1) * kTcTileKeys, r);
+                }
+            };
+            for (int j = 0; j < min(nunits, kPrefetch); ++j) prefetch_unit(j);
             int issued = 0;
-            for (int j = 0; j < ntiles; ++j) {
-                const int st = j % nst, u = j / nst;
-                if (u > 0 && !mbar_wait(&empty[st], (u - 1) & 1, &abort_sh)) break;
-                if (j + kPrefetch < ntiles)
-                    for (int kb = 0; kb < C::KB; ++kb)
-                        tma_prefetch_4d(map, kb * 64, h, t0 + (j + kPrefetch) * kTcTileKeys, r);
-                mbar_arrive_expect_tx(&full[st], C::kTileBytes);
-                for (int kb = 0; kb < C::KB; ++kb)
-                    tma_load_4d(ring + st * C::kTileBytes + kb * 16384, map, &full[st], kb * 64, h,
-                                t0 + j * kTcTileKeys, r);
+            for (int j = 0; j < nunits; ++j) {
+                const int st = j % kU, use = j / kU;
+                if (use > 0 && !mbar_wait(&bars.u_empty[st], (use - 1) & 1, &abort_sh)) break;
+                if (j + kPrefetch < nunits) prefetch_unit(j + kPrefetch);
+                uint8_t* slot = sU + st * C::kUnitBytes;
+                mbar_arrive_expect_tx(&bars.u_full[st],
+                                      (j < ntiles ? C::kTileBytes : 0) + (j >= 1 ? C::kTileBytes : 0));
+                for (int kb = 0; kb < C::KB; ++kb) {
+                    if (j < ntiles)
+                        tma_load_4d(slot + kb * 16384, &tmap_k, &bars.u_full[st], kb * 64, h, t0 + j * kTcTileKeys, r);
+                    if (j >= 1)
+                        tma_load_4d(slot + C::kTileBytes + kb * 16384, &tmap_v, &bars.u_full[st], kb * 64, h,
+                                    t0 + (j - 1) * kTcTileKeys, r);
+                }
                 issued = j + 1;
             }
             if (abort_sh) {  // let the copies still in flight land before the CTA exits
                 volatile int never = 0;
-                for (int j = max(0, issued - nst); j < issued; ++j) mbar_wait(&full[j % nst], (j / nst) & 1, &never);
+                for (int j = max(0, issued - kU); j < issued; ++j) mbar_wait(&bars.u_full[j % kU], (j / kU) & 1, &never);
             }
         }
     } else {
@@ -427,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             // there (even NaN) never reaches O.
             const int lim_last = t1 - (t0 + (ntiles - 1) * kTcTileKeys);
             const int pv_steps_last = (lim_last + 15) / 16;
-            auto issue_pv = [&](int i, int jt, int vs) {
-                const uint32_t vbase = smem_addr(sV + vs * C::kTileBytes);
+            auto issue_pv = [&](int i, int jt, int st) {
+                const uint32_t vbase = smem_addr(sU + st * C::kUnitBytes + C::kTileBytes);
                 const int nk = jt == ntiles - 1 ? pv_steps_last : kTcTileKeys / 16;
 #pragma unroll
                 for (int kk = 0; kk < kTcTileKeys / 16; ++kk) {
@@ -440,12 +440,12 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             // Per tile j and row tile i: P.V of tile j-1 first (it needs only V(j-1) and
             // P_i), then Q.K^T of tile j into the same TMEM columns, then one commit.
             for (int j = 0; ok && j <= ntiles; ++j) {
-                const int vs = (j - 1) % kVS;  // used only when j > 0
-                if (j > 0 && !mbar_wait(&bars.v_full[vs], ((j - 1) / kVS) & 1, &abort_sh)) { ok = false; break; }
+                const int st = j % kU;  // unit j: K(j) and V(j-1)
+                if (!mbar_wait(&bars.u_full[st], (j / kU) & 1, &abort_sh)) { ok = false; break; }
                 if (j == ntiles && (lim_last & 15) != 0) {
                     // zero V rows lim_last .. end of their 16-token step (whole 128-byte rows,
                     // so the swizzle does not matter), then make them visible to the tensor core
-                    uint8_t* vt = sV + vs * C::kTileBytes;
+                    uint8_t* vt = sU + st * C::kUnitBytes + C::kTileBytes;
                     for (int row = lim_last; row < pv_steps_last * 16; ++row)
 #pragma unroll
                         for (int kb = 0; kb < C::KB; ++kb)
@@ -454,23 +454,17 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                                 *reinterpret_cast<uint4*>(vt + kb * 16384 + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
                     fence_proxy_async_smem();
                 }
-                const int ks = j % kKS;
-                bool k_ready = false;
                 for (int i = 0; i < ntile_m; ++i) {
                     if (j > 0) {
                         if (!mbar_wait(&bars.p_full[i], (j - 1) & 1, &abort_sh)) { ok = false; break; }
                         tc_fence_after();
-                        issue_pv(i, j - 1, vs);
+                        issue_pv(i, j - 1, st);
                         if (j == ntiles) mma_commit(&bars.o_full[i]);  // O_i complete
                     }
                     if (j < ntiles) {
-                        if (!k_ready) {
-                            if (!mbar_wait(&bars.k_full[ks], (j / kKS) & 1, &abort_sh)) { ok = false; break; }
-                            k_ready = true;
-                        }
                         tc_fence_after();
                         const uint32_t qbase = smem_addr(sQ + i * C::kTileBytes);
-                        const uint32_t kbase = smem_addr(sK + ks * C::kTileBytes);
+                        const uint32_t kbase = smem_addr(sU + st * C::kUnitBytes);
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -481,8 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                     }
                 }
                 if (!ok) break;
-                if (j < ntiles) mma_commit(&bars.k_empty[ks]);
-                if (j > 0) mma_commit(&bars.v_empty[vs]);
+                mma_commit(&bars.u_empty[st]);
             }
             if (!ok) {
                 abort_sh = 1;
