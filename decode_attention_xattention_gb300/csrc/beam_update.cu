@@ -7,10 +7,10 @@
 // Reading used here: the token a beam emits at step s is written once, to the fresh slot
 // s*BW + b (for a request the BW new tokens fill one contiguous run of slots, so the K/V
 // write is a straight copy). Only the small ancestry table changes otherwise:
-// row b becomes its parent's row followed by the new slot. Rows are rewritten in place by
-// one CTA per request that stages a band of table columns in shared memory (all reads,
-// barrier, all writes), so no entry is read after it has been overwritten. Column i of
-// the new table depends only on column i of the old one, which is what makes banding safe.
+// row b becomes its parent's row followed by the new slot. Column i of the new table
+// depends only on column i of the old one, so the table is rewritten in place by CTAs that
+// each own a range of columns and stage it in shared memory (all reads, barrier, all
+// writes): no entry is read after it has been overwritten.
 #include "xattn_internal.cuh"
 
 namespace xattn {
@@ -18,6 +18,13 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kTableInts = 8192;  // shared-memory band: 32 KB
+
+// Table columns per table CTA: at most a 32 KB band, and about 2048 entries so that long
+// tables are spread over many CTAs.
+__host__ __device__ inline int table_cols(int BW, int step) {
+    const int c = 2048 / BW;
+    return c < 1 ? 1 : (c > step ? step : c);
+}
 
 __global__ void __launch_bounds__(kThreads) beam_update_kernel(
     int BW, int HkvD, int S, int Tmax, int step, int copy_ctas, const int32_t* __restrict__ parent,
@@ -50,33 +57,39 @@ __global__ void __launch_bounds__(kThreads) beam_update_kernel(
         return;
     }
 
-    // 2. Ancestry table of request r, in place, by the request's last CTA (which copies
-    //    nothing, so the table's few dependent loads overlap the copies of the others).
+    // 2. Ancestry table of request r, in place. Column i of the new table depends only on
+    //    column i of the old one, so the columns are split into ranges of `cols` columns, one
+    //    per table CTA (blockIdx.y - copy_ctas); each stages its range in shared memory (all
+    //    reads, barrier, all writes). These CTAs copy nothing, so their dependent loads
+    //    overlap the copies of the others.
     __shared__ int32_t band[kTableInts];
+    const int tc = (int)blockIdx.y - copy_ctas;
     int32_t* tab = idx + (size_t)r * BW * Tmax;
     const int32_t* par = parent ? parent + (size_t)r * BW : nullptr;
-    const int cols = max(1, min(step, kTableInts / BW));
-    for (int b = threadIdx.x; b < BW; b += kThreads) {
-        tab[(size_t)b * Tmax + step] = step * BW + b;  // column `step` is never read below
-        if (step > 0) {
-            const int p = par[b];
-            if (p < 0 || p >= BW) set_status(status, XATTN_STATUS_BAD_PARENT);
+    if (tc == 0) {
+        for (int b = threadIdx.x; b < BW; b += kThreads) {
+            tab[(size_t)b * Tmax + step] = step * BW + b;  // column `step` is never read below
+            if (step > 0) {
+                const int p = par[b];
+                if (p < 0 || p >= BW) set_status(status, XATTN_STATUS_BAD_PARENT);
+            }
         }
     }
     if (step == 0) return;
-    for (int c0 = 0; c0 < step; c0 += cols) {
-        const int cc = min(cols, step - c0);
-        __syncthreads();  // previous band fully written before it is reused
-        for (int i = threadIdx.x; i < BW * cc; i += kThreads) {
-            const int b = i / cc, c = i - b * cc;
-            band[i] = tab[(size_t)b * Tmax + c0 + c];
-        }
-        __syncthreads();  // every old entry of the band read before any is overwritten
-        for (int i = threadIdx.x; i < BW * cc; i += kThreads) {
-            const int b = i / cc, c = i - b * cc;
-            const int p = par[b];
-            tab[(size_t)b * Tmax + c0 + c] = (p >= 0 && p < BW) ? band[p * cc + c] : -1;
-        }
+    const int cols = table_cols(BW, step);
+    const int c0 = tc * cols, cc = min(cols, step - c0);
+    if (cc <= 0) return;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < BW * cc; i += kThreads) {
+        const int b = i / cc, c = i - b * cc;
+        band[i] = tab[(size_t)b * Tmax + c0 + c];
+    }
+    __syncthreads();  // every old entry of the range read before any is overwritten
+#pragma unroll 4
+    for (int i = threadIdx.x; i < BW * cc; i += kThreads) {
+        const int b = i / cc, c = i - b * cc;
+        const int p = __ldg(par + b);
+        tab[(size_t)b * Tmax + c0 + c] = (p >= 0 && p < BW) ? band[p * cc + c] : -1;
     }
 }
 
@@ -91,7 +104,8 @@ cudaError_t launch_beam_update(int R, int BW, int Hkv, int d, int S, int Tmax, i
     const size_t n16 = (size_t)BW * Hkv * d / 8;
     int ybl = (int)((n16 + kThreads - 1) / kThreads);  // about one vector of K and V per thread
     ybl = max(1, min(ybl, 1024));
-    dim3 grid(R, ybl + 1);  // the last CTA of each request rewrites its ancestry table
+    const int tcols = step > 0 ? (step + table_cols(BW, step) - 1) / table_cols(BW, step) : 1;
+    dim3 grid(R, ybl + tcols);  // the last tcols CTAs of each request rewrite its ancestry table
     beam_update_kernel<<<grid, kThreads, 0, stream>>>(BW, Hkv * d, S, Tmax, step, ybl, parent, new_k, new_v,
                                                       pool_k, pool_v, idx, status);
     return cudaGetLastError();

@@ -7,16 +7,20 @@
 // combine is the log-sum-exp rule: lse = log(sum_i exp(lse_i)), out = sum_i exp(lse_i - lse) o_i,
 // over every piece of the prefix the Shared stage produced and the Non-Shared part.
 //
-// Two kernels:
-//   ns_merge_kernel    one warp per (request r, beam b, KV head h) serves the G query heads
-//                      of that KV head (each gathered pool row is read once for all G);
-//                      lanes split the head dimension. It walks the beam's ancestry tokens
-//                      itself when there are few (<= kNsDirectMax), then folds in every
-//                      piece stored in the workspace and writes out / lse.
-//   ns_partial_kernel  for long Non-Shared parts (e.g. a 512-token unshared suffix per
-//                      sequence): CTA = (r, b, h, piece of kNsChunk ancestry positions), four
-//                      warps with four tokens in flight each; writes the piece's normalised
-//                      output and LSE into the workspace after the prefix pieces.
+// Kernels:
+//   ns_piece_kernel    one warp per (request r, beam b, KV head h, piece of at most kNsChunk
+//                      ancestry positions): the Non-Shared stage of that piece, written into
+//                      the workspace after the prefix pieces. With one piece (step <= 32) it
+//                      runs ahead of the Shared-stage kernel, whose epilogue merges; for long
+//                      Non-Shared parts (e.g. a 512-token unshared suffix per sequence) the
+//                      pieces are merged by merge_rows_kernel.
+//   ns_merge_kernel    one warp per (r, b, h): the G query heads of that KV head (each
+//                      gathered pool row is read once for all G); lanes split the head
+//                      dimension. It walks the beam's ancestry tokens itself (<= 32 of
+//                      them), then folds in every prefix piece stored in the workspace and
+//                      writes out / lse (split prefixes).
+//   merge_rows_kernel  one warp per query row: folds every stored piece (prefix and
+//                      Non-Shared) and writes out / lse.
 #include "xattn_internal.cuh"
 
 namespace xattn {
@@ -172,117 +176,155 @@ __device__ __forceinline__ bool ns_walk(const Geometry& g, int r, int b, int h, 
     return true;
 }
 
-// Non-Shared part alone of one (request, beam, KV head), stored as piece `nsplit` of the
-// workspace for the Shared-stage kernel to merge (its epilogue also reports prefix-length
-// problems and empty rows). Lane mapping: lane = (query head within a group of HG heads,
-// slice of EL consecutive elements of d), so a dot product reduces over LP = 32 / HG lanes
-// only, and each lane keeps one head's slice of q and of the output. Groups of more than
-// four heads are done in passes over the same pool rows. As soon as the ancestry slots are
-// known every pool row the beam needs is prefetched into L1, so of the walk's dependent
-// loads only the first token's waits on memory; the walk then takes one token per step
-// with few registers (many resident warps).
+// 16-byte asynchronous global -> shared copy (L2 only) and its group bookkeeping.
+__device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_dst), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+constexpr int kRingTok = 8;        // Non-Shared tokens in flight per warp
+constexpr int kPieceWarps = 8;     // warps per CTA of ns_piece_kernel
+
+// Non-Shared stage of one (request, beam, KV head) over one piece of its ancestry positions
+// (at most kNsChunk of them), stored as workspace piece `nsplit + piece` for the Shared-
+// stage epilogue (one piece: step <= 32) or the row-merge kernel to merge; prefix-length
+// problems and empty rows are reported by those.
+//
+// The pool rows are gathered with cp.async into a per-warp ring of kRingTok tokens in shared
+// memory (one instruction per token: half the lanes copy the K row, half the V row), so
+// eight tokens' loads are in flight while one is computed, without registers held for them.
+// Lane mapping for the arithmetic: lane = (query head within a group of HG heads, slice of EL
+// consecutive elements of d), so a dot product reduces over LP = 32 / HG lanes only; groups
+// of more than four heads are done in passes over the piece.
 template <int D, int G>
-__global__ void __launch_bounds__(256, 4) ns_piece_kernel(
-    Geometry g, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ pool_k,
+__global__ void __launch_bounds__(kPieceWarps * 32, D * (G < 4 ? G : 4) / 32 >= 16 ? 3 : 4) ns_piece_kernel(
+    Geometry g, int npc, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ pool_k,
     const __nv_bfloat16* __restrict__ pool_v, const int32_t* __restrict__ idx, float* __restrict__ part_o,
     float* __restrict__ part_lse, int32_t* status) {
     constexpr int HG = G < 4 ? G : 4;  // heads per pass
     constexpr int LP = 32 / HG;        // lanes per head
     constexpr int EL = D / LP;         // elements of d per lane (2 .. 16)
     constexpr int NV = EL / 2;         // bf16 pairs per lane
-    constexpr int kLines = D * 2 / 128;  // 128-byte lines per pool row
-    const int lane = threadIdx.x & 31;
-    const long warp_id = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (warp_id >= (long)g.R * g.BW * g.Hkv) return;
-    const int h = (int)(warp_id % g.Hkv);
-    const int b = (int)((warp_id / g.Hkv) % g.BW);
-    const int r = (int)(warp_id / ((long)g.Hkv * g.BW));
+    constexpr int RB = D * 2;          // bytes of one pool row (one head)
+    constexpr int LR = RB / 16;        // lanes copying one row
+    static_assert(2 * LR <= 32, "one cp.async per lane covers the K and the V row of a token");
+    static_assert(kNsChunk <= 64, "a lane holds the slots of positions lane and lane + 32");
+    __shared__ __align__(16) uint8_t ring[kPieceWarps][kRingTok][2 * RB];
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    long w = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (w >= (long)g.R * g.BW * g.Hkv * npc) return;
+    const int c = (int)(w % npc);  // piece: ancestry positions [c * kNsChunk, ...)
+    w /= npc;
+    const int h = (int)(w % g.Hkv);
+    const int b = (int)((w / g.Hkv) % g.BW);
+    const int r = (int)(w / ((long)g.Hkv * g.BW));
     const int hg = lane / LP, sl = lane % LP;
     const size_t qrow0 = ((size_t)r * g.BW + b) * g.Hq + (size_t)h * G;
-    const size_t prow0 = (((size_t)r * g.Hkv + h) * g.pieces + g.nsplit) * g.M + (size_t)b * G;
-    const int32_t* row_idx = idx + ((size_t)r * g.BW + b) * g.Tmax;
-    const int step = g.step;
-    const int my_slot = lane < step ? __ldg(row_idx + lane) : 0;
-    const bool slot_bad = __any_sync(0xffffffffu, lane < step && (my_slot < 0 || my_slot >= g.S));
+    const size_t prow0 = (((size_t)r * g.Hkv + h) * g.pieces + g.nsplit + c) * g.M + (size_t)b * G;
+    const int i0 = c * kNsChunk;
+    const int n = min(kNsChunk, g.step - i0);  // positions of this piece
+    const int32_t* row_idx = idx + ((size_t)r * g.BW + b) * g.Tmax + i0;
+    const int slot_a = lane < n ? __ldg(row_idx + lane) : 0;
+    const int slot_b = lane + 32 < n ? __ldg(row_idx + lane + 32) : 0;
+    const bool slot_bad = __any_sync(0xffffffffu, (lane < n && (slot_a < 0 || slot_a >= g.S)) ||
+                                                       (lane + 32 < n && (slot_b < 0 || slot_b >= g.S)));
     if (slot_bad && lane == 0) set_status(status, XATTN_STATUS_BAD_SLOT);
-    const size_t head_off = (size_t)h * D;
-    if (!slot_bad) {
-        // prefetch every (token, K/V, line) of the walk: 32 lanes per pass
-        constexpr int kPerTok = 2 * kLines;
-        for (int base = 0; base < step * kPerTok; base += 32) {
-            const int e = base + lane;
-            const int t = min(e / kPerTok, 31);
-            const int slot = __shfl_sync(0xffffffffu, my_slot, t);
-            if (e < step * kPerTok) {
-                const int kv = (e / kLines) & 1, line = e % kLines;
-                const __nv_bfloat16* row = (kv ? pool_v : pool_k) + ((size_t)r * g.S + slot) * g.Hkv * D + head_off;
-                asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const char*>(row) + line * 128));
-            }
-        }
-    }
-    const size_t kv_lane = head_off + (size_t)sl * EL;  // offset of this lane's slice in a pool row
+    const int nw = slot_bad ? 0 : n;  // tokens walked
 
-    auto load_pairs = [](const __nv_bfloat16* p, uint32_t (&w)[NV]) {
-        if constexpr (NV >= 4) {
-#pragma unroll
-            for (int c = 0; c < NV / 4; ++c) {
-                const uint4 u = __ldg(reinterpret_cast<const uint4*>(p) + c);
-                w[4 * c] = u.x; w[4 * c + 1] = u.y; w[4 * c + 2] = u.z; w[4 * c + 3] = u.w;
-            }
-        } else if constexpr (NV == 2) {
-            const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
-            w[0] = u.x; w[1] = u.y;
-        } else {
-            w[0] = __ldg(reinterpret_cast<const uint32_t*>(p));
+    // copy role of this lane: the K row (lanes 0..LR-1) or the V row (LR..2LR-1) of a token
+    const bool copier = lane < 2 * LR;
+    const __nv_bfloat16* src_base = (lane < LR ? pool_k : pool_v) + (size_t)h * D + (lane % LR) * 8;
+    const uint32_t ring_base = (uint32_t)__cvta_generic_to_shared(&ring[wib][0][0]) + (lane < LR ? 0 : RB) + (lane % LR) * 16;
+    auto issue = [&](int t) {  // token t of the piece into ring slot t % kRingTok (always one group)
+        const int sa = __shfl_sync(0xffffffffu, slot_a, t & 31);
+        const int sb = __shfl_sync(0xffffffffu, slot_b, t & 31);
+        if (copier && t < nw) {
+            const int slot = t < 32 ? sa : sb;
+            cp_async16(ring_base + (t % kRingTok) * (2 * RB), src_base + ((size_t)r * g.S + slot) * g.Hkv * D);
         }
+        cp_async_commit();
     };
     // bf16 pair -> two floats (a bf16 is the top half of its fp32)
-    auto lo = [](uint32_t w) { return __uint_as_float(w << 16); };
-    auto hi = [](uint32_t w) { return __uint_as_float(w & 0xffff0000u); };
+    auto lo = [](uint32_t x) { return __uint_as_float(x << 16); };
+    auto hi = [](uint32_t x) { return __uint_as_float(x & 0xffff0000u); };
 
 #pragma unroll 1
     for (int pass = 0; pass < G / HG; ++pass) {
         const int gg = pass * HG + hg;
         uint32_t qw[NV];
-        load_pairs(q + (qrow0 + gg) * D + sl * EL, qw);
+        {
+            const __nv_bfloat16* qp = q + (qrow0 + gg) * D + sl * EL;
+            if constexpr (NV >= 4) {
+#pragma unroll
+                for (int k = 0; k < NV / 4; ++k) {
+                    const uint4 u = __ldg(reinterpret_cast<const uint4*>(qp) + k);
+                    qw[4 * k] = u.x; qw[4 * k + 1] = u.y; qw[4 * k + 2] = u.z; qw[4 * k + 3] = u.w;
+                }
+            } else if constexpr (NV == 2) {
+                const uint2 u = __ldg(reinterpret_cast<const uint2*>(qp));
+                qw[0] = u.x; qw[1] = u.y;
+            } else {
+                qw[0] = __ldg(reinterpret_cast<const uint32_t*>(qp));
+            }
+        }
         float m = -INFINITY, l = 0.f, acc[EL];
 #pragma unroll
         for (int e = 0; e < EL; ++e) acc[e] = 0.f;
-        if (!slot_bad) {
-            for (int t = 0; t < step; ++t) {
-                const int slot = __shfl_sync(0xffffffffu, my_slot, t);
-                const size_t off = ((size_t)r * g.S + slot) * g.Hkv * D + kv_lane;
-                uint32_t kw[NV], vw[NV];
-                load_pairs(pool_k + off, kw);
-                load_pairs(pool_v + off, vw);
-                float sc = 0.f;
+        for (int t = 0; t < kRingTok; ++t) issue(t);
+        for (int t = 0; t < nw; ++t) {
+            cp_async_wait<kRingTok - 1>();  // this lane's copy of token t has landed
+            __syncwarp();                   // ... and every other lane's
+            const uint8_t* tok = &ring[wib][t % kRingTok][0];
+            uint32_t kw[NV], vw[NV];
 #pragma unroll
-                for (int c = 0; c < NV; ++c) {
-                    sc = fmaf(lo(qw[c]), lo(kw[c]), sc);
-                    sc = fmaf(hi(qw[c]), hi(kw[c]), sc);
+            for (int k = 0; k < NV; k += 4 > NV ? NV : 4) {
+                if constexpr (NV >= 4) {
+                    const uint4 ku = *reinterpret_cast<const uint4*>(tok + sl * EL * 2 + k * 4);
+                    const uint4 vu = *reinterpret_cast<const uint4*>(tok + RB + sl * EL * 2 + k * 4);
+                    kw[k] = ku.x; kw[k + 1] = ku.y; kw[k + 2] = ku.z; kw[k + 3] = ku.w;
+                    vw[k] = vu.x; vw[k + 1] = vu.y; vw[k + 2] = vu.z; vw[k + 3] = vu.w;
+                } else if constexpr (NV == 2) {
+                    const uint2 ku = *reinterpret_cast<const uint2*>(tok + sl * EL * 2);
+                    const uint2 vu = *reinterpret_cast<const uint2*>(tok + RB + sl * EL * 2);
+                    kw[0] = ku.x; kw[1] = ku.y; vw[0] = vu.x; vw[1] = vu.y;
+                } else {
+                    kw[0] = *reinterpret_cast<const uint32_t*>(tok + sl * EL * 2);
+                    vw[0] = *reinterpret_cast<const uint32_t*>(tok + RB + sl * EL * 2);
                 }
-#pragma unroll
-                for (int o = LP / 2; o > 0; o >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, o);
-                const float s2 = sc * g.scale_log2;
-                const float mn = fmaxf(m, s2);
-                const float alpha = ex2(m - mn), p = ex2(s2 - mn);
-                l = l * alpha + p;
-#pragma unroll
-                for (int c = 0; c < NV; ++c) {
-                    acc[2 * c] = fmaf(p, lo(vw[c]), acc[2 * c] * alpha);
-                    acc[2 * c + 1] = fmaf(p, hi(vw[c]), acc[2 * c + 1] * alpha);
-                }
-                m = mn;
             }
+            __syncwarp();  // the slot is read: it may be refilled
+            issue(t + kRingTok);
+            float sc = 0.f;
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                sc = fmaf(lo(qw[k]), lo(kw[k]), sc);
+                sc = fmaf(hi(qw[k]), hi(kw[k]), sc);
+            }
+#pragma unroll
+            for (int o = LP / 2; o > 0; o >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, o);
+            const float s2 = sc * g.scale_log2;
+            const float mn = fmaxf(m, s2);
+            const float alpha = ex2(m - mn), p = ex2(s2 - mn);
+            l = l * alpha + p;
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                acc[2 * k] = fmaf(p, lo(vw[k]), acc[2 * k] * alpha);
+                acc[2 * k + 1] = fmaf(p, hi(vw[k]), acc[2 * k + 1] * alpha);
+            }
+            m = mn;
         }
+        cp_async_wait<0>();  // nothing of this pass stays in flight
+        __syncwarp();
         const bool empty = !(l > 0.f);
         const float inv = empty ? 0.f : 1.f / l;
         float* po = part_o + (prow0 + gg) * D + sl * EL;
         if constexpr (EL >= 4) {
 #pragma unroll
-            for (int c = 0; c < EL / 4; ++c)
-                reinterpret_cast<float4*>(po)[c] =
-                    make_float4(acc[4 * c] * inv, acc[4 * c + 1] * inv, acc[4 * c + 2] * inv, acc[4 * c + 3] * inv);
+            for (int k = 0; k < EL / 4; ++k)
+                reinterpret_cast<float4*>(po)[k] =
+                    make_float4(acc[4 * k] * inv, acc[4 * k + 1] * inv, acc[4 * k + 2] * inv, acc[4 * k + 3] * inv);
         } else {
             *reinterpret_cast<float2*>(po) = make_float2(acc[0] * inv, acc[1] * inv);
         }
@@ -509,129 +551,22 @@ __global__ void __launch_bounds__(256) merge_rows_kernel(
     if (lane == 0) lse[row] = bad ? __uint_as_float(kNaN) : (mx + __log2f(lsum)) * kLn2;
 }
 
-// One piece of a long Non-Shared part: ancestry positions [c*kNsChunk, (c+1)*kNsChunk) of
-// beam b. Warp w takes groups of four consecutive positions, w*4, w*4 + 16, ...; the four
-// tokens' K and V rows are loaded before any is used.
-constexpr int kPartWarps = 4;
-constexpr int kUnroll = 4;
-static_assert(kNsChunk == 64, "slots of a piece are held as two 32-lane registers");
-
-template <int D, int G>
-__global__ void __launch_bounds__(kPartWarps * 32) ns_partial_kernel(
-    Geometry g, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ pool_k,
-    const __nv_bfloat16* __restrict__ pool_v, const int32_t* __restrict__ idx, float* __restrict__ part_o,
-    float* __restrict__ part_lse, int32_t* status) {
-    constexpr int E = D / 32;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    long t = blockIdx.x;
-    const int c = (int)(t % g.ns_pieces);
-    t /= g.ns_pieces;
-    const int h = (int)(t % g.Hkv);
-    const int b = (int)((t / g.Hkv) % g.BW);
-    const int r = (int)(t / ((long)g.Hkv * g.BW));
-    const int i0 = c * kNsChunk, i1 = min(i0 + kNsChunk, g.step);
-    const size_t qrow0 = ((size_t)r * g.BW + b) * g.Hq + (size_t)h * G;
-
-    float qv[G][E];
-#pragma unroll
-    for (int gg = 0; gg < G; ++gg) LaneVec<D>::load(q + (qrow0 + gg) * D + lane * E, qv[gg]);
-    const int32_t* row_idx = idx + ((size_t)r * g.BW + b) * g.Tmax;
-    // this piece's slots: lane l holds positions i0 + l and i0 + 32 + l
-    const int sl0 = (i0 + lane < i1) ? __ldg(row_idx + i0 + lane) : 0;
-    const int sl1 = (i0 + 32 + lane < i1) ? __ldg(row_idx + i0 + 32 + lane) : 0;
-
-    RowState<E, G> st;
-    st.init();
-    bool bad = false;
-    for (int base = warp * kUnroll; base < kNsChunk; base += kPartWarps * kUnroll) {
-        float kv[kUnroll][E], vv[kUnroll][E];
-        bool use[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int pos = base + u;  // position within the piece, < 64
-            const int s0 = __shfl_sync(0xffffffffu, sl0, pos & 31);
-            const int s1 = __shfl_sync(0xffffffffu, sl1, pos & 31);
-            const int slot = pos < 32 ? s0 : s1;
-            use[u] = i0 + pos < i1;
-            if (use[u] && (slot < 0 || slot >= g.S)) {
-                bad = true;
-                use[u] = false;
-            }
-            if (use[u]) {
-                const size_t off = (((size_t)r * g.S + slot) * g.Hkv + h) * D + lane * E;
-                LaneVec<D>::load(pool_k + off, kv[u]);
-                LaneVec<D>::load(pool_v + off, vv[u]);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            if (!use[u]) continue;
-#pragma unroll
-            for (int gg = 0; gg < G; ++gg) {
-                float s = 0.f;
-#pragma unroll
-                for (int e = 0; e < E; ++e) s = fmaf(qv[gg][e], kv[u][e], s);
-                st.add(gg, warp_sum(s) * g.scale_log2, vv[u]);
-            }
-        }
-    }
-    if (bad && lane == 0) set_status(status, XATTN_STATUS_BAD_SLOT);
-
-    // combine the four warps' states per row and write the piece
-    __shared__ float sm_m[kPartWarps][G], sm_l[kPartWarps][G];
-    __shared__ float sm_acc[kPartWarps][G][D];
-    __shared__ int sm_bad;
-    if (threadIdx.x == 0) sm_bad = 0;
-    __syncthreads();
-    if (bad) sm_bad = 1;
-#pragma unroll
-    for (int gg = 0; gg < G; ++gg) {
-        if (lane == 0) {
-            sm_m[warp][gg] = st.m[gg];
-            sm_l[warp][gg] = st.l[gg];
-        }
-#pragma unroll
-        for (int e = 0; e < E; ++e) sm_acc[warp][gg][lane * E + e] = st.acc[gg][e];
-    }
-    __syncthreads();
-    const size_t prow0 = (((size_t)r * g.Hkv + h) * g.pieces + g.nsplit + c) * g.M + (size_t)b * G;
-    for (int gg = warp; gg < G; gg += kPartWarps) {
-        float M = -INFINITY;
-        for (int w = 0; w < kPartWarps; ++w) M = fmaxf(M, sm_m[w][gg]);
-        float wt[kPartWarps], wsum = 0.f;
-        for (int w = 0; w < kPartWarps; ++w) {
-            wt[w] = (sm_m[w][gg] == -INFINITY) ? 0.f : ex2(sm_m[w][gg] - M);
-            wsum += sm_l[w][gg] * wt[w];
-        }
-        const bool empty = !(wsum > 0.f);
-        const float inv = empty ? 0.f : 1.f / wsum;
-        for (int e = lane; e < D; e += 32) {
-            float o = 0.f;
-            for (int w = 0; w < kPartWarps; ++w) o += sm_acc[w][gg][e] * wt[w];
-            part_o[(prow0 + gg) * D + e] = o * inv;
-        }
-        if (lane == 0)
-            part_lse[prow0 + gg] = sm_bad ? __uint_as_float(kNaN) : (empty ? -INFINITY : (M + __log2f(wsum)) * kLn2);
-    }
-}
-
 template <int D>
 cudaError_t launch_d(const Geometry& g, cudaStream_t st, const __nv_bfloat16* q, const __nv_bfloat16* pk,
                      const __nv_bfloat16* pv, const int32_t* idx, const int32_t* slen, float* po, float* pl,
                      void* out, float* lse, int32_t* status) {
     const dim3 grid((unsigned)(((long)g.R * g.BW * g.Hkv + 7) / 8)), block(256);
-    const long part_ctas = (long)g.R * g.BW * g.Hkv * g.ns_pieces;
-    if (part_ctas > 0x7fffffffL) return cudaErrorInvalidValue;
+    static_assert(kPieceWarps == 8, "ns_piece_kernel runs 8 warps per CTA, like the other kernels here");
+    const int npc = g.ns_to_piece ? 1 : g.ns_pieces;  // Non-Shared pieces per (r, b, h)
+    const long piece_ctas = ((long)g.R * g.BW * g.Hkv * npc + 7) / 8;
+    if (piece_ctas > 0x7fffffffL) return cudaErrorInvalidValue;
     const unsigned rows_ctas = (unsigned)(((long)g.R * g.BW * g.Hq + 7) / 8);
     switch (g.G) {
 #define XATTN_G(GV)                                                                                              \
     case GV:                                                                                                     \
-        if (g.ns_to_piece) {                                                                                     \
-            ns_piece_kernel<D, GV><<<grid, block, 0, st>>>(g, q, pk, pv, idx, po, pl, status);                  \
-        } else if (g.ns_pieces > 0) {                                                                            \
-            ns_partial_kernel<D, GV><<<(unsigned)part_ctas, kPartWarps * 32, 0, st>>>(g, q, pk, pv, idx, po, pl, \
-                                                                                       status);                 \
-            merge_rows_kernel<D><<<rows_ctas, block, 0, st>>>(g, slen, po, pl, out, lse, status);               \
+        if (g.ns_to_piece || g.ns_pieces > 0) {                                                                  \
+            ns_piece_kernel<D, GV><<<(unsigned)piece_ctas, block, 0, st>>>(g, npc, q, pk, pv, idx, po, pl, status); \
+            if (!g.ns_to_piece) merge_rows_kernel<D><<<rows_ctas, block, 0, st>>>(g, slen, po, pl, out, lse, status); \
         } else {                                                                                                 \
             ns_merge_kernel<D, GV><<<grid, block, 0, st>>>(g, q, pk, pv, idx, slen, po, pl, out, lse, status); \
         }                                                                                                        \
