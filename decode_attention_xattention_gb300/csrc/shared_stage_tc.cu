@@ -131,6 +131,23 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     const long unit = t / g.nsplit;
     const int h = (int)(unit % g.Hkv);
     const int r = (int)(unit / g.Hkv);
+    // Softmax threads prefetch their Q row (into L1) and, for the fused epilogue, their row of
+    // the Non-Shared piece (into L2, kept there) before anything else: the latencies overlap
+    // the prefix-length load, the barrier set-up, the TMEM allocation and the main loop.
+    if (warp < 8) {
+        const int mt0 = 2 * mp + (warp >> 2), row0 = mt0 * kTileRows + (tid & 127);
+        if (mt0 < g.row_tiles && row0 < g.M) {
+            const int b0 = row0 / g.G, g0 = row0 - (row0 / g.G) * g.G;
+            const char* qp = reinterpret_cast<const char*>(q + (((size_t)r * g.BW + b0) * g.Hq + (size_t)h * g.G + g0) * D);
+#pragma unroll
+            for (int ln = 0; ln < D * 2 / 128; ++ln) asm volatile("prefetch.global.L1 [%0];" ::"l"(qp + ln * 128));
+            if (fa.enabled && g.step > 0) {
+                const char* np = reinterpret_cast<const char*>(part_o + (((size_t)unit * g.pieces + g.nsplit) * g.M + row0) * D);
+#pragma unroll
+                for (int ln = 0; ln < D * 4 / 128; ++ln) asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(np + ln * 128));
+            }
+        }
+    }
     const int L_raw = shared_len[r];
     const bool bad_len = L_raw < 0 || L_raw > g.Lmax;
     const int L = bad_len ? 0 : L_raw;
@@ -178,12 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         bool ok = true;
         if (tile_ok && ntiles > 0) {
             {  // Q tile -> shared memory, K-major, 128-byte swizzle; rows past M are zero
-                const __nv_bfloat16* src = row_ok ? q + (((size_t)r * g.BW + b) * g.Hq + (size_t)h * g.G + gg) * D
-                                                  : nullptr;
+                const uint4* src = reinterpret_cast<const uint4*>(q + (((size_t)r * g.BW + b) * g.Hq + (size_t)h * g.G + gg) * D);
 #pragma unroll
                 for (int ch = 0; ch < D / 8; ++ch) {
-                    uint4 v = make_uint4(0, 0, 0, 0);
-                    if (row_ok) v = __ldg(reinterpret_cast<const uint4*>(src) + ch);
+                    const uint4 v = row_ok ? __ldg(src + ch) : make_uint4(0, 0, 0, 0);
                     *reinterpret_cast<uint4*>(sQw + sw128_offset(rloc, ch)) = v;
                 }
                 fence_proxy_async_smem();
@@ -390,12 +405,11 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                     if (j >= 1) tma_prefetch_4d(&tmap_v, kb * 64, h, t0 + (j - 1) * kTcTileKeys, r);
                 }
             };
-            for (int j = 0; j < min(nunits, kPrefetch); ++j) prefetch_unit(j);
             int issued = 0;
             for (int j = 0; j < nunits; ++j) {
                 const int st = j % kU, use = j / kU;
                 if (use > 0 && !mbar_wait(&bars.u_empty[st], (use - 1) & 1, &abort_sh)) break;
-                if (j + kPrefetch < nunits) prefetch_unit(j + kPrefetch);
+                if (j >= kU && j + kPrefetch < nunits) prefetch_unit(j + kPrefetch);
                 uint8_t* slot = sU + st * C::kUnitBytes;
                 mbar_arrive_expect_tx(&bars.u_full[st],
                                       (j < ntiles ? C::kTileBytes : 0) + (j >= 1 ? C::kTileBytes : 0));
@@ -407,6 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                                     t0 + (j - 1) * kTcTileKeys, r);
                 }
                 issued = j + 1;
+                if (j == kU - 1)  // the first units' loads went out before any L2 prefetch
+                    for (int jp = kU; jp < min(nunits, kU + kPrefetch); ++jp) prefetch_unit(jp);
             }
             if (abort_sh) {  // let the copies still in flight land before the CTA exits
                 volatile int never = 0;
