@@ -103,12 +103,13 @@ struct FusedArgs {
     void* out;
     float* lse;
     int enabled;
+    int q_tma;  // the producer loads the Q tiles with TMA (tmap_q); else the softmax threads do
 };
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-    Geometry g, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ shared_len,
+    const __grid_constant__ CUtensorMap tmap_q, Geometry g, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ shared_len,
     float* __restrict__ part_o, float* __restrict__ part_lse, int32_t* status, FusedArgs fa) {
     using C = Cfg<D>;
     constexpr int kU = C::kUnits;
@@ -131,16 +132,17 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     const long unit = t / g.nsplit;
     const int h = (int)(unit % g.Hkv);
     const int r = (int)(unit / g.Hkv);
-    // Softmax threads prefetch their Q row (into L1) and, for the fused epilogue, their row of
-    // the Non-Shared piece (into L2, kept there) before anything else: the latencies overlap
-    // the prefix-length load, the barrier set-up, the TMEM allocation and the main loop.
+    // Softmax threads prefetch their Q row into L1 (when they load Q themselves) and, for the
+    // fused epilogue, their row of the Non-Shared piece into L2 (kept there): the latencies
+    // overlap the prefix-length load and the main loop.
     if (warp < 8) {
         const int mt0 = 2 * mp + (warp >> 2), row0 = mt0 * kTileRows + (tid & 127);
         if (mt0 < g.row_tiles && row0 < g.M) {
             const int b0 = row0 / g.G, g0 = row0 - (row0 / g.G) * g.G;
             const char* qp = reinterpret_cast<const char*>(q + (((size_t)r * g.BW + b0) * g.Hq + (size_t)h * g.G + g0) * D);
+            if (!fa.q_tma)
 #pragma unroll
-            for (int ln = 0; ln < D * 2 / 128; ++ln) asm volatile("prefetch.global.L1 [%0];" ::"l"(qp + ln * 128));
+                for (int ln = 0; ln < D * 2 / 128; ++ln) asm volatile("prefetch.global.L1 [%0];" ::"l"(qp + ln * 128));
             if (fa.enabled && g.step > 0) {
                 const char* np = reinterpret_cast<const char*>(part_o + (((size_t)unit * g.pieces + g.nsplit) * g.M + row0) * D);
 #pragma unroll
@@ -164,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars.s_full[i], 1);
             mbar_init(&bars.p_full[i], 4);
-            mbar_init(&bars.q_ready[i], 128);
+            mbar_init(&bars.q_ready[i], fa.q_tma ? 1 : 128);
         }
         mbar_init(&bars.o_full[0], 1);
         mbar_init(&bars.o_full[1], 1);
@@ -194,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         if (tile_ok && ntiles > 0) {
-            {  // Q tile -> shared memory, K-major, 128-byte swizzle; rows past M are zero
+            if (!fa.q_tma) {  // Q tile -> shared memory, K-major, 128-byte swizzle; rows past M are zero
                 const uint4* src = reinterpret_cast<const uint4*>(q + (((size_t)r * g.BW + b) * g.Hq + (size_t)h * g.G + gg) * D);
 #pragma unroll
                 for (int ch = 0; ch < D / 8; ++ch) {
@@ -396,6 +398,15 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         // unit j - kU has been consumed; L2 prefetch kPrefetch units ahead hides most of the
         // HBM latency of the later load.
         if (lane == 0 && ntiles > 0) {
+            if (fa.q_tma) {  // the Q tiles first: 128 rows x 64 d boxes, rows past BW zero-filled
+                prefetch_tmap(&tmap_q);
+                for (int i = 0; i < ntile_m; ++i) {
+                    mbar_arrive_expect_tx(&bars.q_ready[i], C::kTileBytes);
+                    for (int kb = 0; kb < C::KB; ++kb)
+                        tma_load_4d(sQ + i * C::kTileBytes + kb * 16384, &tmap_q, &bars.q_ready[i], kb * 64, h * g.G,
+                                    ((2 * mp + i) * kTileRows) / g.G, r);
+                }
+            }
             prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
             const int nunits = ntiles + 1;
@@ -427,6 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             if (abort_sh) {  // let the copies still in flight land before the CTA exits
                 volatile int never = 0;
                 for (int j = max(0, issued - kU); j < issued; ++j) mbar_wait(&bars.u_full[j % kU], (j / kU) & 1, &never);
+                if (fa.q_tma)
+                    for (int i = 0; i < ntile_m; ++i) mbar_wait(&bars.q_ready[i], 0, &never);
             }
         }
     } else {
@@ -511,9 +524,9 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
 }
 
 template <int D>
-cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap& tv, const __nv_bfloat16* q,
-                     const int32_t* slen, float* po, float* pl, int32_t* status, const FusedArgs& fa,
-                     cudaStream_t stream) {
+cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                     const __nv_bfloat16* q, const int32_t* slen, float* po, float* pl, int32_t* status,
+                     const FusedArgs& fa, cudaStream_t stream) {
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -524,8 +537,8 @@ cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
     const long ctas = shared_tc_ctas_for(g);
-    shared_stage_tc_kernel<D><<<(unsigned)ctas, kThreads, Cfg<D>::kSmemBytes, stream>>>(tk, tv, g, q, slen, po, pl,
-                                                                                         status, fa);
+    shared_stage_tc_kernel<D><<<(unsigned)ctas, kThreads, Cfg<D>::kSmemBytes, stream>>>(tk, tv, tq, g, q, slen, po,
+                                                                                         pl, status, fa);
     return cudaGetLastError();
 }
 
@@ -534,12 +547,13 @@ cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap
 int shared_tc_ctas_for(const Geometry& g) { return g.R * g.Hkv * g.nsplit * ((g.row_tiles + 1) / 2); }
 
 cudaError_t launch_shared_stage_tc(const Geometry& g, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
-                                   const __nv_bfloat16* q, const int32_t* shared_len, float* part_o,
-                                   float* part_lse, int32_t* status, void* out, float* lse, bool fused,
-                                   cudaStream_t stream) {
-    FusedArgs fa{out, lse, fused ? 1 : 0};
-    if (g.d == 128) return launch_d<128>(g, tmap_k, tmap_v, q, shared_len, part_o, part_lse, status, fa, stream);
-    if (g.d == 64) return launch_d<64>(g, tmap_k, tmap_v, q, shared_len, part_o, part_lse, status, fa, stream);
+                                   const CUtensorMap* tmap_q, const __nv_bfloat16* q, const int32_t* shared_len,
+                                   float* part_o, float* part_lse, int32_t* status, void* out, float* lse,
+                                   bool fused, cudaStream_t stream) {
+    FusedArgs fa{out, lse, fused ? 1 : 0, tmap_q ? 1 : 0};
+    const CUtensorMap& tq = tmap_q ? *tmap_q : tmap_k;  // unused when the threads load Q
+    if (g.d == 128) return launch_d<128>(g, tmap_k, tmap_v, tq, q, shared_len, part_o, part_lse, status, fa, stream);
+    if (g.d == 64) return launch_d<64>(g, tmap_k, tmap_v, tq, q, shared_len, part_o, part_lse, status, fa, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -134,6 +134,23 @@ CUresult make_kv_map(CUtensorMap* map, const void* base, const Geometry& g) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// Q [R, BW, Hq, d] viewed innermost-first as {d, Hq, BW, R}; box = 64 x G x (128 / G) x 1:
+// the 128 stacked rows (beam, query head of KV head h) of one row tile, row m = b*G + g.
+// Only when G divides 128; otherwise the kernel's softmax threads load Q themselves.
+bool q_map_usable(const Geometry& g) { return g.G <= 128 && 128 % g.G == 0; }
+
+CUresult make_q_map(CUtensorMap* map, const void* base, const Geometry& g) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return CUDA_ERROR_NOT_FOUND;
+    cuuint64_t dims[4] = {(cuuint64_t)g.d, (cuuint64_t)g.Hq, (cuuint64_t)g.BW, (cuuint64_t)g.R};
+    cuuint64_t strides[3] = {(cuuint64_t)g.d * 2, (cuuint64_t)g.Hq * g.d * 2, (cuuint64_t)g.BW * g.Hq * g.d * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)g.G, (cuuint32_t)(kTileRows / g.G), 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 }  // namespace
 }  // namespace xattn
 
@@ -225,11 +242,13 @@ int run_shared(const Geometry& g, int kernel, const void* q, const void* shared_
     auto qb = reinterpret_cast<const __nv_bfloat16*>(q);
     cudaError_t e = cudaSuccess;
     if (kernel == 1) {
-        CUtensorMap mk, mv;
+        CUtensorMap mk, mv, mq;
         if (make_kv_map(&mk, shared_k, g) != CUDA_SUCCESS || make_kv_map(&mv, shared_v, g) != CUDA_SUCCESS)
             return XATTN_ERR_CUDA;
-        e = launch_shared_stage_tc(g, mk, mv, qb, shared_len, ws.part_o, ws.part_lse, ws.status, out, lse, fused,
-                                   st);
+        const bool q_tma = q_map_usable(g);
+        if (q_tma && make_q_map(&mq, q, g) != CUDA_SUCCESS) return XATTN_ERR_CUDA;
+        e = launch_shared_stage_tc(g, mk, mv, q_tma ? &mq : nullptr, qb, shared_len, ws.part_o, ws.part_lse,
+                                   ws.status, out, lse, fused, st);
     } else if (kernel == 2) {
         e = launch_shared_stage_simt(g, qb, reinterpret_cast<const __nv_bfloat16*>(shared_k),
                                      reinterpret_cast<const __nv_bfloat16*>(shared_v), shared_len, ws.part_o,
