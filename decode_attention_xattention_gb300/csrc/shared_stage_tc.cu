@@ -85,12 +85,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return r;
 }
 
-// Byte offset of 16-byte chunk `ch` (along the contraction dim) of row `row` in a tile
-// stored as [ch/8 block][128 rows][128 B] with the 128-byte swizzle (chunk ^= row % 8).
-__device__ __forceinline__ uint32_t sw128_offset(int row, int ch) {
-    return (uint32_t)((ch >> 3) * 16384 + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
-}
-
 struct Bars {
     uint64_t u_full[kMaxStages], u_empty[kMaxStages];
     uint64_t s_full[2], p_full[2], q_ready[2];
@@ -103,7 +97,6 @@ struct FusedArgs {
     void* out;
     float* lse;
     int enabled;
-    int q_tma;  // the producer loads the Q tiles with TMA (tmap_q); else the softmax threads do
 };
 
 template <int D>
@@ -132,22 +125,14 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     const long unit = t / g.nsplit;
     const int h = (int)(unit % g.Hkv);
     const int r = (int)(unit / g.Hkv);
-    // Softmax threads prefetch their Q row into L1 (when they load Q themselves) and, for the
-    // fused epilogue, their row of the Non-Shared piece into L2 (kept there): the latencies
-    // overlap the prefix-length load and the main loop.
-    if (warp < 8) {
+    // For the fused epilogue, softmax threads prefetch their row of the Non-Shared piece into
+    // L2 (kept there): the latency overlaps the main loop.
+    if (warp < 8 && fa.enabled && g.step > 0) {
         const int mt0 = 2 * mp + (warp >> 2), row0 = mt0 * kTileRows + (tid & 127);
         if (mt0 < g.row_tiles && row0 < g.M) {
-            const int b0 = row0 / g.G, g0 = row0 - (row0 / g.G) * g.G;
-            const char* qp = reinterpret_cast<const char*>(q + (((size_t)r * g.BW + b0) * g.Hq + (size_t)h * g.G + g0) * D);
-            if (!fa.q_tma)
+            const char* np = reinterpret_cast<const char*>(part_o + (((size_t)unit * g.pieces + g.nsplit) * g.M + row0) * D);
 #pragma unroll
-                for (int ln = 0; ln < D * 2 / 128; ++ln) asm volatile("prefetch.global.L1 [%0];" ::"l"(qp + ln * 128));
-            if (fa.enabled && g.step > 0) {
-                const char* np = reinterpret_cast<const char*>(part_o + (((size_t)unit * g.pieces + g.nsplit) * g.M + row0) * D);
-#pragma unroll
-                for (int ln = 0; ln < D * 4 / 128; ++ln) asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(np + ln * 128));
-            }
+            for (int ln = 0; ln < D * 4 / 128; ++ln) asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(np + ln * 128));
         }
     }
     const int L_raw = shared_len[r];
@@ -166,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars.s_full[i], 1);
             mbar_init(&bars.p_full[i], 4);
-            mbar_init(&bars.q_ready[i], fa.q_tma ? 1 : 128);
+            mbar_init(&bars.q_ready[i], 1);
         }
         mbar_init(&bars.o_full[0], 1);
         mbar_init(&bars.o_full[1], 1);
@@ -192,20 +177,9 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         const int row = mt * kTileRows + rloc;
         const bool row_ok = tile_ok && row < g.M;
         const int b = row / g.G, gg = row - (row / g.G) * g.G;
-        uint8_t* sQw = sQ + wg * C::kTileBytes;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         if (tile_ok && ntiles > 0) {
-            if (!fa.q_tma) {  // Q tile -> shared memory, K-major, 128-byte swizzle; rows past M are zero
-                const uint4* src = reinterpret_cast<const uint4*>(q + (((size_t)r * g.BW + b) * g.Hq + (size_t)h * g.G + gg) * D);
-#pragma unroll
-                for (int ch = 0; ch < D / 8; ++ch) {
-                    const uint4 v = row_ok ? __ldg(src + ch) : make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4*>(sQw + sw128_offset(rloc, ch)) = v;
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(&bars.q_ready[wg]);
-            }
             const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
             const uint32_t tS = tmem + lane_base + wg * 128;
             const uint32_t tO = tmem + lane_base + kTmemO + wg * 128;
@@ -398,14 +372,14 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         // unit j - kU has been consumed; L2 prefetch kPrefetch units ahead hides most of the
         // HBM latency of the later load.
         if (lane == 0 && ntiles > 0) {
-            if (fa.q_tma) {  // the Q tiles first: 128 rows x 64 d boxes, rows past BW zero-filled
-                prefetch_tmap(&tmap_q);
-                for (int i = 0; i < ntile_m; ++i) {
-                    mbar_arrive_expect_tx(&bars.q_ready[i], C::kTileBytes);
-                    for (int kb = 0; kb < C::KB; ++kb)
-                        tma_load_4d(sQ + i * C::kTileBytes + kb * 16384, &tmap_q, &bars.q_ready[i], kb * 64, h * g.G,
-                                    ((2 * mp + i) * kTileRows) / g.G, r);
-                }
+            // the Q tiles first: per row tile one 64 d x G heads x 128/G beams box per 64 d
+            // (128-byte swizzle, the K-major layout the MMA reads); beams past BW are zero-filled
+            prefetch_tmap(&tmap_q);
+            for (int i = 0; i < ntile_m; ++i) {
+                mbar_arrive_expect_tx(&bars.q_ready[i], C::kTileBytes);
+                for (int kb = 0; kb < C::KB; ++kb)
+                    tma_load_4d(sQ + i * C::kTileBytes + kb * 16384, &tmap_q, &bars.q_ready[i], kb * 64, h * g.G,
+                                ((2 * mp + i) * kTileRows) / g.G, r);
             }
             prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
@@ -438,8 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             if (abort_sh) {  // let the copies still in flight land before the CTA exits
                 volatile int never = 0;
                 for (int j = max(0, issued - kU); j < issued; ++j) mbar_wait(&bars.u_full[j % kU], (j / kU) & 1, &never);
-                if (fa.q_tma)
-                    for (int i = 0; i < ntile_m; ++i) mbar_wait(&bars.q_ready[i], 0, &never);
+                for (int i = 0; i < ntile_m; ++i) mbar_wait(&bars.q_ready[i], 0, &never);
             }
         }
     } else {
@@ -547,11 +520,10 @@ cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap
 int shared_tc_ctas_for(const Geometry& g) { return g.R * g.Hkv * g.nsplit * ((g.row_tiles + 1) / 2); }
 
 cudaError_t launch_shared_stage_tc(const Geometry& g, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
-                                   const CUtensorMap* tmap_q, const __nv_bfloat16* q, const int32_t* shared_len,
+                                   const CUtensorMap& tq, const __nv_bfloat16* q, const int32_t* shared_len,
                                    float* part_o, float* part_lse, int32_t* status, void* out, float* lse,
                                    bool fused, cudaStream_t stream) {
-    FusedArgs fa{out, lse, fused ? 1 : 0, tmap_q ? 1 : 0};
-    const CUtensorMap& tq = tmap_q ? *tmap_q : tmap_k;  // unused when the threads load Q
+    FusedArgs fa{out, lse, fused ? 1 : 0};
     if (g.d == 128) return launch_d<128>(g, tmap_k, tmap_v, tq, q, shared_len, part_o, part_lse, status, fa, stream);
     if (g.d == 64) return launch_d<64>(g, tmap_k, tmap_v, tq, q, shared_len, part_o, part_lse, status, fa, stream);
     return cudaErrorInvalidValue;

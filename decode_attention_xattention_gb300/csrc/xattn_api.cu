@@ -135,9 +135,8 @@ CUresult make_kv_map(CUtensorMap* map, const void* base, const Geometry& g) {
 }
 
 // Q [R, BW, Hq, d] viewed innermost-first as {d, Hq, BW, R}; box = 64 x G x (128 / G) x 1:
-// the 128 stacked rows (beam, query head of KV head h) of one row tile, row m = b*G + g.
-// Only when G divides 128; otherwise the kernel's softmax threads load Q themselves.
-bool q_map_usable(const Geometry& g) { return g.G <= 128 && 128 % g.G == 0; }
+// the 128 stacked rows (beam, query head of KV head h) of one row tile, row m = b*G + g
+// (G is a power of two up to 16, so it divides 128).
 
 CUresult make_q_map(CUtensorMap* map, const void* base, const Geometry& g) {
     auto enc = tensor_map_encoder();
@@ -245,10 +244,9 @@ int run_shared(const Geometry& g, int kernel, const void* q, const void* shared_
         CUtensorMap mk, mv, mq;
         if (make_kv_map(&mk, shared_k, g) != CUDA_SUCCESS || make_kv_map(&mv, shared_v, g) != CUDA_SUCCESS)
             return XATTN_ERR_CUDA;
-        const bool q_tma = q_map_usable(g);
-        if (q_tma && make_q_map(&mq, q, g) != CUDA_SUCCESS) return XATTN_ERR_CUDA;
-        e = launch_shared_stage_tc(g, mk, mv, q_tma ? &mq : nullptr, qb, shared_len, ws.part_o, ws.part_lse,
-                                   ws.status, out, lse, fused, st);
+        if (make_q_map(&mq, q, g) != CUDA_SUCCESS) return XATTN_ERR_CUDA;
+        e = launch_shared_stage_tc(g, mk, mv, mq, qb, shared_len, ws.part_o, ws.part_lse, ws.status, out, lse,
+                                   fused, st);
     } else if (kernel == 2) {
         e = launch_shared_stage_simt(g, qb, reinterpret_cast<const __nv_bfloat16*>(shared_k),
                                      reinterpret_cast<const __nv_bfloat16*>(shared_v), shared_len, ws.part_o,
