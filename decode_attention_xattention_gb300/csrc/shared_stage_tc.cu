@@ -429,14 +429,21 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             // there (even NaN) never reaches O.
             const int lim_last = t1 - (t0 + (ntiles - 1) * kTcTileKeys);
             const int pv_steps_last = (lim_last + 15) / 16;
+            // Descriptors are built once; an operand's descriptor for a byte offset only adds
+            // offset / 16 to the start-address field (addresses stay below 256 KB, so no carry
+            // leaves the field): few instructions per MMA for a thread that shares its issue
+            // slots with two busy softmax warps.
+            const uint64_t qdesc = smem_desc_sw128(smem_addr(sQ), 16, 1024);
+            const uint64_t kdesc = smem_desc_sw128(smem_addr(sU), 16, 1024);
+            const uint64_t vdesc = smem_desc_sw128(smem_addr(sU + C::kTileBytes), 16384, 1024);
             auto issue_pv = [&](int i, int jt, int st) {
-                const uint32_t vbase = smem_addr(sU + st * C::kUnitBytes + C::kTileBytes);
+                const uint32_t vo = st * C::kUnitBytes;
                 const int nk = jt == ntiles - 1 ? pv_steps_last : kTcTileKeys / 16;
 #pragma unroll
                 for (int kk = 0; kk < kTcTileKeys / 16; ++kk) {
                     if (kk >= nk) break;
-                    const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, 16384, 1024);
-                    mma_ts(tmem + kTmemO + i * 128, tmem + i * 128 + kk * 8, bd, idesc_pv, (jt > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tmem + kTmemO + i * 128, tmem + i * 128 + kk * 8, desc_at(vdesc, vo + kk * 2048), idesc_pv,
+                           (jt > 0 || kk > 0) ? 1u : 0u);
                 }
             };
             // Per tile j and row tile i: P.V of tile j-1 first (it needs only V(j-1) and
@@ -465,13 +472,12 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                     }
                     if (j < ntiles) {
                         tc_fence_after();
-                        const uint32_t qbase = smem_addr(sQ + i * C::kTileBytes);
-                        const uint32_t kbase = smem_addr(sU + st * C::kUnitBytes);
+                        const uint32_t qo = i * C::kTileBytes, ko = st * C::kUnitBytes;
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                            mma_ss(tmem + i * 128, smem_desc_sw128(qbase + off, 16, 1024),
-                                   smem_desc_sw128(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                            mma_ss(tmem + i * 128, desc_at(qdesc, qo + off), desc_at(kdesc, ko + off), idesc_qk,
+                                   kk > 0 ? 1u : 0u);
                         }
                         mma_commit(&bars.s_full[i]);
                     }

@@ -279,6 +279,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return desc;
 }
 
+// The descriptor of the same operand layout `byte_off` bytes further on: only the 14-bit
+// start-address field (low word) changes; valid while the address stays below 256 KB.
+__device__ __forceinline__ uint64_t desc_at(uint64_t base, uint32_t byte_off) {
+    const uint32_t lo = (uint32_t)base + (byte_off >> 4);
+    return ((uint64_t)(uint32_t)(base >> 32) << 32) | lo;
+}
+
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 D. a_mn / b_mn select an
 // MN-major (transposed) operand; N in multiples of 8 (8..256), M in {64, 128}.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
