@@ -79,6 +79,28 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Two fp32 lanes in one 64-bit register for the packed (f32x2) FMA-pipe instructions.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
@@ -212,19 +234,23 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 const float m_use = resc ? m_new : m_run;
                 // P = exp2(S*scale*log2e - m) as bf16, written over the consumed S columns
                 // (columns past the prefix hold -inf, so their P is exactly 0).
-                const float neg_m = -m_use;
-                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+                // (column pairs through the packed fp32x2 FMA and add: fewer issue slots, which
+                // the MMA warp on the same sub-partition needs)
+                const uint64_t scale2 = f2_pack(g.scale_log2, g.scale_log2);
+                const uint64_t negm2 = f2_pack(-m_use, -m_use);
+                uint64_t sum2[2] = {0ull, 0ull};  // (0.f, 0.f)
                 uint32_t p[kTcTileKeys / 2];
 #pragma unroll
                 for (int i = 0; i < kTcTileKeys / 2; ++i) {
-                    const float x0 = fmaf(__uint_as_float(s[2 * i]), g.scale_log2, neg_m);
-                    const float x1 = fmaf(__uint_as_float(s[2 * i + 1]), g.scale_log2, neg_m);
-                    const float p0 = ex2(x0), p1 = ex2(x1);
-                    sum4[i & 3] += p0 + p1;
+                    const float2 x = f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
+                                                      scale2, negm2));
+                    const float p0 = ex2(x.x), p1 = ex2(x.y);
+                    sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(p0, p1));
                     p[i] = pack_bf16(p0, p1);
                 }
                 tmem_st64(tS, p);
-                const float tile_sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+                const float2 sa = f2_unpack(sum2[0]), sb = f2_unpack(sum2[1]);
+                const float tile_sum = (sa.x + sb.x) + (sa.y + sb.y);
                 l_run = l_run * alpha + tile_sum;
                 m_run = m_use;
                 if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
