@@ -111,6 +111,7 @@ struct Bars {
     uint64_t u_full[kMaxStages], u_empty[kMaxStages];
     uint64_t s_full[2], p_full[2], q_ready[2];
     uint64_t o_full[2], final_mma;
+    uint64_t q_free, ns_full[2];  // last Q.K^T done; Non-Shared piece of row tile i staged
 };
 
 // Fused epilogue: fold the Non-Shared piece (written into the workspace by the
@@ -124,7 +125,7 @@ struct FusedArgs {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-    const __grid_constant__ CUtensorMap tmap_q, Geometry g, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ shared_len,
+    const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_ns, Geometry g, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ shared_len,
     float* __restrict__ part_o, float* __restrict__ part_lse, int32_t* status, FusedArgs fa) {
     using C = Cfg<D>;
     constexpr int kU = C::kUnits;
@@ -178,6 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         mbar_init(&bars.o_full[0], 1);
         mbar_init(&bars.o_full[1], 1);
         mbar_init(&bars.final_mma, 1);
+        mbar_init(&bars.q_free, 1);
+        mbar_init(&bars.ns_full[0], 1);
+        mbar_init(&bars.ns_full[1], 1);
         abort_sh = 0;
         fence_barrier_init();
     }
@@ -273,22 +277,18 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         const uint32_t tO = tmem + ((uint32_t)((warp & 3) * 32) << 16) + kTmemO + wg * 128;
         const bool have_o = tile_ok && ntiles > 0;  // O_i holds accumulated P.V (TMEM allocated)
 
-        // Fused path: the Non-Shared piece of this row (LSE and the first half of its output
-        // row) is loaded before the wait for the last P.V, so the two latencies overlap.
+        // Fused path: the Non-Shared piece of this row. With prefix tiles it is staged in shared
+        // memory by the producer (tile 0 over the Q tiles, tile 1 over the last unit's slot);
+        // its LSE is loaded before the wait for the last P.V.
         const bool fused_ns = fa.enabled && row_ok && g.step > 0;
+        const bool ns_staged = fa.enabled && g.step > 0 && have_o;  // warp-uniform
         const size_t nsrow = ((size_t)unit * g.pieces + g.nsplit) * g.M + row;
-        const float4* pn = reinterpret_cast<const float4*>(part_o + nsrow * D);
+        const uint8_t* ns_sm = (wg == 0 ? sQ : sU + ((ntiles - 1) % kU) * C::kUnitBytes) + rloc * 128;
         float lns = -INFINITY;
-        float4 nq[2][8];
-        if (fused_ns) {
-            lns = __ldg(part_lse + nsrow);
-#pragma unroll
-            for (int u = 0; u < 2; ++u)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) nq[u][i] = __ldg(pn + u * 8 + i);
-        }
+        if (fused_ns) lns = __ldg(part_lse + nsrow);
         if (have_o) {
             if (ok && !mbar_wait_warp(&bars.o_full[wg], 0, &abort_sh)) ok = false;
+            if (ok && ns_staged && !mbar_wait_warp(&bars.ns_full[wg], 0, &abort_sh)) ok = false;
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
             if (!ok) {
@@ -336,16 +336,15 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 if (w_ns != 0.f) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const float4 v = nq[k & 1][i];
+                        // staged: 16-byte chunk i of this row's quarter k sits at chunk i ^ (row % 8)
+                        const float4 v = ns_staged
+                                             ? *reinterpret_cast<const float4*>(ns_sm + k * 16384 + ((i ^ (rloc & 7)) << 4))
+                                             : __ldg(reinterpret_cast<const float4*>(part_o + nsrow * D) + k * 8 + i);
                         of[4 * i] = fmaf(w_ns, v.x, of[4 * i]);
                         of[4 * i + 1] = fmaf(w_ns, v.y, of[4 * i + 1]);
                         of[4 * i + 2] = fmaf(w_ns, v.z, of[4 * i + 2]);
                         of[4 * i + 3] = fmaf(w_ns, v.w, of[4 * i + 3]);
                     }
-                }
-                if (fused_ns && k + 2 < D / 32) {  // refill this buffer with quarter k + 2
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) nq[k & 1][i] = __ldg(pn + (k + 2) * 8 + i);
                 }
                 if (row_ok) {
                     if (g.out_f32) {
@@ -435,10 +434,29 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 if (j == kU - 1)  // the first units' loads went out before any L2 prefetch
                     for (int jp = kU; jp < min(nunits, kU + kPrefetch); ++jp) prefetch_unit(jp);
             }
+            // Fused decode: stage each row tile's Non-Shared piece (128 rows x d fp32, as 128-byte
+            // swizzled boxes of 32 columns) for the epilogue: row tile 0 into the Q tiles once the
+            // last Q.K^T is done, row tile 1 into the slot of unit ntiles - 1 once it is consumed.
+            bool ns_issued[2] = {false, false};
+            if (fa.enabled && g.step > 0 && issued == nunits) {
+                for (int i = 0; i < ntile_m; ++i) {
+                    const int jl = ntiles - 1, st = jl % kU;
+                    if (i == 0 ? !mbar_wait(&bars.q_free, 0, &abort_sh)
+                               : !mbar_wait(&bars.u_empty[st], (jl / kU) & 1, &abort_sh))
+                        break;
+                    uint8_t* dst = i == 0 ? sQ : sU + st * C::kUnitBytes;
+                    const int row0 = (int)(((size_t)unit * g.pieces + g.nsplit) * g.M) + (2 * mp + i) * kTileRows;
+                    mbar_arrive_expect_tx(&bars.ns_full[i], (D / 32) * 16384);
+                    for (int k = 0; k < D / 32; ++k) tma_load_2d(dst + k * 16384, &tmap_ns, &bars.ns_full[i], k * 32, row0);
+                    ns_issued[i] = true;
+                }
+            }
             if (abort_sh) {  // let the copies still in flight land before the CTA exits
                 volatile int never = 0;
                 for (int j = max(0, issued - kU); j < issued; ++j) mbar_wait(&bars.u_full[j % kU], (j / kU) & 1, &never);
                 for (int i = 0; i < ntile_m; ++i) mbar_wait(&bars.q_ready[i], 0, &never);
+                for (int i = 0; i < 2; ++i)
+                    if (ns_issued[i]) mbar_wait(&bars.ns_full[i], 0, &never);
             }
         }
     } else {
@@ -509,6 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                     }
                 }
                 if (!ok) break;
+                if (j == ntiles - 1) mma_commit(&bars.q_free);  // the Q tiles are no longer read
                 mma_commit(&bars.u_empty[st]);
             }
             if (!ok) {
@@ -530,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
 
 template <int D>
 cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
-                     const __nv_bfloat16* q, const int32_t* slen, float* po, float* pl, int32_t* status,
+                     const CUtensorMap& tn, const __nv_bfloat16* q, const int32_t* slen, float* po, float* pl, int32_t* status,
                      const FusedArgs& fa, cudaStream_t stream) {
     static bool attr_done[64] = {};
     int dev = 0;
@@ -542,8 +561,8 @@ cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
     const long ctas = shared_tc_ctas_for(g);
-    shared_stage_tc_kernel<D><<<(unsigned)ctas, kThreads, Cfg<D>::kSmemBytes, stream>>>(tk, tv, tq, g, q, slen, po,
-                                                                                         pl, status, fa);
+    shared_stage_tc_kernel<D><<<(unsigned)ctas, kThreads, Cfg<D>::kSmemBytes, stream>>>(tk, tv, tq, tn, g, q, slen,
+                                                                                         po, pl, status, fa);
     return cudaGetLastError();
 }
 
@@ -552,12 +571,15 @@ cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap
 int shared_tc_ctas_for(const Geometry& g) { return g.R * g.Hkv * g.nsplit * ((g.row_tiles + 1) / 2); }
 
 cudaError_t launch_shared_stage_tc(const Geometry& g, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
-                                   const CUtensorMap& tq, const __nv_bfloat16* q, const int32_t* shared_len,
+                                   const CUtensorMap& tq, const CUtensorMap& tn, const __nv_bfloat16* q,
+                                   const int32_t* shared_len,
                                    float* part_o, float* part_lse, int32_t* status, void* out, float* lse,
                                    bool fused, cudaStream_t stream) {
     FusedArgs fa{out, lse, fused ? 1 : 0};
-    if (g.d == 128) return launch_d<128>(g, tmap_k, tmap_v, tq, q, shared_len, part_o, part_lse, status, fa, stream);
-    if (g.d == 64) return launch_d<64>(g, tmap_k, tmap_v, tq, q, shared_len, part_o, part_lse, status, fa, stream);
+    if (g.d == 128)
+        return launch_d<128>(g, tmap_k, tmap_v, tq, tn, q, shared_len, part_o, part_lse, status, fa, stream);
+    if (g.d == 64)
+        return launch_d<64>(g, tmap_k, tmap_v, tq, tn, q, shared_len, part_o, part_lse, status, fa, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -150,6 +150,21 @@ CUresult make_q_map(CUtensorMap* map, const void* base, const Geometry& g) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// part_o [rows, d] fp32 viewed as {d, rows}; box = 32 x 128 (128 bytes x 128 rows, 128-byte
+// swizzle): a quarter of the d columns of one 128-row tile of a piece, for the fused
+// epilogue's staging of the Non-Shared piece in shared memory.
+CUresult make_ns_map(CUtensorMap* map, const void* part_o, const Geometry& g) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return CUDA_ERROR_NOT_FOUND;
+    cuuint64_t dims[2] = {(cuuint64_t)g.d, (cuuint64_t)part_rows(g)};
+    cuuint64_t strides[1] = {(cuuint64_t)g.d * 4};
+    cuuint32_t box[2] = {32, (cuuint32_t)kTileRows};
+    cuuint32_t es[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(part_o), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 }  // namespace
 }  // namespace xattn
 
@@ -241,11 +256,12 @@ int run_shared(const Geometry& g, int kernel, const void* q, const void* shared_
     auto qb = reinterpret_cast<const __nv_bfloat16*>(q);
     cudaError_t e = cudaSuccess;
     if (kernel == 1) {
-        CUtensorMap mk, mv, mq;
+        CUtensorMap mk, mv, mq, mn;
         if (make_kv_map(&mk, shared_k, g) != CUDA_SUCCESS || make_kv_map(&mv, shared_v, g) != CUDA_SUCCESS)
             return XATTN_ERR_CUDA;
-        if (make_q_map(&mq, q, g) != CUDA_SUCCESS) return XATTN_ERR_CUDA;
-        e = launch_shared_stage_tc(g, mk, mv, mq, qb, shared_len, ws.part_o, ws.part_lse, ws.status, out, lse,
+        if (make_q_map(&mq, q, g) != CUDA_SUCCESS || make_ns_map(&mn, ws.part_o, g) != CUDA_SUCCESS)
+            return XATTN_ERR_CUDA;
+        e = launch_shared_stage_tc(g, mk, mv, mq, mn, qb, shared_len, ws.part_o, ws.part_lse, ws.status, out, lse,
                                    fused, st);
     } else if (kernel == 2) {
         e = launch_shared_stage_simt(g, qb, reinterpret_cast<const __nv_bfloat16*>(shared_k),

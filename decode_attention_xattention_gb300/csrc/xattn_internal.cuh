@@ -47,9 +47,11 @@ inline size_t part_rows(const Geometry& g) { return (size_t)g.R * g.Hkv * g.piec
 // workspace and writes out / lse (requires a single prefix piece); otherwise it writes the
 // piece's partial result into part_o / part_lse.
 // tmap_q: the Q tiles by TMA (box 64 x G x 128/G; G divides 128 since it is a power of two
-// up to 16).
+// up to 16); tmap_ns: part_o as {d, rows} fp32, box 32 x 128 (the fused epilogue stages the
+// Non-Shared piece through it).
 cudaError_t launch_shared_stage_tc(const Geometry& g, const CUtensorMap& tmap_k,
-                                   const CUtensorMap& tmap_v, const CUtensorMap& tmap_q, const __nv_bfloat16* q,
+                                   const CUtensorMap& tmap_v, const CUtensorMap& tmap_q,
+                                   const CUtensorMap& tmap_ns, const __nv_bfloat16* q,
                                    const int32_t* shared_len, float* part_o, float* part_lse,
                                    int32_t* status, void* out, float* lse, bool fused,
                                    cudaStream_t stream);
