@@ -210,6 +210,9 @@ __global__ void __launch_bounds__(kPieceWarps * 32, D * (G < 4 ? G : 4) / 32 >= 
     constexpr int RB = D * 2;          // bytes of one pool row (one head)
     constexpr int LR = RB / 16;        // lanes copying one row
     static_assert(2 * LR <= 32, "one cp.async per lane covers the K and the V row of a token");
+    // the Shared-stage kernel that follows in the fused decode may start its CTAs now; it
+    // reads this kernel's output only after waiting for its completion
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     static_assert(kNsChunk <= 64, "a lane holds the slots of positions lane and lane + 32");
     __shared__ __align__(16) uint8_t ring[kPieceWarps][kRingTok][2 * RB];
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;

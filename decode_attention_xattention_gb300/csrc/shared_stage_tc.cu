@@ -148,16 +148,6 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     const long unit = t / g.nsplit;
     const int h = (int)(unit % g.Hkv);
     const int r = (int)(unit / g.Hkv);
-    // For the fused epilogue, softmax threads prefetch their row of the Non-Shared piece into
-    // L2 (kept there): the latency overlaps the main loop.
-    if (warp < 8 && fa.enabled && g.step > 0) {
-        const int mt0 = 2 * mp + (warp >> 2), row0 = mt0 * kTileRows + (tid & 127);
-        if (mt0 < g.row_tiles && row0 < g.M) {
-            const char* np = reinterpret_cast<const char*>(part_o + (((size_t)unit * g.pieces + g.nsplit) * g.M + row0) * D);
-#pragma unroll
-            for (int ln = 0; ln < D * 4 / 128; ++ln) asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(np + ln * 128));
-        }
-    }
     const int L_raw = shared_len[r];
     const bool bad_len = L_raw < 0 || L_raw > g.Lmax;
     const int L = bad_len ? 0 : L_raw;
@@ -285,7 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         const size_t nsrow = ((size_t)unit * g.pieces + g.nsplit) * g.M + row;
         const uint8_t* ns_sm = (wg == 0 ? sQ : sU + ((ntiles - 1) % kU) * C::kUnitBytes) + rloc * 128;
         float lns = -INFINITY;
-        if (fused_ns) lns = __ldg(part_lse + nsrow);
+        if (fused_ns) {
+            grid_dependency_wait();  // the Non-Shared kernel launched before this one has finished
+            lns = __ldg(part_lse + nsrow);
+        }
         if (have_o) {
             if (ok && !mbar_wait_warp(&bars.o_full[wg], 0, &abort_sh)) ok = false;
             if (ok && ns_staged && !mbar_wait_warp(&bars.ns_full[wg], 0, &abort_sh)) ok = false;
@@ -439,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             // last Q.K^T is done, row tile 1 into the slot of unit ntiles - 1 once it is consumed.
             bool ns_issued[2] = {false, false};
             if (fa.enabled && g.step > 0 && issued == nunits) {
+                grid_dependency_wait();  // the Non-Shared kernel launched before this one has finished
                 for (int i = 0; i < ntile_m; ++i) {
                     const int jl = ntiles - 1, st = jl % kU;
                     if (i == 0 ? !mbar_wait(&bars.q_free, 0, &abort_sh)
@@ -561,9 +555,20 @@ cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
     const long ctas = shared_tc_ctas_for(g);
-    shared_stage_tc_kernel<D><<<(unsigned)ctas, kThreads, Cfg<D>::kSmemBytes, stream>>>(tk, tv, tq, tn, g, q, slen,
-                                                                                         po, pl, status, fa);
-    return cudaGetLastError();
+    // In the fused decode the Non-Shared kernel runs just before this one and signals early
+    // launch: CTAs of this kernel may start while its last wave drains (only the epilogue
+    // reads its result, after griddepcontrol.wait).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (fa.enabled && g.step > 0) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, shared_stage_tc_kernel<D>, tk, tv, tq, tn, g, q, slen, po, pl, status, fa);
 }
 
 }  // namespace

@@ -139,6 +139,11 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 // ---- tcgen05 ---------------------------------------------------------------------------
 // Allocation is warp-wide; the TMEM base address is written to *dst (shared memory).
+// Programmatic dependent launch: let the next kernel in the stream start its CTAs now /
+// wait until the kernel this one depends on has completed and its writes are visible.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  ::"r"(smem_addr(dst)), "r"(ncols) : "memory");
