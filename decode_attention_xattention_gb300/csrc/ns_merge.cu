@@ -336,6 +336,137 @@ __global__ void __launch_bounds__(kPieceWarps * 32, D * (G < 4 ? G : 4) / 32 >= 
     }
 }
 
+// Short Non-Shared part (the fused decode's common case: a few tokens per beam): one warp
+// per (request, beam) for every KV head. The ancestry slots are the same for all heads, and
+// a pool slot keeps its heads' rows contiguous, so after the one index load the warp copies
+// the beam's whole Non-Shared K/V (step x Hkv rows each) and its Hq query rows into its own
+// shared memory with cp.async in one round trip, then computes every head from there. Few,
+// fat warps (under one wave) instead of one thin warp per head with its own dependent loads.
+constexpr int kBeamWarps = 4;  // warps per CTA of ns_beam_kernel
+
+// Shared memory of one warp of ns_beam_kernel: step x Hkv x {K, V} rows, then Hq rows of q.
+inline size_t ns_beam_warp_bytes(const Geometry& g) {
+    return ((size_t)g.step * g.Hkv * 2 + g.Hq) * g.d * 2;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kBeamWarps * 32) ns_beam_kernel(
+    Geometry g, int warp_bytes, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ pool_k,
+    const __nv_bfloat16* __restrict__ pool_v, const int32_t* __restrict__ idx, float* __restrict__ part_o,
+    float* __restrict__ part_lse, int32_t* status) {
+    constexpr int HG = G < 4 ? G : 4;  // query heads per pass
+    constexpr int LP = 32 / HG;        // lanes per query head
+    constexpr int EL = D / LP;         // elements of d per lane (2 .. 16)
+    constexpr int NV = EL / 2;         // bf16 pairs per lane
+    constexpr int RB = D * 2;          // bytes of one row (one head)
+    constexpr int CH = RB / 16;        // 16-byte chunks per row
+    extern __shared__ __align__(16) uint8_t dsm[];
+    // the Shared-stage kernel that follows may start its CTAs now (it waits for this one's
+    // completion before reading its output)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const long w = (long)blockIdx.x * kBeamWarps + wib;
+    if (w >= (long)g.R * g.BW) return;
+    const int b = (int)(w % g.BW), r = (int)(w / g.BW);
+    const int T = g.step, Hkv = g.Hkv;
+    uint8_t* wsm = dsm + (size_t)wib * warp_bytes;
+    const uint32_t wsm_s = (uint32_t)__cvta_generic_to_shared(wsm);
+    const int kv_bytes = T * Hkv * 2 * RB;  // then the q rows
+
+    const int32_t* row_idx = idx + ((size_t)r * g.BW + b) * g.Tmax;
+    const int my_slot = lane < T ? __ldg(row_idx + lane) : 0;
+    const bool slot_bad = __any_sync(0xffffffffu, lane < T && (my_slot < 0 || my_slot >= g.S));
+    if (slot_bad && lane == 0) set_status(status, XATTN_STATUS_BAD_SLOT);
+    {   // the beam's q rows (Hq rows, contiguous) and, per token, the K and V rows of all heads
+        const uint8_t* qs = reinterpret_cast<const uint8_t*>(q + ((size_t)r * g.BW + b) * g.Hq * D);
+        for (int e = lane; e < g.Hq * CH; e += 32) cp_async16(wsm_s + kv_bytes + e * 16, qs + e * 16);
+        if (!slot_bad) {
+            for (int t = 0; t < T; ++t) {
+                const int slot = __shfl_sync(0xffffffffu, my_slot, t);
+                const size_t off = ((size_t)r * g.S + slot) * Hkv * RB;  // bytes
+                const uint8_t* ks = reinterpret_cast<const uint8_t*>(pool_k) + off;
+                const uint8_t* vs = reinterpret_cast<const uint8_t*>(pool_v) + off;
+                const uint32_t kd = wsm_s + (2 * t) * Hkv * RB, vd = wsm_s + (2 * t + 1) * Hkv * RB;
+                for (int e = lane; e < Hkv * CH; e += 32) {
+                    cp_async16(kd + e * 16, ks + e * 16);
+                    cp_async16(vd + e * 16, vs + e * 16);
+                }
+            }
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncwarp();
+    }
+    const int hg = lane / LP, sl = lane % LP;
+    auto lo = [](uint32_t x) { return __uint_as_float(x << 16); };
+    auto hi = [](uint32_t x) { return __uint_as_float(x & 0xffff0000u); };
+    auto read_pairs = [](const uint8_t* p, uint32_t (&w)[NV]) {
+        if constexpr (NV >= 4) {
+#pragma unroll
+            for (int k = 0; k < NV / 4; ++k) {
+                const uint4 u = *reinterpret_cast<const uint4*>(p + k * 16);
+                w[4 * k] = u.x; w[4 * k + 1] = u.y; w[4 * k + 2] = u.z; w[4 * k + 3] = u.w;
+            }
+        } else if constexpr (NV == 2) {
+            const uint2 u = *reinterpret_cast<const uint2*>(p);
+            w[0] = u.x; w[1] = u.y;
+        } else {
+            w[0] = *reinterpret_cast<const uint32_t*>(p);
+        }
+    };
+#pragma unroll 1
+    for (int h = 0; h < Hkv; ++h) {
+#pragma unroll 1
+        for (int pass = 0; pass < G / HG; ++pass) {
+            const int gg = pass * HG + hg;
+            uint32_t qw[NV];
+            read_pairs(wsm + kv_bytes + (h * G + gg) * RB + sl * EL * 2, qw);
+            float m = -INFINITY, l = 0.f, acc[EL];
+#pragma unroll
+            for (int e = 0; e < EL; ++e) acc[e] = 0.f;
+            if (!slot_bad) {
+                for (int t = 0; t < T; ++t) {
+                    uint32_t kw[NV], vw[NV];
+                    read_pairs(wsm + ((2 * t) * Hkv + h) * RB + sl * EL * 2, kw);
+                    read_pairs(wsm + ((2 * t + 1) * Hkv + h) * RB + sl * EL * 2, vw);
+                    float sc = 0.f;
+#pragma unroll
+                    for (int k = 0; k < NV; ++k) {
+                        sc = fmaf(lo(qw[k]), lo(kw[k]), sc);
+                        sc = fmaf(hi(qw[k]), hi(kw[k]), sc);
+                    }
+#pragma unroll
+                    for (int o = LP / 2; o > 0; o >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, o);
+                    const float s2 = sc * g.scale_log2;
+                    const float mn = fmaxf(m, s2);
+                    const float alpha = ex2(m - mn), p = ex2(s2 - mn);
+                    l = l * alpha + p;
+#pragma unroll
+                    for (int k = 0; k < NV; ++k) {
+                        acc[2 * k] = fmaf(p, lo(vw[k]), acc[2 * k] * alpha);
+                        acc[2 * k + 1] = fmaf(p, hi(vw[k]), acc[2 * k + 1] * alpha);
+                    }
+                    m = mn;
+                }
+            }
+            const size_t prow = (((size_t)r * Hkv + h) * g.pieces + g.nsplit) * g.M + (size_t)b * G + gg;
+            const bool empty = !(l > 0.f);
+            const float inv = empty ? 0.f : 1.f / l;
+            float* po = part_o + prow * D + sl * EL;
+            if constexpr (EL >= 4) {
+#pragma unroll
+                for (int k = 0; k < EL / 4; ++k)
+                    reinterpret_cast<float4*>(po)[k] =
+                        make_float4(acc[4 * k] * inv, acc[4 * k + 1] * inv, acc[4 * k + 2] * inv, acc[4 * k + 3] * inv);
+            } else {
+                *reinterpret_cast<float2*>(po) = make_float2(acc[0] * inv, acc[1] * inv);
+            }
+            if (sl == 0)
+                part_lse[prow] = slot_bad ? __uint_as_float(kNaN) : (empty ? -INFINITY : (m + __log2f(l)) * kLn2);
+        }
+    }
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(256) ns_merge_kernel(
     Geometry g, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ pool_k,
@@ -554,6 +685,28 @@ __global__ void __launch_bounds__(256) merge_rows_kernel(
     if (lane == 0) lse[row] = bad ? __uint_as_float(kNaN) : (mx + __log2f(lsum)) * kLn2;
 }
 
+constexpr int kNsBeamMaxTok = 8;                 // tokens per beam for ns_beam_kernel
+constexpr size_t kNsBeamMaxWarpBytes = 48 * 1024;  // its shared memory per warp
+
+template <int D, int G>
+cudaError_t launch_beam(const Geometry& g, cudaStream_t st, const __nv_bfloat16* q, const __nv_bfloat16* pk,
+                        const __nv_bfloat16* pv, const int32_t* idx, float* po, float* pl, int32_t* status) {
+    const int wb = (int)ns_beam_warp_bytes(g);
+    const int smem = kBeamWarps * wb;
+    static int attr_set[64] = {};  // dynamic shared-memory limit raised, per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || attr_set[dev] < smem) {
+        cudaError_t e = cudaFuncSetAttribute(ns_beam_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kBeamWarps * (int)kNsBeamMaxWarpBytes);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_set[dev] = kBeamWarps * (int)kNsBeamMaxWarpBytes;
+    }
+    const unsigned ctas = (unsigned)(((long)g.R * g.BW + kBeamWarps - 1) / kBeamWarps);
+    ns_beam_kernel<D, G><<<ctas, kBeamWarps * 32, smem, st>>>(g, wb, q, pk, pv, idx, po, pl, status);
+    return cudaSuccess;
+}
+
 template <int D>
 cudaError_t launch_d(const Geometry& g, cudaStream_t st, const __nv_bfloat16* q, const __nv_bfloat16* pk,
                      const __nv_bfloat16* pv, const int32_t* idx, const int32_t* slen, float* po, float* pl,
@@ -564,10 +717,15 @@ cudaError_t launch_d(const Geometry& g, cudaStream_t st, const __nv_bfloat16* q,
     const long piece_ctas = ((long)g.R * g.BW * g.Hkv * npc + 7) / 8;
     if (piece_ctas > 0x7fffffffL) return cudaErrorInvalidValue;
     const unsigned rows_ctas = (unsigned)(((long)g.R * g.BW * g.Hq + 7) / 8);
+    // short Non-Shared part ahead of the fused Shared stage: one warp per (request, beam)
+    const bool beam_path = g.ns_to_piece && g.step <= kNsBeamMaxTok && ns_beam_warp_bytes(g) <= kNsBeamMaxWarpBytes;
     switch (g.G) {
 #define XATTN_G(GV)                                                                                              \
     case GV:                                                                                                     \
-        if (g.ns_to_piece || g.ns_pieces > 0) {                                                                  \
+        if (beam_path) {                                                                                         \
+            cudaError_t e = launch_beam<D, GV>(g, st, q, pk, pv, idx, po, pl, status);                          \
+            if (e != cudaSuccess) return e;                                                                      \
+        } else if (g.ns_to_piece || g.ns_pieces > 0) {                                                           \
             ns_piece_kernel<D, GV><<<(unsigned)piece_ctas, block, 0, st>>>(g, npc, q, pk, pv, idx, po, pl, status); \
             if (!g.ns_to_piece) merge_rows_kernel<D><<<rows_ctas, block, 0, st>>>(g, slen, po, pl, out, lse, status); \
         } else {                                                                                                 \
