@@ -89,6 +89,27 @@ def test_long_non_shared_parts(T, d):
     assert db.plan().fused == 0
 
 
+@pytest.mark.parametrize("T,d,Hq,Hkv", [(9, 128, 8, 2), (16, 64, 8, 2), (32, 128, 16, 2), (20, 128, 4, 4)])
+def test_medium_non_shared_parts_fused(T, d, Hq, Hkv):
+    """9..32 ancestry tokens per beam with a one-piece prefix: the fused decode computes the
+    Non-Shared part with the per-head piece kernel (one piece) ahead of the Shared stage."""
+    w = wl.custom(R=2, BW=6, Hq=Hq, Hkv=Hkv, d=d, lens=(700, 129), T=T, seed=40 + T)
+    _, db, _ = run_and_check(w, split_tokens=4096)
+    assert db.plan().fused == 1
+
+
+@pytest.mark.parametrize("shape", [(3, 8, 8, 1, 64, 8), (2, 5, 32, 2, 128, 7), (1, 4, 16, 16, 128, 8)],
+                         ids=["G8_d64_t8", "G16_d128_t7", "G1_Hkv16_t8_wide_rows"])
+def test_short_non_shared_beam_kernel_shapes(shape):
+    """Short Non-Shared parts (step <= 8) go through the warp-per-beam kernel when the beam's
+    rows fit its shared memory, else through the per-head piece kernel (the last shape:
+    16 KV heads x 8 tokens x K and V rows exceed it)."""
+    R, BW, Hq, Hkv, d, T = shape
+    w = wl.custom(R=R, BW=BW, Hq=Hq, Hkv=Hkv, d=d, lens=(300,) * R, T=T, seed=50 + T)
+    _, db, _ = run_and_check(w, split_tokens=4096)
+    assert db.plan().fused == 1
+
+
 def test_tiny_config_both_kernels():
     for k in (0, 1, 2):
         stats, _, _ = run_and_check(wl.TINY, shared_kernel=k)
