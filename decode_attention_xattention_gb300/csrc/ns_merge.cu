@@ -22,6 +22,7 @@
 //   merge_rows_kernel  one warp per query row: folds every stored piece (prefix and
 //                      Non-Shared) and writes out / lse.
 #include "xattn_internal.cuh"
+#include "sm100_ptx.cuh"
 
 namespace xattn {
 namespace {
@@ -184,155 +185,242 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-constexpr int kRingTok = 8;        // Non-Shared tokens in flight per warp
-constexpr int kPieceWarps = 8;     // warps per CTA of ns_piece_kernel
+// Warp-level tensor-core MMA, m16n8k16, bf16 inputs, fp32 accumulators (d += a * b).
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Four 8x8 bf16 matrices from shared memory (lane i gives row i % 8 of matrix i / 8), plain
+// or transposed.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&t);
+}
+
+constexpr int kPieceBlk = 16;                        // tokens per block (the k of one P.V MMA)
+constexpr int kPieceBlocks = kNsChunk / kPieceBlk;   // blocks of a full piece
+constexpr int kPieceHead = 128;                      // bytes before the staged rows: mbarriers, flag
+// Shared-memory row stride of a staged pool row: the row plus 16 bytes, so that the eight
+// rows one ldmatrix reads start in eight different groups of four banks.
+__host__ __device__ constexpr int piece_row_stride(int D) { return D * 2 + 16; }
+// Dynamic shared memory of ns_piece_kernel for pieces of up to `tok` tokens.
+inline int piece_smem_bytes(int D, int tok) {
+    const int cap = (tok + kPieceBlk - 1) / kPieceBlk * kPieceBlk;
+    return kPieceHead + 2 * cap * piece_row_stride(D);
+}
 
 // Non-Shared stage of one (request, beam, KV head) over one piece of its ancestry positions
 // (at most kNsChunk of them), stored as workspace piece `nsplit + piece` for the Shared-
 // stage epilogue (one piece: step <= 32) or the row-merge kernel to merge; prefix-length
-// problems and empty rows are reported by those.
+// problems and empty rows are reported by those. One warp per CTA.
 //
-// The pool rows are gathered with cp.async into a per-warp ring of kRingTok tokens in shared
-// memory (one instruction per token: half the lanes copy the K row, half the V row), so
-// eight tokens' loads are in flight while one is computed, without registers held for them.
-// Lane mapping for the arithmetic: lane = (query head within a group of HG heads, slice of EL
-// consecutive elements of d), so a dot product reduces over LP = 32 / HG lanes only; groups
-// of more than four heads are done in passes over the piece.
+// Data movement: after the one index load, every K and V row of the piece (one pool row
+// of this head is 2d contiguous bytes) is requested at once by bulk copies, one per row,
+// completing on one mbarrier per block of 16 tokens; the rows are never reused, so the
+// whole piece is in flight while the first block is computed.
+// Arithmetic: the G query heads of the KV head are the rows of one 16-row MMA tile (rows
+// G..15 zero), so a block of 16 tokens costs D/8 MMAs for S = Q K^T and D/8 for O += P V:
+// S is held in the accumulator layout, whose registers are also the A operand of P V once
+// rounded to bf16 (as the Shared-stage kernel rounds P), and the online softmax rescales O
+// once per block. Q, K and P enter the MMAs as bf16 with fp32 accumulation.
 template <int D, int G>
-__global__ void __launch_bounds__(kPieceWarps * 32, D * (G < 4 ? G : 4) / 32 >= 16 ? 3 : 4) ns_piece_kernel(
-    Geometry g, int npc, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ pool_k,
+__global__ void __launch_bounds__(32, 1) ns_piece_kernel(
+    Geometry g, int npc, int tok_cap, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ pool_k,
     const __nv_bfloat16* __restrict__ pool_v, const int32_t* __restrict__ idx, float* __restrict__ part_o,
     float* __restrict__ part_lse, int32_t* status) {
-    constexpr int HG = G < 4 ? G : 4;  // heads per pass
-    constexpr int LP = 32 / HG;        // lanes per head
-    constexpr int EL = D / LP;         // elements of d per lane (2 .. 16)
-    constexpr int NV = EL / 2;         // bf16 pairs per lane
-    constexpr int RB = D * 2;          // bytes of one pool row (one head)
-    constexpr int LR = RB / 16;        // lanes copying one row
-    static_assert(2 * LR <= 32, "one cp.async per lane covers the K and the V row of a token");
+    static_assert(G <= 16, "the query heads of a KV head fill at most one 16-row MMA tile");
+    static_assert(kNsChunk <= 64 && kNsChunk % kPieceBlk == 0, "a lane holds the slots of positions lane, lane + 32");
+    constexpr int RB = D * 2;                   // bytes of one pool row (one head)
+    constexpr int RS = piece_row_stride(D);     // its stride in shared memory
+    constexpr int KS = D / 16;                  // k-steps of Q K^T
+    constexpr int NT = D / 8;                   // 8-column tiles of O
+    constexpr bool kHi = G > 8;                 // rows 8..15 of the tile are query heads
     // the Shared-stage kernel that follows in the fused decode may start its CTAs now; it
     // reads this kernel's output only after waiting for its completion
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    static_assert(kNsChunk <= 64, "a lane holds the slots of positions lane and lane + 32");
-    __shared__ __align__(16) uint8_t ring[kPieceWarps][kRingTok][2 * RB];
-    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-    long w = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (w >= (long)g.R * g.BW * g.Hkv * npc) return;
+    extern __shared__ __align__(128) uint8_t psm[];
+    uint64_t* bar = reinterpret_cast<uint64_t*>(psm);
+    volatile int* abort_sh = reinterpret_cast<volatile int*>(psm + kPieceBlocks * 8);
+    uint8_t* k_sm = psm + kPieceHead;
+    uint8_t* v_sm = k_sm + tok_cap * RS;
+    const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+    long w = blockIdx.x;
     const int c = (int)(w % npc);  // piece: ancestry positions [c * kNsChunk, ...)
     w /= npc;
     const int h = (int)(w % g.Hkv);
     const int b = (int)((w / g.Hkv) % g.BW);
     const int r = (int)(w / ((long)g.Hkv * g.BW));
-    const int hg = lane / LP, sl = lane % LP;
-    const size_t qrow0 = ((size_t)r * g.BW + b) * g.Hq + (size_t)h * G;
     const size_t prow0 = (((size_t)r * g.Hkv + h) * g.pieces + g.nsplit + c) * g.M + (size_t)b * G;
     const int i0 = c * kNsChunk;
-    const int n = min(kNsChunk, g.step - i0);  // positions of this piece
+    const int n = min(min(kNsChunk, tok_cap), g.step - i0);  // positions of this piece
     const int32_t* row_idx = idx + ((size_t)r * g.BW + b) * g.Tmax + i0;
     const int slot_a = lane < n ? __ldg(row_idx + lane) : 0;
     const int slot_b = lane + 32 < n ? __ldg(row_idx + lane + 32) : 0;
     const bool slot_bad = __any_sync(0xffffffffu, (lane < n && (slot_a < 0 || slot_a >= g.S)) ||
                                                        (lane + 32 < n && (slot_b < 0 || slot_b >= g.S)));
     if (slot_bad && lane == 0) set_status(status, XATTN_STATUS_BAD_SLOT);
-    const int nw = slot_bad ? 0 : n;  // tokens walked
+    const int nw = slot_bad ? 0 : max(n, 0);  // tokens walked
+    const int nb = (nw + kPieceBlk - 1) / kPieceBlk;
 
-    // copy role of this lane: the K row (lanes 0..LR-1) or the V row (LR..2LR-1) of a token
-    const bool copier = lane < 2 * LR;
-    const __nv_bfloat16* src_base = (lane < LR ? pool_k : pool_v) + (size_t)h * D + (lane % LR) * 8;
-    const uint32_t ring_base = (uint32_t)__cvta_generic_to_shared(&ring[wib][0][0]) + (lane < LR ? 0 : RB) + (lane % LR) * 16;
-    auto issue = [&](int t) {  // token t of the piece into ring slot t % kRingTok (always one group)
-        const int sa = __shfl_sync(0xffffffffu, slot_a, t & 31);
-        const int sb = __shfl_sync(0xffffffffu, slot_b, t & 31);
-        if (copier && t < nw) {
-            const int slot = t < 32 ? sa : sb;
-            cp_async16(ring_base + (t % kRingTok) * (2 * RB), src_base + ((size_t)r * g.S + slot) * g.Hkv * D);
-        }
-        cp_async_commit();
-    };
-    // bf16 pair -> two floats (a bf16 is the top half of its fp32)
-    auto lo = [](uint32_t x) { return __uint_as_float(x << 16); };
-    auto hi = [](uint32_t x) { return __uint_as_float(x & 0xffff0000u); };
+    // 1. request the piece: barrier j counts the bytes of tokens [16 j, 16 j + 16)
+    if (lane == 0) {
+        for (int j = 0; j < kPieceBlocks; ++j) ptx::mbar_init(&bar[j], 1);
+        *abort_sh = 0;
+        ptx::fence_barrier_init();
+        for (int j = 0; j < nb; ++j) ptx::mbar_arrive_expect_tx(&bar[j], (uint32_t)(min(kPieceBlk, nw - j * kPieceBlk) * 2 * RB));
+    }
+    __syncwarp();
+    const size_t head_off = (size_t)h * D;
+    for (int t = lane; t < nw; t += 32) {
+        const int slot = t < 32 ? slot_a : slot_b;
+        const size_t off = ((size_t)r * g.S + slot) * g.Hkv * D + head_off;
+        ptx::bulk_load(k_sm + t * RS, pool_k + off, RB, &bar[t / kPieceBlk]);
+        ptx::bulk_load(v_sm + t * RS, pool_v + off, RB, &bar[t / kPieceBlk]);
+    }
+    // V rows of the last block's ragged tail are read by the MMA with weight 0: make them 0
+    for (int e = lane; e < (nb * kPieceBlk - nw) * (RB / 16); e += 32)
+        *reinterpret_cast<uint4*>(v_sm + (nw + e / (RB / 16)) * RS + (e % (RB / 16)) * 16) = make_uint4(0, 0, 0, 0);
 
+    // 2. Q as the A operand: rows gid (a0, a2) and gid + 8 (a1, a3), zero beyond G
+    const __nv_bfloat16* qb = q + (((size_t)r * g.BW + b) * g.Hq + (size_t)h * G) * D + tig * 2;
+    uint32_t qa[KS][4];
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+        const bool lo_ok = gid < G, hi_ok = kHi && gid + 8 < G;
+        qa[kk][0] = lo_ok ? __ldg(reinterpret_cast<const uint32_t*>(qb + gid * D + kk * 16)) : 0u;
+        qa[kk][2] = lo_ok ? __ldg(reinterpret_cast<const uint32_t*>(qb + gid * D + kk * 16 + 8)) : 0u;
+        qa[kk][1] = hi_ok ? __ldg(reinterpret_cast<const uint32_t*>(qb + (gid + 8) * D + kk * 16)) : 0u;
+        qa[kk][3] = hi_ok ? __ldg(reinterpret_cast<const uint32_t*>(qb + (gid + 8) * D + kk * 16 + 8)) : 0u;
+    }
+    __syncwarp();  // the zeroed tail rows are written before any lane's ldmatrix
+
+    // per-lane ldmatrix row addresses (K: tokens (lane/16)*8 + lane%8, k half (lane/8)%2;
+    // V transposed: tokens ((lane/8)%2)*8 + lane%8, d half lane/16)
+    const uint32_t k_addr = ptx::smem_addr(k_sm) + ((lane >> 4) * 8 + (lane & 7)) * RS + ((lane >> 3) & 1) * 16;
+    const uint32_t v_addr = ptx::smem_addr(v_sm) + (((lane >> 3) & 1) * 8 + (lane & 7)) * RS + (lane >> 4) * 16;
+
+    float o[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+    float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+    bool ok = true;
+    int jw = 0;  // blocks waited for
 #pragma unroll 1
-    for (int pass = 0; pass < G / HG; ++pass) {
-        const int gg = pass * HG + hg;
-        uint32_t qw[NV];
+    for (int j = 0; j < nb; ++j) {
+        if (!ptx::mbar_wait_warp(&bar[j], 0, abort_sh)) { ok = false; break; }
+        jw = j + 1;
+        // S = Q K^T over tokens 16 j .. 16 j + 15 (two 8-token column tiles)
+        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            uint32_t kb[4];
+            ldsm_x4(k_addr + j * kPieceBlk * RS + kk * 32, kb);
+            mma16816(s[0], qa[kk], kb[0], kb[1]);
+            mma16816(s[1], qa[kk], kb[2], kb[3]);
+        }
+        // scale to log2 units; tokens past the piece get -inf
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int tok = j * kPieceBlk + nt * 8 + tig * 2 + (e & 1);
+                s[nt][e] = tok < nw ? s[nt][e] * g.scale_log2 : -INFINITY;
+            }
+        // block maxima of rows gid and gid + 8 (the four lanes of a row hold its 16 columns)
+        float bm_lo = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+        bm_lo = fmaxf(bm_lo, __shfl_xor_sync(0xffffffffu, bm_lo, 1));
+        bm_lo = fmaxf(bm_lo, __shfl_xor_sync(0xffffffffu, bm_lo, 2));
+        const float mn_lo = fmaxf(m_lo, bm_lo);  // finite: token 16 j is in the piece
+        const float al_lo = ex2(m_lo - mn_lo);
+        m_lo = mn_lo;
+        // P: fp32 weights into the running sum, bf16-rounded into the A operand of P V
+        uint32_t pa[4];
         {
-            const __nv_bfloat16* qp = q + (qrow0 + gg) * D + sl * EL;
-            if constexpr (NV >= 4) {
-#pragma unroll
-                for (int k = 0; k < NV / 4; ++k) {
-                    const uint4 u = __ldg(reinterpret_cast<const uint4*>(qp) + k);
-                    qw[4 * k] = u.x; qw[4 * k + 1] = u.y; qw[4 * k + 2] = u.z; qw[4 * k + 3] = u.w;
-                }
-            } else if constexpr (NV == 2) {
-                const uint2 u = __ldg(reinterpret_cast<const uint2*>(qp));
-                qw[0] = u.x; qw[1] = u.y;
-            } else {
-                qw[0] = __ldg(reinterpret_cast<const uint32_t*>(qp));
-            }
+            const float p00 = ex2(s[0][0] - mn_lo), p01 = ex2(s[0][1] - mn_lo);
+            const float p10 = ex2(s[1][0] - mn_lo), p11 = ex2(s[1][1] - mn_lo);
+            l_lo = l_lo * al_lo + ((p00 + p01) + (p10 + p11));
+            pa[0] = pack_bf16(p00, p01);
+            pa[2] = pack_bf16(p10, p11);
         }
-        float m = -INFINITY, l = 0.f, acc[EL];
+        float al_hi = 1.f;
+        if constexpr (kHi) {
+            float bm_hi = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+            bm_hi = fmaxf(bm_hi, __shfl_xor_sync(0xffffffffu, bm_hi, 1));
+            bm_hi = fmaxf(bm_hi, __shfl_xor_sync(0xffffffffu, bm_hi, 2));
+            const float mn_hi = fmaxf(m_hi, bm_hi);
+            al_hi = ex2(m_hi - mn_hi);
+            m_hi = mn_hi;
+            const float p02 = ex2(s[0][2] - mn_hi), p03 = ex2(s[0][3] - mn_hi);
+            const float p12 = ex2(s[1][2] - mn_hi), p13 = ex2(s[1][3] - mn_hi);
+            l_hi = l_hi * al_hi + ((p02 + p03) + (p12 + p13));
+            pa[1] = pack_bf16(p02, p03);
+            pa[3] = pack_bf16(p12, p13);
+        } else {
+            pa[1] = pa[3] = 0u;
+        }
+        // rescale O when a running maximum moved (a warp-uniform test)
+        if (__any_sync(0xffffffffu, al_lo != 1.f || al_hi != 1.f)) {
 #pragma unroll
-        for (int e = 0; e < EL; ++e) acc[e] = 0.f;
-        for (int t = 0; t < kRingTok; ++t) issue(t);
-        for (int t = 0; t < nw; ++t) {
-            cp_async_wait<kRingTok - 1>();  // this lane's copy of token t has landed
-            __syncwarp();                   // ... and every other lane's
-            const uint8_t* tok = &ring[wib][t % kRingTok][0];
-            uint32_t kw[NV], vw[NV];
-#pragma unroll
-            for (int k = 0; k < NV; k += 4 > NV ? NV : 4) {
-                if constexpr (NV >= 4) {
-                    const uint4 ku = *reinterpret_cast<const uint4*>(tok + sl * EL * 2 + k * 4);
-                    const uint4 vu = *reinterpret_cast<const uint4*>(tok + RB + sl * EL * 2 + k * 4);
-                    kw[k] = ku.x; kw[k + 1] = ku.y; kw[k + 2] = ku.z; kw[k + 3] = ku.w;
-                    vw[k] = vu.x; vw[k + 1] = vu.y; vw[k + 2] = vu.z; vw[k + 3] = vu.w;
-                } else if constexpr (NV == 2) {
-                    const uint2 ku = *reinterpret_cast<const uint2*>(tok + sl * EL * 2);
-                    const uint2 vu = *reinterpret_cast<const uint2*>(tok + RB + sl * EL * 2);
-                    kw[0] = ku.x; kw[1] = ku.y; vw[0] = vu.x; vw[1] = vu.y;
-                } else {
-                    kw[0] = *reinterpret_cast<const uint32_t*>(tok + sl * EL * 2);
-                    vw[0] = *reinterpret_cast<const uint32_t*>(tok + RB + sl * EL * 2);
+            for (int t = 0; t < NT; ++t) {
+                o[t][0] *= al_lo;
+                o[t][1] *= al_lo;
+                if constexpr (kHi) {
+                    o[t][2] *= al_hi;
+                    o[t][3] *= al_hi;
                 }
             }
-            __syncwarp();  // the slot is read: it may be refilled
-            issue(t + kRingTok);
-            float sc = 0.f;
-#pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                sc = fmaf(lo(qw[k]), lo(kw[k]), sc);
-                sc = fmaf(hi(qw[k]), hi(kw[k]), sc);
-            }
-#pragma unroll
-            for (int o = LP / 2; o > 0; o >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, o);
-            const float s2 = sc * g.scale_log2;
-            const float mn = fmaxf(m, s2);
-            const float alpha = ex2(m - mn), p = ex2(s2 - mn);
-            l = l * alpha + p;
-#pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                acc[2 * k] = fmaf(p, lo(vw[k]), acc[2 * k] * alpha);
-                acc[2 * k + 1] = fmaf(p, hi(vw[k]), acc[2 * k + 1] * alpha);
-            }
-            m = mn;
         }
-        cp_async_wait<0>();  // nothing of this pass stays in flight
+        // O += P V (V rows transposed by ldmatrix into the B operand)
+#pragma unroll
+        for (int dp = 0; dp < D / 16; ++dp) {
+            uint32_t vb[4];
+            ldsm_x4_trans(v_addr + j * kPieceBlk * RS + dp * 32, vb);
+            mma16816(o[2 * dp], pa, vb[0], vb[1]);
+            mma16816(o[2 * dp + 1], pa, vb[2], vb[3]);
+        }
+    }
+    if (!ok) {
+        // a wait gave up: record it, then let the copies still in flight land (bounded)
+        if (lane == 0) {
+            set_status(status, XATTN_STATUS_TIMEOUT);
+            for (int j = jw; j < nb; ++j) ptx::mbar_wait(&bar[j], 0, abort_sh);
+        }
         __syncwarp();
+    }
+
+    // 3. the piece's partial result of rows gid and gid + 8
+    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+#pragma unroll
+    for (int half = 0; half < (kHi ? 2 : 1); ++half) {
+        const int row = gid + half * 8;
+        if (row >= G) continue;
+        const float l = half ? l_hi : l_lo, m = half ? m_hi : m_lo;
         const bool empty = !(l > 0.f);
         const float inv = empty ? 0.f : 1.f / l;
-        float* po = part_o + (prow0 + gg) * D + sl * EL;
-        if constexpr (EL >= 4) {
+        float* po = part_o + (prow0 + row) * D + tig * 2;
 #pragma unroll
-            for (int k = 0; k < EL / 4; ++k)
-                reinterpret_cast<float4*>(po)[k] =
-                    make_float4(acc[4 * k] * inv, acc[4 * k + 1] * inv, acc[4 * k + 2] * inv, acc[4 * k + 3] * inv);
-        } else {
-            *reinterpret_cast<float2*>(po) = make_float2(acc[0] * inv, acc[1] * inv);
-        }
-        if (sl == 0)
-            part_lse[prow0 + gg] = slot_bad ? __uint_as_float(kNaN) : (empty ? -INFINITY : (m + __log2f(l)) * kLn2);
+        for (int t = 0; t < NT; ++t)
+            *reinterpret_cast<float2*>(po + t * 8) = make_float2(o[t][2 * half] * inv, o[t][2 * half + 1] * inv);
+        if (tig == 0)
+            part_lse[prow0 + row] = (slot_bad || !ok) ? __uint_as_float(kNaN)
+                                                      : (empty ? -INFINITY : (m + __log2f(l)) * kLn2);
     }
 }
 
@@ -712,10 +800,11 @@ cudaError_t launch_d(const Geometry& g, cudaStream_t st, const __nv_bfloat16* q,
                      const __nv_bfloat16* pv, const int32_t* idx, const int32_t* slen, float* po, float* pl,
                      void* out, float* lse, int32_t* status) {
     const dim3 grid((unsigned)(((long)g.R * g.BW * g.Hkv + 7) / 8)), block(256);
-    static_assert(kPieceWarps == 8, "ns_piece_kernel runs 8 warps per CTA, like the other kernels here");
     const int npc = g.ns_to_piece ? 1 : g.ns_pieces;  // Non-Shared pieces per (r, b, h)
-    const long piece_ctas = ((long)g.R * g.BW * g.Hkv * npc + 7) / 8;
+    const long piece_ctas = (long)g.R * g.BW * g.Hkv * npc;  // one warp each
     if (piece_ctas > 0x7fffffffL) return cudaErrorInvalidValue;
+    const int tok_cap = g.step < kNsChunk ? (g.step + kPieceBlk - 1) / kPieceBlk * kPieceBlk : kNsChunk;
+    const int piece_smem = piece_smem_bytes(D, tok_cap);
     const unsigned rows_ctas = (unsigned)(((long)g.R * g.BW * g.Hq + 7) / 8);
     // short Non-Shared part ahead of the fused Shared stage: one warp per (request, beam)
     const bool beam_path = g.ns_to_piece && g.step <= kNsBeamMaxTok && ns_beam_warp_bytes(g) <= kNsBeamMaxWarpBytes;
@@ -726,7 +815,7 @@ cudaError_t launch_d(const Geometry& g, cudaStream_t st, const __nv_bfloat16* q,
             cudaError_t e = launch_beam<D, GV>(g, st, q, pk, pv, idx, po, pl, status);                          \
             if (e != cudaSuccess) return e;                                                                      \
         } else if (g.ns_to_piece || g.ns_pieces > 0) {                                                           \
-            ns_piece_kernel<D, GV><<<(unsigned)piece_ctas, block, 0, st>>>(g, npc, q, pk, pv, idx, po, pl, status); \
+            ns_piece_kernel<D, GV><<<(unsigned)piece_ctas, 32, piece_smem, st>>>(g, npc, tok_cap, q, pk, pv, idx, po, pl, status); \
             if (!g.ns_to_piece) merge_rows_kernel<D><<<rows_ctas, block, 0, st>>>(g, slen, po, pl, out, lse, status); \
         } else {                                                                                                 \
             ns_merge_kernel<D, GV><<<grid, block, 0, st>>>(g, q, pk, pv, idx, slen, po, pl, out, lse, status); \

@@ -1,5 +1,5 @@
-// Thin inline-PTX wrappers for the sm_100-family features the Shared-stage kernel uses:
-// mbarriers, TMA tile loads, and the 5th-generation tensor core (tcgen05: TMEM
+// Thin inline-PTX wrappers for the sm_100-family features the attention kernels use:
+// mbarriers, TMA tile and bulk loads, and the 5th-generation tensor core (tcgen05: TMEM
 // allocation, MMA, commit, TMEM loads/stores). Written against the public PTX ISA.
 #pragma once
 
@@ -97,6 +97,14 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
         : "memory");
+}
+
+// Bulk (untiled) copy of `bytes` contiguous bytes global -> shared, completion signalled on
+// `bar` (complete_tx bytes). Both addresses 16-byte aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_addr(smem_dst)), "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
 }
 
 // Prefetch of a 4-D tile into L2 (no shared memory, no completion tracking).

@@ -89,6 +89,31 @@ def test_long_non_shared_parts(T, d):
     assert db.plan().fused == 0
 
 
+@pytest.mark.parametrize("Hq,Hkv,d,T", [(16, 1, 128, 77), (32, 2, 64, 50), (2, 1, 64, 45), (8, 1, 128, 100),
+                                         (4, 4, 64, 40)],
+                         ids=["G16_d128", "G16_d64", "G2_d64", "G8_d128", "G1_d64"])
+def test_long_non_shared_parts_group_sizes(Hq, Hkv, d, T):
+    """The piece kernel holds the G query heads of a KV head as rows of one 16-row MMA tile:
+    every group size (rows 8..15 in use only for G = 16), both head dims, ragged blocks."""
+    w = wl.custom(R=2, BW=5, Hq=Hq, Hkv=Hkv, d=d, lens=(260, 0), T=T, seed=60 + T)
+    _, db, _ = run_and_check(w)
+    assert db.plan().fused == 0
+
+
+def test_bad_slot_in_long_part():
+    """An out-of-range ancestry slot in the second piece of a long Non-Shared part: status
+    BAD_SLOT and a NaN row for that beam only."""
+    w = wl.custom(R=1, BW=4, Hq=8, Hkv=2, d=128, lens=(200,), T=100, seed=3)
+    db = DeviceBatch(wl.make_inputs(w))
+    db.build_cache()
+    db.idx[0, 2, 70] = -5
+    xattn.check(db.decode())
+    assert db.read_status() & xattn.XATTN_STATUS_BAD_SLOT
+    o = db.out.float().cpu()
+    assert torch.isnan(o[0, 2]).all()
+    assert torch.isfinite(o[0, [0, 1, 3]]).all()
+
+
 @pytest.mark.parametrize("T,d,Hq,Hkv", [(9, 128, 8, 2), (16, 64, 8, 2), (32, 128, 16, 2), (20, 128, 4, 4)])
 def test_medium_non_shared_parts_fused(T, d, Hq, Hkv):
     """9..32 ancestry tokens per beam with a one-piece prefix: the fused decode computes the
