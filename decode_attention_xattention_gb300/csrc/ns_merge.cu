@@ -206,221 +206,327 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
                  : "r"(addr)
                  : "memory");
 }
+// Transpose of an 8x8 bf16 matrix held in the MMA fragment layout (lane l: row l/4,
+// columns 2(l%4), 2(l%4)+1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     const __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&t);
 }
 
-constexpr int kPieceBlk = 16;                        // tokens per block (the k of one P.V MMA)
-constexpr int kPieceBlocks = kNsChunk / kPieceBlk;   // blocks of a full piece
-constexpr int kPieceHead = 128;                      // bytes before the staged rows: mbarriers, flag
+constexpr int kPieceBlk = 16;    // positions per block (the k of one P.V MMA)
+constexpr int kRingBlocks = 2;   // blocks staged per warp: one being computed, one in flight
+constexpr int kPieceHead = 128;  // bytes before the staged rows: mbarriers and flags
 // Shared-memory row stride of a staged pool row: the row plus 16 bytes, so that the eight
 // rows one ldmatrix reads start in eight different groups of four banks.
 __host__ __device__ constexpr int piece_row_stride(int D) { return D * 2 + 16; }
-// Dynamic shared memory of ns_piece_kernel for pieces of up to `tok` tokens.
-inline int piece_smem_bytes(int D, int tok) {
-    const int cap = (tok + kPieceBlk - 1) / kPieceBlk * kPieceBlk;
-    return kPieceHead + 2 * cap * piece_row_stride(D);
+// Dynamic shared memory of one ns_piece_kernel warp (CTA): the K and V rows of the ring.
+__host__ __device__ constexpr int piece_smem_bytes(int D) {
+    return kPieceHead + 2 * kRingBlocks * kPieceBlk * piece_row_stride(D);
+}
+// CTAs per SM the shared memory admits (228 KB per SM, 1 KB of it reserved per CTA); the
+// kernel's register budget is sized for that many.
+__host__ __device__ constexpr int piece_ctas_per_sm(int D) {
+    return (228 * 1024) / (piece_smem_bytes(D) + 1024) > 16 ? 16 : (228 * 1024) / (piece_smem_bytes(D) + 1024);
 }
 
-// Non-Shared stage of one (request, beam, KV head) over one piece of its ancestry positions
-// (at most kNsChunk of them), stored as workspace piece `nsplit + piece` for the Shared-
-// stage epilogue (one piece: step <= 32) or the row-merge kernel to merge; prefix-length
-// problems and empty rows are reported by those. One warp per CTA.
+// Coordinates of a Non-Shared piece: request r, beam b, KV head h, piece c of the beam's
+// ancestry positions, n of them (>= 1).
+struct NsPiece {
+    int r, b, h, c, n;
+};
+__device__ __forceinline__ NsPiece ns_piece_of(const Geometry& g, unsigned npc, unsigned t) {
+    NsPiece k;
+    const unsigned rbh = t / npc;
+    k.c = (int)(t - rbh * npc);
+    const unsigned rb = rbh / (unsigned)g.Hkv;
+    k.h = (int)(rbh - rb * (unsigned)g.Hkv);
+    k.r = (int)(rb / (unsigned)g.BW);
+    k.b = (int)(rb - (unsigned)k.r * (unsigned)g.BW);
+    k.n = min(kNsChunk, g.step - k.c * kNsChunk);
+    return k;
+}
+
+// Non-Shared stage of (request, beam, KV head) pieces of at most kNsChunk ancestry positions,
+// each stored as workspace piece `nsplit + piece` for the Shared-stage epilogue (one piece:
+// step <= 32) or the row-merge kernel to merge; prefix-length problems and empty rows are
+// reported by those.
 //
-// Data movement: after the one index load, every K and V row of the piece (one pool row
-// of this head is 2d contiguous bytes) is requested at once by bulk copies, one per row,
-// completing on one mbarrier per block of 16 tokens; the rows are never reused, so the
-// whole piece is in flight while the first block is computed.
-// Arithmetic: the G query heads of the KV head are the rows of one 16-row MMA tile (rows
-// G..15 zero), so a block of 16 tokens costs D/8 MMAs for S = Q K^T and D/8 for O += P V:
-// S is held in the accumulator layout, whose registers are also the A operand of P V once
-// rounded to bf16 (as the Shared-stage kernel rounds P), and the online softmax rescales O
-// once per block. Q, K and P enter the MMAs as bf16 with fp32 accumulation.
+// One warp per CTA, persistent: the grid is one wave of resident CTAs and CTA w takes the
+// pieces w, w + gridDim.x, ... in turn. A piece is cut into blocks of 16 positions; the
+// warp's blocks, across piece boundaries, stream through a ring of kRingBlocks buffers:
+// every pool row of a block (2d contiguous bytes of one head) is requested by one bulk copy
+// completing on the buffer's mbarrier, and a buffer is refilled with the block kRingBlocks
+// ahead as soon as its block is computed. The ring is kept short so that many warps fit on
+// an SM: the warps' arithmetic is a chain of dependent steps, and it is the number of
+// warps, not the depth of one warp's ring, that keeps both the SM and HBM busy. The
+// ancestry slots of the next piece are loaded a piece ahead, its Q rows as soon as the
+// current piece's last Q K^T has been issued.
+// Arithmetic, transposed so that the 16 positions of a block are the M dimension of the MMA
+// (m16n8k16, bf16 inputs, fp32 accumulators) and the G query heads of the KV head its N
+// dimension, 8 heads per tile: S^T = K Q^T costs D/16 MMAs per head tile and O^T = V^T P^T
+// D/16 more, with K and V read by ldmatrix straight from the staged rows (V transposed).
+// The online softmax runs down the columns of S^T (one column per query head), P^T is
+// rounded to bf16 (as the Shared-stage kernel rounds P) and moved from the accumulator
+// layout to the B operand layout by movmatrix, and O^T is rescaled once per block. The
+// running sums take the fp32 weights.
 template <int D, int G>
-__global__ void __launch_bounds__(32, 1) ns_piece_kernel(
-    Geometry g, int npc, int tok_cap, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ pool_k,
+__global__ void __launch_bounds__(32, piece_ctas_per_sm(D)) ns_piece_kernel(
+    Geometry g, int npc, int ntasks, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ pool_k,
     const __nv_bfloat16* __restrict__ pool_v, const int32_t* __restrict__ idx, float* __restrict__ part_o,
     float* __restrict__ part_lse, int32_t* status) {
-    static_assert(G <= 16, "the query heads of a KV head fill at most one 16-row MMA tile");
+    static_assert(G <= 16, "at most two tiles of 8 query heads");
     static_assert(kNsChunk <= 64 && kNsChunk % kPieceBlk == 0, "a lane holds the slots of positions lane, lane + 32");
+    static_assert(kPieceBlk == 16 && 32 % kPieceBlk == 0, "a block's positions lie on one side of position 32");
+    static_assert(kRingBlocks >= 2 && kRingBlocks <= 8, "ring of 2..8 buffers (mbarriers at offset 0, flags at 64)");
     constexpr int RB = D * 2;                   // bytes of one pool row (one head)
     constexpr int RS = piece_row_stride(D);     // its stride in shared memory
-    constexpr int KS = D / 16;                  // k-steps of Q K^T
-    constexpr int NT = D / 8;                   // 8-column tiles of O
-    constexpr bool kHi = G > 8;                 // rows 8..15 of the tile are query heads
+    constexpr int KS = D / 16;                  // k-steps of K Q^T, and 16-row tiles of O^T
+    constexpr int NH = (G + 7) / 8;             // tiles of 8 query heads
     // the Shared-stage kernel that follows in the fused decode may start its CTAs now; it
     // reads this kernel's output only after waiting for its completion
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ __align__(128) uint8_t psm[];
-    uint64_t* bar = reinterpret_cast<uint64_t*>(psm);
-    volatile int* abort_sh = reinterpret_cast<volatile int*>(psm + kPieceBlocks * 8);
+    uint64_t* full = reinterpret_cast<uint64_t*>(psm);              // one per ring buffer
+    int* buf_bad = reinterpret_cast<int*>(psm + 64);                // the buffer's piece has a bad slot
+    volatile int* abort_sh = reinterpret_cast<volatile int*>(psm + 96);
     uint8_t* k_sm = psm + kPieceHead;
-    uint8_t* v_sm = k_sm + tok_cap * RS;
+    uint8_t* v_sm = k_sm + kRingBlocks * kPieceBlk * RS;
     const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
-    long w = blockIdx.x;
-    const int c = (int)(w % npc);  // piece: ancestry positions [c * kNsChunk, ...)
-    w /= npc;
-    const int h = (int)(w % g.Hkv);
-    const int b = (int)((w / g.Hkv) % g.BW);
-    const int r = (int)(w / ((long)g.Hkv * g.BW));
-    const size_t prow0 = (((size_t)r * g.Hkv + h) * g.pieces + g.nsplit + c) * g.M + (size_t)b * G;
-    const int i0 = c * kNsChunk;
-    const int n = min(min(kNsChunk, tok_cap), g.step - i0);  // positions of this piece
-    const int32_t* row_idx = idx + ((size_t)r * g.BW + b) * g.Tmax + i0;
-    const int slot_a = lane < n ? __ldg(row_idx + lane) : 0;
-    const int slot_b = lane + 32 < n ? __ldg(row_idx + lane + 32) : 0;
-    const bool slot_bad = __any_sync(0xffffffffu, (lane < n && (slot_a < 0 || slot_a >= g.S)) ||
-                                                       (lane + 32 < n && (slot_b < 0 || slot_b >= g.S)));
-    if (slot_bad && lane == 0) set_status(status, XATTN_STATUS_BAD_SLOT);
-    const int nw = slot_bad ? 0 : max(n, 0);  // tokens walked
-    const int nb = (nw + kPieceBlk - 1) / kPieceBlk;
-
-    // 1. request the piece: barrier j counts the bytes of tokens [16 j, 16 j + 16)
+    const int stride = (int)gridDim.x;
     if (lane == 0) {
-        for (int j = 0; j < kPieceBlocks; ++j) ptx::mbar_init(&bar[j], 1);
+        for (int j = 0; j < kRingBlocks; ++j) ptx::mbar_init(&full[j], 1);
         *abort_sh = 0;
         ptx::fence_barrier_init();
-        for (int j = 0; j < nb; ++j) ptx::mbar_arrive_expect_tx(&bar[j], (uint32_t)(min(kPieceBlk, nw - j * kPieceBlk) * 2 * RB));
     }
     __syncwarp();
-    const size_t head_off = (size_t)h * D;
-    for (int t = lane; t < nw; t += 32) {
-        const int slot = t < 32 ? slot_a : slot_b;
-        const size_t off = ((size_t)r * g.S + slot) * g.Hkv * D + head_off;
-        ptx::bulk_load(k_sm + t * RS, pool_k + off, RB, &bar[t / kPieceBlk]);
-        ptx::bulk_load(v_sm + t * RS, pool_v + off, RB, &bar[t / kPieceBlk]);
-    }
-    // V rows of the last block's ragged tail are read by the MMA with weight 0: make them 0
-    for (int e = lane; e < (nb * kPieceBlk - nw) * (RB / 16); e += 32)
-        *reinterpret_cast<uint4*>(v_sm + (nw + e / (RB / 16)) * RS + (e % (RB / 16)) * 16) = make_uint4(0, 0, 0, 0);
 
-    // 2. Q as the A operand: rows gid (a0, a2) and gid + 8 (a1, a3), zero beyond G
-    const __nv_bfloat16* qb = q + (((size_t)r * g.BW + b) * g.Hq + (size_t)h * G) * D + tig * 2;
-    uint32_t qa[KS][4];
+    // ancestry slots of a piece's positions lane and lane + 32
+    auto load_slots = [&](const NsPiece& k, int& sa, int& sb) {
+        const int32_t* ri = idx + ((size_t)k.r * g.BW + k.b) * g.Tmax + k.c * kNsChunk;
+        sa = lane < k.n ? __ldg(ri + lane) : 0;
+        sb = lane + 32 < k.n ? __ldg(ri + lane + 32) : 0;
+    };
+    // Q^T of a piece as the B operand: head nh*8 + gid, elements 2 tig, 2 tig + 1 (b0) and
+    // 8 more (b1) of each 16-element k-step; zero for heads past G
+    auto load_q = [&](const NsPiece& k, uint32_t (&f)[KS][NH][2]) {
+        const __nv_bfloat16* qb = q + (((size_t)k.r * g.BW + k.b) * g.Hq + (size_t)k.h * G) * D + tig * 2;
 #pragma unroll
-    for (int kk = 0; kk < KS; ++kk) {
-        const bool lo_ok = gid < G, hi_ok = kHi && gid + 8 < G;
-        qa[kk][0] = lo_ok ? __ldg(reinterpret_cast<const uint32_t*>(qb + gid * D + kk * 16)) : 0u;
-        qa[kk][2] = lo_ok ? __ldg(reinterpret_cast<const uint32_t*>(qb + gid * D + kk * 16 + 8)) : 0u;
-        qa[kk][1] = hi_ok ? __ldg(reinterpret_cast<const uint32_t*>(qb + (gid + 8) * D + kk * 16)) : 0u;
-        qa[kk][3] = hi_ok ? __ldg(reinterpret_cast<const uint32_t*>(qb + (gid + 8) * D + kk * 16 + 8)) : 0u;
-    }
-    __syncwarp();  // the zeroed tail rows are written before any lane's ldmatrix
-
-    // per-lane ldmatrix row addresses (K: tokens (lane/16)*8 + lane%8, k half (lane/8)%2;
-    // V transposed: tokens ((lane/8)%2)*8 + lane%8, d half lane/16)
-    const uint32_t k_addr = ptx::smem_addr(k_sm) + ((lane >> 4) * 8 + (lane & 7)) * RS + ((lane >> 3) & 1) * 16;
-    const uint32_t v_addr = ptx::smem_addr(v_sm) + (((lane >> 3) & 1) * 8 + (lane & 7)) * RS + (lane >> 4) * 16;
-
-    float o[NT][4];
+        for (int nh = 0; nh < NH; ++nh) {
+            const int hh = nh * 8 + gid;
 #pragma unroll
-    for (int t = 0; t < NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
-    float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
-    bool ok = true;
-    int jw = 0;  // blocks waited for
-#pragma unroll 1
-    for (int j = 0; j < nb; ++j) {
-        if (!ptx::mbar_wait_warp(&bar[j], 0, abort_sh)) { ok = false; break; }
-        jw = j + 1;
-        // S = Q K^T over tokens 16 j .. 16 j + 15 (two 8-token column tiles)
-        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-            uint32_t kb[4];
-            ldsm_x4(k_addr + j * kPieceBlk * RS + kk * 32, kb);
-            mma16816(s[0], qa[kk], kb[0], kb[1]);
-            mma16816(s[1], qa[kk], kb[2], kb[3]);
-        }
-        // scale to log2 units; tokens past the piece get -inf
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int tok = j * kPieceBlk + nt * 8 + tig * 2 + (e & 1);
-                s[nt][e] = tok < nw ? s[nt][e] * g.scale_log2 : -INFINITY;
+            for (int kk = 0; kk < KS; ++kk) {
+                f[kk][nh][0] = hh < G ? __ldg(reinterpret_cast<const uint32_t*>(qb + hh * D + kk * 16)) : 0u;
+                f[kk][nh][1] = hh < G ? __ldg(reinterpret_cast<const uint32_t*>(qb + hh * D + kk * 16 + 8)) : 0u;
             }
-        // block maxima of rows gid and gid + 8 (the four lanes of a row hold its 16 columns)
-        float bm_lo = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
-        bm_lo = fmaxf(bm_lo, __shfl_xor_sync(0xffffffffu, bm_lo, 1));
-        bm_lo = fmaxf(bm_lo, __shfl_xor_sync(0xffffffffu, bm_lo, 2));
-        const float mn_lo = fmaxf(m_lo, bm_lo);  // finite: token 16 j is in the piece
-        const float al_lo = ex2(m_lo - mn_lo);
-        m_lo = mn_lo;
-        // P: fp32 weights into the running sum, bf16-rounded into the A operand of P V
-        uint32_t pa[4];
-        {
-            const float p00 = ex2(s[0][0] - mn_lo), p01 = ex2(s[0][1] - mn_lo);
-            const float p10 = ex2(s[1][0] - mn_lo), p11 = ex2(s[1][1] - mn_lo);
-            l_lo = l_lo * al_lo + ((p00 + p01) + (p10 + p11));
-            pa[0] = pack_bf16(p00, p01);
-            pa[2] = pack_bf16(p10, p11);
         }
-        float al_hi = 1.f;
-        if constexpr (kHi) {
-            float bm_hi = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
-            bm_hi = fmaxf(bm_hi, __shfl_xor_sync(0xffffffffu, bm_hi, 1));
-            bm_hi = fmaxf(bm_hi, __shfl_xor_sync(0xffffffffu, bm_hi, 2));
-            const float mn_hi = fmaxf(m_hi, bm_hi);
-            al_hi = ex2(m_hi - mn_hi);
-            m_hi = mn_hi;
-            const float p02 = ex2(s[0][2] - mn_hi), p03 = ex2(s[0][3] - mn_hi);
-            const float p12 = ex2(s[1][2] - mn_hi), p13 = ex2(s[1][3] - mn_hi);
-            l_hi = l_hi * al_hi + ((p02 + p03) + (p12 + p13));
-            pa[1] = pack_bf16(p02, p03);
-            pa[3] = pack_bf16(p12, p13);
-        } else {
-            pa[1] = pa[3] = 0u;
+    };
+
+    // ---- request side: the next block to stage is block ib of piece it (coordinates ip) -
+    int it = (int)blockIdx.x, ib = 0;
+    uint32_t iseq = 0;  // blocks requested so far
+    NsPiece ip = ns_piece_of(g, npc, it), inx = ip;
+    int is_a, is_b, nx_a = 0, nx_b = 0;
+    load_slots(ip, is_a, is_b);
+    if (it + stride < ntasks) {
+        inx = ns_piece_of(g, npc, it + stride);
+        load_slots(inx, nx_a, nx_b);
+    }
+    bool ibad = false;
+    auto check_slots = [&]() {  // piece ip, its slots in is_a / is_b
+        ibad = __any_sync(0xffffffffu, (lane < ip.n && (is_a < 0 || is_a >= g.S)) ||
+                                           (lane + 32 < ip.n && (is_b < 0 || is_b >= g.S)));
+        if (ibad && lane == 0) set_status(status, XATTN_STATUS_BAD_SLOT);
+    };
+    auto request_block = [&]() {  // it < ntasks
+        const int buf = (int)(iseq % kRingBlocks);
+        const int t0 = ib * kPieceBlk;
+        const int cnt = min(kPieceBlk, ip.n - t0);
+        // this lane's earlier shared-memory accesses to the buffer (MMA operand reads, the
+        // zeroing below) are ordered before the copies that overwrite it
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            buf_bad[buf] = ibad ? 1 : 0;
+            ptx::mbar_arrive_expect_tx(&full[buf], ibad ? 0u : (uint32_t)(cnt * 2 * RB));
         }
-        // rescale O when a running maximum moved (a warp-uniform test)
-        if (__any_sync(0xffffffffu, al_lo != 1.f || al_hi != 1.f)) {
-#pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                o[t][0] *= al_lo;
-                o[t][1] *= al_lo;
-                if constexpr (kHi) {
-                    o[t][2] *= al_hi;
-                    o[t][3] *= al_hi;
+        const int tl = t0 + (lane & 15);  // lanes 0..15: K rows, 16..31: V rows of the block
+        const int sv = __shfl_sync(0xffffffffu, t0 < 32 ? is_a : is_b, tl & 31);
+        if (!ibad && (lane & 15) < cnt) {
+            const size_t off = (((size_t)ip.r * g.S + sv) * g.Hkv + ip.h) * D;
+            uint8_t* dst = (lane < 16 ? k_sm : v_sm) + (buf * kPieceBlk + (lane & 15)) * RS;
+            ptx::bulk_load(dst, (lane < 16 ? pool_k : pool_v) + off, RB, &full[buf]);
+        }
+        if (cnt < kPieceBlk) {
+            // V rows past the piece are read by the MMA with weight 0: make them 0
+            for (int e = lane; e < (kPieceBlk - cnt) * (RB / 16); e += 32)
+                *reinterpret_cast<uint4*>(v_sm + (buf * kPieceBlk + cnt + e / (RB / 16)) * RS + (e % (RB / 16)) * 16) =
+                    make_uint4(0, 0, 0, 0);
+        }
+        ++iseq;
+        if (++ib * kPieceBlk >= ip.n) {  // on to this warp's next piece
+            ib = 0;
+            it += stride;
+            if (it < ntasks) {
+                ip = inx;
+                is_a = nx_a;
+                is_b = nx_b;
+                if (it + stride < ntasks) {
+                    inx = ns_piece_of(g, npc, it + stride);
+                    load_slots(inx, nx_a, nx_b);
                 }
+                check_slots();
             }
         }
-        // O += P V (V rows transposed by ldmatrix into the B operand)
+    };
+
+    // ---- compute side ---------------------------------------------------------------------
+    uint32_t qf[KS][NH][2];
+    NsPiece cp = ip;  // the piece being computed
+    load_q(cp, qf);
+    check_slots();
+    for (int j = 0; j < kRingBlocks && it < ntasks; ++j) request_block();
+
+    // per-lane ldmatrix row offsets. K as the A operand (positions x d): matrix i/8 of the
+    // x4 load covers positions ((i/8)%2)*8.., d half (i/16). V^T as the A operand (d x
+    // positions, read transposed): positions (i/16)*8.., d half (i/8)%2.
+    const uint32_t k_addr = ptx::smem_addr(k_sm) + (((lane >> 3) & 1) * 8 + (lane & 7)) * RS + (lane >> 4) * 16;
+    const uint32_t v_addr = ptx::smem_addr(v_sm) + ((lane >> 4) * 8 + (lane & 7)) * RS + ((lane >> 3) & 1) * 16;
+    uint32_t cseq = 0;  // blocks computed so far
+    bool ok = true;
+#pragma unroll 1
+    for (int ct = (int)blockIdx.x; ct < ntasks; ct += stride) {
+        const bool has_next = ct + stride < ntasks;
+        const NsPiece cn = has_next ? ns_piece_of(g, npc, ct + stride) : cp;
+        // O^T: d rows mt*16 + gid (c0, c1) and + 8 (c2, c3), heads nh*8 + 2 tig + {0, 1}
+        float o[KS][NH][4];
 #pragma unroll
-        for (int dp = 0; dp < D / 16; ++dp) {
-            uint32_t vb[4];
-            ldsm_x4_trans(v_addr + j * kPieceBlk * RS + dp * 32, vb);
-            mma16816(o[2 * dp], pa, vb[0], vb[1]);
-            mma16816(o[2 * dp + 1], pa, vb[2], vb[3]);
+        for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+            for (int nh = 0; nh < NH; ++nh) o[mt][nh][0] = o[mt][nh][1] = o[mt][nh][2] = o[mt][nh][3] = 0.f;
+        // running maximum and lane-partial sum of heads nh*8 + 2 tig + j
+        float m[NH][2], l[NH][2];
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh) m[nh][0] = m[nh][1] = -INFINITY, l[nh][0] = l[nh][1] = 0.f;
+        bool bad = false;
+        const int nbk = (cp.n + kPieceBlk - 1) / kPieceBlk;
+#pragma unroll 1
+        for (int cb = 0; cb < nbk; ++cb) {
+            const int buf = (int)(cseq % kRingBlocks);
+            if (!ptx::mbar_wait_warp(&full[buf], (cseq / kRingBlocks) & 1, abort_sh)) { ok = false; break; }
+            bad = bad || buf_bad[buf] != 0;
+            const bool last = cb == nbk - 1;
+            if (!bad) {
+                const uint32_t kb_addr = k_addr + buf * kPieceBlk * RS, vb_addr = v_addr + buf * kPieceBlk * RS;
+                // S^T = K Q^T: positions gid (c0, c1) and gid + 8 (c2, c3) of the block
+                float s[NH][4];
+#pragma unroll
+                for (int nh = 0; nh < NH; ++nh) s[nh][0] = s[nh][1] = s[nh][2] = s[nh][3] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk) {
+                    uint32_t ka[4];
+                    ldsm_x4(kb_addr + kk * 32, ka);
+#pragma unroll
+                    for (int nh = 0; nh < NH; ++nh) mma16816(s[nh], ka, qf[kk][nh][0], qf[kk][nh][1]);
+                }
+                if (last && has_next) load_q(cn, qf);  // Q of the piece after this one
+                const int lim = cp.n - cb * kPieceBlk;  // positions of the block in the piece
+                uint32_t pb[NH][2];
+                float al[NH][2];
+                bool moved = false;
+#pragma unroll
+                for (int nh = 0; nh < NH; ++nh) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) s[nh][e] *= g.scale_log2;
+                    if (lim < kPieceBlk) {  // ragged last block: positions past the piece get -inf
+                        if (gid >= lim) s[nh][0] = s[nh][1] = -INFINITY;
+                        if (gid + 8 >= lim) s[nh][2] = s[nh][3] = -INFINITY;
+                    }
+                    float p[4];
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        // column maximum over the 16 positions (lanes of equal tig hold a column)
+                        float bm = fmaxf(s[nh][j], s[nh][2 + j]);
+                        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+                        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+                        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+                        const float mn = fmaxf(m[nh][j], bm);  // finite: the block's first position is in
+                        al[nh][j] = ex2(m[nh][j] - mn);
+                        moved = moved || al[nh][j] != 1.f;
+                        m[nh][j] = mn;
+                        p[j] = ex2(s[nh][j] - mn);
+                        p[2 + j] = ex2(s[nh][2 + j] - mn);
+                        l[nh][j] = l[nh][j] * al[nh][j] + (p[j] + p[2 + j]);
+                    }
+                    // P^T as the B operand: positions 2 tig.. (b0: 0..7, b1: 8..15) of head gid
+                    pb[nh][0] = movmatrix_trans(pack_bf16(p[0], p[1]));
+                    pb[nh][1] = movmatrix_trans(pack_bf16(p[2], p[3]));
+                }
+                // rescale O^T when a running maximum moved (a warp-uniform test)
+                if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                        for (int nh = 0; nh < NH; ++nh) {
+                            o[mt][nh][0] *= al[nh][0];
+                            o[mt][nh][1] *= al[nh][1];
+                            o[mt][nh][2] *= al[nh][0];
+                            o[mt][nh][3] *= al[nh][1];
+                        }
+                }
+                // O^T += V^T P^T
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    uint32_t va[4];
+                    ldsm_x4_trans(vb_addr + mt * 32, va);
+#pragma unroll
+                    for (int nh = 0; nh < NH; ++nh) mma16816(o[mt][nh], va, pb[nh][0], pb[nh][1]);
+                }
+            } else if (last && has_next) {
+                load_q(cn, qf);
+            }
+            ++cseq;
+            if (it < ntasks) request_block();  // refill the buffer just computed
         }
+        if (!ok) break;
+
+        // the piece's partial result: head nh*8 + 2 tig + j, d rows mt*16 + gid (+ 8)
+        const size_t prow0 = (((size_t)cp.r * g.Hkv + cp.h) * g.pieces + g.nsplit + cp.c) * g.M + (size_t)cp.b * G;
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float lt = l[nh][j];
+                lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+                lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+                lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+                const int hh = nh * 8 + tig * 2 + j;
+                if (hh >= G) continue;
+                const bool empty = !(lt > 0.f);
+                const float inv = (empty || bad) ? 0.f : 1.f / lt;
+                float* po = part_o + (prow0 + hh) * D + gid;
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    po[mt * 16] = o[mt][nh][j] * inv;
+                    po[mt * 16 + 8] = o[mt][nh][2 + j] * inv;
+                }
+                if (gid == 0)
+                    part_lse[prow0 + hh] =
+                        bad ? __uint_as_float(kNaN) : (empty ? -INFINITY : (m[nh][j] + __log2f(lt)) * kLn2);
+            }
+        cp = cn;
     }
     if (!ok) {
         // a wait gave up: record it, then let the copies still in flight land (bounded)
         if (lane == 0) {
             set_status(status, XATTN_STATUS_TIMEOUT);
-            for (int j = jw; j < nb; ++j) ptx::mbar_wait(&bar[j], 0, abort_sh);
+            for (uint32_t sq = cseq; sq < iseq; ++sq) ptx::mbar_wait(&full[sq % kRingBlocks], (sq / kRingBlocks) & 1, abort_sh);
         }
         __syncwarp();
-    }
-
-    // 3. the piece's partial result of rows gid and gid + 8
-    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
-    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
-    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
-    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-#pragma unroll
-    for (int half = 0; half < (kHi ? 2 : 1); ++half) {
-        const int row = gid + half * 8;
-        if (row >= G) continue;
-        const float l = half ? l_hi : l_lo, m = half ? m_hi : m_lo;
-        const bool empty = !(l > 0.f);
-        const float inv = empty ? 0.f : 1.f / l;
-        float* po = part_o + (prow0 + row) * D + tig * 2;
-#pragma unroll
-        for (int t = 0; t < NT; ++t)
-            *reinterpret_cast<float2*>(po + t * 8) = make_float2(o[t][2 * half] * inv, o[t][2 * half + 1] * inv);
-        if (tig == 0)
-            part_lse[prow0 + row] = (slot_bad || !ok) ? __uint_as_float(kNaN)
-                                                      : (empty ? -INFINITY : (m + __log2f(l)) * kLn2);
     }
 }
 
@@ -795,16 +901,38 @@ cudaError_t launch_beam(const Geometry& g, cudaStream_t st, const __nv_bfloat16*
     return cudaSuccess;
 }
 
+// One wave of resident one-warp CTAs (fewer when there are fewer pieces).
+template <int D, int G>
+cudaError_t launch_piece(const Geometry& g, int npc, cudaStream_t st, const __nv_bfloat16* q, const __nv_bfloat16* pk,
+                         const __nv_bfloat16* pv, const int32_t* idx, float* po, float* pl, int32_t* status) {
+    const long ntasks = (long)g.R * g.BW * g.Hkv * npc;
+    if (ntasks <= 0) return cudaSuccess;
+    if (ntasks > 0x7fffffffL) return cudaErrorInvalidValue;
+    const int smem = piece_smem_bytes(D);
+    static int resident[64] = {};  // CTAs of one wave, per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (resident[dev] == 0) {
+        int per_sm = 0, sms = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ns_piece_kernel<D, G>, 32, smem);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        resident[dev] = (per_sm > 0 ? per_sm : 1) * (sms > 0 ? sms : 1);
+    }
+    const int grid = (int)(ntasks < resident[dev] ? ntasks : resident[dev]);
+    ns_piece_kernel<D, G><<<grid, 32, smem, st>>>(g, npc, (int)ntasks, q, pk, pv, idx, po, pl, status);
+    return cudaSuccess;
+}
+
 template <int D>
 cudaError_t launch_d(const Geometry& g, cudaStream_t st, const __nv_bfloat16* q, const __nv_bfloat16* pk,
                      const __nv_bfloat16* pv, const int32_t* idx, const int32_t* slen, float* po, float* pl,
                      void* out, float* lse, int32_t* status) {
     const dim3 grid((unsigned)(((long)g.R * g.BW * g.Hkv + 7) / 8)), block(256);
     const int npc = g.ns_to_piece ? 1 : g.ns_pieces;  // Non-Shared pieces per (r, b, h)
-    const long piece_ctas = (long)g.R * g.BW * g.Hkv * npc;  // one warp each
-    if (piece_ctas > 0x7fffffffL) return cudaErrorInvalidValue;
-    const int tok_cap = g.step < kNsChunk ? (g.step + kPieceBlk - 1) / kPieceBlk * kPieceBlk : kNsChunk;
-    const int piece_smem = piece_smem_bytes(D, tok_cap);
     const unsigned rows_ctas = (unsigned)(((long)g.R * g.BW * g.Hq + 7) / 8);
     // short Non-Shared part ahead of the fused Shared stage: one warp per (request, beam)
     const bool beam_path = g.ns_to_piece && g.step <= kNsBeamMaxTok && ns_beam_warp_bytes(g) <= kNsBeamMaxWarpBytes;
@@ -815,7 +943,8 @@ cudaError_t launch_d(const Geometry& g, cudaStream_t st, const __nv_bfloat16* q,
             cudaError_t e = launch_beam<D, GV>(g, st, q, pk, pv, idx, po, pl, status);                          \
             if (e != cudaSuccess) return e;                                                                      \
         } else if (g.ns_to_piece || g.ns_pieces > 0) {                                                           \
-            ns_piece_kernel<D, GV><<<(unsigned)piece_ctas, 32, piece_smem, st>>>(g, npc, tok_cap, q, pk, pv, idx, po, pl, status); \
+            cudaError_t e = launch_piece<D, GV>(g, npc, st, q, pk, pv, idx, po, pl, status);                   \
+            if (e != cudaSuccess) return e;                                                                      \
             if (!g.ns_to_piece) merge_rows_kernel<D><<<rows_ctas, block, 0, st>>>(g, slen, po, pl, out, lse, status); \
         } else {                                                                                                 \
             ns_merge_kernel<D, GV><<<grid, block, 0, st>>>(g, q, pk, pv, idx, slen, po, pl, out, lse, status); \
