@@ -793,14 +793,17 @@ __global__ void __launch_bounds__(256) ns_merge_kernel(
 }
 
 // Row-parallel merge for calls whose Non-Shared part is already in pieces: one warp per
-// query row (r, b, h) folds every piece. Lanes first take the pieces' LSEs (lane l holds
-// pieces l, l+32, ...) for the row's maximum and total weight, then split the head
-// dimension while eight pieces' outputs are in flight.
+// query row (r, b, h) folds every piece, lanes splitting the head dimension. The row's loads
+// are issued without waiting on one another: the LSEs of up to 64 pieces stay in registers
+// (lane l: pieces l and l + 32) and reach the other lanes by shuffles, and the output
+// vectors of a batch of pieces are requested while the previous batch is folded, whatever
+// the pieces' weights (a piece without keys has weight 0 and its vector is never used).
 template <int D>
 __global__ void __launch_bounds__(256) merge_rows_kernel(
     Geometry g, const int32_t* __restrict__ shared_len, const float* __restrict__ part_o,
     const float* __restrict__ part_lse, void* __restrict__ out, float* __restrict__ lse, int32_t* status) {
     constexpr int E = D / 32;
+    constexpr int B = 8;  // output vectors per batch
     const int lane = threadIdx.x & 31;
     const long row = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // (r*BW + b)*Hq + hq
     if (row >= (long)g.R * g.BW * g.Hq) return;
@@ -813,9 +816,29 @@ __global__ void __launch_bounds__(256) merge_rows_kernel(
     if (bad && lane == 0 && hq == 0 && b == 0) set_status(status, XATTN_STATUS_BAD_SHARED_LEN);
     const int np = g.nsplit + g.ns_pieces;
     const size_t prow_b = ((size_t)r * g.Hkv + h) * g.pieces * g.M + (size_t)b * g.G + gg;  // + c*M
-    float mx = -INFINITY;
-    bool nan_seen = false;
-    for (int c = lane; c < np; c += 32) {
+    auto load_o = [&](int c, float (&v)[E]) {  // this lane's slice of piece c's output (0 past np)
+        if (c < np) {
+            const float* po = part_o + (prow_b + (size_t)c * g.M) * D + lane * E;
+            if constexpr (E == 4) {
+                const float4 t = __ldg(reinterpret_cast<const float4*>(po));
+                v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+            } else {
+                const float2 t = __ldg(reinterpret_cast<const float2*>(po));
+                v[0] = t.x; v[1] = t.y;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) v[e] = 0.f;
+        }
+    };
+    float ov[2][B][E];
+#pragma unroll
+    for (int k = 0; k < B; ++k) load_o(k, ov[0][k]);  // the first batch rides with the LSEs
+    const float lc0 = lane < np ? __ldg(part_lse + prow_b + (size_t)lane * g.M) : -INFINITY;
+    const float lc1 = lane + 32 < np ? __ldg(part_lse + prow_b + (size_t)(lane + 32) * g.M) : -INFINITY;
+    bool nan_seen = (lc0 != lc0) || (lc1 != lc1);
+    float mx = fmaxf(lc0, lc1) * kLog2e;
+    for (int c = lane + 64; c < np; c += 32) {
         const float lc = __ldg(part_lse + prow_b + (size_t)c * g.M);
         nan_seen |= (lc != lc);
         mx = fmaxf(mx, lc * kLog2e);
@@ -823,43 +846,40 @@ __global__ void __launch_bounds__(256) merge_rows_kernel(
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     bad = bad || __any_sync(0xffffffffu, nan_seen);
-    float lsum = 0.f;
-    for (int c = lane; c < np; c += 32) {
+    // weights (base 2, relative to the row maximum) of pieces lane and lane + 32
+    const float w0 = lc0 > -INFINITY ? ex2(lc0 * kLog2e - mx) : 0.f;
+    const float w1 = lc1 > -INFINITY ? ex2(lc1 * kLog2e - mx) : 0.f;
+    float lsum = w0 + w1;
+    for (int c = lane + 64; c < np; c += 32) {
         const float lc = __ldg(part_lse + prow_b + (size_t)c * g.M);
-        lsum += (lc > -INFINITY) ? ex2(lc * kLog2e - mx) : 0.f;
+        lsum += lc > -INFINITY ? ex2(lc * kLog2e - mx) : 0.f;
     }
     lsum = warp_sum(lsum);
     float acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    for (int c0 = 0; c0 < np; c0 += 8) {
-        float ov[8][E], wv[8];
+#pragma unroll 1
+    for (int c0 = 0; c0 < np; c0 += 2 * B) {
+        // two batches per trip so that the double buffer is indexed statically
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int c = c0 + u;
-            wv[u] = 0.f;
+        for (int half = 0; half < 2; ++half) {
+            const int cb = c0 + half * B;
+            if (cb >= np) break;
 #pragma unroll
-            for (int e = 0; e < E; ++e) ov[u][e] = 0.f;
-            if (c < np) {
-                const size_t prow = prow_b + (size_t)c * g.M;
-                const float lc = __ldg(part_lse + prow);
-                if (lc > -INFINITY) {
-                    wv[u] = ex2(lc * kLog2e - mx);
-                    const float* po = part_o + prow * D + lane * E;
-                    if constexpr (E == 4) {
-                        const float4 t = __ldg(reinterpret_cast<const float4*>(po));
-                        ov[u][0] = t.x; ov[u][1] = t.y; ov[u][2] = t.z; ov[u][3] = t.w;
-                    } else {
-                        const float2 t = __ldg(reinterpret_cast<const float2*>(po));
-                        ov[u][0] = t.x; ov[u][1] = t.y;
-                    }
+            for (int k = 0; k < B; ++k) load_o(cb + B + k, ov[half ^ 1][k]);  // next batch in flight
+#pragma unroll
+            for (int k = 0; k < B; ++k) {
+                const int c = cb + k;
+                float w = __shfl_sync(0xffffffffu, c < 32 ? w0 : w1, c & 31);
+                if (c >= 64 && c < np) {
+                    const float lc = __ldg(part_lse + prow_b + (size_t)c * g.M);
+                    w = lc > -INFINITY ? ex2(lc * kLog2e - mx) : 0.f;
                 }
+                if (c >= np) w = 0.f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] = w > 0.f ? fmaf(w, ov[half][k][e], acc[e]) : acc[e];
             }
         }
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-#pragma unroll
-            for (int e = 0; e < E; ++e) acc[e] = fmaf(wv[u], ov[u][e], acc[e]);
     }
     bad = bad || !(lsum > 0.f);
     const float inv = bad ? __uint_as_float(kNaN) : 1.f / lsum;

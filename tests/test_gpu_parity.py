@@ -100,6 +100,16 @@ def test_long_non_shared_parts_group_sizes(Hq, Hkv, d, T):
     assert db.plan().fused == 0
 
 
+@pytest.mark.parametrize("lens,T,d", [((5000, 300), 130, 128), ((9000, 0), 70, 64)], ids=["43_pieces", "73_pieces"])
+def test_row_merge_many_pieces(lens, T, d):
+    """The row merge keeps the LSEs of 64 pieces in registers and reloads the rest: 128-token
+    prefix pieces plus a long Non-Shared part give 43 and 73 pieces per row, with empty prefix
+    pieces (request 1's shorter or absent prefix) among them."""
+    w = wl.custom(R=2, BW=3, Hq=8, Hkv=2, d=d, lens=lens, T=T, seed=70 + T)
+    _, db, _ = run_and_check(w, split_tokens=128)
+    assert db.plan().fused == 0
+
+
 def test_bad_slot_in_long_part():
     """An out-of-range ancestry slot in the second piece of a long Non-Shared part: status
     BAD_SLOT and a NaN row for that beam only."""
