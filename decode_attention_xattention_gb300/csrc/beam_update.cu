@@ -27,19 +27,19 @@ __host__ __device__ inline int table_cols(int BW, int step) {
 }
 
 __global__ void __launch_bounds__(kThreads) beam_update_kernel(
-    int BW, int HkvD, int S, int Tmax, int step, int copy_ctas, const int32_t* __restrict__ parent,
-    const __nv_bfloat16* __restrict__ new_k, const __nv_bfloat16* __restrict__ new_v,
-    __nv_bfloat16* __restrict__ pool_k, __nv_bfloat16* __restrict__ pool_v,
-    int32_t* __restrict__ idx, int32_t* status) {
+    int BW, int row16, int S, int Tmax, int step, int copy_ctas, const int32_t* __restrict__ parent,
+    const uint4* __restrict__ new_k, const uint4* __restrict__ new_v, uint4* __restrict__ pool_k,
+    uint4* __restrict__ pool_v, int32_t* __restrict__ idx, int32_t* status) {
     const int r = blockIdx.x;
     if ((int)blockIdx.y < copy_ctas) {
-        // 1. K/V of the new tokens: [BW, Hkv, d] of request r -> slots step*BW .. step*BW+BW-1.
-        //    All loads of a thread are issued before its stores (independent 16-byte vectors).
-        const size_t n16 = (size_t)BW * HkvD / 8;  // 16-byte vectors (HkvD is a multiple of 8)
-        const uint4* sk = reinterpret_cast<const uint4*>(new_k + (size_t)r * BW * HkvD);
-        const uint4* sv = reinterpret_cast<const uint4*>(new_v + (size_t)r * BW * HkvD);
-        uint4* dk = reinterpret_cast<uint4*>(pool_k + ((size_t)r * S + (size_t)step * BW) * HkvD);
-        uint4* dv = reinterpret_cast<uint4*>(pool_v + ((size_t)r * S + (size_t)step * BW) * HkvD);
+        // 1. K/V of the new tokens: [BW, Hkv, d] of request r -> slots step*BW .. step*BW+BW-1
+        //    (row16: 16-byte vectors per slot). All loads of a thread are issued before its
+        //    stores (independent 16-byte vectors).
+        const size_t n16 = (size_t)BW * row16;
+        const uint4* sk = new_k + (size_t)r * BW * row16;
+        const uint4* sv = new_v + (size_t)r * BW * row16;
+        uint4* dk = pool_k + ((size_t)r * S + (size_t)step * BW) * row16;
+        uint4* dv = pool_v + ((size_t)r * S + (size_t)step * BW) * row16;
         const size_t stride = (size_t)copy_ctas * kThreads;
         size_t i = (size_t)blockIdx.y * kThreads + threadIdx.x;
         for (; i + 3 * stride < n16; i += 4 * stride) {
@@ -95,19 +95,20 @@ __global__ void __launch_bounds__(kThreads) beam_update_kernel(
 
 }  // namespace
 
-cudaError_t launch_beam_update(int R, int BW, int Hkv, int d, int S, int Tmax, int step,
-                               const int32_t* parent, const __nv_bfloat16* new_k,
-                               const __nv_bfloat16* new_v, __nv_bfloat16* pool_k,
-                               __nv_bfloat16* pool_v, int32_t* idx, int32_t* status,
-                               cudaStream_t stream) {
+cudaError_t launch_beam_update(int R, int BW, int Hkv, int d, int elem_bytes, int S, int Tmax, int step,
+                               const int32_t* parent, const void* new_k, const void* new_v, void* pool_k,
+                               void* pool_v, int32_t* idx, int32_t* status, cudaStream_t stream) {
     if (BW > kTableInts) return cudaErrorInvalidValue;
-    const size_t n16 = (size_t)BW * Hkv * d / 8;
+    if (((size_t)Hkv * d * elem_bytes) % 16 != 0) return cudaErrorInvalidValue;
+    const int row16 = (int)((size_t)Hkv * d * elem_bytes / 16);  // 16-byte vectors per slot
+    const size_t n16 = (size_t)BW * row16;
     int ybl = (int)((n16 + kThreads - 1) / kThreads);  // about one vector of K and V per thread
     ybl = max(1, min(ybl, 1024));
     const int tcols = step > 0 ? (step + table_cols(BW, step) - 1) / table_cols(BW, step) : 1;
     dim3 grid(R, ybl + tcols);  // the last tcols CTAs of each request rewrite its ancestry table
-    beam_update_kernel<<<grid, kThreads, 0, stream>>>(BW, Hkv * d, S, Tmax, step, ybl, parent, new_k, new_v,
-                                                      pool_k, pool_v, idx, status);
+    beam_update_kernel<<<grid, kThreads, 0, stream>>>(
+        BW, row16, S, Tmax, step, ybl, parent, static_cast<const uint4*>(new_k), static_cast<const uint4*>(new_v),
+        static_cast<uint4*>(pool_k), static_cast<uint4*>(pool_v), idx, status);
     return cudaGetLastError();
 }
 

@@ -48,6 +48,10 @@ struct LaneVec<128> {  // 4 bf16 per lane = 8 bytes
         float2 fb = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u.y));
         x[0] = fa.x; x[1] = fa.y; x[2] = fb.x; x[3] = fb.y;
     }
+    static __device__ __forceinline__ void load(const float* p, float (&x)[4]) {  // fp32 storage
+        const float4 u = __ldg(reinterpret_cast<const float4*>(p));
+        x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+    }
     static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&x)[4]) {
         __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]);
         __nv_bfloat162 b = __floats2bfloat162_rn(x[2], x[3]);
@@ -62,6 +66,10 @@ struct LaneVec<64> {  // 2 bf16 per lane = 4 bytes
     static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&x)[2]) {
         float2 f = __bfloat1622float2(__ldg(reinterpret_cast<const __nv_bfloat162*>(p)));
         x[0] = f.x; x[1] = f.y;
+    }
+    static __device__ __forceinline__ void load(const float* p, float (&x)[2]) {  // fp32 storage
+        const float2 u = __ldg(reinterpret_cast<const float2*>(p));
+        x[0] = u.x; x[1] = u.y;
     }
     static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&x)[2]) {
         *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(x[0], x[1]);
@@ -104,10 +112,10 @@ struct RowState {
 // loaded together, the kNsTok x G partial dot products are reduced across the warp in one
 // interleaved butterfly, and the running state takes one rescale per round. Lanes split the
 // head dimension. Returns false (status BAD_SLOT) when an ancestry slot is out of range.
-template <int D, int G>
+template <int D, int G, typename T>
 __device__ __forceinline__ bool ns_walk(const Geometry& g, int r, int b, int h, int lane,
-                                        const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ pool_k,
-                                        const __nv_bfloat16* __restrict__ pool_v, const int32_t* __restrict__ idx,
+                                        const T* __restrict__ q, const T* __restrict__ pool_k,
+                                        const T* __restrict__ pool_v, const int32_t* __restrict__ idx,
                                         RowState<D / 32, G>& st, int32_t* status) {
     constexpr int E = D / 32;
     const size_t qrow0 = ((size_t)r * g.BW + b) * g.Hq + (size_t)h * G;
@@ -661,10 +669,11 @@ __global__ void __launch_bounds__(kBeamWarps * 32) ns_beam_kernel(
     }
 }
 
-template <int D, int G>
+// T: storage type of q and the pools (bf16, or fp32 inputs used unrounded).
+template <int D, int G, typename T>
 __global__ void __launch_bounds__(256) ns_merge_kernel(
-    Geometry g, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ pool_k,
-    const __nv_bfloat16* __restrict__ pool_v, const int32_t* __restrict__ idx,
+    Geometry g, const T* __restrict__ q, const T* __restrict__ pool_k,
+    const T* __restrict__ pool_v, const int32_t* __restrict__ idx,
     const int32_t* __restrict__ shared_len, float* __restrict__ part_o,
     float* __restrict__ part_lse, void* __restrict__ out, float* __restrict__ lse,
     int32_t* status) {
@@ -692,7 +701,7 @@ __global__ void __launch_bounds__(256) ns_merge_kernel(
     RowState<E, G> st;
     st.init();
     bool slot_bad = false;
-    if (g.ns_pieces == 0 && g.step > 0 && !bad && !ns_walk<D, G>(g, r, b, h, lane, q, pool_k, pool_v, idx, st, status)) {
+    if (g.ns_pieces == 0 && g.step > 0 && !bad && !ns_walk<D, G, T>(g, r, b, h, lane, q, pool_k, pool_v, idx, st, status)) {
         bad = true;
         slot_bad = true;
     }
@@ -948,10 +957,30 @@ cudaError_t launch_piece(const Geometry& g, int npc, cudaStream_t st, const __nv
 }
 
 template <int D>
-cudaError_t launch_d(const Geometry& g, cudaStream_t st, const __nv_bfloat16* q, const __nv_bfloat16* pk,
-                     const __nv_bfloat16* pv, const int32_t* idx, const int32_t* slen, float* po, float* pl,
-                     void* out, float* lse, int32_t* status) {
+cudaError_t launch_d(const Geometry& g, cudaStream_t st, const void* qv, const void* pkv, const void* pvv,
+                     const int32_t* idx, const int32_t* slen, float* po, float* pl, void* out, float* lse,
+                     int32_t* status) {
     const dim3 grid((unsigned)(((long)g.R * g.BW * g.Hkv + 7) / 8)), block(256);
+    if (g.in_f32) {
+        // fp32 storage: the direct walk (step <= kNsDirectMax, checked on the host) and the merge
+        if (g.ns_to_piece || g.ns_pieces > 0) return cudaErrorInvalidValue;
+        const float* q = static_cast<const float*>(qv);
+        const float* pk = static_cast<const float*>(pkv);
+        const float* pv = static_cast<const float*>(pvv);
+        switch (g.G) {
+#define XATTN_G32(GV)                                                                                             \
+    case GV:                                                                                                     \
+        ns_merge_kernel<D, GV, float><<<grid, block, 0, st>>>(g, q, pk, pv, idx, slen, po, pl, out, lse, status); \
+        break;
+            XATTN_G32(1) XATTN_G32(2) XATTN_G32(4) XATTN_G32(8) XATTN_G32(16)
+#undef XATTN_G32
+            default: return cudaErrorInvalidValue;
+        }
+        return cudaGetLastError();
+    }
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(qv);
+    const __nv_bfloat16* pk = static_cast<const __nv_bfloat16*>(pkv);
+    const __nv_bfloat16* pv = static_cast<const __nv_bfloat16*>(pvv);
     const int npc = g.ns_to_piece ? 1 : g.ns_pieces;  // Non-Shared pieces per (r, b, h)
     const unsigned rows_ctas = (unsigned)(((long)g.R * g.BW * g.Hq + 7) / 8);
     // short Non-Shared part ahead of the fused Shared stage: one warp per (request, beam)
@@ -967,7 +996,7 @@ cudaError_t launch_d(const Geometry& g, cudaStream_t st, const __nv_bfloat16* q,
             if (e != cudaSuccess) return e;                                                                      \
             if (!g.ns_to_piece) merge_rows_kernel<D><<<rows_ctas, block, 0, st>>>(g, slen, po, pl, out, lse, status); \
         } else {                                                                                                 \
-            ns_merge_kernel<D, GV><<<grid, block, 0, st>>>(g, q, pk, pv, idx, slen, po, pl, out, lse, status); \
+            ns_merge_kernel<D, GV, __nv_bfloat16><<<grid, block, 0, st>>>(g, q, pk, pv, idx, slen, po, pl, out, lse, status); \
         }                                                                                                        \
         break;
         XATTN_G(1) XATTN_G(2) XATTN_G(4) XATTN_G(8) XATTN_G(16)
@@ -985,8 +1014,8 @@ int merge_ctas_for(const Geometry& g) {
     return (int)((warps + 7) / 8);
 }
 
-cudaError_t launch_ns_merge(const Geometry& g, const __nv_bfloat16* q, const __nv_bfloat16* pool_k,
-                            const __nv_bfloat16* pool_v, const int32_t* beam_tok_idx, const int32_t* shared_len,
+cudaError_t launch_ns_merge(const Geometry& g, const void* q, const void* pool_k,
+                            const void* pool_v, const int32_t* beam_tok_idx, const int32_t* shared_len,
                             const float* part_o, const float* part_lse, void* out, float* lse, int32_t* status,
                             cudaStream_t stream) {
     float* po = const_cast<float*>(part_o);

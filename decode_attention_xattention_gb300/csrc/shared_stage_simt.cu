@@ -27,8 +27,9 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// E consecutive elements (bf16 or fp32 storage) as floats.
 template <int E>
-__device__ __forceinline__ void load_bf16(const __nv_bfloat16* p, float (&x)[E]) {
+__device__ __forceinline__ void load_in(const __nv_bfloat16* p, float (&x)[E]) {
     if constexpr (E == 4) {
         uint2 u = *reinterpret_cast<const uint2*>(p);
         float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u.x));
@@ -39,12 +40,22 @@ __device__ __forceinline__ void load_bf16(const __nv_bfloat16* p, float (&x)[E])
         x[0] = a.x; x[1] = a.y;
     }
 }
+template <int E>
+__device__ __forceinline__ void load_in(const float* p, float (&x)[E]) {
+    if constexpr (E == 4) {
+        const float4 u = *reinterpret_cast<const float4*>(p);
+        x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+    } else {
+        const float2 u = *reinterpret_cast<const float2*>(p);
+        x[0] = u.x; x[1] = u.y;
+    }
+}
 
-template <int D>
+// T: storage type of q, shared_k and shared_v (bf16, or fp32 inputs used unrounded).
+template <int D, typename T>
 __global__ void __launch_bounds__(kWarps * 32) shared_stage_simt_kernel(
-    Geometry g, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ sk,
-    const __nv_bfloat16* __restrict__ sv, const int32_t* __restrict__ shared_len,
-    float* __restrict__ part_o, float* __restrict__ part_lse) {
+    Geometry g, const T* __restrict__ q, const T* __restrict__ sk, const T* __restrict__ sv,
+    const int32_t* __restrict__ shared_len, float* __restrict__ part_o, float* __restrict__ part_lse) {
     constexpr int E = D / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nrb = (g.M + kRB - 1) / kRB;
@@ -67,7 +78,7 @@ __global__ void __launch_bounds__(kWarps * 32) shared_stage_simt_kernel(
         const int row = rb * kRB + i;
         if (row < g.M) {
             const int b = row / g.G, gg = row - b * g.G;
-            load_bf16<E>(q + (((size_t)r * g.BW + b) * g.Hq + (size_t)h * g.G + gg) * D + lane * E, qv[i]);
+            load_in<E>(q + (((size_t)r * g.BW + b) * g.Hq + (size_t)h * g.G + gg) * D + lane * E, qv[i]);
         } else {
 #pragma unroll
             for (int e = 0; e < E; ++e) qv[i][e] = 0.f;
@@ -79,8 +90,8 @@ __global__ void __launch_bounds__(kWarps * 32) shared_stage_simt_kernel(
     }
 
     const size_t tok_stride = (size_t)g.Hkv * D;
-    const __nv_bfloat16* kbase = sk + ((size_t)r * g.Lmax * g.Hkv + h) * D + lane * E;
-    const __nv_bfloat16* vbase = sv + ((size_t)r * g.Lmax * g.Hkv + h) * D + lane * E;
+    const T* kbase = sk + ((size_t)r * g.Lmax * g.Hkv + h) * D + lane * E;
+    const T* vbase = sv + ((size_t)r * g.Lmax * g.Hkv + h) * D + lane * E;
     // Warp w takes groups of kUnroll consecutive tokens (w*kUnroll, w*kUnroll + 16, ...);
     // the group's K and V rows are loaded before any is used.
     for (int j0 = t0 + warp * kUnroll; j0 < t1; j0 += kWarps * kUnroll) {
@@ -88,8 +99,8 @@ __global__ void __launch_bounds__(kWarps * 32) shared_stage_simt_kernel(
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             if (j0 + u < t1) {
-                load_bf16<E>(kbase + (size_t)(j0 + u) * tok_stride, kv[u]);
-                load_bf16<E>(vbase + (size_t)(j0 + u) * tok_stride, vv[u]);
+                load_in<E>(kbase + (size_t)(j0 + u) * tok_stride, kv[u]);
+                load_in<E>(vbase + (size_t)(j0 + u) * tok_stride, vv[u]);
             }
         }
 #pragma unroll
@@ -152,20 +163,24 @@ __global__ void __launch_bounds__(kWarps * 32) shared_stage_simt_kernel(
 
 }  // namespace
 
-cudaError_t launch_shared_stage_simt(const Geometry& g, const __nv_bfloat16* q,
-                                     const __nv_bfloat16* shared_k, const __nv_bfloat16* shared_v,
-                                     const int32_t* shared_len, float* part_o, float* part_lse,
-                                     int32_t* status, cudaStream_t stream) {
+cudaError_t launch_shared_stage_simt(const Geometry& g, const void* q, const void* shared_k, const void* shared_v,
+                                     const int32_t* shared_len, float* part_o, float* part_lse, int32_t* status,
+                                     cudaStream_t stream) {
     (void)status;
     const long nrb = (g.M + kRB - 1) / kRB;
     const long ctas = (long)g.R * g.Hkv * nrb * g.nsplit;
     if (ctas > 0x7fffffffL) return cudaErrorInvalidValue;
-    if (g.d == 128)
-        shared_stage_simt_kernel<128><<<(unsigned)ctas, kWarps * 32, 0, stream>>>(g, q, shared_k, shared_v, shared_len, part_o, part_lse);
-    else if (g.d == 64)
-        shared_stage_simt_kernel<64><<<(unsigned)ctas, kWarps * 32, 0, stream>>>(g, q, shared_k, shared_v, shared_len, part_o, part_lse);
-    else
-        return cudaErrorInvalidValue;
+    auto go = [&](auto kernel, auto tag) {
+        using T = decltype(tag);
+        kernel<<<(unsigned)ctas, kWarps * 32, 0, stream>>>(g, static_cast<const T*>(q), static_cast<const T*>(shared_k),
+                                                           static_cast<const T*>(shared_v), shared_len, part_o,
+                                                           part_lse);
+    };
+    if (g.d == 128 && g.in_f32) go(shared_stage_simt_kernel<128, float>, float{});
+    else if (g.d == 128) go(shared_stage_simt_kernel<128, __nv_bfloat16>, __nv_bfloat16{});
+    else if (g.d == 64 && g.in_f32) go(shared_stage_simt_kernel<64, float>, float{});
+    else if (g.d == 64) go(shared_stage_simt_kernel<64, __nv_bfloat16>, __nv_bfloat16{});
+    else return cudaErrorInvalidValue;
     return cudaGetLastError();
 }
 

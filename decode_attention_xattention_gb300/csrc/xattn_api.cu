@@ -48,7 +48,11 @@ int check_desc(const xattn_desc* d) {
     if (!(d->softmax_scale >= 0.f) || !std::isfinite(d->softmax_scale)) return XATTN_ERR_INVALID_ARG;
     if (d->split_tokens < 0 || d->split_tokens % kPieceGrain != 0) return XATTN_ERR_INVALID_ARG;
     if (d->shared_kernel < 0 || d->shared_kernel > 2) return XATTN_ERR_INVALID_ARG;
-    if (d->dtype != XATTN_DTYPE_BF16) return XATTN_ERR_UNSUPPORTED;
+    if (d->dtype != XATTN_DTYPE_BF16 && d->dtype != XATTN_DTYPE_F32) return XATTN_ERR_UNSUPPORTED;
+    // fp32 inputs run on the CUDA-core kernels: the CUDA-core Shared stage and the direct
+    // walk of at most kNsDirectMax Non-Shared tokens
+    if (d->dtype == XATTN_DTYPE_F32 && (d->shared_kernel == 1 || d->max_steps > kNsDirectMax))
+        return XATTN_ERR_UNSUPPORTED;
     if (d->out_dtype != XATTN_DTYPE_BF16 && d->out_dtype != XATTN_DTYPE_F32) return XATTN_ERR_UNSUPPORTED;
     if (d->head_dim != 64 && d->head_dim != 128) return XATTN_ERR_UNSUPPORTED;
     const int G = d->num_q_heads / d->num_kv_heads;
@@ -82,13 +86,14 @@ void plan(const xattn_desc* d, int step, Geometry* g, int* kernel) {
     const float scale = d->softmax_scale > 0.f ? d->softmax_scale : 1.0f / std::sqrt((float)g->d);
     g->scale_log2 = scale * 1.4426950408889634f;
     g->out_f32 = d->out_dtype == XATTN_DTYPE_F32 ? 1 : 0;
+    g->in_f32 = d->dtype == XATTN_DTYPE_F32 ? 1 : 0;
 
     // Tensor cores by default, even for few stacked rows: a 128-row tile that is mostly
     // padding still streams the prefix at HBM speed (the MMA and exp work hide under the
     // loads), which the CUDA-core kernel does not reach. The CUDA-core kernel stays
     // selectable (shared_kernel = 2).
     int k = 0;
-    if (g->Lmax > 0) k = d->shared_kernel ? d->shared_kernel : 1;
+    if (g->Lmax > 0) k = g->in_f32 ? 2 : (d->shared_kernel ? d->shared_kernel : 1);
     *kernel = k;
     const int tiles = g->Lmax > 0 ? cdiv(g->Lmax, kPieceGrain) : 1;
     if (d->split_tokens > 0) {
@@ -253,9 +258,9 @@ int run_shared(const Geometry& g, int kernel, const void* q, const void* shared_
                const int32_t* shared_len, const WsView& ws, cudaStream_t st, bool fused = false,
                const void* ns_k_pool = nullptr, const void* ns_v_pool = nullptr,
                const int32_t* beam_tok_idx = nullptr, void* out = nullptr, float* lse = nullptr) {
-    auto qb = reinterpret_cast<const __nv_bfloat16*>(q);
     cudaError_t e = cudaSuccess;
     if (kernel == 1) {
+        auto qb = reinterpret_cast<const __nv_bfloat16*>(q);
         CUtensorMap mk, mv, mq, mn;
         if (make_kv_map(&mk, shared_k, g) != CUDA_SUCCESS || make_kv_map(&mv, shared_v, g) != CUDA_SUCCESS)
             return XATTN_ERR_CUDA;
@@ -264,9 +269,7 @@ int run_shared(const Geometry& g, int kernel, const void* q, const void* shared_
         e = launch_shared_stage_tc(g, mk, mv, mq, mn, qb, shared_len, ws.part_o, ws.part_lse, ws.status, out, lse,
                                    fused, st);
     } else if (kernel == 2) {
-        e = launch_shared_stage_simt(g, qb, reinterpret_cast<const __nv_bfloat16*>(shared_k),
-                                     reinterpret_cast<const __nv_bfloat16*>(shared_v), shared_len, ws.part_o,
-                                     ws.part_lse, ws.status, st);
+        e = launch_shared_stage_simt(g, q, shared_k, shared_v, shared_len, ws.part_o, ws.part_lse, ws.status, st);
     }
     return e == cudaSuccess ? XATTN_OK : XATTN_ERR_CUDA;
 }
@@ -274,9 +277,7 @@ int run_shared(const Geometry& g, int kernel, const void* q, const void* shared_
 int run_merge(const Geometry& g, const xattn_desc* desc, const void* q, const int32_t* shared_len,
               const void* ns_k_pool, const void* ns_v_pool, const int32_t* beam_tok_idx, void* out, float* lse,
               const WsView& ws, cudaStream_t st) {
-    cudaError_t e = launch_ns_merge(g, reinterpret_cast<const __nv_bfloat16*>(q),
-                                    reinterpret_cast<const __nv_bfloat16*>(ns_k_pool),
-                                    reinterpret_cast<const __nv_bfloat16*>(ns_v_pool), beam_tok_idx,
+    cudaError_t e = launch_ns_merge(g, q, ns_k_pool, ns_v_pool, beam_tok_idx,
                                     desc->max_shared_len > 0 ? shared_len : nullptr, ws.part_o, ws.part_lse,
                                     out, lse, ws.status, st);
     return e == cudaSuccess ? XATTN_OK : XATTN_ERR_CUDA;
@@ -362,10 +363,9 @@ int xattn_beam_update(const xattn_desc* desc, const int32_t* parent, const void*
         !aligned(beam_tok_idx, 4) || (parent && !aligned(parent, 4)) || (status && !aligned(status, 4)))
         return XATTN_ERR_MISALIGNED;
     cudaError_t e = launch_beam_update(
-        desc->num_requests, desc->beam_width, desc->num_kv_heads, desc->head_dim, desc->ns_slots, desc->max_steps,
-        step, parent, reinterpret_cast<const __nv_bfloat16*>(new_k), reinterpret_cast<const __nv_bfloat16*>(new_v),
-        reinterpret_cast<__nv_bfloat16*>(ns_k_pool), reinterpret_cast<__nv_bfloat16*>(ns_v_pool), beam_tok_idx,
-        status, reinterpret_cast<cudaStream_t>(stream));
+        desc->num_requests, desc->beam_width, desc->num_kv_heads, desc->head_dim,
+        desc->dtype == XATTN_DTYPE_F32 ? 4 : 2, desc->ns_slots, desc->max_steps, step, parent, new_k, new_v,
+        ns_k_pool, ns_v_pool, beam_tok_idx, status, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? XATTN_OK : XATTN_ERR_CUDA;
 }
 

@@ -35,6 +35,7 @@ struct Geometry {
     int ns_pieces;    // Non-Shared pieces of this call (0: the merge kernel walks the tokens)
     int pieces;       // piece stride of the workspace: nsplit + Non-Shared pieces for max_steps
     int ns_to_piece;  // ns_merge_kernel writes the Non-Shared part as piece `nsplit` (no merge)
+    int in_f32;       // q, K and V stored as fp32 (CUDA-core kernels only), else bf16
 };
 
 // Workspace layout: [status (256 B)] [part_o: R*Hkv*pieces*M*d fp32] [part_lse: R*Hkv*pieces*M fp32].
@@ -55,20 +56,20 @@ cudaError_t launch_shared_stage_tc(const Geometry& g, const CUtensorMap& tmap_k,
                                    const int32_t* shared_len, float* part_o, float* part_lse,
                                    int32_t* status, void* out, float* lse, bool fused,
                                    cudaStream_t stream);
-cudaError_t launch_shared_stage_simt(const Geometry& g, const __nv_bfloat16* q,
-                                     const __nv_bfloat16* shared_k, const __nv_bfloat16* shared_v,
+// q, shared_k, shared_v: bf16, or fp32 when g.in_f32.
+cudaError_t launch_shared_stage_simt(const Geometry& g, const void* q, const void* shared_k, const void* shared_v,
                                      const int32_t* shared_len, float* part_o, float* part_lse,
                                      int32_t* status, cudaStream_t stream);
-cudaError_t launch_ns_merge(const Geometry& g, const __nv_bfloat16* q,
-                            const __nv_bfloat16* pool_k, const __nv_bfloat16* pool_v,
+// q and the pools: bf16, or fp32 when g.in_f32 (then only the direct walk of at most
+// kNsDirectMax Non-Shared tokens, which the host checks).
+cudaError_t launch_ns_merge(const Geometry& g, const void* q, const void* pool_k, const void* pool_v,
                             const int32_t* beam_tok_idx, const int32_t* shared_len,
                             const float* part_o, const float* part_lse, void* out,
                             float* lse, int32_t* status, cudaStream_t stream);
-cudaError_t launch_beam_update(int R, int BW, int Hkv, int d, int S, int Tmax, int step,
-                               const int32_t* parent, const __nv_bfloat16* new_k,
-                               const __nv_bfloat16* new_v, __nv_bfloat16* pool_k,
-                               __nv_bfloat16* pool_v, int32_t* idx, int32_t* status,
-                               cudaStream_t stream);
+// elem_bytes: bytes per K/V element (2: bf16, 4: fp32).
+cudaError_t launch_beam_update(int R, int BW, int Hkv, int d, int elem_bytes, int S, int Tmax, int step,
+                               const int32_t* parent, const void* new_k, const void* new_v, void* pool_k,
+                               void* pool_v, int32_t* idx, int32_t* status, cudaStream_t stream);
 
 int merge_ctas_for(const Geometry& g);
 // Whether xattn_decode runs the Shared stage and the Merge in one tensor-core kernel (after

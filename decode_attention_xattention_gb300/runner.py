@@ -28,9 +28,14 @@ class DeviceBatch:
     """All device tensors of one decode batch (inputs resident in HBM)."""
 
     def __init__(self, inp: wl.Inputs, device="cuda", shared_kernel=0, split_tokens=0, stream=None,
-                 extra_steps=0, out_fp32=False):
-        inp = inp.as_bf16()
+                 extra_steps=0, out_fp32=False, input_f32=False):
+        """input_f32: hold the inputs as fp32, unrounded (XATTN_DTYPE_F32: the CUDA-core
+        kernels); otherwise they are rounded to bf16 (a no-op for bf16 workloads)."""
         w = inp.w
+        self.input_f32 = bool(input_f32)
+        if not self.input_f32:
+            inp = inp.as_bf16()
+        self.inputs = inp  # the values the device holds
         self.w = w
         self.device = device
         self.stream = stream
@@ -39,18 +44,26 @@ class DeviceBatch:
         self.S = BW * self.Tmax
         self.desc = xattn.make_desc(R, BW, Hq, Hkv, d, w.max_shared_len, self.S, self.Tmax, w.softmax_scale,
                                     shared_kernel, split_tokens,
-                                    xattn.XATTN_DTYPE_F32 if out_fp32 else xattn.XATTN_DTYPE_BF16)
-        self.q = to_bf16_tensor(inp.q, device)
+                                    xattn.XATTN_DTYPE_F32 if out_fp32 else xattn.XATTN_DTYPE_BF16,
+                                    xattn.XATTN_DTYPE_F32 if self.input_f32 else xattn.XATTN_DTYPE_BF16)
+        if self.input_f32:
+            def dev(x):
+                return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device)
+        else:
+            def dev(x):
+                return to_bf16_tensor(x, device)
+        self.q = dev(inp.q)
         if w.max_shared_len > 0:
-            self.shared_k = to_bf16_tensor(inp.shared_k, device)
-            self.shared_v = to_bf16_tensor(inp.shared_v, device)
+            self.shared_k = dev(inp.shared_k)
+            self.shared_v = dev(inp.shared_v)
         else:
             self.shared_k = self.shared_v = None
         self.shared_len = torch.from_numpy(inp.shared_len.astype(np.int32)).to(device)
-        self.new_k = to_bf16_tensor(inp.new_k, device) if w.steps > 0 else None
-        self.new_v = to_bf16_tensor(inp.new_v, device) if w.steps > 0 else None
+        self.new_k = dev(inp.new_k) if w.steps > 0 else None
+        self.new_v = dev(inp.new_v) if w.steps > 0 else None
         self.parents = torch.from_numpy(inp.parents.astype(np.int32)).to(device)
-        self.pool_k = torch.zeros((R, self.S, Hkv, d), dtype=torch.bfloat16, device=device)
+        self.pool_k = torch.zeros((R, self.S, Hkv, d), dtype=torch.float32 if self.input_f32 else torch.bfloat16,
+                                  device=device)
         self.pool_v = torch.zeros_like(self.pool_k)
         self.idx = torch.zeros((R, BW, max(self.Tmax, 1)), dtype=torch.int32, device=device)
         self.out = torch.empty((R, BW, Hq, d), dtype=torch.float32 if out_fp32 else torch.bfloat16, device=device)

@@ -113,8 +113,8 @@ def _stream(s):
 
 
 def make_desc(R, BW, Hq, Hkv, d, Lmax, S, Tmax, scale=0.0, shared_kernel=0, split_tokens=0,
-              out_dtype=XATTN_DTYPE_BF16) -> xattn_desc:
-    return xattn_desc(R, BW, Hq, Hkv, d, Lmax, S, Tmax, float(scale), XATTN_DTYPE_BF16,
+              out_dtype=XATTN_DTYPE_BF16, dtype=XATTN_DTYPE_BF16) -> xattn_desc:
+    return xattn_desc(R, BW, Hq, Hkv, d, Lmax, S, Tmax, float(scale), dtype,
                       shared_kernel, split_tokens, out_dtype)
 
 

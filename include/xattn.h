@@ -88,7 +88,10 @@ typedef struct xattn_desc {
     int32_t ns_slots;       /* S: pool slots per request (>= BW * max_steps)               */
     int32_t max_steps;      /* Tmax: row length of beam_tok_idx                            */
     float softmax_scale;    /* 0 selects 1/sqrt(d)                                         */
-    int32_t dtype;          /* XATTN_DTYPE_BF16 (q, k, v, out)                             */
+    int32_t dtype;          /* storage of q, K, V, the pools and new tokens: XATTN_DTYPE_BF16,
+                               or XATTN_DTYPE_F32 (used unrounded, on the CUDA-core kernels:
+                               shared_kernel must be 0 or 2 and max_steps <= 32, else
+                               XATTN_ERR_UNSUPPORTED)                                      */
     int32_t shared_kernel;  /* Shared-stage kernel: 0 automatic (tensor cores), 1 tensor
                                cores, 2 CUDA cores                                         */
     int32_t split_tokens;   /* prefix tokens per Shared-stage piece: 0 automatic, else a
@@ -104,10 +107,10 @@ XATTN_API size_t xattn_decode_workspace_size(const xattn_desc* desc);
 
 /* One decode step of attention: Shared stage (prefix, tensor cores, split along the
  * prefix), Non-Shared stage (ancestry-indexed gathers) and the log-sum-exp Merge.
- *   q             [R, BW, Hq, d]        bf16
- *   shared_k/v    [R, Lmax, Hkv, d]     bf16   prefix KV, stored once per request
+ *   q             [R, BW, Hq, d]        bf16 (fp32 when desc->dtype is XATTN_DTYPE_F32)
+ *   shared_k/v    [R, Lmax, Hkv, d]     bf16 (or fp32)  prefix KV, stored once per request
  *   shared_len    [R]                   int32  valid prefix tokens per request (<= Lmax)
- *   ns_k/v_pool   [R, S, Hkv, d]        bf16   Non-Shared tokens, one slot per token
+ *   ns_k/v_pool   [R, S, Hkv, d]        bf16 (or fp32)  Non-Shared tokens, one slot per token
  *   beam_tok_idx  [R, BW, Tmax]         int32  ancestry: slots of the beam's tokens
  *   step          0 <= step <= Tmax: positions 0 .. step-1 of each ancestry row are used
  *   out           [R, BW, Hq, d]        bf16 (or fp32, desc->out_dtype)  normalised output
@@ -146,7 +149,7 @@ XATTN_API int xattn_decode_merge(const xattn_desc* desc, const void* q, const in
 
 /* Bookkeeping of one beam-search step, in place (section 2.1, token-granularity
  * management and in-place updates). For every request r and beam b:
- *   the new token's K/V, new_k/new_v[r, b] ([R, BW, Hkv, d] bf16), is written to pool
+ *   the new token's K/V, new_k/new_v[r, b] ([R, BW, Hkv, d], desc->dtype), is written to pool
  *   slot step*BW + b (no other slot changes: nothing is copied when beams fork);
  *   beam_tok_idx[r, b, 0:step] becomes the old beam_tok_idx[r, parent[r, b], 0:step]
  *   and beam_tok_idx[r, b, step] becomes step*BW + b.

@@ -110,6 +110,25 @@ def test_split_plan_covers_prefix(lib):
             assert p.shared_kernel == 1
 
 
+def test_fp32_inputs_plan_and_limits(lib):
+    """fp32 storage runs on the CUDA-core kernels: the planner picks the CUDA-core Shared
+    stage and the unfused path; the tensor-core kernel and Non-Shared parts longer than the
+    direct walk (32 tokens) are rejected before any launch, as is an unknown dtype."""
+    f32 = xattn.XATTN_DTYPE_F32
+    d = xattn.make_desc(1, 4, 2, 1, 64, 256, 12, 3, 0.0, 0, 0, f32, f32)
+    rc, p = xattn.xattn_query_plan(d, 3)
+    assert rc == 0 and p.shared_kernel == 2 and p.fused == 0
+    assert xattn.xattn_decode_workspace_size(d) > 0
+    for bad in (xattn.make_desc(1, 4, 2, 1, 64, 256, 12, 3, 0.0, 1, 0, f32, f32),
+                xattn.make_desc(1, 4, 2, 1, 64, 256, 4 * 33, 33, 0.0, 0, 0, f32, f32),
+                xattn.make_desc(1, 4, 2, 1, 64, 256, 12, 3, 0.0, 0, 0, f32, 7)):
+        assert xattn.xattn_decode_workspace_size(bad) == 0
+        rc, _ = xattn.xattn_query_plan(bad, 3)
+        assert rc == xattn.XATTN_ERR_UNSUPPORTED
+        assert xattn.xattn_beam_update(bad, None, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0) == \
+            xattn.XATTN_ERR_UNSUPPORTED
+
+
 def test_kernel_choice(lib):
     # tensor cores by default, also for plain per-sequence decode (4 stacked rows)
     d = xattn.make_desc(64, 1, 32, 8, 128, 8192, 512, 512)

@@ -150,6 +150,44 @@ def test_tiny_config_both_kernels():
         stats, _, _ = run_and_check(wl.TINY, shared_kernel=k)
 
 
+# fp32 inputs kept unrounded (CUDA-core kernels, fp32 arithmetic): against the fp64 oracle
+# on the same unrounded values the error is that of fp32 accumulation and the approximate
+# exp2, far below the bf16 bounds.
+TOL_F32 = (2e-5, 2e-6, 2e-5)
+
+
+@pytest.mark.parametrize("kernel", [0, 2])
+def test_tiny_config_native_fp32(kernel):
+    """The Tiny configuration as specified: fp32 Q/K/V used unrounded (no bf16 step)."""
+    stats, db, _ = run_and_check(wl.TINY, shared_kernel=kernel, input_f32=True, tol=TOL_F32)
+    assert db.input_f32 and db.plan().shared_kernel == 2 and db.pool_k.dtype == torch.float32
+
+
+@pytest.mark.parametrize("shape", [(2, 6, 8, 2, 128, (300, 129), 5), (1, 3, 16, 1, 64, (0,), 32),
+                                   (2, 4, 4, 4, 128, (513, 7), 0)],
+                         ids=["G4_d128_split", "G16_d64_ns_only_32tok", "G1_d128_shared_only"])
+def test_fp32_inputs_shapes(shape):
+    """fp32 storage through every part the fp32 path has: split prefixes, a Non-Shared-only
+    request (empty prefix), 32 ancestry tokens (the most the direct walk takes), step 0."""
+    R, BW, Hq, Hkv, d, lens, T = shape
+    w = wl.custom(R=R, BW=BW, Hq=Hq, Hkv=Hkv, d=d, lens=lens, T=max(T, 1), seed=80 + T, input_dtype="fp32",
+                  lmax=256 if max(lens) == 0 else 0)
+    run_and_check(w, input_f32=True, tol=TOL_F32, split_tokens=128, step=T)
+
+
+def test_fp32_bf16_out():
+    """fp32 inputs with bf16 output: the fp32 result rounded once at the store."""
+    w = wl.custom(R=1, BW=4, Hq=8, Hkv=2, d=128, lens=(200,), T=3, seed=9, input_dtype="fp32")
+    outs = []
+    for fp32_out in (True, False):
+        db = DeviceBatch(wl.make_inputs(w), out_fp32=fp32_out, input_f32=True)
+        db.build_cache()
+        xattn.check(db.decode())
+        torch.cuda.synchronize()
+        outs.append(db.out.clone())
+    assert torch.equal(outs[0].to(torch.bfloat16), outs[1])
+
+
 def test_shared_only_and_ns_only():
     w = wl.custom(R=2, BW=6, Hq=8, Hkv=2, d=128, lens=(777, 300), T=3, seed=5)
     run_and_check(w, step=0)  # Shared stage alone
