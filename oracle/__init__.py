@@ -33,6 +33,8 @@ MUTANTS = {
     7: "new token recorded under the parent's slot",
     8: "ancestry not inherited from the parent",
     9: "merge weights not normalised",
+    10: "beam selection: equal scores ordered by the larger index",
+    11: "beam selection: the beam's own score not added",
 }
 
 
@@ -82,8 +84,9 @@ class Oracle:
         self.lib.oracle_decode_rows.argtypes = [ctypes.POINTER(_Dims)] + [vp] * 7 + [i32, vp, i64, vp, vp, i32]
         self.lib.oracle_merge.argtypes = [i32, i64, i32, vp, vp, vp, vp]
         self.lib.oracle_beam_update.argtypes = [ctypes.POINTER(_Dims), vp, vp, vp, vp, vp, vp, i32]
+        self.lib.oracle_beam_select.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         for f in ("oracle_partial_rows", "oracle_decode_rows", "oracle_merge", "oracle_beam_update",
-                  "oracle_mutant_id", "oracle_max_threads"):
+                  "oracle_beam_select", "oracle_mutant_id", "oracle_max_threads"):
             getattr(self.lib, f).restype = ctypes.c_int
 
     @staticmethod
@@ -150,6 +153,25 @@ class Oracle:
                                          _p(pool_k), _p(pool_v), _p(idx), step)
         if rc != 0:
             raise ValueError("oracle_beam_update rejected its arguments")
+
+
+    # -- beam selection -------------------------------------------------------------
+    def beam_select(self, beam_score, cand_logp, cand_token, out_width):
+        """beam_score [R, BW], cand_logp / cand_token [R, BW, K] -> (parent, token, score),
+        each [R, out_width], best first (full sort; ties to the smaller flat index)."""
+        cand_logp = _f32(cand_logp)
+        R, BW, K = cand_logp.shape
+        beam_score, cand_token = _f32(beam_score), _i32(cand_token)
+        if beam_score.shape != (R, BW) or cand_token.shape != (R, BW, K):
+            raise ValueError("beam_select: shapes do not match")
+        parent = np.zeros((R, out_width), np.int32)
+        token = np.zeros((R, out_width), np.int32)
+        score = np.zeros((R, out_width), np.float32)
+        rc = self.lib.oracle_beam_select(R, BW, K, out_width, _p(beam_score), _p(cand_logp), _p(cand_token),
+                                         _p(parent), _p(token), _p(score))
+        if rc != 0:
+            raise ValueError("oracle_beam_select rejected its arguments")
+        return parent, token, score
 
 
 def load(mutant: int = 0) -> Oracle:

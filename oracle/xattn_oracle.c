@@ -273,6 +273,68 @@ int oracle_beam_update(const oracle_dims* D, const int32_t* parent, const float*
     return 0;
 }
 
+/* Beam selection of one beam-search step (xGR: Efficient Generative Recommendation Serving at
+ * Scale, section 2.2, xBeam "early sort termination": the Top-K sequences are chosen from the
+ * pool of every beam's candidates; the pages prune that choice with a global min-heap because
+ * the log-probabilities within a beam are already in order). The pruning only saves work;
+ * the chosen set has a plain definition, which is what this function writes out:
+ *   candidate (b, k) of request r, b < BW, k < K, scores
+ *     s = beam_score[r, b] + cand_logp[r, b, k]        (one float32 addition)
+ *   and the W candidates with the largest s are chosen, best first, equal scores ordered by
+ *   the smaller flat index b*K + k (reading: the pages fix no tie rule).
+ * Full sort of all BW*K candidates (qsort). Outputs [R, W]: parent = b, token =
+ * cand_token[r, b, k], score = s. Returns 0, or -1 on bad sizes or a NaN score. */
+typedef struct {
+    float s;
+    int32_t flat;
+} sel_cand;
+
+static int sel_cmp(const void* pa, const void* pb) {
+    const sel_cand* a = (const sel_cand*)pa;
+    const sel_cand* b = (const sel_cand*)pb;
+    if (a->s != b->s) return a->s > b->s ? -1 : 1;
+#if ORACLE_MUTANT == 10
+    return a->flat > b->flat ? -1 : (a->flat < b->flat); /* planted: ties to the larger index */
+#else
+    return a->flat < b->flat ? -1 : (a->flat > b->flat);
+#endif
+}
+
+int oracle_beam_select(int32_t R, int32_t BW, int32_t K, int32_t W, const float* beam_score,
+                       const float* cand_logp, const int32_t* cand_token, int32_t* parent,
+                       int32_t* token, float* score) {
+    if (R < 1 || BW < 1 || K < 1 || W < 1 || (int64_t)BW * K > (1 << 30) || W > BW * K) return -1;
+    const int n = BW * K;
+    sel_cand* c = (sel_cand*)malloc(sizeof(sel_cand) * (size_t)n);
+    if (!c) return -1;
+    for (int r = 0; r < R; ++r) {
+        for (int b = 0; b < BW; ++b)
+            for (int k = 0; k < K; ++k) {
+                const float lp = cand_logp[((size_t)r * BW + b) * K + k];
+#if ORACLE_MUTANT == 11
+                const float s = lp; /* planted: the beam's own score not added */
+#else
+                const float s = beam_score[(size_t)r * BW + b] + lp;
+#endif
+                if (s != s) {
+                    free(c);
+                    return -1;
+                }
+                c[b * K + k].s = s;
+                c[b * K + k].flat = b * K + k;
+            }
+        qsort(c, (size_t)n, sizeof(sel_cand), sel_cmp);
+        for (int j = 0; j < W; ++j) {
+            const int b = c[j].flat / K, k = c[j].flat % K;
+            parent[(size_t)r * W + j] = b;
+            token[(size_t)r * W + j] = cand_token[((size_t)r * BW + b) * K + k];
+            score[(size_t)r * W + j] = c[j].s;
+        }
+    }
+    free(c);
+    return 0;
+}
+
 int oracle_mutant_id(void) { return ORACLE_MUTANT; }
 
 int oracle_max_threads(void) {

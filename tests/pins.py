@@ -317,10 +317,89 @@ def check_ancestry_table_structure(orc):
         assert np.all(idx[:, :, i] // w.beam_width == i)
 
 
+# -- beam selection (xBeam) ----------------------------------------------------------------
+def check_golden_beam_select(orc):
+    g = json.load(open(os.path.join(GOLDEN, "beam_select_hand.json")))
+    par, tok, sc = orc.beam_select(_arr(g["beam_score"]), _arr(g["cand_logp"]), _arr(g["cand_token"], np.int32),
+                                   g["out_width"])
+    np.testing.assert_array_equal(par, np.asarray(g["expect_parent"], np.int32))
+    np.testing.assert_array_equal(tok, np.asarray(g["expect_token"], np.int32))
+    np.testing.assert_array_equal(sc, np.asarray(g["expect_score"], np.float32))
+
+
+def _select_case(rng, R, BW, K, levels):
+    """Per-beam lists in non-increasing order drawn from a few multiples of 1/8 (many
+    equal scores, every float32 sum exact), beam scores likewise, distinct tokens."""
+    lp = -np.sort(rng.integers(0, levels, size=(R, BW, K)), axis=2).astype(np.float32) / 8
+    bs = -rng.integers(0, levels, size=(R, BW)).astype(np.float32) / 8
+    tok = rng.permutation(R * BW * K).astype(np.int32).reshape(R, BW, K)
+    return bs, lp, tok
+
+
+def _select_by_repeated_max(bs, lp, tok, W):
+    """Independent restatement: W times, take the best remaining candidate (largest
+    score, then smallest flat index) by a plain scan."""
+    R, BW, K = lp.shape
+    par = np.zeros((R, W), np.int32)
+    tk = np.zeros((R, W), np.int32)
+    sc = np.zeros((R, W), np.float32)
+    for r in range(R):
+        taken = set()
+        for j in range(W):
+            best = None
+            for b in range(BW):
+                for k in range(K):
+                    if (b, k) in taken:
+                        continue
+                    s = np.float32(bs[r, b]) + np.float32(lp[r, b, k])
+                    if best is None or s > best[0] or (s == best[0] and b * K + k < best[1] * K + best[2]):
+                        best = (s, b, k)
+            taken.add((best[1], best[2]))
+            par[r, j], tk[r, j], sc[r, j] = best[1], tok[r, best[1], best[2]], best[0]
+    return par, tk, sc
+
+
+def check_beam_select_brute_force(orc):
+    rng = np.random.default_rng(11)
+    for R, BW, K, W, levels in ((1, 3, 4, 5, 4), (2, 4, 3, 12, 3), (1, 5, 6, 7, 20), (2, 2, 5, 1, 2)):
+        bs, lp, tok = _select_case(rng, R, BW, K, levels)
+        got = orc.beam_select(bs, lp, tok, W)
+        want = _select_by_repeated_max(bs, lp, tok, W)
+        for a, b in zip(got, want):
+            np.testing.assert_array_equal(a, b)
+
+
+def check_beam_select_shift_invariance(orc):
+    """Adding one constant to every beam score (exactly, multiples of 1/8) shifts every
+    chosen score by it and changes no choice."""
+    rng = np.random.default_rng(12)
+    bs, lp, tok = _select_case(rng, 2, 6, 5, 6)
+    p0, t0, s0 = orc.beam_select(bs, lp, tok, 9)
+    p1, t1, s1 = orc.beam_select(bs + np.float32(8.0), lp, tok, 9)
+    np.testing.assert_array_equal(p0, p1)
+    np.testing.assert_array_equal(t0, t1)
+    np.testing.assert_array_equal(s1, s0 + np.float32(8.0))
+
+
+def check_beam_select_prefix_structure(orc):
+    """What early termination rests on: with every beam's list in order, the chosen
+    candidates of each beam are a prefix of its list, and the scores come out in order."""
+    rng = np.random.default_rng(13)
+    bs, lp, tok = _select_case(rng, 3, 8, 6, 12)
+    par, tk, sc = orc.beam_select(bs, lp, tok, 10)
+    assert np.all(np.diff(sc, axis=1) <= 0)
+    for r in range(3):
+        for b in range(8):
+            toks = [int(t) for t, p in zip(tk[r], par[r]) if p == b]
+            assert toks == [int(t) for t in tok[r, b, :len(toks)]], (r, b)
+
+
 ALL_CHECKS = [
     check_golden_decode, check_golden_beam_update, check_closed_form_single_key,
     check_closed_form_equal_keys, check_closed_form_constant_v, check_closed_form_dominant_logit,
     check_against_torch_sdpa, check_plain_decode_special_case, check_split_merge_equals_unsplit,
     check_prefix_permutation_invariance, check_prefix_token_moved_to_pool,
     check_equal_ancestry_equal_output, check_ancestry_table_structure,
+    check_golden_beam_select, check_beam_select_brute_force, check_beam_select_shift_invariance,
+    check_beam_select_prefix_structure,
 ]
