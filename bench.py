@@ -308,6 +308,50 @@ def config_of(w, extra=None):
 
 
 # ----------------------------------------------------------------------------------------
+def time_beam_select(device, stream, with_oracle: bool) -> dict:
+    """The beam selection (xGR section 2.2, xBeam) timed alone through the C ABI on the
+    pages' two candidate-pool sizes (128 x 128 and 512 x 512 per request), CUDA events over
+    200 calls on the launching stream; inputs (0.5 / 4 MB) stay in L2. With `with_oracle`,
+    the oracle's full sort of the same call is timed on the host beside it."""
+    import torch
+
+    import oracle
+    from decode_attention_xattention_gb300 import workloads as wl, xattn
+
+    out = {"note": "not part of the decode step; per-beam sorted synthetic candidate lists, L2-resident"}
+    for name, (R, BW, K, Wd) in (("pool_128x128", (8, 128, 128, 128)), ("pool_512x512", (4, 512, 512, 512))):
+        bs, lp, tok = wl.make_candidates(R, BW, K, seed=7)
+        d_bs, d_lp, d_tok = (torch.from_numpy(a).to(device) for a in (bs, lp, tok))
+        par = torch.empty((R, Wd), dtype=torch.int32, device=device)
+        tk = torch.empty_like(par)
+        sc = torch.empty((R, Wd), dtype=torch.float32, device=device)
+
+        def call():
+            xattn.check(xattn.xattn_beam_select(R, BW, K, Wd, d_bs, d_lp, d_tok, par, tk, sc, stream))
+
+        n = 200
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                call()
+            e0.record(stream)
+            for _ in range(n):
+                call()
+            e1.record(stream)
+        e1.synchronize()
+        us = e0.elapsed_time(e1) / n * 1e3
+        entry = {"requests": R, "beam_width": BW, "cand_per_beam": K, "out_width": Wd, "us_per_call": us,
+                 "beams_selected_per_s": R * Wd / (us * 1e-6), "gpu_launches_per_call": 1}
+        if with_oracle:
+            orc = oracle.load()
+            t0 = time.perf_counter()
+            orc.beam_select(bs, lp, tok, Wd)
+            entry["oracle_us_per_call"] = (time.perf_counter() - t0) * 1e6
+            entry["oracle_cores"] = 1
+        out[name] = entry
+    return out
+
+
 def main():
     args = parse_args()
     from decode_attention_xattention_gb300 import workloads as wl
@@ -524,6 +568,7 @@ def main():
         "gpu_launches": launches_per_step(plan, T) * K,
         "clocks": clocks,
     }
+    line["beam_select"] = time_beam_select(f"cuda:{local}", stream, rank == 0 and not args.no_cpu_baseline)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample = cpu_oracle_sample(w, inputs[0], args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "beams/s", "cores": cores, "kind": "oracle", "sample": sample}

@@ -369,6 +369,22 @@ int xattn_beam_update(const xattn_desc* desc, const int32_t* parent, const void*
     return e == cudaSuccess ? XATTN_OK : XATTN_ERR_CUDA;
 }
 
+int xattn_beam_select(int32_t num_requests, int32_t beam_width, int32_t cand_per_beam, int32_t out_width,
+                      const float* beam_score, const float* cand_logp, const int32_t* cand_token, int32_t* parent,
+                      int32_t* token, float* score, xattn_stream_t stream) {
+    if (num_requests < 1 || beam_width < 1 || cand_per_beam < 1 || out_width < 1) return XATTN_ERR_INVALID_ARG;
+    if ((int64_t)beam_width * cand_per_beam > (1ll << 30)) return XATTN_ERR_UNSUPPORTED;
+    if (out_width > (int64_t)beam_width * cand_per_beam) return XATTN_ERR_INVALID_ARG;
+    if (beam_width > 1024 || out_width > 1024) return XATTN_ERR_UNSUPPORTED;
+    if (!beam_score || !cand_logp || !cand_token || !parent || !token || !score) return XATTN_ERR_INVALID_ARG;
+    if (!aligned(beam_score, 4) || !aligned(cand_logp, 4) || !aligned(cand_token, 4) || !aligned(parent, 4) ||
+        !aligned(token, 4) || !aligned(score, 4))
+        return XATTN_ERR_MISALIGNED;
+    cudaError_t e = launch_beam_select(num_requests, beam_width, cand_per_beam, out_width, beam_score, cand_logp,
+                                       cand_token, parent, token, score, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? XATTN_OK : XATTN_ERR_CUDA;
+}
+
 int xattn_read_status(void* workspace, int32_t* status_out, int32_t clear, xattn_stream_t stream) {
     if (!workspace || !status_out) return XATTN_ERR_INVALID_ARG;
     if (!aligned(workspace, 4)) return XATTN_ERR_MISALIGNED;

@@ -219,3 +219,31 @@ def sample_rows(w: Workload, n: int, seed: int = 1) -> np.ndarray:
         if int(e) not in forced:
             rows.append(int(e))
     return np.asarray(sorted(rows), dtype=np.int64)
+
+
+# --------------------------------------------------------------------------------------
+# Beam-selection inputs (xGR section 2.2, xBeam): every beam's candidate list as a per-beam
+# top-K returns it, best first.
+
+def make_candidates(R: int, BW: int, K: int, seed: int = 0, vocab: int = 0, tie_levels: int = 0,
+                    masked_frac: float = 0.0):
+    """Seeded (beam_score [R, BW], cand_logp [R, BW, K], cand_token [R, BW, K]).
+
+    cand_logp[r, b] is non-increasing: minus a running sum of positive exponential steps
+    (or, with tie_levels > 0, sorted multiples of 1/8 from that many levels, which gives many
+    equal scores and exact float32 sums); beam_score holds the beams' running scores (minus
+    exponential, or multiples of 1/8). masked_frac of each list's tail is set to -inf (masked
+    candidates, still in order). Tokens are drawn from a vocabulary of `vocab` (default 4K)."""
+    rng = np.random.default_rng(seed)
+    if tie_levels > 0:
+        lp = -np.sort(rng.integers(0, tie_levels, size=(R, BW, K)), axis=2).astype(np.float32) / 8
+        bs = -rng.integers(0, tie_levels, size=(R, BW)).astype(np.float32) / 8
+    else:
+        steps = rng.exponential(0.5, size=(R, BW, K)).astype(np.float32)
+        lp = -np.cumsum(steps, axis=2, dtype=np.float32)
+        bs = -rng.exponential(3.0, size=(R, BW)).astype(np.float32)
+    if masked_frac > 0:
+        keep = max(1, int(round(K * (1 - masked_frac))))
+        lp[:, :, keep:] = -np.inf
+    tok = rng.integers(0, vocab if vocab > 0 else 4 * K, size=(R, BW, K)).astype(np.int32)
+    return np.ascontiguousarray(bs), np.ascontiguousarray(lp), np.ascontiguousarray(tok)

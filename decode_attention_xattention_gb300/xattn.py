@@ -34,7 +34,7 @@ XATTN_DTYPE_F32 = 1
 # Every symbol include/xattn.h declares.
 EXPORTS = ("xattn_decode_workspace_size", "xattn_decode", "xattn_decode_shared", "xattn_decode_merge",
            "xattn_beam_update", "xattn_read_status", "xattn_query_plan", "xattn_status_string",
-           "xattn_decode_noalloc")
+           "xattn_decode_noalloc", "xattn_beam_select")
 
 XATTN_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -86,6 +86,8 @@ def load(path: str = LIB_PATH):
     lib.xattn_decode_noalloc.restype = ctypes.c_int
     lib.xattn_beam_update.argtypes = [pdesc, vp, vp, vp, vp, vp, vp, i32, vp, vp]
     lib.xattn_beam_update.restype = ctypes.c_int
+    lib.xattn_beam_select.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
+    lib.xattn_beam_select.restype = ctypes.c_int
     lib.xattn_read_status.argtypes = [vp, ctypes.POINTER(i32), i32, vp]
     lib.xattn_read_status.restype = ctypes.c_int
     lib.xattn_query_plan.argtypes = [pdesc, i32, ctypes.POINTER(xattn_plan)]
@@ -156,6 +158,13 @@ def xattn_beam_update(desc, parent, new_k, new_v, ns_k_pool, ns_v_pool, beam_tok
     return int(load().xattn_beam_update(ctypes.byref(desc), _ptr(parent), _ptr(new_k), _ptr(new_v),
                                         _ptr(ns_k_pool), _ptr(ns_v_pool), _ptr(beam_tok_idx), int(step),
                                         _ptr(status), _stream(stream)))
+
+
+def xattn_beam_select(num_requests, beam_width, cand_per_beam, out_width, beam_score, cand_logp, cand_token,
+                      parent, token, score, stream=None) -> int:
+    return int(load().xattn_beam_select(int(num_requests), int(beam_width), int(cand_per_beam), int(out_width),
+                                        _ptr(beam_score), _ptr(cand_logp), _ptr(cand_token), _ptr(parent),
+                                        _ptr(token), _ptr(score), _stream(stream)))
 
 
 def xattn_read_status(workspace, clear: bool = True, stream=None) -> tuple[int, int]:

@@ -161,6 +161,26 @@ XATTN_API int xattn_beam_update(const xattn_desc* desc, const int32_t* parent, c
                       int32_t* beam_tok_idx, int32_t step, int32_t* status,
                       xattn_stream_t stream);
 
+/* Beam selection of one beam-search step (section 2.2, xBeam: early sort termination). For
+ * each request r, candidate (b, k) with b < BW = beam_width and k < K = cand_per_beam scores
+ *   beam_score[r, b] + cand_logp[r, b, k]          (one fp32 addition)
+ * and the W = out_width candidates with the largest scores are selected, equal scores
+ * ordered by the smaller flat index b*K + k, and written best first:
+ *   parent[r, j] = b,   token[r, j] = cand_token[r, b, k],   score[r, j] = its score.
+ * Each list cand_logp[r, b, 0:K] must be in non-increasing order (as a per-beam top-K
+ * returns it); -inf is allowed (masked candidates), NaN is not. The walk down a beam's list
+ * stops at the first candidate that cannot enter the best W found so far, so the work
+ * follows the lists' order, not BW*K. One CTA per request.
+ *   beam_score [R, BW] fp32, cand_logp [R, BW, K] fp32, cand_token [R, BW, K] int32: device
+ *   parent, token [R, W] int32, score [R, W] fp32: device, written
+ * Returns INVALID_ARG for a size < 1, W > BW*K or a NULL pointer; UNSUPPORTED for
+ * BW > 1024, W > 1024 or BW*K > 2^30; MISALIGNED for a pointer not 4-byte aligned. Lists
+ * out of order give an unspecified selection (not detected). */
+XATTN_API int xattn_beam_select(int32_t num_requests, int32_t beam_width, int32_t cand_per_beam,
+                                int32_t out_width, const float* beam_score, const float* cand_logp,
+                                const int32_t* cand_token, int32_t* parent, int32_t* token, float* score,
+                                xattn_stream_t stream);
+
 /* Allocation-free decode. The paper has no counterpart to this call; it exists for callers
  * that cannot allocate device memory or hand the library a workspace (a runtime that owns
  * every allocation, a latency-critical thread that must not trigger cudaMalloc, a fixed

@@ -141,3 +141,17 @@ def test_kernel_choice(lib):
     d = xattn.make_desc(8, 128, 32, 8, 128, 2048, 384, 3)
     rc, p = xattn.xattn_query_plan(d, 3)
     assert rc == 0 and p.fused == 1 and p.merge_ctas == 0 and p.num_splits == 1
+
+
+def test_beam_select_rejected_on_host(lib):
+    """Sizes, pointers and alignment of the beam selection are checked before any launch."""
+    f = xattn.xattn_beam_select
+    P = 0x1000
+    assert f(0, 4, 4, 4, P, P, P, P, P, P) == xattn.XATTN_ERR_INVALID_ARG
+    assert f(1, 4, 0, 4, P, P, P, P, P, P) == xattn.XATTN_ERR_INVALID_ARG
+    assert f(1, 4, 2, 9, P, P, P, P, P, P) == xattn.XATTN_ERR_INVALID_ARG      # W > BW*K
+    assert f(1, 1025, 4, 4, P, P, P, P, P, P) == xattn.XATTN_ERR_UNSUPPORTED   # BW > 1024
+    assert f(1, 64, 64, 1025, P, P, P, P, P, P) == xattn.XATTN_ERR_UNSUPPORTED  # W > 1024
+    assert f(1, 1024, 1 << 21, 4, P, P, P, P, P, P) == xattn.XATTN_ERR_UNSUPPORTED  # BW*K > 2^30
+    assert f(1, 4, 4, 4, P, None, P, P, P, P) == xattn.XATTN_ERR_INVALID_ARG
+    assert f(1, 4, 4, 4, P, P + 2, P, P, P, P) == xattn.XATTN_ERR_MISALIGNED
