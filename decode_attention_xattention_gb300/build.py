@@ -1,5 +1,6 @@
-"""Builds libxattn.so in-tree for sm_103a with nvcc (one object per kernel file, compiled in
-parallel, then linked with the CUDA runtime). Output: <package>/_build/libxattn.so."""
+"""Builds libxattn.so in-tree for sm_103a with nvcc (one object per kernel file and per
+host C++ file, compiled in parallel, then linked with the CUDA runtime). Output:
+<package>/_build/libxattn.so."""
 
 from __future__ import annotations
 
@@ -38,11 +39,11 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     nv = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [nv, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
         if ptxas_info:
             cmd += ["-Xptxas", "-v"]

@@ -34,7 +34,9 @@ XATTN_DTYPE_F32 = 1
 # Every symbol include/xattn.h declares.
 EXPORTS = ("xattn_decode_workspace_size", "xattn_decode", "xattn_decode_shared", "xattn_decode_merge",
            "xattn_beam_update", "xattn_read_status", "xattn_query_plan", "xattn_status_string",
-           "xattn_decode_noalloc", "xattn_beam_select")
+           "xattn_decode_noalloc", "xattn_beam_select",
+           "xattn_cht_create", "xattn_cht_destroy", "xattn_cht_insert", "xattn_cht_best", "xattn_cht_admit",
+           "xattn_cht_finish", "xattn_cht_cancel", "xattn_cht_missing", "xattn_cht_counts")
 
 XATTN_NOALLOC_SCRATCH_BYTES = 32 << 20
 
