@@ -352,6 +352,63 @@ def time_beam_select(device, stream, with_oracle: bool) -> dict:
     return out
 
 
+def time_cht(with_oracle: bool) -> dict:
+    """The chunked hash tree (Feather's prefix-aware batching structure, host code) timed on
+    the host through its binding: 4096 waiting prompts of 1280-2304 tokens in 8 prefix
+    groups (blocks of 16 tokens), then batches of 64 formed by best + admit and released by
+    finish until the queue is empty. With `with_oracle`, one brute-force `best` over 256
+    waiting and 8 active prompts of the same kind is timed beside it."""
+    import numpy as np
+
+    from decode_attention_xattention_gb300.cht import ChunkedHashTree
+
+    rng = np.random.default_rng(3)
+    B, n, groups, batch = 16, 4096, 8, 64
+    bases = [rng.integers(0, 32000, size=2048).astype(np.int32) for _ in range(groups)]
+    prompts = [np.concatenate([bases[i % groups][: int(rng.integers(1024, 2049))],
+                               rng.integers(0, 32000, size=256).astype(np.int32)]) for i in range(n)]
+    t = ChunkedHashTree(B)
+    t0 = time.perf_counter()
+    for i, p in enumerate(prompts):
+        t.insert(i, p)
+    t_insert = time.perf_counter() - t0
+    t_pick = t_finish = 0.0
+    picks = 0
+    while True:
+        chosen = []
+        t0 = time.perf_counter()
+        for _ in range(batch):
+            rc, rid, _ = t.best()
+            if rc != 1:
+                break
+            t.admit(rid)
+            chosen.append(rid)
+        t_pick += time.perf_counter() - t0
+        picks += len(chosen)
+        if not chosen:
+            break
+        t0 = time.perf_counter()
+        for rid in chosen:
+            t.finish(rid)
+        t_finish += time.perf_counter() - t0
+    out = {"note": "host code through the ctypes binding (a call costs about 1 us of Python itself)",
+           "waiting": n, "block_tokens": B, "batch": batch,
+           "insert_us_per_request": t_insert / n * 1e6, "best_admit_us_per_request": t_pick / picks * 1e6,
+           "finish_us_per_request": t_finish / picks * 1e6}
+    if with_oracle:
+        from oracle.cht import BruteForceScheduler
+
+        bf = BruteForceScheduler(B)
+        for i in range(256):
+            bf.insert(i, prompts[i].tolist())
+        for i in range(8):
+            bf.admit(i)
+        t0 = time.perf_counter()
+        bf.best()
+        out["oracle_best_us_at_256_waiting_8_active"] = (time.perf_counter() - t0) * 1e6
+    return out
+
+
 def main():
     args = parse_args()
     from decode_attention_xattention_gb300 import workloads as wl
@@ -569,6 +626,8 @@ def main():
         "clocks": clocks,
     }
     line["beam_select"] = time_beam_select(f"cuda:{local}", stream, rank == 0 and not args.no_cpu_baseline)
+    if rank == 0:
+        line["cht"] = time_cht(not args.no_cpu_baseline)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample = cpu_oracle_sample(w, inputs[0], args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "beams/s", "cores": cores, "kind": "oracle", "sample": sample}
