@@ -409,6 +409,63 @@ def time_cht(with_oracle: bool) -> dict:
     return out
 
 
+def time_valid_path(device, stream, with_oracle: bool) -> dict:
+    """The valid-path masks timed through the C ABI on a synthetic catalogue: 262144 items as
+    3-token paths over V = 8192 tokens, 1024 rows (8 requests x 128 beams) following item
+    paths; the dense mask at step 0 (about every token valid) and the sparse best-128 list at
+    step 1 (about 32 valid tokens per row), CUDA events over 100 calls each."""
+    import numpy as np
+    import torch
+
+    from decode_attention_xattention_gb300 import xattn
+
+    rng = np.random.default_rng(4)
+    N, L, V, rows, C = 262144, 3, 8192, 1024, 128
+    items = rng.integers(0, V, size=(N, L)).astype(np.int32)
+    t0 = time.perf_counter()
+    off, tok = xattn.trie_build(items)
+    t_build = time.perf_counter() - t0
+    pre = items[rng.integers(0, N, size=rows)].copy()
+    logp = rng.standard_normal((rows, V)).astype(np.float32)
+    d_off, d_tok, d_pre, d_logp = (torch.from_numpy(np.ascontiguousarray(a)).to(device) for a in (off, tok, pre, logp))
+    nodes = len(off) - 1
+    ct = torch.empty((rows, C), dtype=torch.int32, device=device)
+    cl = torch.empty((rows, C), dtype=torch.float32, device=device)
+    cnt = torch.empty((rows,), dtype=torch.int32, device=device)
+    st = torch.zeros((1,), dtype=torch.int32, device=device)
+
+    def timed(fn, n=100):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / n * 1e3
+
+    us_dense = timed(lambda: xattn.check(xattn.xattn_valid_path_mask(d_off, d_tok, nodes, L, d_pre, L, 0, rows, V,
+                                                                     d_logp, cnt, st, stream)))
+    dense_valid = float(cnt.float().mean().item())
+    us_sparse = timed(lambda: xattn.check(xattn.xattn_valid_path_topk(d_off, d_tok, nodes, L, d_pre, L, 1, rows, V,
+                                                                      d_logp, C, ct, cl, cnt, st, stream)))
+    out = {"note": "not part of the decode step; synthetic catalogue",
+           "items": N, "path_len": L, "V": V, "rows": rows, "trie_nodes": nodes, "trie_build_ms_host": t_build * 1e3,
+           "dense_step0": {"us_per_call": us_dense, "mean_valid": dense_valid,
+                           "masked_per_row": V - dense_valid},
+           "sparse_step1": {"us_per_call": us_sparse, "C": C, "mean_valid": float(cnt.float().mean().item())},
+           "status": int(st.item())}
+    if with_oracle:
+        from oracle.valid_path import valid_next
+
+        t0 = time.perf_counter()
+        valid_next(items, pre[0], 1)
+        out["oracle_us_per_row_step1"] = (time.perf_counter() - t0) * 1e6
+    return out
+
+
 def main():
     args = parse_args()
     from decode_attention_xattention_gb300 import workloads as wl
@@ -628,6 +685,7 @@ def main():
     line["beam_select"] = time_beam_select(f"cuda:{local}", stream, rank == 0 and not args.no_cpu_baseline)
     if rank == 0:
         line["cht"] = time_cht(not args.no_cpu_baseline)
+    line["valid_path"] = time_valid_path(f"cuda:{local}", stream, rank == 0 and not args.no_cpu_baseline)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample = cpu_oracle_sample(w, inputs[0], args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "beams/s", "cores": cores, "kind": "oracle", "sample": sample}

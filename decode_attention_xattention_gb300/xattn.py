@@ -27,6 +27,8 @@ XATTN_STATUS_BAD_SLOT = 2
 XATTN_STATUS_BAD_PARENT = 4
 XATTN_STATUS_EMPTY_ROW = 8
 XATTN_STATUS_TIMEOUT = 16
+XATTN_STATUS_BAD_TRIE = 32
+XATTN_STATUS_TOO_MANY_VALID = 64
 
 XATTN_DTYPE_BF16 = 0
 XATTN_DTYPE_F32 = 1
@@ -36,7 +38,8 @@ EXPORTS = ("xattn_decode_workspace_size", "xattn_decode", "xattn_decode_shared",
            "xattn_beam_update", "xattn_read_status", "xattn_query_plan", "xattn_status_string",
            "xattn_decode_noalloc", "xattn_beam_select",
            "xattn_cht_create", "xattn_cht_destroy", "xattn_cht_insert", "xattn_cht_best", "xattn_cht_admit",
-           "xattn_cht_finish", "xattn_cht_cancel", "xattn_cht_missing", "xattn_cht_counts")
+           "xattn_cht_finish", "xattn_cht_cancel", "xattn_cht_missing", "xattn_cht_counts",
+           "xattn_trie_size", "xattn_trie_build", "xattn_valid_path_mask", "xattn_valid_path_topk")
 
 XATTN_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -90,6 +93,13 @@ def load(path: str = LIB_PATH):
     lib.xattn_beam_update.restype = ctypes.c_int
     lib.xattn_beam_select.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
     lib.xattn_beam_select.restype = ctypes.c_int
+    i64 = ctypes.c_int64
+    lib.xattn_trie_size.argtypes = [vp, i64, i32, ctypes.POINTER(i64)]
+    lib.xattn_trie_build.argtypes = [vp, i64, i32, i64, vp, vp]
+    lib.xattn_valid_path_mask.argtypes = [vp, vp, i64, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp]
+    lib.xattn_valid_path_topk.argtypes = [vp, vp, i64, i32, vp, i32, i32, i32, i32, vp, i32, vp, vp, vp, vp, vp]
+    for f in ("xattn_trie_size", "xattn_trie_build", "xattn_valid_path_mask", "xattn_valid_path_topk"):
+        getattr(lib, f).restype = ctypes.c_int
     lib.xattn_read_status.argtypes = [vp, ctypes.POINTER(i32), i32, vp]
     lib.xattn_read_status.restype = ctypes.c_int
     lib.xattn_query_plan.argtypes = [pdesc, i32, ctypes.POINTER(xattn_plan)]
@@ -167,6 +177,38 @@ def xattn_beam_select(num_requests, beam_width, cand_per_beam, out_width, beam_s
     return int(load().xattn_beam_select(int(num_requests), int(beam_width), int(cand_per_beam), int(out_width),
                                         _ptr(beam_score), _ptr(cand_logp), _ptr(cand_token), _ptr(parent),
                                         _ptr(token), _ptr(score), _stream(stream)))
+
+
+def trie_build(items):
+    """Host trie of the item catalogue `items` [N, L] (int32 array): (child_off, child_tok)
+    numpy arrays, laid out as xattn_valid_path.h describes."""
+    import numpy as np
+
+    items = np.ascontiguousarray(items, dtype=np.int32)
+    N, L = items.shape
+    lib = load()
+    n = ctypes.c_int64(0)
+    check(int(lib.xattn_trie_size(items.ctypes.data_as(ctypes.c_void_p), N, L, ctypes.byref(n))))
+    off = np.zeros(n.value + 1, np.int32)
+    tok = np.zeros(max(n.value - 1, 1), np.int32)
+    check(int(lib.xattn_trie_build(items.ctypes.data_as(ctypes.c_void_p), N, L, n.value,
+                                   off.ctypes.data_as(ctypes.c_void_p), tok.ctypes.data_as(ctypes.c_void_p))))
+    return off, tok[: n.value - 1]
+
+
+def xattn_valid_path_mask(child_off, child_tok, num_nodes, path_len, prefix, prefix_stride, step, rows, V, logp,
+                          valid_count=None, status=None, stream=None) -> int:
+    return int(load().xattn_valid_path_mask(_ptr(child_off), _ptr(child_tok), int(num_nodes), int(path_len),
+                                            _ptr(prefix), int(prefix_stride), int(step), int(rows), int(V), _ptr(logp),
+                                            _ptr(valid_count), _ptr(status), _stream(stream)))
+
+
+def xattn_valid_path_topk(child_off, child_tok, num_nodes, path_len, prefix, prefix_stride, step, rows, V, logp, C,
+                          cand_token, cand_logp, valid_count=None, status=None, stream=None) -> int:
+    return int(load().xattn_valid_path_topk(_ptr(child_off), _ptr(child_tok), int(num_nodes), int(path_len),
+                                            _ptr(prefix), int(prefix_stride), int(step), int(rows), int(V), _ptr(logp),
+                                            int(C), _ptr(cand_token), _ptr(cand_logp), _ptr(valid_count),
+                                            _ptr(status), _stream(stream)))
 
 
 def xattn_read_status(workspace, clear: bool = True, stream=None) -> tuple[int, int]:

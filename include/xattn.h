@@ -72,7 +72,9 @@ enum {
     XATTN_STATUS_BAD_SLOT = 2,       /* beam_tok_idx entry outside [0, ns_slots)        */
     XATTN_STATUS_BAD_PARENT = 4,     /* parent[r, b] outside [0, beam_width)            */
     XATTN_STATUS_EMPTY_ROW = 8,      /* shared_len[r] == 0 and step == 0: no keys       */
-    XATTN_STATUS_TIMEOUT = 16        /* an on-chip wait gave up (internal error)        */
+    XATTN_STATUS_TIMEOUT = 16,       /* an on-chip wait gave up (internal error)        */
+    XATTN_STATUS_BAD_TRIE = 32,      /* valid-path trie index out of range              */
+    XATTN_STATUS_TOO_MANY_VALID = 64 /* sparse valid-path list: > 4096 valid tokens      */
 };
 
 enum { XATTN_DTYPE_BF16 = 0, XATTN_DTYPE_F32 = 1 };
