@@ -16,6 +16,7 @@
 // outnumber live ones.
 #include <cstdint>
 #include <new>
+#include <stdexcept>
 #include <queue>
 #include <unordered_map>
 #include <vector>
@@ -59,6 +60,19 @@ struct Holder {  // a waiting request holding a block hash (seq identifies the i
     int64_t id;
     uint64_t seq;
 };
+
+// Runs `body` (which returns an XATTN_* code) so that no C++ exception crosses the C ABI:
+// a failed allocation becomes XATTN_ERR_HOST_MEMORY.
+template <typename F>
+int guarded(F body) {
+    try {
+        return body();
+    } catch (const std::bad_alloc&) {
+        return XATTN_ERR_HOST_MEMORY;
+    } catch (...) {
+        return XATTN_ERR_INVALID_ARG;
+    }
+}
 
 }  // namespace
 
@@ -113,106 +127,120 @@ extern "C" {
 
 xattn_cht* xattn_cht_create(int32_t block_tokens) {
     if (block_tokens < 1) return nullptr;
-    xattn_cht* t = new (std::nothrow) xattn_cht();
-    if (t) t->block = block_tokens;
-    return t;
+    try {
+        xattn_cht* t = new xattn_cht();
+        t->block = block_tokens;
+        return t;
+    } catch (...) {
+        return nullptr;
+    }
 }
 
 void xattn_cht_destroy(xattn_cht* cht) { delete cht; }
 
 int xattn_cht_insert(xattn_cht* cht, int64_t request_id, const int32_t* tokens, int64_t num_tokens) {
-    if (!cht || num_tokens < 0 || (num_tokens > 0 && !tokens)) return XATTN_ERR_INVALID_ARG;
-    if (cht->reqs.count(request_id)) return XATTN_ERR_INVALID_ARG;
-    Request r;
-    const int64_t nb = num_tokens / cht->block;
-    r.hashes.reserve((size_t)nb);
-    uint64_t h = 0x6A09E667F3BCC909ull;  // any fixed start value
-    for (int64_t i = 0; i < nb * cht->block; ++i) {
-        h = mix64(h + (uint64_t)(uint32_t)tokens[i] + 0x9E3779B97F4A7C15ull);
-        if ((i + 1) % cht->block == 0) r.hashes.push_back(h);
-    }
-    // covered blocks are a prefix: find its length by binary search on membership
-    int32_t lo = 0, hi = (int32_t)r.hashes.size();
-    while (lo < hi) {
-        const int32_t mid = (lo + hi) / 2;
-        if (cht->working.count(r.hashes[(size_t)mid])) lo = mid + 1;
-        else hi = mid;
-    }
-    r.covered = lo;
-    r.seq = cht->next_seq++;
-    for (uint64_t bh : r.hashes) cht->holders[bh].push_back(Holder{request_id, r.seq});
-    auto ins = cht->reqs.emplace(request_id, std::move(r));
-    cht->push(request_id, ins.first->second);
-    ++cht->waiting;
-    return XATTN_OK;
+    return guarded([&]() -> int {
+        if (!cht || num_tokens < 0 || (num_tokens > 0 && !tokens)) return XATTN_ERR_INVALID_ARG;
+        if (cht->reqs.count(request_id)) return XATTN_ERR_INVALID_ARG;
+        Request r;
+        const int64_t nb = num_tokens / cht->block;
+        r.hashes.reserve((size_t)nb);
+        uint64_t h = 0x6A09E667F3BCC909ull;  // any fixed start value
+        for (int64_t i = 0; i < nb * cht->block; ++i) {
+            h = mix64(h + (uint64_t)(uint32_t)tokens[i] + 0x9E3779B97F4A7C15ull);
+            if ((i + 1) % cht->block == 0) r.hashes.push_back(h);
+        }
+        // covered blocks are a prefix: find its length by binary search on membership
+        int32_t lo = 0, hi = (int32_t)r.hashes.size();
+        while (lo < hi) {
+            const int32_t mid = (lo + hi) / 2;
+            if (cht->working.count(r.hashes[(size_t)mid])) lo = mid + 1;
+            else hi = mid;
+        }
+        r.covered = lo;
+        r.seq = cht->next_seq++;
+        for (uint64_t bh : r.hashes) cht->holders[bh].push_back(Holder{request_id, r.seq});
+        auto ins = cht->reqs.emplace(request_id, std::move(r));
+        cht->push(request_id, ins.first->second);
+        ++cht->waiting;
+        return XATTN_OK;
+    });
 }
 
 int xattn_cht_best(xattn_cht* cht, int64_t* request_id, int32_t* missing_blocks) {
-    if (!cht || !request_id || !missing_blocks) return XATTN_ERR_INVALID_ARG;
-    while (!cht->heap.empty()) {
-        const Entry e = cht->heap.top();
-        if (!cht->live(e)) {
-            cht->heap.pop();
-            continue;
+    return guarded([&]() -> int {
+        if (!cht || !request_id || !missing_blocks) return XATTN_ERR_INVALID_ARG;
+        while (!cht->heap.empty()) {
+            const Entry e = cht->heap.top();
+            if (!cht->live(e)) {
+                cht->heap.pop();
+                continue;
+            }
+            *request_id = e.id;
+            *missing_blocks = e.missing;
+            return 1;
         }
-        *request_id = e.id;
-        *missing_blocks = e.missing;
-        return 1;
-    }
-    return 0;
+        return 0;
+    });
 }
 
 int xattn_cht_admit(xattn_cht* cht, int64_t request_id) {
-    if (!cht) return XATTN_ERR_INVALID_ARG;
-    auto it = cht->reqs.find(request_id);
-    if (it == cht->reqs.end() || it->second.state != State::kWaiting) return XATTN_ERR_INVALID_ARG;
-    Request& r = it->second;
-    r.state = State::kActive;  // its own holder entries and heap entries are now stale
-    --cht->waiting;
-    ++cht->active;
-    for (uint64_t h : r.hashes)
-        if (++cht->working[h] == 1) cht->adjust_holders(h, +1);
-    cht->maybe_rebuild();
-    return XATTN_OK;
+    return guarded([&]() -> int {
+        if (!cht) return XATTN_ERR_INVALID_ARG;
+        auto it = cht->reqs.find(request_id);
+        if (it == cht->reqs.end() || it->second.state != State::kWaiting) return XATTN_ERR_INVALID_ARG;
+        Request& r = it->second;
+        r.state = State::kActive;  // its own holder entries and heap entries are now stale
+        --cht->waiting;
+        ++cht->active;
+        for (uint64_t h : r.hashes)
+            if (++cht->working[h] == 1) cht->adjust_holders(h, +1);
+        cht->maybe_rebuild();
+        return XATTN_OK;
+    });
 }
 
 int xattn_cht_finish(xattn_cht* cht, int64_t request_id) {
-    if (!cht) return XATTN_ERR_INVALID_ARG;
-    auto it = cht->reqs.find(request_id);
-    if (it == cht->reqs.end() || it->second.state != State::kActive) return XATTN_ERR_INVALID_ARG;
-    for (uint64_t h : it->second.hashes) {
-        auto w = cht->working.find(h);
-        if (w != cht->working.end() && --w->second == 0) {
-            cht->working.erase(w);
-            cht->adjust_holders(h, -1);
+    return guarded([&]() -> int {
+        if (!cht) return XATTN_ERR_INVALID_ARG;
+        auto it = cht->reqs.find(request_id);
+        if (it == cht->reqs.end() || it->second.state != State::kActive) return XATTN_ERR_INVALID_ARG;
+        for (uint64_t h : it->second.hashes) {
+            auto w = cht->working.find(h);
+            if (w != cht->working.end() && --w->second == 0) {
+                cht->working.erase(w);
+                cht->adjust_holders(h, -1);
+            }
         }
-    }
-    cht->reqs.erase(it);
-    --cht->active;
-    cht->maybe_rebuild();
-    return XATTN_OK;
+        cht->reqs.erase(it);
+        --cht->active;
+        cht->maybe_rebuild();
+        return XATTN_OK;
+    });
 }
 
 int xattn_cht_cancel(xattn_cht* cht, int64_t request_id) {
-    if (!cht) return XATTN_ERR_INVALID_ARG;
-    auto it = cht->reqs.find(request_id);
-    if (it == cht->reqs.end() || it->second.state != State::kWaiting) return XATTN_ERR_INVALID_ARG;
-    for (uint64_t h : it->second.hashes) {  // its holder entries go now; heap entries lazily
-        auto hv = cht->holders.find(h);
-        if (hv == cht->holders.end()) continue;
-        std::vector<Holder>& v = hv->second;
-        for (size_t i = 0; i < v.size(); ++i)
-            if (v[i].id == request_id && v[i].seq == it->second.seq) {
-                v[i] = v.back();
-                v.pop_back();
-                break;
-            }
-        if (v.empty()) cht->holders.erase(hv);
-    }
-    cht->reqs.erase(it);
-    --cht->waiting;
-    cht->maybe_rebuild();
-    return XATTN_OK;
+    return guarded([&]() -> int {
+        if (!cht) return XATTN_ERR_INVALID_ARG;
+        auto it = cht->reqs.find(request_id);
+        if (it == cht->reqs.end() || it->second.state != State::kWaiting) return XATTN_ERR_INVALID_ARG;
+        for (uint64_t h : it->second.hashes) {  // its holder entries go now; heap entries lazily
+            auto hv = cht->holders.find(h);
+            if (hv == cht->holders.end()) continue;
+            std::vector<Holder>& v = hv->second;
+            for (size_t i = 0; i < v.size(); ++i)
+                if (v[i].id == request_id && v[i].seq == it->second.seq) {
+                    v[i] = v.back();
+                    v.pop_back();
+                    break;
+                }
+            if (v.empty()) cht->holders.erase(hv);
+        }
+        cht->reqs.erase(it);
+        --cht->waiting;
+        cht->maybe_rebuild();
+        return XATTN_OK;
+    });
 }
 
 int xattn_cht_missing(const xattn_cht* cht, int64_t request_id, int32_t* missing_blocks) {

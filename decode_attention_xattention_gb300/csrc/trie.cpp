@@ -9,6 +9,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <new>
 #include <numeric>
 #include <vector>
 
@@ -63,35 +64,52 @@ int64_t walk(const int32_t* items, int32_t L, const std::vector<int64_t>& order,
     return nodes;
 }
 
+// Runs `body` so that no C++ exception crosses the C ABI (a failed allocation becomes
+// XATTN_ERR_HOST_MEMORY).
+template <typename F>
+int guarded(F body) {
+    try {
+        return body();
+    } catch (const std::bad_alloc&) {
+        return XATTN_ERR_HOST_MEMORY;
+    } catch (...) {
+        return XATTN_ERR_INVALID_ARG;
+    }
+}
+
 }  // namespace
 
 extern "C" {
 
 int xattn_trie_size(const int32_t* items, int64_t num_items, int32_t path_len, int64_t* num_nodes) {
-    if (!items || !num_nodes || num_items < 1 || path_len < 1) return XATTN_ERR_INVALID_ARG;
-    std::vector<int64_t> order;
-    if (!sorted_unique(items, num_items, path_len, &order)) return XATTN_ERR_INVALID_ARG;
-    const int64_t n = walk(items, path_len, order, [](int32_t) {}, [] {});
-    if (n > 0x7fffffffLL) return XATTN_ERR_INVALID_ARG;
-    *num_nodes = n;
-    return XATTN_OK;
+    return guarded([&]() -> int {
+        if (!items || !num_nodes || num_items < 1 || path_len < 1) return XATTN_ERR_INVALID_ARG;
+        std::vector<int64_t> order;
+        if (!sorted_unique(items, num_items, path_len, &order)) return XATTN_ERR_INVALID_ARG;
+        const int64_t n = walk(items, path_len, order, [](int32_t) {}, [] {});
+        if (n > 0x7fffffffLL) return XATTN_ERR_INVALID_ARG;
+        *num_nodes = n;
+        return XATTN_OK;
+    });
 }
 
 int xattn_trie_build(const int32_t* items, int64_t num_items, int32_t path_len, int64_t num_nodes,
                      int32_t* child_off, int32_t* child_tok) {
-    if (!items || !child_off || num_items < 1 || path_len < 1 || num_nodes < 1 || num_nodes > 0x7fffffffLL ||
-        (num_nodes > 1 && !child_tok))
-        return XATTN_ERR_INVALID_ARG;
-    std::vector<int64_t> order;
-    if (!sorted_unique(items, num_items, path_len, &order)) return XATTN_ERR_INVALID_ARG;
-    // count first, so that nothing is written past the caller's buffers
-    if (walk(items, path_len, order, [](int32_t) {}, [] {}) != num_nodes) return XATTN_ERR_INVALID_ARG;
-    int64_t edges = 0, closed = 0;
-    child_off[0] = 0;
-    walk(
-        items, path_len, order, [&](int32_t tok) { child_tok[edges++] = tok; },
-        [&] { child_off[++closed] = (int32_t)edges; });
-    return closed == num_nodes && edges == num_nodes - 1 ? XATTN_OK : XATTN_ERR_INVALID_ARG;
+    return guarded([&]() -> int {
+        if (!items || !child_off || num_items < 1 || path_len < 1 || num_nodes < 1 || num_nodes > 0x7fffffffLL ||
+            (num_nodes > 1 && !child_tok))
+            return XATTN_ERR_INVALID_ARG;
+        std::vector<int64_t> order;
+        if (!sorted_unique(items, num_items, path_len, &order)) return XATTN_ERR_INVALID_ARG;
+        // count first, so that nothing is written past the caller's buffers
+        if (walk(items, path_len, order, [](int32_t) {}, [] {}) != num_nodes) return XATTN_ERR_INVALID_ARG;
+        int64_t edges = 0, closed = 0;
+        child_off[0] = 0;
+        walk(
+            items, path_len, order, [&](int32_t tok) { child_tok[edges++] = tok; },
+            [&] { child_off[++closed] = (int32_t)edges; });
+        return closed == num_nodes && edges == num_nodes - 1 ? XATTN_OK : XATTN_ERR_INVALID_ARG;
+    });
 }
 
 }  // extern "C"

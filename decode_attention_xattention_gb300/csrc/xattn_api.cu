@@ -403,6 +403,7 @@ const char* xattn_status_string(int code) {
         case XATTN_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
         case XATTN_ERR_MISALIGNED: return "tensor not 16-byte aligned";
         case XATTN_ERR_CUDA: return "CUDA error";
+        case XATTN_ERR_HOST_MEMORY: return "host allocation failed";
         default: return "unknown status";
     }
 }

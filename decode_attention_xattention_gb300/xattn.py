@@ -21,6 +21,7 @@ XATTN_ERR_UNSUPPORTED = -2
 XATTN_ERR_WORKSPACE_TOO_SMALL = -3
 XATTN_ERR_MISALIGNED = -4
 XATTN_ERR_CUDA = -5
+XATTN_ERR_HOST_MEMORY = -6
 
 XATTN_STATUS_BAD_SHARED_LEN = 1
 XATTN_STATUS_BAD_SLOT = 2

@@ -63,7 +63,8 @@ enum {
     XATTN_ERR_UNSUPPORTED = -2,          /* valid but not implemented (e.g. head_dim 96)    */
     XATTN_ERR_WORKSPACE_TOO_SMALL = -3,  /* workspace_bytes < xattn_decode_workspace_size   */
     XATTN_ERR_MISALIGNED = -4,           /* a tensor is not 16-byte aligned                 */
-    XATTN_ERR_CUDA = -5                  /* a CUDA call or launch failed                    */
+    XATTN_ERR_CUDA = -5,                 /* a CUDA call or launch failed                    */
+    XATTN_ERR_HOST_MEMORY = -6           /* a host allocation failed (host-side structures) */
 };
 
 /* Bits of the device status word (sticky until read with clear = 1). */

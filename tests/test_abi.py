@@ -42,7 +42,7 @@ def test_desc_layout_matches_header():
 
 
 def test_status_strings(lib):
-    for code in (0, -1, -2, -3, -4, -5):
+    for code in (0, -1, -2, -3, -4, -5, -6):
         assert xattn.xattn_status_string(code)
     assert xattn.xattn_status_string(-99) == "unknown status"
 
