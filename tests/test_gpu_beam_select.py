@@ -78,8 +78,9 @@ def test_masked_candidates_and_signed_zero():
 @pytest.mark.gpu
 def test_early_termination_leaves_lists_unread():
     """Beams that cannot enter the best W stop after a few positions: half the beams score
-    -1e6 lower; in round 0 they fill the empty array, in round 1 the other beams' candidates
-    push them out, and by round 2 each of them meets a full array it cannot enter. Their
+    -1e6 lower; at list position 0 they fill the empty array, at position 1 the other beams'
+    candidates push them out, and by position 2 each of them meets a full array it cannot
+    enter. Their
     lists past position 2 are poisoned with NaN, which would win every comparison it entered
     (and which the oracle's full scan rejects): the selection must come out unchanged."""
     R, BW, K, W = 2, 64, 64, 64
