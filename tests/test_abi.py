@@ -111,6 +111,46 @@ def test_split_plan_covers_prefix(lib):
             assert p.shared_kernel == 1
 
 
+def test_plan_properties_over_shapes(lib):
+    """The host plan over a grid of shapes: the prefix pieces cover the prefix in whole
+    128-token tiles, the decode is fused exactly when the tensor-core Shared stage has one
+    piece and at most 32 Non-Shared tokens, the workspace holds every piece row the kernels
+    address, and merge launches exist only when the decode is not fused."""
+    import itertools
+    import math
+    for (R, BW, Hq, Hkv, d), Lmax, Tmax, split, kernel in itertools.product(
+            [(1, 4, 2, 1, 64), (8, 128, 32, 8, 128), (2, 5, 16, 1, 128), (3, 33, 8, 8, 64)],
+            [0, 1, 127, 129, 2048, 40000], [0, 1, 3, 32, 33, 64, 200], [0, 128, 640], [0, 1, 2]):
+        if Lmax == 0 and Tmax == 0:
+            continue
+        G = Hq // Hkv
+        M = BW * G
+        S = BW * max(Tmax, 1)
+        desc = xattn.make_desc(R, BW, Hq, Hkv, d, Lmax, S, Tmax, 0.0, kernel, split)
+        for step in sorted({0, min(1, Tmax), Tmax // 2, Tmax}):
+            if Lmax == 0 and step == 0:
+                continue
+            rc, p = xattn.xattn_query_plan(desc, step)
+            assert rc == 0, (R, BW, Hq, Hkv, d, Lmax, Tmax, split, kernel, step)
+            assert p.rows_per_unit == M and p.row_tiles == math.ceil(M / 128)
+            if Lmax > 0:
+                assert p.shared_kernel == (kernel or 1)
+                assert p.split_tokens > 0 and p.split_tokens % 128 == 0
+                assert (p.num_splits - 1) * p.split_tokens < Lmax <= p.num_splits * p.split_tokens
+                if split:
+                    assert p.split_tokens == split
+            else:
+                assert p.shared_kernel == 0 and p.num_splits == 0
+            ns_pieces = math.ceil(Tmax / 64) if Tmax > 32 else (1 if Tmax > 0 else 0)
+            assert p.piece_stride == p.num_splits + ns_pieces
+            fused = p.shared_kernel == 1 and p.num_splits == 1 and step <= 32
+            assert p.fused == int(fused)
+            assert (p.merge_ctas == 0) == bool(p.fused)
+            ws = xattn.xattn_decode_workspace_size(desc)
+            rows = R * Hkv * p.piece_stride * M
+            assert ws >= 256 + rows * d * 4 + rows * 4
+
+
 def test_fp32_inputs_plan_and_limits(lib):
     """fp32 storage runs on the CUDA-core kernels: the planner picks the CUDA-core Shared
     stage and the unfused path; the tensor-core kernel and Non-Shared parts longer than the
