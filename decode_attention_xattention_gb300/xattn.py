@@ -40,7 +40,8 @@ EXPORTS = ("xattn_decode_workspace_size", "xattn_decode", "xattn_decode_shared",
            "xattn_decode_noalloc", "xattn_beam_select",
            "xattn_cht_create", "xattn_cht_destroy", "xattn_cht_insert", "xattn_cht_best", "xattn_cht_admit",
            "xattn_cht_finish", "xattn_cht_cancel", "xattn_cht_missing", "xattn_cht_counts",
-           "xattn_trie_size", "xattn_trie_build", "xattn_valid_path_mask", "xattn_valid_path_topk")
+           "xattn_trie_size", "xattn_trie_build", "xattn_valid_path_mask", "xattn_valid_path_topk",
+           "xattn_check_bounded_wait")
 
 XATTN_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -101,6 +102,8 @@ def load(path: str = LIB_PATH):
     lib.xattn_valid_path_topk.argtypes = [vp, vp, i64, i32, vp, i32, i32, i32, i32, vp, i32, vp, vp, vp, vp, vp]
     for f in ("xattn_trie_size", "xattn_trie_build", "xattn_valid_path_mask", "xattn_valid_path_topk"):
         getattr(lib, f).restype = ctypes.c_int
+    lib.xattn_check_bounded_wait.argtypes = [i64, vp, vp, vp]
+    lib.xattn_check_bounded_wait.restype = ctypes.c_int
     lib.xattn_read_status.argtypes = [vp, ctypes.POINTER(i32), i32, vp]
     lib.xattn_read_status.restype = ctypes.c_int
     lib.xattn_query_plan.argtypes = [pdesc, i32, ctypes.POINTER(xattn_plan)]
@@ -210,6 +213,11 @@ def xattn_valid_path_topk(child_off, child_tok, num_nodes, path_len, prefix, pre
                                             _ptr(prefix), int(prefix_stride), int(step), int(rows), int(V), _ptr(logp),
                                             int(C), _ptr(cand_token), _ptr(cand_logp), _ptr(valid_count),
                                             _ptr(status), _stream(stream)))
+
+
+def xattn_check_bounded_wait(limit_cycles, status, waited_cycles=None, stream=None) -> int:
+    return int(load().xattn_check_bounded_wait(int(limit_cycles), _ptr(status), _ptr(waited_cycles),
+                                               _stream(stream)))
 
 
 def xattn_read_status(workspace, clear: bool = True, stream=None) -> tuple[int, int]:

@@ -179,6 +179,15 @@ XATTN_API int xattn_beam_update(const xattn_desc* desc, const int32_t* parent, c
  * Returns INVALID_ARG for a size < 1, W > BW*K or a NULL pointer; UNSUPPORTED for
  * BW > 1024, W > 1024 or BW*K > 2^30; MISALIGNED for a pointer not 4-byte aligned. Lists
  * out of order give an unspecified selection (not detected). */
+/* Self-check of the bounded on-chip waits: one CTA waits, through the same bounded mbarrier
+ * wait as the kernels, on a phase that nothing completes; after about limit_cycles SM cycles
+ * (0 .. 2^32) it gives up, sets XATTN_STATUS_TIMEOUT in *status (device int32) and returns;
+ * *waited_cycles (device int64, may be NULL) gets the cycles it waited. This exercises the
+ * kernels' timeout path without a fault; the context stays usable. INVALID_ARG for a NULL
+ * status or a limit out of range, MISALIGNED for a misaligned pointer. */
+XATTN_API int xattn_check_bounded_wait(int64_t limit_cycles, int32_t* status, int64_t* waited_cycles,
+                                       xattn_stream_t stream);
+
 XATTN_API int xattn_beam_select(int32_t num_requests, int32_t beam_width, int32_t cand_per_beam,
                                 int32_t out_width, const float* beam_score, const float* cand_logp,
                                 const int32_t* cand_token, int32_t* parent, int32_t* token, float* score,

@@ -196,3 +196,12 @@ def test_beam_select_rejected_on_host(lib):
     assert f(1, 1024, 1 << 21, 4, P, P, P, P, P, P) == xattn.XATTN_ERR_UNSUPPORTED  # BW*K > 2^30
     assert f(1, 4, 4, 4, P, None, P, P, P, P) == xattn.XATTN_ERR_INVALID_ARG
     assert f(1, 4, 4, 4, P, P + 2, P, P, P, P) == xattn.XATTN_ERR_MISALIGNED
+
+
+def test_bounded_wait_check_rejected_on_host(lib):
+    P = 0x1000
+    assert xattn.xattn_check_bounded_wait(1000, None) == xattn.XATTN_ERR_INVALID_ARG
+    assert xattn.xattn_check_bounded_wait(-1, P) == xattn.XATTN_ERR_INVALID_ARG
+    assert xattn.xattn_check_bounded_wait(1 << 33, P) == xattn.XATTN_ERR_INVALID_ARG
+    assert xattn.xattn_check_bounded_wait(1000, P + 2) == xattn.XATTN_ERR_MISALIGNED
+    assert xattn.xattn_check_bounded_wait(1000, P, P + 4) == xattn.XATTN_ERR_MISALIGNED

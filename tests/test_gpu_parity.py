@@ -303,6 +303,20 @@ def test_cuda_graph_capture_replay():
 
 
 # -- device-detected data errors: status word + NaN rows, no trap --------------------------
+def test_bounded_wait_gives_up_and_context_stays_usable():
+    """The timeout path of the bounded on-chip waits, without a fault: a wait on a phase that
+    nothing completes gives up after its limit and records XATTN_STATUS_TIMEOUT; afterwards
+    an ordinary decode still runs and matches the oracle."""
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    waited = torch.zeros(1, dtype=torch.int64, device="cuda")
+    limit = 2_000_000  # SM cycles, about a millisecond
+    xattn.check(xattn.xattn_check_bounded_wait(limit, st, waited))
+    torch.cuda.synchronize()
+    assert int(st.item()) & xattn.XATTN_STATUS_TIMEOUT
+    assert int(waited.item()) >= limit
+    run_and_check(wl.custom(R=1, BW=4, Hq=4, Hkv=2, d=128, lens=(300,), T=3, seed=2))
+
+
 def test_bad_slot_sets_status_and_nan_row():
     w = wl.custom(R=1, BW=4, Hq=4, Hkv=2, d=128, lens=(200,), T=2, seed=1)
     db = DeviceBatch(wl.make_inputs(w))
