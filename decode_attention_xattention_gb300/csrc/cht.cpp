@@ -10,9 +10,9 @@
 // since a block hash is cumulative (it fixes every token before the block's end), the
 // covered blocks are a prefix and missing = blocks - covered. An inverted index from block
 // hash to the waiting requests holding it lets admission and removal adjust exactly the
-// requests whose coverage changes; each adjustment pushes a fresh heap entry and bumps the
-// request's version, and entries whose version is stale are dropped when they surface
-// (lazy deletion). The heap is rebuilt from the waiting requests when stale entries
+// requests whose coverage changes; each admission or removal then pushes one fresh heap
+// entry per request it touched and bumps that request's version, and entries whose version
+// is stale are dropped when they surface (lazy deletion). The heap is rebuilt from the waiting requests when stale entries
 // outnumber live ones.
 #include <cstdint>
 #include <new>
@@ -40,6 +40,7 @@ struct Request {
     int32_t covered = 0;           // blocks in the working set (waiting requests only)
     uint64_t seq = 0;              // insertion order (ties) and identity of this insertion
     uint32_t version = 0;          // bumped whenever the heap key changes
+    uint64_t touched = 0;          // last admission / removal that changed `covered`
     State state = State::kWaiting;
     int32_t missing() const { return (int32_t)hashes.size() - covered; }
 };
@@ -79,6 +80,8 @@ int guarded(F body) {
 struct xattn_cht {
     int32_t block = 1;
     uint64_t next_seq = 0;
+    uint64_t op = 0;                // admissions and removals so far
+    std::vector<int64_t> touched;   // waiting requests whose coverage the current one changed
     int64_t waiting = 0, active = 0;
     std::unordered_map<int64_t, Request> reqs;
     std::unordered_map<uint64_t, int32_t> working;  // block hash -> active requests holding it
@@ -94,7 +97,8 @@ struct xattn_cht {
     }
 
     // The waiting holders of hash h whose covered count moves by `delta`; holders that are
-    // no longer waiting (or were re-inserted) are dropped from the list on the way.
+    // no longer waiting (or were re-inserted) are dropped from the list on the way. Each
+    // holder is listed once per operation in `touched`; flush() then gives it one heap entry.
     void adjust_holders(uint64_t h, int32_t delta) {
         auto it = holders.find(h);
         if (it == holders.end()) return;
@@ -106,11 +110,23 @@ struct xattn_cht {
             v[keep++] = v[i];
             Request& r = rq->second;
             r.covered += delta;
-            ++r.version;
-            push(v[i].id, r);
+            if (r.touched != op) {
+                r.touched = op;
+                touched.push_back(v[i].id);
+            }
         }
         v.resize(keep);
         if (v.empty()) holders.erase(it);
+    }
+
+    // One fresh heap entry per request whose coverage the current operation changed.
+    void flush() {
+        for (int64_t id : touched) {
+            Request& r = reqs.find(id)->second;
+            ++r.version;
+            push(id, r);
+        }
+        touched.clear();
     }
 
     void maybe_rebuild() {
@@ -193,8 +209,10 @@ int xattn_cht_admit(xattn_cht* cht, int64_t request_id) {
         r.state = State::kActive;  // its own holder entries and heap entries are now stale
         --cht->waiting;
         ++cht->active;
+        ++cht->op;
         for (uint64_t h : r.hashes)
             if (++cht->working[h] == 1) cht->adjust_holders(h, +1);
+        cht->flush();
         cht->maybe_rebuild();
         return XATTN_OK;
     });
@@ -205,6 +223,7 @@ int xattn_cht_finish(xattn_cht* cht, int64_t request_id) {
         if (!cht) return XATTN_ERR_INVALID_ARG;
         auto it = cht->reqs.find(request_id);
         if (it == cht->reqs.end() || it->second.state != State::kActive) return XATTN_ERR_INVALID_ARG;
+        ++cht->op;
         for (uint64_t h : it->second.hashes) {
             auto w = cht->working.find(h);
             if (w != cht->working.end() && --w->second == 0) {
@@ -212,6 +231,7 @@ int xattn_cht_finish(xattn_cht* cht, int64_t request_id) {
                 cht->adjust_holders(h, -1);
             }
         }
+        cht->flush();
         cht->reqs.erase(it);
         --cht->active;
         cht->maybe_rebuild();
