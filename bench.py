@@ -48,6 +48,10 @@ def parse_args():
     ap.add_argument("--workload", default="gr_r8_bw128_h32x8_d128_L2048_t3")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="wall budget of the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="time the default workload only")
+    ap.add_argument("--configs", default="", help="comma-separated name prefixes of the other workloads to time")
+    ap.add_argument("--config-cpu-seconds", type=float, default=2.5,
+                    help="wall budget of each other workload's CPU-baseline sample")
     return ap.parse_args()
 
 
@@ -154,19 +158,19 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------------------
-def unique_bytes(w, idx_np, shared_lens):
+def unique_bytes(w, idx_np, shared_lens, elem=2):
     """Bytes the step must move at least once: prefix K/V over valid tokens (once per
     request), the distinct Non-Shared pool rows the ancestry references, q, out, lse and the
-    ancestry entries read."""
+    ancestry entries read. elem: bytes per stored q/K/V element (2 bf16, 4 fp32)."""
     import numpy as np
 
     d, Hkv = w.head_dim, w.num_kv_heads
-    prefix = int(sum(shared_lens)) * Hkv * d * 2 * 2
+    prefix = int(sum(shared_lens)) * Hkv * d * 2 * elem
     T = w.steps
     distinct = sum(len(np.unique(idx_np[r, :, :T])) for r in range(w.num_requests)) if T > 0 else 0
-    ns = distinct * Hkv * d * 2 * 2
+    ns = distinct * Hkv * d * 2 * elem
     rows = w.num_requests * w.beam_width * w.num_q_heads
-    q = rows * d * 2
+    q = rows * d * elem
     out = rows * d * 2 + rows * 4
     idx = w.num_requests * w.beam_width * T * 4
     return prefix + ns + q + out + idx, {"prefix_kv": prefix, "ns_kv": ns, "q": q, "out_lse": out, "idx": idx}
@@ -205,20 +209,21 @@ def profile_traffic(kernel_file: str, workload: str):
 
 def launches_per_step(plan, step):
     """Kernels of this library launched by one timed step: the beam update, then the
-    decode (Non-Shared piece kernel + Shared stage with merging epilogue when fused; else
+    decode (the Shared-stage kernel alone when it gathers the Non-Shared part itself; the
+    Non-Shared kernel + Shared stage with merging epilogue when fused; else
     the Shared stage, if the prefix has storage, and the Non-Shared/Merge kernel, or the
     Non-Shared piece and row-merge kernels when the Non-Shared part is long)."""
     n = 1
     if plan.fused:
-        n += (1 if step > 0 else 0) + 1
+        n += (1 if (step > 0 and not plan.ns_tile) else 0) + 1
     else:
         n += (1 if plan.shared_kernel != 0 else 0) + (2 if step > 32 else 1)
     return n
 
 
 # ----------------------------------------------------------------------------------------
-def cpu_oracle_sample(w, inp, budget_s, rows_override=None):
-    """Times the fp64 oracle (as it stands, all host cores) on whole beams of request 0
+def cpu_oracle_sample(w, inp, budget_s, nthreads=0):
+    """Times the fp64 oracle (as it stands; all host cores, or `nthreads`) on whole beams
     until about budget_s of wall time. Returns (beams/s, cores, description)."""
     import numpy as np
 
@@ -228,14 +233,15 @@ def cpu_oracle_sample(w, inp, budget_s, rows_override=None):
     pk, pv, idx = oracle.build_cache(orc, inp)
     D = oracle.dims_of(w)
     Hq = w.num_q_heads
-    cores = orc.max_threads()
+    cores = nthreads if nthreads > 0 else orc.max_threads()
 
     def run(nbeams, offset=0):
         b0 = offset % w.num_beams
         beams = [(b0 + i) % w.num_beams for i in range(nbeams)]
         rows = np.asarray([b * Hq + h for b in beams for h in range(Hq)], np.int64)
         t0 = time.perf_counter()
-        orc.decode(D, inp.q, inp.shared_k, inp.shared_v, inp.shared_len, pk, pv, idx, w.steps, rows=rows)
+        orc.decode(D, inp.q, inp.shared_k, inp.shared_v, inp.shared_len, pk, pv, idx, w.steps, rows=rows,
+                   nthreads=nthreads)
         return time.perf_counter() - t0
 
     t = run(1)
@@ -466,6 +472,198 @@ def time_valid_path(device, stream, with_oracle: bool) -> dict:
     return out
 
 
+# The measured configuration list, in order: the default (headline) workload first.
+CONFIG_ORDER = ["gr_r8_bw128_h32x8_d128_L2048_t3", "tiny_r1_bw4_h2x1_d64_L256_t3", "wide_r4_bw512_h16x4_d128_L4096_t4",
+                "long_r2_bw256_h32x8_d128_L32768+20000_t8", "feather_g1_seq64_h32x8_d128_L8192_s512",
+                "feather_g8_seq64_h32x8_d128_L8192_s512", "feather_g64_seq64_h32x8_d128_L8192_s512"]
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # 152 SMs x 128 fp32 FMA lanes x 2 flop x 2.07 GHz
+
+
+def ns_merge_bytes(w, plan, idx_np, elem):
+    """Algorithmic bytes of the Non-Shared + Merge kernels (xattn_decode_merge): the distinct
+    pool rows the ancestry references (K and V), q, the prefix pieces' partials read back,
+    out and lse written, the ancestry entries read."""
+    import numpy as np
+
+    T, d, Hkv = w.steps, w.head_dim, w.num_kv_heads
+    rows = w.num_requests * w.beam_width * w.num_q_heads
+    distinct = sum(len(np.unique(idx_np[r, :, :T])) for r in range(w.num_requests)) if T > 0 else 0
+    M = w.beam_width * w.group_size
+    parts = w.num_requests * Hkv * plan.num_splits * M * (d + 1) * 4
+    return distinct * Hkv * d * 2 * elem + rows * d * elem + parts + rows * (d * 2 + 4) + \
+        w.num_requests * w.beam_width * T * 4
+
+
+def beam_update_bytes(w, elem):
+    """Algorithmic bytes of one beam update: the BW new tokens' K/V read and written into the
+    pool, the ancestry table read and rewritten, the parents read."""
+    R, BW, T = w.num_requests, w.beam_width, w.steps
+    return 2 * R * BW * w.num_kv_heads * w.head_dim * 2 * elem + 2 * R * BW * T * 4 + R * BW * 4
+
+
+def measure_config(w, local, stream, peaks, peak_src, l2, cpu_budget_s, target_s=0.3):
+    """One workload measured the way the headline line is: CUDA-graph replays of one step
+    (beam update + decode) on inputs resident in HBM, with either rotating copies of the
+    inputs that together exceed twice the L2, or (small workloads) the L2 flushed before
+    every timed step; each stage timed alone the same way; the roofline of the dominant
+    kernel; the oracle timed on a bounded sample of beams (all host cores)."""
+    import numpy as np
+    import torch
+
+    from decode_attention_xattention_gb300 import workloads as wl, xattn
+    from decode_attention_xattention_gb300.runner import DeviceBatch
+
+    T = w.steps
+    f32 = w.input_dtype == "fp32"
+    elem = 4 if f32 else 2
+    inp = wl.make_inputs(w)
+    if not f32:
+        inp = inp.as_bf16()
+    base = DeviceBatch(inp, device=f"cuda:{local}", stream=stream, input_f32=f32)
+    with torch.cuda.stream(stream):
+        base.build_cache(steps=T - 1)
+    set_bytes = sum(t.numel() * t.element_size() for t in
+                    (base.q, base.shared_k, base.shared_v, base.pool_k, base.pool_v, base.out, base.lse,
+                     base.workspace) if t is not None)
+    flush = set_bytes * 8 < l2  # too small to rotate past the L2: flush it before each step
+    sets = [base]
+    while not flush and (len(sets) < 2 or len(sets) * set_bytes < 2 * l2):
+        sets.append(base.clone())
+    nsets = len(sets)
+    plan = base.plan()
+    flush_buf = torch.empty(int(2 * l2) // 4 + 1, dtype=torch.int32, device=f"cuda:{local}") if flush else None
+
+    def step(db):
+        xattn.check(db.beam_update(T - 1))
+        xattn.check(db.decode())
+
+    with torch.cuda.stream(stream):
+        for db in sets:
+            step(db)
+            if w.max_shared_len > 0:
+                xattn.check(db.decode_shared())
+            if not plan.fused:
+                xattn.check(db.decode_merge())
+            xattn.check(db.beam_update(T - 1))
+    stream.synchronize()
+    for db in sets:
+        assert db.read_status() == 0, f"{w.name}: device status set"
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    graphs = {"step": [capture(lambda db=db: step(db)) for db in sets],
+              "decode": [capture(lambda db=db: xattn.check(db.decode())) for db in sets],
+              "beam_update": [capture(lambda db=db: xattn.check(db.beam_update(T - 1))) for db in sets]}
+    if w.max_shared_len > 0:
+        graphs["shared_stage_alone"] = [capture(lambda db=db: xattn.check(db.decode_shared())) for db in sets]
+    if not plan.fused:
+        graphs["merge_alone"] = [capture(lambda db=db: xattn.check(db.decode_merge())) for db in sets]
+
+    def timed(gs, K, W=3):
+        with torch.cuda.stream(stream):
+            for k in range(W):
+                if flush:
+                    flush_buf.zero_()
+                gs[k % nsets].replay()
+        stream.synchronize()
+        if not flush:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for k in range(K):
+                    gs[k % nsets].replay()
+                e1.record(stream)
+            e1.synchronize()
+            return e0.elapsed_time(e1) / K
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        with torch.cuda.stream(stream):
+            for k in range(K):
+                flush_buf.zero_()
+                ev[k][0].record(stream)
+                gs[k % nsets].replay()
+                ev[k][1].record(stream)
+        stream.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / K
+
+    est = timed(graphs["step"], 20)
+    K = int(max(200, min(20000, target_s / max(est * 1e-3, 1e-6))))
+    if flush:
+        K = min(K, 2000)
+    ms = {name: timed(gs, K if name == "step" else max(200, K // 2)) for name, gs in graphs.items()}
+    for db in sets:
+        assert db.read_status() == 0, f"{w.name}: device status set during timing"
+
+    idx_np = base.idx.cpu().numpy()
+    ub, ub_parts = unique_bytes(w, idx_np, inp.shared_len, elem)
+    flops = shared_stage_flops(w)
+    kernels = {}
+    if "shared_stage_alone" in ms:
+        M = w.beam_width * w.group_size
+        sbytes = sum(w.shared_lens) * w.num_kv_heads * w.head_dim * 2 * elem + \
+            w.num_requests * w.beam_width * w.num_q_heads * w.head_dim * elem + \
+            w.num_requests * w.num_kv_heads * plan.num_splits * M * (w.head_dim + 1) * 4
+        kernels["shared_stage_alone"] = (
+            "shared_stage_tc" if plan.shared_kernel == 1 else "shared_stage_simt", flops, sbytes,
+            "tensor" if plan.shared_kernel == 1 else "alu")
+    if "merge_alone" in ms:
+        kernels["merge_alone"] = ("ns_merge", 0.0, ns_merge_bytes(w, plan, idx_np, elem), None)
+    kernels["beam_update"] = ("beam_update", 0.0, beam_update_bytes(w, elem), None)
+    dom = max(kernels, key=lambda k: ms[k])
+    kname, kflops, kbytes, compute_kind = kernels[dom]
+    t_hbm = kbytes / (peaks["hbm_gbs"] * 1e9)
+    cpeak = peaks["bf16_tflops"] if compute_kind == "tensor" else FP32_ALU_TFLOPS
+    t_c = kflops / (cpeak * 1e12) if kflops > 0 else 0.0
+    s_k = ms[dom] * 1e-3
+    if t_c > t_hbm:
+        roof = {"kernel": kname, "stage": dom, "bound": compute_kind, "achieved": kflops / s_k / 1e12,
+                "peak": cpeak, "unit": "TFLOP/s", "frac": kflops / s_k / 1e12 / cpeak,
+                "algorithmic_per_launch": kflops,
+                "peak_source": f"{peak_src} (burst; kernel timed alone)" if compute_kind == "tensor" else
+                "fp32 FMA issue rate: 152 SMs x 128 lanes x 2 flop x 2.07 GHz"}
+    else:
+        roof = {"kernel": kname, "stage": dom, "bound": "hbm", "achieved": kbytes / s_k / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": kbytes / s_k / 1e9 / peaks["hbm_gbs"],
+                "algorithmic_per_launch": kbytes, "peak_source": f"{peak_src} (copy bandwidth)"}
+    src = {"shared_stage_tc": "shared_stage_tc.cu", "shared_stage_simt": "shared_stage_simt.cu",
+           "ns_merge": "ns_merge.cu", "beam_update": "beam_update.cu"}[kname]
+    roof["traffic"] = profile_traffic(src, w.name)
+    step_s = ms["step"] * 1e-3
+    t_bind = max(ub / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
+    entry = {
+        "config": config_of(w, {"shared_splits": plan.num_splits, "split_tokens": plan.split_tokens,
+                                "shared_kernel": {0: "none", 1: "tcgen05", 2: "cuda-core"}[plan.shared_kernel],
+                                "fused_ns_merge": bool(plan.fused), "dtype": "f32" if f32 else "bf16"}),
+        "l2": (f"L2 flushed (a {flush_buf.numel() * 4 / 1e6:.0f} MB write) before every timed step; per-step CUDA "
+               f"events" if flush else f"{nsets} rotating copies of the {set_bytes / 1e6:.0f} MB input set "
+                                       f"(> 2x the {l2 / 1e6:.0f} MB L2); CUDA graph replays between CUDA events"),
+        "steps_timed": K,
+        "us_per_step": ms["step"] * 1e3,
+        "beams_per_s": w.num_beams / step_s,
+        "attention_us_per_step": ms["decode"] * 1e3,
+        "stage_us": {k: v * 1e3 for k, v in ms.items() if k != "step"},
+        "hbm": {"unique_bytes_per_step": ub, "parts": ub_parts, "achieved_gbs": ub / step_s / 1e9,
+                "frac_of_8tbs": ub / step_s / 1e9 / NOMINAL_HBM_GBS,
+                "frac_of_peak": ub / step_s / 1e9 / peaks["hbm_gbs"]},
+        "tensor": {"shared_stage_flops": flops,
+                   "frac_of_peak": (flops / (ms["shared_stage_alone"] * 1e-3) / 1e12 / peaks["bf16_tflops"]
+                                    if "shared_stage_alone" in ms and plan.shared_kernel == 1 else None)},
+        "binding_roofline_frac": t_bind / step_s,
+        "roofline": roof,
+        "gpu_launches_per_step": launches_per_step(plan, T),
+    }
+    if cpu_budget_s > 0:
+        v, cores, sample = cpu_oracle_sample(w, inp, cpu_budget_s)
+        entry["cpu_baseline"] = {"value": v, "unit": "beams/s", "cores": cores, "kind": "oracle", "sample": sample}
+    del sets, graphs, base
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return entry
+
+
 def main():
     args = parse_args()
     from decode_attention_xattention_gb300 import workloads as wl
@@ -627,45 +825,92 @@ def main():
     #    inputs go up and step k-1's results come down (two slots of device inputs and
     #    outputs, one upload and one readback stream). Every step still copies its own
     #    inputs from pinned host memory and reads its own out / lse back.
-    up, down = torch.cuda.Stream(device=f"cuda:{local}"), torch.cuda.Stream(device=f"cuda:{local}")
+    # Two pipelined schedules. Both alternate two slots of device inputs and outputs, so
+    # that the upload of step k+1 and the readback of step k-1 overlap step k, and every step
+    # still copies its own inputs from pinned host memory and reads its own out / lse back.
+    #  eager: each step's calls issued from the host; one upload and one readback stream,
+    #         one copy per tensor.
+    #  graph: GRAPH_STEPS steps captured once as a CUDA graph (the library's calls are
+    #         capturable) and replayed; the upload is cut into ~1 MB pieces over NU streams
+    #         and the readback over ND, so several copy engines move them at once.
+    NU, ND, GRAPH_STEPS = 4, 2, 16
+    dev = f"cuda:{local}"
+    ups = [torch.cuda.Stream(device=dev) for _ in range(NU)]
+    downs = [torch.cuda.Stream(device=dev) for _ in range(ND)]
     slots = [{"q": torch.empty_like(db.q), "nk": torch.empty_like(d_nk), "nv": torch.empty_like(d_nv),
               "par": torch.empty_like(d_par), "out": torch.empty_like(db.out), "lse": torch.empty_like(db.lse)}
              for _ in range(2)]
     h_outs = [h_out, torch.empty_like(h_out).pin_memory()]
     h_lses = [h_lse, torch.empty_like(h_lse).pin_memory()]
-    up_done = [torch.cuda.Event() for _ in range(2)]
-    comp_done = [torch.cuda.Event() for _ in range(2)]
-    down_done = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_pipelined(n, collect=None):
+    def chunks(t, n):
+        return list(torch.chunk(t, n, dim=0)) if (n > 1 and t.shape[0] >= n) else [t]
+
+    def upload_plan(sl, nu, fine):
+        pieces = list(zip(chunks(sl["q"], w.num_requests if fine else 1), chunks(h_q, w.num_requests if fine else 1)))
+        pieces += list(zip(chunks(sl["nk"], 2 if fine else 1), chunks(h_nk, 2 if fine else 1)))
+        pieces += list(zip(chunks(sl["nv"], 2 if fine else 1), chunks(h_nv, 2 if fine else 1)))
+        pieces.append((sl["par"], h_par))
+        return [pieces[i::nu] for i in range(nu)]
+
+    def readback_plan(sl, ho, hl, nd, fine):
+        pieces = list(zip(chunks(ho, 2 * nd if fine else 1), chunks(sl["out"], 2 * nd if fine else 1)))
+        pieces.append((hl, sl["lse"]))
+        return [pieces[i::nd] for i in range(nd)]
+
+    def e2e_pipelined(n, collect=None, graph=False):
+        """Enqueue n pipelined steps (graph: NU / ND streams and fine pieces, for capture)."""
+        nu, nd = (NU, ND) if graph else (1, 1)
+        us_, ds_ = ups[:nu], downs[:nd]
+        up_done = [[torch.cuda.Event() for _ in range(nu)] for _ in range(2)]
+        comp_done = [torch.cuda.Event() for _ in range(2)]
+        down_done = [[torch.cuda.Event() for _ in range(nd)] for _ in range(2)]
+        start = torch.cuda.Event()
+        start.record(stream)
         for k in range(n):
-            sl = slots[k % 2]
-            up.wait_event(comp_done[k % 2])  # the slot's inputs were read by step k-2
-            with torch.cuda.stream(up):
-                sl["q"].copy_(h_q, non_blocking=True)
-                sl["nk"].copy_(h_nk, non_blocking=True)
-                sl["nv"].copy_(h_nv, non_blocking=True)
-                sl["par"].copy_(h_par, non_blocking=True)
-                up_done[k % 2].record(up)
-            stream.wait_event(up_done[k % 2])
-            stream.wait_event(down_done[k % 2])  # the slot's outputs were read back by step k-2
+            s = k % 2
+            sl = slots[s]
+            plan_up = upload_plan(sl, nu, graph)
+            for i, us in enumerate(us_):
+                us.wait_event(start if k < 2 else comp_done[s])  # the slot's inputs were read by step k-2
+                with torch.cuda.stream(us):
+                    for dst, src in plan_up[i]:
+                        dst.copy_(src, non_blocking=True)
+                    up_done[s][i].record(us)
+            for i in range(nu):
+                stream.wait_event(up_done[s][i])
+            if k >= 2:
+                for j in range(nd):
+                    stream.wait_event(down_done[s][j])  # the slot's outputs were read back by step k-2
             with torch.cuda.stream(stream):
                 xattn.check(xattn.xattn_beam_update(db.desc, sl["par"], sl["nk"], sl["nv"], db.pool_k, db.pool_v,
                                                     db.idx, T - 1, db.status, stream))
                 xattn.check(xattn.xattn_decode(db.desc, sl["q"], db.shared_k, db.shared_v, db.shared_len, db.pool_k,
                                                db.pool_v, db.idx, T, sl["out"], sl["lse"], db.workspace, db.ws_bytes,
                                                stream))
-                comp_done[k % 2].record(stream)
-            down.wait_event(comp_done[k % 2])
-            with torch.cuda.stream(down):
-                ho, hl = collect[k] if collect is not None else (h_outs[k % 2], h_lses[k % 2])
-                ho.copy_(sl["out"], non_blocking=True)
-                hl.copy_(sl["lse"], non_blocking=True)
-                down_done[k % 2].record(down)
+                comp_done[s].record(stream)
+            ho, hl = collect[k] if collect is not None else (h_outs[s], h_lses[s])
+            plan_dn = readback_plan(sl, ho, hl, nd, graph)
+            for j, ds in enumerate(ds_):
+                ds.wait_event(comp_done[s])
+                with torch.cuda.stream(ds):
+                    for dst, src in plan_dn[j]:
+                        dst.copy_(src, non_blocking=True)
+                    down_done[s][j].record(ds)
+        for x in us_ + ds_:  # join every side stream back into `stream`
+            ev = torch.cuda.Event()
+            ev.record(x)
+            stream.wait_event(ev)
+
+    def capture_pipeline(n, collect=None):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            e2e_pipelined(n, collect, graph=True)
+        return g
 
     def pipelined_e2e_checked_and_timed():
-        """Bitwise check of the pipelined schedule against the serial one, then its
-        timing; returns (check passed, ms per step or None)."""
+        """Bitwise check of both pipelined schedules against the serial one, then their
+        timings; returns (checks passed, eager ms per step, graph ms per step)."""
         torch.cuda.synchronize()
         state = [t.clone() for t in (db.pool_k, db.pool_v, db.idx)]
         n_chk = 6
@@ -675,37 +920,63 @@ def main():
                 e2e_step()
                 stream.synchronize()
                 serial.append((h_out.clone(), h_lse.clone()))
-        for t, s0 in zip((db.pool_k, db.pool_v, db.idx), state):
-            t.copy_(s0)
-        torch.cuda.synchronize()
+
+        def restore():
+            torch.cuda.synchronize()
+            for t, s0 in zip((db.pool_k, db.pool_v, db.idx), state):
+                t.copy_(s0)
+            torch.cuda.synchronize()
+
+        def same(piped):
+            return all(torch.equal(a[0], b_[0]) and torch.equal(a[1], b_[1]) for a, b_ in zip(serial, piped))
+
+        restore()
         piped = [(torch.empty_like(h_out).pin_memory(), torch.empty_like(h_lse).pin_memory()) for _ in range(n_chk)]
         e2e_pipelined(n_chk, piped)
         torch.cuda.synchronize()
-        pipe_ok = all(torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]) for a, b in zip(serial, piped))
-        pipe_ok = pipe_ok and db.read_status() == 0
-        ms_pipe = None
-        if pipe_ok:
+        ok_eager = same(piped) and db.read_status() == 0
+        restore()
+        piped_g = [(torch.empty_like(h_out).pin_memory(), torch.empty_like(h_lse).pin_memory()) for _ in range(n_chk)]
+        gchk = capture_pipeline(n_chk, piped_g)
+        gchk.replay()
+        torch.cuda.synchronize()
+        ok_graph = same(piped_g) and db.read_status() == 0
+        ms_eager = ms_graph = None
+        if ok_eager:
             e2e_pipelined(W)
             torch.cuda.synchronize()
-            if world > 1:
-                dist.barrier()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(up)  # before the first upload
-            e2e_pipelined(Ke)
-            e1.record(down)  # after the last readback, which follows every other step of the run
+            e0.record(stream)
+            e2e_pipelined(Ke)  # every side stream joins `stream` at the end
+            e1.record(stream)
             e1.synchronize()
+            ms_eager = max_over_ranks(e0.elapsed_time(e1) / Ke, f"cuda:{local}")
+        if ok_graph:
+            gt = capture_pipeline(GRAPH_STEPS)
+            for _ in range(2):
+                gt.replay()
             torch.cuda.synchronize()
-            ms_pipe = max_over_ranks(e0.elapsed_time(e1) / Ke, f"cuda:{local}")
-        return pipe_ok, ms_pipe
+            reps = max(4, Ke // GRAPH_STEPS)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                gt.replay()
+            e1.record(stream)
+            e1.synchronize()
+            ms_graph = max_over_ranks(e0.elapsed_time(e1) / (reps * GRAPH_STEPS), f"cuda:{local}")
+        return (ok_eager, ok_graph), ms_eager, ms_graph
 
     # self-check before timing: the pipelined steps give, bit for bit, the serial steps'
     # results from the same starting state (the kernels are deterministic)
-    pipe_ok, ms_pipe, pipe_err = False, None, None
+    oks, ms_pipe, ms_graph, pipe_err = (False, False), None, None, None
     try:
-        pipe_ok, ms_pipe = pipelined_e2e_checked_and_timed()
+        oks, ms_pipe, ms_graph = pipelined_e2e_checked_and_timed()
     except Exception as ex:  # reported in the JSON line; the serial figure stands
         torch.cuda.synchronize()
-        pipe_err = repr(ex)[:200]
+        pipe_err = repr(ex)[:300]
+    e2e_candidates = [("serial", ms_e2e)] + ([("eager_pipelined", ms_pipe)] if ms_pipe else []) + \
+        ([("graph_pipelined", ms_graph)] if ms_graph else [])
+    e2e_kind, e2e_ms = min(e2e_candidates, key=lambda kv: kv[1])
 
     # -- derived figures ------------------------------------------------------------------
     beams = w.num_beams * world
@@ -747,7 +1018,9 @@ def main():
         "attention_us_per_step": ms_decode * 1e3,
         "stage_us": {"beam_update": ms_bu * 1e3, "decode": ms_decode * 1e3, "shared_stage_alone": ms_dom * 1e3,
                      "merge_alone": ms_merge * 1e3,
-                     "note": ("decode = Non-Shared piece kernel + Shared-stage kernel with merging epilogue"
+                     "note": ("decode = one Shared-stage kernel that also gathers and attends to the "
+                              "Non-Shared part" if plan.ns_tile else
+                              "decode = Non-Shared piece kernel + Shared-stage kernel with merging epilogue"
                               if plan.fused else "decode = Shared-stage kernel + Non-Shared/Merge kernel")},
         "hbm": {"unique_bytes_per_step": ub, "parts": ub_parts, "achieved_gbs": hbm_gbs,
                 "frac_of_8tbs": hbm_gbs / NOMINAL_HBM_GBS, "frac_of_peak": hbm_gbs / peaks["hbm_gbs"],
@@ -760,15 +1033,18 @@ def main():
                      "unit": unit, "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} (burst; kernel timed alone)",
                      "algorithmic_per_launch": flops if bound == "tensor" else sbytes},
-        "e2e": {"value": whole_job_beams_per_s(w.num_beams, world, ms_pipe if ms_pipe else ms_e2e),
+        "e2e": {"value": whole_job_beams_per_s(w.num_beams, world, e2e_ms),
                 "unit": "beams/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": ms_pipe if ms_pipe else ms_e2e,
-                "schedule": ("pipelined: upload of step k+1 and readback of step k-1 overlap step k "
-                             "(two slots, three streams)") if ms_pipe else
-                            "serial (the pipelined schedule did not reproduce the serial results)",
-                "serial_ms_per_step": ms_e2e,
-                "pipeline_check": ("bitwise equal to the serial schedule over 6 steps" if pipe_ok else
-                                   ("error: " + pipe_err if pipe_err else "failed"))},
+                "ms_per_step": e2e_ms, "schedule": {
+                    "serial": "each step: upload, beam update + decode, readback, one stream, calls from the host",
+                    "eager_pipelined": "upload of step k+1 and readback of step k-1 overlap step k (two slots, one "
+                                       "upload and one readback stream), calls from the host",
+                    "graph_pipelined": f"the same pipeline, {GRAPH_STEPS} steps captured once as a CUDA graph and "
+                                       f"replayed; uploads in ~1 MB pieces over {NU} streams, readback over {ND}"}[e2e_kind],
+                "serial_ms_per_step": ms_e2e, "eager_pipelined_ms_per_step": ms_pipe,
+                "graph_pipelined_ms_per_step": ms_graph,
+                "pipeline_check": (f"bitwise equal to the serial schedule over 6 steps: eager {oks[0]}, graph {oks[1]}"
+                                   if pipe_err is None else "error: " + pipe_err)},
         "gpu_launches": launches_per_step(plan, T) * K,
         "clocks": clocks,
     }
@@ -779,6 +1055,26 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample = cpu_oracle_sample(w, inputs[0], args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "beams/s", "cores": cores, "kind": "oracle", "sample": sample}
+        v1, _, sample1 = cpu_oracle_sample(w, inputs[0], args.cpu_seconds / 2, nthreads=1)
+        line["cpu_baseline_1core"] = {"value": v1, "unit": "beams/s", "cores": 1, "kind": "oracle",
+                                      "sample": sample1}
+
+    # -- every other workload of the measured configuration list, each on its own ----------
+    if world == 1 and not args.no_configs:
+        del g_step, g_bu, g_decode, g_dominant, g_merge, sets, slots
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        names = [n for n in CONFIG_ORDER if n != w.name]
+        if args.configs:
+            names = [n for n in names if any(n.startswith(p) for p in args.configs.split(","))]
+        sampler = ClockSampler(local)
+        sampler.start()
+        line["configs"] = {}
+        for name in names:
+            line["configs"][name] = measure_config(
+                wl.ALL[name], local, stream, peaks, peak_src, l2,
+                0.0 if (args.no_cpu_baseline or rank != 0) else args.config_cpu_seconds)
+        line["configs_clocks"] = sampler.stop()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -1,5 +1,5 @@
 // Shared stage on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), sm_103a,
-// optionally with the Merge in its epilogue.
+// optionally with the Non-Shared stage and the Merge in the same kernel.
 //
 // xGR: Efficient Generative Recommendation Serving at Scale, section 2.1 (xAttention): the
 // prompt KV is stored once per request, so the Shared stage serves every beam of a
@@ -23,11 +23,24 @@
 // max is raised only when it grows by more than 2^8, so O is rescaled rarely and every P
 // stays below 2^8.
 //
-// Epilogue. When the prefix is one piece and the Non-Shared part is short, xattn_decode
-// first runs the Non-Shared kernel, which leaves each row's Non-Shared (normalised output,
-// LSE) as a piece in the workspace; this kernel's epilogue then merges that piece with its
-// O (log-sum-exp rule) and writes the final output and LSE. Otherwise it writes the
-// prefix piece's normalised output and LSE for the separate Merge kernel.
+// P enters the P.V product rounded to bf16 while the row sum adds the unrounded values. A
+// row dominated by one key would then carry that key's rounding error (up to 2^-9
+// relative) straight into its output, so each row also tracks its largest score (and the
+// reference max its p was computed with), and the output is normalised by the row sum with
+// that one term rounded as the tensor core saw it; the LSE keeps the exact row sum.
+//
+// Non-Shared part, three ways:
+//   * in the tile (xattn_decode, one prefix piece, (128/G) x step <= 128): each softmax
+//     warpgroup first copies its row tile's Non-Shared K/V rows from the pool (through the
+//     ancestry index) into the two unit slots, laid out like a prefix K/V tile (key c of row tile i
+//     = token c % step of its beam c / step). Each row tile attends to that tile first, with
+//     every key outside its own beam's masked, and then to the prefix tiles: the online
+//     softmax merges the two parts, and the epilogue writes out / lse.
+//   * staged (one prefix piece, longer Non-Shared parts): the Non-Shared kernel runs first
+//     and leaves each row's (normalised output, LSE) as a piece in the workspace; the
+//     epilogue merges it with O (log-sum-exp rule) and writes out / lse.
+//   * separate: this kernel writes the prefix piece's normalised output and LSE for the
+//     Merge kernel.
 //
 // Every on-chip wait is bounded: on a timeout the CTA records XATTN_STATUS_TIMEOUT, writes
 // NaN, waits (bounded) for its own TMA copies and MMAs, frees TMEM and returns.
@@ -39,9 +52,10 @@ namespace {
 
 using namespace ptx;
 
-// Warp roles: 0-7 two softmax warpgroups; 8 TMA producer; 9 MMA issuer (and TMEM owner).
-// Every role that spins on an mbarrier has a warp of its own: divergent lanes of one warp
-// run one path at a time, so a spinning lane would starve its neighbours.
+// Warp roles: 0-7 two softmax warpgroups (which first gather their row tile's Non-Shared
+// rows, in-tile mode); 8 TMA producer; 9 MMA issuer (and TMEM owner). Every role that spins
+// on an mbarrier has a warp of its own: divergent lanes of one warp run one path at a time,
+// so a spinning lane would starve its neighbours.
 constexpr int kThreads = 320;
 constexpr int kWarpLoad = 8, kWarpMma = 9;
 constexpr int kMaxStages = 4;
@@ -56,7 +70,10 @@ constexpr uint32_t kNaN = 0x7fc00000u;
 // (Q.K^T), so the producer loads them together as load unit j = {K(j), V(j-1)} under one
 // mbarrier: one data wait per tile on the MMA warp. Two unit slots at d = 128 (four at
 // d = 64), each one K tile and one V tile; the shared memory admits one CTA per SM, so a
-// CTA never waits for another's 512 TMEM columns.
+// CTA never waits for another's 512 TMEM columns. With the Non-Shared part in the tile,
+// units 0 and 1 are the gathered Non-Shared K tiles (both row tiles) and V tiles (their own
+// barriers, one per row tile), and the prefix units follow as units 2, 3, ...; the full
+// barrier of slot 0 or 1 then sees its first TMA unit as phase 0.
 template <int D>
 struct Cfg {
     static constexpr int kUnits = D == 64 ? 4 : 2;
@@ -111,22 +128,30 @@ struct Bars {
     uint64_t u_full[kMaxStages], u_empty[kMaxStages];
     uint64_t s_full[2], p_full[2], q_ready[2];
     uint64_t o_full[2], final_mma;
-    uint64_t q_free, ns_full[2];  // last Q.K^T done; Non-Shared piece of row tile i staged
+    uint64_t q_free, ns_full[2];  // last Q.K^T done; staged Non-Shared piece of row tile i in place
+    uint64_t ns_kfull[2], ns_vfull[2];  // in-tile mode: row tile i's gathered K / V rows (and flags) in place
 };
 
-// Fused epilogue: fold the Non-Shared piece (written into the workspace by the
-// Non-Shared kernel that runs just before, when step > 0) into O and write out / lse.
+// Epilogue mode and the Non-Shared inputs of the fused decode.
 struct FusedArgs {
     void* out;
     float* lse;
-    int enabled;
+    int enabled;  // write out / lse (else the prefix piece's partial result)
+    int ns_tile;  // with enabled and step > 0: the Non-Shared part is gathered into tile 0
+    const __nv_bfloat16* pool_k;
+    const __nv_bfloat16* pool_v;
+    const int32_t* idx;
 };
 
-template <int D>
+// NST: the in-tile Non-Shared mode, compiled as its own instantiation so that the other
+// modes' loops carry none of its branches (the MMA-issuing thread shares its issue slots
+// with two softmax warps, and every instruction in its loop shows in the tile period).
+template <int D, bool NST>
 __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-    const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_ns, Geometry g, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ shared_len,
-    float* __restrict__ part_o, float* __restrict__ part_lse, int32_t* status, FusedArgs fa) {
+    const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_ns, Geometry g,
+    const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ shared_len, float* __restrict__ part_o,
+    float* __restrict__ part_lse, int32_t* status, FusedArgs fa) {
     using C = Cfg<D>;
     constexpr int kU = C::kUnits;
     extern __shared__ uint8_t smem_raw[];
@@ -136,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     __shared__ Bars bars;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
+    __shared__ uint32_t bad_beam[2][4];  // in-tile Non-Shared part: local beams with a bad ancestry slot
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -153,8 +179,15 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     const int L = bad_len ? 0 : L_raw;
     const int t0 = c * g.split_tokens;
     const int t1 = min(t0 + g.split_tokens, L);
-    const int ntiles = t1 > t0 ? (t1 - t0 + kTcTileKeys - 1) / kTcTileKeys : 0;
+    const int ntiles = t1 > t0 ? (t1 - t0 + kTcTileKeys - 1) / kTcTileKeys : 0;  // prefix tiles
     const int ntile_m = (2 * mp + 1 < g.row_tiles) ? 2 : 1;  // row tiles this CTA owns
+    // In-tile Non-Shared part (uniform over the grid): (128 / G) beams per row tile, `step`
+    // keys each, at most 128 keys (checked by the host).
+    constexpr bool ns = NST;  // the host launches this instantiation only for fused decodes with step > 0
+    const int nb = kTileRows / g.G;
+    const int nk = ns ? nb * g.step : 0;
+    const int nt = ntiles + (ns ? 1 : 0);  // tiles every row tile attends to (tile 0: Non-Shared)
+    const int u0 = ns ? 2 : 0;             // unit index of prefix unit 0
 
     if (tid == 0) {
         for (int s = 0; s < kU; ++s) {
@@ -172,10 +205,15 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         mbar_init(&bars.q_free, 1);
         mbar_init(&bars.ns_full[0], 1);
         mbar_init(&bars.ns_full[1], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.ns_kfull[i], 4);  // one arrival per warp of the gathering warpgroup
+            mbar_init(&bars.ns_vfull[i], 4);
+        }
         abort_sh = 0;
         fence_barrier_init();
     }
-    if (warp == kWarpMma && ntiles > 0) {
+    if (tid < 8) bad_beam[tid >> 2][tid & 3] = 0u;
+    if (warp == kWarpMma && nt > 0) {
         tmem_alloc(&tmem_base_sh, kTmemCols);
         tmem_relinquish();
     }
@@ -194,23 +232,80 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         const bool row_ok = tile_ok && row < g.M;
         const int b = row / g.G, gg = row - (row / g.G) * g.G;
         float m_run = -INFINITY, l_run = 0.f;
+        // the row's largest raw score so far and the reference max its p was computed with
+        float s_top = -INFINITY, m_top = 0.f;
         bool ok = true;
-        if (tile_ok && ntiles > 0) {
+        if (ns && tile_ok) {
+            // ---- Non-Shared gather of this warpgroup's row tile (in-tile mode). Key c < nk is
+            // token c % step of the tile's local beam c / step; its K row goes to row c of the
+            // K tile in slot 0 (row tile i at i * kTileBytes), its V row to the same row of the
+            // V tile in slot 1, in the 128-byte-swizzled layout TMA gives a prefix tile (16-byte
+            // chunk x of row c at chunk x ^ (c % 8)). Thread rloc copies chunk rloc % CH of
+            // keys rloc / CH + KPS * j. A slot outside the pool is not read: the row is zeroed,
+            // the beam marked bad (NaN output) and XATTN_STATUS_BAD_SLOT set.
+            constexpr int CH = D / 8;       // 16-byte chunks per row
+            constexpr int KPS = 128 / CH;   // keys per sweep of the warpgroup
+            constexpr int NSW = kTcTileKeys / KPS;
+            const int ch = rloc % CH, kb0 = rloc / CH;
+            const int b0 = mt * nb;
+            int sl[NSW];  // the slots first, every load in flight at once
+#pragma unroll
+            for (int j = 0; j < NSW; ++j) {
+                const int cc = kb0 + KPS * j, bl = cc / g.step, bg = b0 + bl;
+                sl[j] = (cc < nk && bg < g.BW) ? __ldg(fa.idx + ((size_t)r * g.BW + bg) * g.Tmax + (cc - bl * g.step))
+                                               : -1;
+                if (ch == 0 && cc < nk && bg < g.BW && (sl[j] < 0 || sl[j] >= g.S)) {
+                    atomicOr(&bad_beam[wg][bl >> 5], 1u << (bl & 31));
+                    set_status(status, XATTN_STATUS_BAD_SLOT);
+                }
+            }
+            const uint32_t toff = (uint32_t)wg * C::kTileBytes + (ch >> 3) * 16384;
+#pragma unroll
+            for (int pass = 0; pass < 2; ++pass) {  // K rows, then V rows (two commit groups)
+                const __nv_bfloat16* pool = pass == 0 ? fa.pool_k : fa.pool_v;
+                const uint32_t dt = smem_addr(sU) + pass * C::kUnitBytes + toff;
+#pragma unroll
+                for (int j = 0; j < NSW; ++j) {
+                    const int cc = kb0 + KPS * j;
+                    if (cc < nk) {
+                        const uint32_t dst = dt + cc * 128 + (((ch & 7) ^ (cc & 7)) << 4);
+                        if (sl[j] >= 0 && sl[j] < g.S)
+                            cp_async_16(dst, pool + (((size_t)r * g.S + sl[j]) * g.Hkv + h) * D + ch * 8);
+                        else
+                            st_shared_zero16(dst);
+                    } else if (pass == 1 && cc < ((nk + 15) & ~15)) {
+                        // V rows past the last key, up to the end of its 16-key step: zero
+                        st_shared_zero16(dt + cc * 128 + (((ch & 7) ^ (cc & 7)) << 4));
+                    }
+                }
+                cp_async_commit_group();
+            }
+            cp_async_wait_group<1>();  // this thread's K rows have landed
+            fence_proxy_async_smem();  // ... and are visible to the tensor core
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.ns_kfull[wg]);
+            cp_async_wait_group<0>();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.ns_vfull[wg]);
+        }
+        if (tile_ok && nt > 0) {
             const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
             const uint32_t tS = tmem + lane_base + wg * 128;
             const uint32_t tO = tmem + lane_base + kTmemO + wg * 128;
-            for (int j = 0; j < ntiles; ++j) {
-                if (!mbar_wait_warp(&bars.s_full[wg], j & 1, &abort_sh)) { ok = false; break; }
+            // One tile: its S row in, P (bf16) back over it, running max and sum, O rescaled when
+            // the max moved; valid columns [lo, lo + cnt), the rest get -inf.
+            auto tile = [&](uint32_t parity, unsigned lo, unsigned cnt, bool first) -> bool {
+                if (!mbar_wait_warp(&bars.s_full[wg], parity, &abort_sh)) return false;
                 tc_fence_after();
-                const int lim = t1 - (t0 + j * kTcTileKeys);  // valid columns of this tile (>= 1)
                 // the whole 128-column row of S in registers with one wide load
                 uint32_t s[kTcTileKeys];
                 tmem_ld128(tS, s);
                 tmem_wait_ld();
-                if (lim < kTcTileKeys) {  // ragged last tile: columns past the prefix get -inf
+                if (lo != 0u || cnt < (unsigned)kTcTileKeys) {
 #pragma unroll
                     for (int i = 0; i < kTcTileKeys; ++i)
-                        if (i >= lim) s[i] = 0xff800000u;
+                        if ((unsigned)i - lo >= cnt) s[i] = 0xff800000u;
                 }
                 float mx;
                 {  // row max: eight independent chains of three-input max
@@ -226,8 +321,12 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 const bool resc = m_new > m_run + kRescaleThreshold;
                 const float alpha = resc ? ex2(m_run - m_new) : 1.f;
                 const float m_use = resc ? m_new : m_run;
+                if (mx > s_top) {  // the row's largest p so far is this tile's
+                    s_top = mx;
+                    m_top = m_use;
+                }
                 // P = exp2(S*scale*log2e - m) as bf16, written over the consumed S columns
-                // (columns past the prefix hold -inf, so their P is exactly 0).
+                // (masked columns hold -inf, so their P is exactly 0).
                 // (column pairs through the packed fp32x2 FMA and add: fewer issue slots, which
                 // the MMA warp on the same sub-partition needs)
                 const uint64_t scale2 = f2_pack(g.scale_log2, g.scale_log2);
@@ -247,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 const float tile_sum = (sa.x + sb.x) + (sa.y + sb.y);
                 l_run = l_run * alpha + tile_sum;
                 m_run = m_use;
-                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                if (!first && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
                     for (int k = 0; k < D / 32; ++k) {
                         uint32_t o[32];
@@ -262,16 +361,32 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars.p_full[wg]);  // one arrival per warp
-            }
+                return true;
+            };
+            // In-tile mode: the Non-Shared tile first (only this row's beam's `step` keys count),
+            // then the prefix tiles; a ragged last prefix tile ends at the prefix.
+            if (ns) ok = tile(0u, (unsigned)((rloc / g.G) * g.step), (unsigned)g.step, true);
+            for (int j = 0; ok && j < ntiles; ++j)
+                ok = tile((uint32_t)(j + (ns ? 1 : 0)) & 1u, 0u,
+                          (unsigned)min(kTcTileKeys, t1 - (t0 + j * kTcTileKeys)), !ns && j == 0);
         }
         const uint32_t tO = tmem + ((uint32_t)((warp & 3) * 32) << 16) + kTmemO + wg * 128;
-        const bool have_o = tile_ok && ntiles > 0;  // O_i holds accumulated P.V (TMEM allocated)
+        const bool have_o = tile_ok && nt > 0;  // O_i holds accumulated P.V (TMEM allocated)
+        // O is normalised by the row sum with its largest term as the tensor core saw it: that
+        // p recomputed with the element's own arithmetic, its bf16 rounding error carried to the
+        // final reference max.
+        float l_nrm = l_run;
+        if (s_top > -INFINITY) {
+            const float pt = ex2(fmaf(s_top, g.scale_log2, -m_top));
+            l_nrm += (__bfloat162float(__float2bfloat16_rn(pt)) - pt) * ex2(m_top - m_run);
+        }
 
-        // Fused path: the Non-Shared piece of this row. With prefix tiles it is staged in shared
-        // memory by the producer (tile 0 over the Q tiles, tile 1 over the last unit's slot);
-        // its LSE is loaded before the wait for the last P.V.
-        const bool fused_ns = fa.enabled && row_ok && g.step > 0;
-        const bool ns_staged = fa.enabled && g.step > 0 && have_o;  // warp-uniform
+        // Staged Non-Shared piece of this row (Non-Shared kernel ran first). With prefix tiles it
+        // is staged in shared memory by the producer (tile 0 over the Q tiles, tile 1 over the
+        // last unit's slot); its LSE is loaded before the wait for the last P.V.
+        const bool staged = fa.enabled && g.step > 0 && !ns;
+        const bool fused_ns = staged && row_ok;
+        const bool ns_staged = staged && have_o;  // warp-uniform
         const size_t nsrow = ((size_t)unit * g.pieces + g.nsplit) * g.M + row;
         const uint8_t* ns_sm = (wg == 0 ? sQ : sU + ((ntiles - 1) % kU) * C::kUnitBytes) + rloc * 128;
         float lns = -INFINITY;
@@ -279,22 +394,25 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             grid_dependency_wait();  // the Non-Shared kernel launched before this one has finished
             lns = __ldg(part_lse + nsrow);
         }
+        bool beam_bad = false;
         if (have_o) {
             if (ok && !mbar_wait_warp(&bars.o_full[wg], 0, &abort_sh)) ok = false;
             if (ok && ns_staged && !mbar_wait_warp(&bars.ns_full[wg], 0, &abort_sh)) ok = false;
+            if (ok && ns && !mbar_wait_warp(&bars.ns_vfull[wg], 0, &abort_sh)) ok = false;  // bad_beam written
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
             if (!ok) {
                 abort_sh = 1;
                 if (lane == 0) set_status(status, XATTN_STATUS_TIMEOUT);
+            } else if (ns) {
+                const int bl = rloc / g.G;
+                beam_bad = ((bad_beam[wg][bl >> 5] >> (bl & 31)) & 1u) != 0;
             }
         }
 
         if (fa.enabled) {
-            // ---------------------------------------- Merge with the Non-Shared piece
-            // The Non-Shared kernel ran before this one and left each row's normalised
-            // output o_ns and natural-log lse_ns at piece `nsplit` of the workspace.
-            bool bad = !ok || bad_len;
+            // ---------------------------------------- final output (merged with a staged piece)
+            bool bad = !ok || bad_len || beam_bad;
             if (tile_ok && rloc == 0 && mt == 0 && h == 0 && bad_len) set_status(status, XATTN_STATUS_BAD_SHARED_LEN);
             const size_t qrow = ((size_t)r * g.BW + b) * g.Hq + (size_t)h * g.G + gg;
             float m_tot = m_run, w_ns = 0.f, alpha = 1.f;
@@ -309,9 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 bad = true;
                 set_status(status, XATTN_STATUS_EMPTY_ROW);
             }
-            const float l_tot = l_run * alpha + w_ns;
+            const float l_tot = l_run * alpha + w_ns;  // exact: the LSE
             bad = bad || !(l_tot > 0.f);
-            const float inv = bad ? __uint_as_float(kNaN) : 1.f / l_tot;
+            const float inv = bad ? __uint_as_float(kNaN) : 1.f / (l_nrm * alpha + w_ns);
             const size_t obase = qrow * D;
 #pragma unroll
             for (int k = 0; k < D / 32; ++k) {
@@ -361,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         } else if (tile_ok) {
             // ---------------------------------------- this piece's partial result
             const size_t prow = ((size_t)unit * g.pieces + c) * g.M + row;
-            const float inv = !ok ? __uint_as_float(kNaN) : (ntiles > 0 ? 1.f / l_run : 0.f);
+            const float inv = !ok ? __uint_as_float(kNaN) : (ntiles > 0 ? 1.f / l_nrm : 0.f);
 #pragma unroll 1
             for (int k = 0; k < D / 32; ++k) {
                 uint32_t o[32];
@@ -386,10 +504,10 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         }
     } else if (warp == kWarpLoad) {
         // ============================================ TMA producer
-        // Load unit j = {K(j) if j < ntiles, V(j-1) if j >= 1} into slot j % kU as soon as
-        // unit j - kU has been consumed; L2 prefetch kPrefetch units ahead hides most of the
-        // HBM latency of the later load.
-        if (lane == 0 && ntiles > 0) {
+        // Prefix unit p = {K(p) if p < ntiles, V(p-1) if p >= 1} (unit index u0 + p) goes into
+        // slot (u0 + p) % kU as soon as the unit kU before it has been consumed; L2 prefetch
+        // kPrefetch units ahead hides most of the HBM latency of the later load.
+        if (lane == 0 && nt > 0) {
             // the Q tiles first: per row tile one 64 d x G heads x 128/G beams box per 64 d
             // (128-byte swizzle, the K-major layout the MMA reads); beams past BW are zero-filled
             prefetch_tmap(&tmap_q);
@@ -401,37 +519,40 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             }
             prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
-            const int nunits = ntiles + 1;
-            auto prefetch_unit = [&](int j) {
+            const int npu = ntiles > 0 ? ntiles + 1 : 0;  // prefix units
+            auto prefetch_unit = [&](int p) {
                 for (int kb = 0; kb < C::KB; ++kb) {
-                    if (j < ntiles) tma_prefetch_4d(&tmap_k, kb * 64, h, t0 + j * kTcTileKeys, r);
-                    if (j >= 1) tma_prefetch_4d(&tmap_v, kb * 64, h, t0 + (j - 1) * kTcTileKeys, r);
+                    if (p < ntiles) tma_prefetch_4d(&tmap_k, kb * 64, h, t0 + p * kTcTileKeys, r);
+                    if (p >= 1) tma_prefetch_4d(&tmap_v, kb * 64, h, t0 + (p - 1) * kTcTileKeys, r);
                 }
             };
+            // With the Non-Shared tile first, the first prefix loads wait for slots the gathered
+            // tile still holds: bring the first prefix units into L2 meanwhile.
+            if (ns)
+                for (int p = 0; p < min(npu, kPrefetch); ++p) prefetch_unit(p);
             int issued = 0;
-            for (int j = 0; j < nunits; ++j) {
-                const int st = j % kU, use = j / kU;
+            for (int p = 0; p < npu; ++p) {
+                const int u = u0 + p, st = u % kU, use = u / kU;
                 if (use > 0 && !mbar_wait(&bars.u_empty[st], (use - 1) & 1, &abort_sh)) break;
-                if (j >= kU && j + kPrefetch < nunits) prefetch_unit(j + kPrefetch);
+                if (ns ? (p + kPrefetch < npu) : (p >= kU && p + kPrefetch < npu)) prefetch_unit(p + kPrefetch);
                 uint8_t* slot = sU + st * C::kUnitBytes;
-                mbar_arrive_expect_tx(&bars.u_full[st],
-                                      (j < ntiles ? C::kTileBytes : 0) + (j >= 1 ? C::kTileBytes : 0));
+                mbar_arrive_expect_tx(&bars.u_full[st], (p < ntiles ? C::kTileBytes : 0) + (p >= 1 ? C::kTileBytes : 0));
                 for (int kb = 0; kb < C::KB; ++kb) {
-                    if (j < ntiles)
-                        tma_load_4d(slot + kb * 16384, &tmap_k, &bars.u_full[st], kb * 64, h, t0 + j * kTcTileKeys, r);
-                    if (j >= 1)
+                    if (p < ntiles)
+                        tma_load_4d(slot + kb * 16384, &tmap_k, &bars.u_full[st], kb * 64, h, t0 + p * kTcTileKeys, r);
+                    if (p >= 1)
                         tma_load_4d(slot + C::kTileBytes + kb * 16384, &tmap_v, &bars.u_full[st], kb * 64, h,
-                                    t0 + (j - 1) * kTcTileKeys, r);
+                                    t0 + (p - 1) * kTcTileKeys, r);
                 }
-                issued = j + 1;
-                if (j == kU - 1)  // the first units' loads went out before any L2 prefetch
-                    for (int jp = kU; jp < min(nunits, kU + kPrefetch); ++jp) prefetch_unit(jp);
+                issued = p + 1;
+                if (!ns && p == kU - 1)  // the first units' loads went out before any L2 prefetch
+                    for (int pp = kU; pp < min(npu, kU + kPrefetch); ++pp) prefetch_unit(pp);
             }
-            // Fused decode: stage each row tile's Non-Shared piece (128 rows x d fp32, as 128-byte
+            // Staged Non-Shared piece: each row tile's piece (128 rows x d fp32, as 128-byte
             // swizzled boxes of 32 columns) for the epilogue: row tile 0 into the Q tiles once the
             // last Q.K^T is done, row tile 1 into the slot of unit ntiles - 1 once it is consumed.
             bool ns_issued[2] = {false, false};
-            if (fa.enabled && g.step > 0 && issued == nunits) {
+            if (fa.enabled && g.step > 0 && !ns && issued == npu) {
                 grid_dependency_wait();  // the Non-Shared kernel launched before this one has finished
                 for (int i = 0; i < ntile_m; ++i) {
                     const int jl = ntiles - 1, st = jl % kU;
@@ -447,26 +568,31 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             }
             if (abort_sh) {  // let the copies still in flight land before the CTA exits
                 volatile int never = 0;
-                for (int j = max(0, issued - kU); j < issued; ++j) mbar_wait(&bars.u_full[j % kU], (j / kU) & 1, &never);
+                for (int p = max(0, issued - kU); p < issued; ++p) {
+                    const int u = u0 + p;
+                    mbar_wait(&bars.u_full[u % kU], (u / kU - ((ns && u % kU < 2) ? 1 : 0)) & 1, &never);
+                }
                 for (int i = 0; i < ntile_m; ++i) mbar_wait(&bars.q_ready[i], 0, &never);
                 for (int i = 0; i < 2; ++i)
                     if (ns_issued[i]) mbar_wait(&bars.ns_full[i], 0, &never);
             }
         }
-    } else {
+    } else if (warp == kWarpMma) {
         // ============================================ MMA issuer
-        if (lane == 0 && ntiles > 0) {
+        if (lane == 0 && nt > 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kTcTileKeys, 0, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
             bool ok = mbar_wait(&bars.q_ready[0], 0, &abort_sh);
             if (ok && ntile_m > 1) ok = mbar_wait(&bars.q_ready[1], 0, &abort_sh);
             tc_fence_after();
-            // The last tile may be ragged: its P columns past the prefix are exact zeros, the
-            // P.V product stops at the 16-token step holding the last valid token, and the
-            // V rows of that step past the prefix are zeroed, so whatever the cache holds
-            // there (even NaN) never reaches O.
-            const int lim_last = t1 - (t0 + (ntiles - 1) * kTcTileKeys);
+            // The last prefix tile may be ragged: its P columns past the prefix are exact zeros,
+            // the P.V product stops at the 16-token step holding the last valid token, and the
+            // V rows of that step past the prefix are zeroed, so whatever the cache holds there
+            // (even NaN) never reaches O. The gathered Non-Shared V tile has its rows past the
+            // last key of the last 16-key step zeroed by the gather warp.
+            const int lim_last = ntiles > 0 ? t1 - (t0 + (ntiles - 1) * kTcTileKeys) : 0;
             const int pv_steps_last = (lim_last + 15) / 16;
+            const int ns_steps = (nk + 15) / 16;
             // Descriptors are built once; an operand's descriptor for a byte offset only adds
             // offset / 16 to the start-address field (addresses stay below 256 KB, so no carry
             // leaves the field): few instructions per MMA for a thread that shares its issue
@@ -481,36 +607,44 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 for (int kk = 0; kk < kTcTileKeys / 16; ++kk) {
                     if (kk >= nk) break;
                     mma_ts(tmem + kTmemO + i * 128, tmem + i * 128 + kk * 8, desc_at(vdesc, vo + kk * 2048), idesc_pv,
-                           (jt > 0 || kk > 0) ? 1u : 0u);
+                           (jt > 0 || ns || kk > 0) ? 1u : 0u);
                 }
             };
-            // Per tile j and row tile i: P.V of tile j-1 first (it needs only V(j-1) and
-            // P_i), then Q.K^T of tile j into the same TMEM columns, then one commit.
-            for (int j = 0; ok && j <= ntiles; ++j) {
-                const int st = j % kU;  // unit j: K(j) and V(j-1)
-                if (!mbar_wait(&bars.u_full[st], (j / kU) & 1, &abort_sh)) { ok = false; break; }
-                if (j == ntiles && (lim_last & 15) != 0) {
-                    // zero V rows lim_last .. end of their 16-token step (whole 128-byte rows,
-                    // so the swizzle does not matter), then make them visible to the tensor core
-                    uint8_t* vt = sU + st * C::kUnitBytes + C::kTileBytes;
-                    for (int row = lim_last; row < pv_steps_last * 16; ++row)
-#pragma unroll
-                        for (int kb = 0; kb < C::KB; ++kb)
-#pragma unroll
-                            for (int ch = 0; ch < 8; ++ch)
-                                *reinterpret_cast<uint4*>(vt + kb * 16384 + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
-                    fence_proxy_async_smem();
-                }
+            if constexpr (NST) {
+                // ---- in-tile mode. The Non-Shared tile: per row tile, Q.K^T against the gathered
+                // K tile (slot 0), whose slot is then released.
                 for (int i = 0; i < ntile_m; ++i) {
-                    if (j > 0) {
-                        if (!mbar_wait(&bars.p_full[i], (j - 1) & 1, &abort_sh)) { ok = false; break; }
-                        tc_fence_after();
-                        issue_pv(i, j - 1, st);
-                        if (j == ntiles) mma_commit(&bars.o_full[i]);  // O_i complete
+                    if (!mbar_wait(&bars.ns_kfull[i], 0, &abort_sh)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t qo = i * C::kTileBytes, ko = i * C::kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_ss(tmem + i * 128, desc_at(qdesc, qo + off), desc_at(kdesc, ko + off), idesc_qk,
+                               kk > 0 ? 1u : 0u);
                     }
-                    if (j < ntiles) {
+                    mma_commit(&bars.s_full[i]);
+                }
+                if (ok) mma_commit(&bars.u_empty[0]);
+                // Iteration 0: per row tile, P.V of the Non-Shared tile (gathered V tile, slot 1),
+                // then Q.K^T of prefix tile 0 (unit 2, slot 2 % kU, the first phase of its barrier).
+                const int st0 = 2 % kU;
+                if (ok && ntiles > 0 && !mbar_wait(&bars.u_full[st0], 0, &abort_sh)) ok = false;
+                for (int i = 0; ok && i < ntile_m; ++i) {
+                    if (!mbar_wait(&bars.p_full[i], 0, &abort_sh) || !mbar_wait(&bars.ns_vfull[i], 0, &abort_sh)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t vo = C::kUnitBytes + (i - 1) * C::kTileBytes;  // from sU + kTileBytes
+                    for (int kk = 0; kk < ns_steps; ++kk)
+                        mma_ts(tmem + kTmemO + i * 128, tmem + i * 128 + kk * 8, desc_at(vdesc, vo + kk * 2048),
+                               idesc_pv, kk > 0 ? 1u : 0u);
+                    if (ntiles == 0) {
+                        mma_commit(&bars.o_full[i]);  // O_i complete
+                    } else {
                         tc_fence_after();
-                        const uint32_t qo = i * C::kTileBytes, ko = st * C::kUnitBytes;
+                        const uint32_t qo = i * C::kTileBytes, ko = st0 * C::kUnitBytes;
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -520,9 +654,97 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                         mma_commit(&bars.s_full[i]);
                     }
                 }
-                if (!ok) break;
-                if (j == ntiles - 1) mma_commit(&bars.q_free);  // the Q tiles are no longer read
-                mma_commit(&bars.u_empty[st]);
+                if (ok) {
+                    if (ntiles == 1) mma_commit(&bars.q_free);
+                    mma_commit(&bars.u_empty[1]);
+                    if (ntiles > 0) mma_commit(&bars.u_empty[st0]);
+                }
+                // Prefix iterations j >= 1 read unit j + 2 = {K(j), V(j-1)}; its full barrier phase
+                // is one less in slots 0 and 1 (the gathered tiles held them first), and the P
+                // phases are one on (the Non-Shared tile took the first).
+                for (int j = 1; ok && j <= ntiles; ++j) {
+                    const int u = j + 2, st = u % kU;
+                    if (!mbar_wait(&bars.u_full[st], (u / kU - (st < 2 ? 1 : 0)) & 1, &abort_sh)) {
+                        ok = false;
+                        break;
+                    }
+                    if (j == ntiles && (lim_last & 15) != 0) {
+                        uint8_t* vt = sU + st * C::kUnitBytes + C::kTileBytes;
+                        for (int row = lim_last; row < pv_steps_last * 16; ++row)
+#pragma unroll
+                            for (int kb = 0; kb < C::KB; ++kb)
+#pragma unroll
+                                for (int ch = 0; ch < 8; ++ch)
+                                    *reinterpret_cast<uint4*>(vt + kb * 16384 + row * 128 + ch * 16) =
+                                        make_uint4(0, 0, 0, 0);
+                        fence_proxy_async_smem();
+                    }
+                    for (int i = 0; i < ntile_m; ++i) {
+                        if (!mbar_wait(&bars.p_full[i], j & 1, &abort_sh)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_pv(i, j - 1, st);
+                        if (j == ntiles) mma_commit(&bars.o_full[i]);  // O_i complete
+                        if (j < ntiles) {
+                            tc_fence_after();
+                            const uint32_t qo = i * C::kTileBytes, ko = st * C::kUnitBytes;
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                                mma_ss(tmem + i * 128, desc_at(qdesc, qo + off), desc_at(kdesc, ko + off), idesc_qk,
+                                       kk > 0 ? 1u : 0u);
+                            }
+                            mma_commit(&bars.s_full[i]);
+                        }
+                    }
+                    if (!ok) break;
+                    if (j == ntiles - 1) mma_commit(&bars.q_free);  // the Q tiles are no longer read
+                    mma_commit(&bars.u_empty[st]);
+                }
+            } else {
+                // Iteration j reads unit j = {K(j), V(j-1)}: per row tile, P.V of tile j-1 first (it
+                // needs only V(j-1) and P_i), then Q.K^T of tile j into the same TMEM columns, then one
+                // commit.
+                for (int j = 0; ok && j <= ntiles; ++j) {
+                    const int st = j % kU;
+                    if (!mbar_wait(&bars.u_full[st], (j / kU) & 1, &abort_sh)) {
+                        ok = false;
+                        break;
+                    }
+                    if (j == ntiles && (lim_last & 15) != 0) {
+                        // zero V rows lim_last .. end of their 16-token step (whole 128-byte rows,
+                        // so the swizzle does not matter), then make them visible to the tensor core
+                        uint8_t* vt = sU + st * C::kUnitBytes + C::kTileBytes;
+                        for (int row = lim_last; row < pv_steps_last * 16; ++row)
+#pragma unroll
+                            for (int kb = 0; kb < C::KB; ++kb)
+#pragma unroll
+                                for (int ch = 0; ch < 8; ++ch)
+                                    *reinterpret_cast<uint4*>(vt + kb * 16384 + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+                        fence_proxy_async_smem();
+                    }
+                    for (int i = 0; i < ntile_m; ++i) {
+                        if (j > 0) {
+                            if (!mbar_wait(&bars.p_full[i], (j - 1) & 1, &abort_sh)) { ok = false; break; }
+                            tc_fence_after();
+                            issue_pv(i, j - 1, st);
+                            if (j == ntiles) mma_commit(&bars.o_full[i]);  // O_i complete
+                        }
+                        if (j < ntiles) {
+                            tc_fence_after();
+                            const uint32_t qo = i * C::kTileBytes, ko = st * C::kUnitBytes;
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                                mma_ss(tmem + i * 128, desc_at(qdesc, qo + off), desc_at(kdesc, ko + off), idesc_qk,
+                                       kk > 0 ? 1u : 0u);
+                            }
+                            mma_commit(&bars.s_full[i]);
+                        }
+                    }
+                    if (!ok) break;
+                    if (j == ntiles - 1) mma_commit(&bars.q_free);  // the Q tiles are no longer read
+                    mma_commit(&bars.u_empty[st]);
+                }
             }
             if (!ok) {
                 abort_sh = 1;
@@ -538,10 +760,10 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kWarpMma && ntiles > 0) tmem_dealloc(tmem, kTmemCols);
+    if (warp == kWarpMma && nt > 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int D>
+template <int D, bool NST>
 cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
                      const CUtensorMap& tn, const __nv_bfloat16* q, const int32_t* slen, float* po, float* pl, int32_t* status,
                      const FusedArgs& fa, cudaStream_t stream) {
@@ -549,15 +771,15 @@ cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(shared_stage_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Cfg<D>::kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(shared_stage_tc_kernel<D, NST>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
     const long ctas = shared_tc_ctas_for(g);
-    // In the fused decode the Non-Shared kernel runs just before this one and signals early
-    // launch: CTAs of this kernel may start while its last wave drains (only the epilogue
-    // reads its result, after griddepcontrol.wait).
+    // In the staged fused decode the Non-Shared kernel runs just before this one and signals
+    // early launch: CTAs of this kernel may start while its last wave drains (only the
+    // epilogue reads its result, after griddepcontrol.wait).
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ctas);
     cfg.blockDim = dim3(kThreads);
@@ -567,8 +789,8 @@ cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = (fa.enabled && g.step > 0) ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, shared_stage_tc_kernel<D>, tk, tv, tq, tn, g, q, slen, po, pl, status, fa);
+    cfg.numAttrs = (fa.enabled && g.step > 0 && !fa.ns_tile) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, shared_stage_tc_kernel<D, NST>, tk, tv, tq, tn, g, q, slen, po, pl, status, fa);
 }
 
 }  // namespace
@@ -577,14 +799,18 @@ int shared_tc_ctas_for(const Geometry& g) { return g.R * g.Hkv * g.nsplit * ((g.
 
 cudaError_t launch_shared_stage_tc(const Geometry& g, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                    const CUtensorMap& tq, const CUtensorMap& tn, const __nv_bfloat16* q,
-                                   const int32_t* shared_len,
-                                   float* part_o, float* part_lse, int32_t* status, void* out, float* lse,
-                                   bool fused, cudaStream_t stream) {
-    FusedArgs fa{out, lse, fused ? 1 : 0};
+                                   const int32_t* shared_len, float* part_o, float* part_lse, int32_t* status, void* out,
+                                   float* lse, bool fused, const NsTileArgs& nst_args, cudaStream_t stream) {
+    FusedArgs fa{out, lse, fused ? 1 : 0, nst_args.enabled ? 1 : 0,
+                 reinterpret_cast<const __nv_bfloat16*>(nst_args.pool_k),
+                 reinterpret_cast<const __nv_bfloat16*>(nst_args.pool_v), nst_args.idx};
+    const bool nst = fused && nst_args.enabled && g.step > 0;
     if (g.d == 128)
-        return launch_d<128>(g, tmap_k, tmap_v, tq, tn, q, shared_len, part_o, part_lse, status, fa, stream);
+        return nst ? launch_d<128, true>(g, tmap_k, tmap_v, tq, tn, q, shared_len, part_o, part_lse, status, fa, stream)
+                   : launch_d<128, false>(g, tmap_k, tmap_v, tq, tn, q, shared_len, part_o, part_lse, status, fa, stream);
     if (g.d == 64)
-        return launch_d<64>(g, tmap_k, tmap_v, tq, tn, q, shared_len, part_o, part_lse, status, fa, stream);
+        return nst ? launch_d<64, true>(g, tmap_k, tmap_v, tq, tn, q, shared_len, part_o, part_lse, status, fa, stream)
+                   : launch_d<64, false>(g, tmap_k, tmap_v, tq, tn, q, shared_len, part_o, part_lse, status, fa, stream);
     return cudaErrorInvalidValue;
 }
 

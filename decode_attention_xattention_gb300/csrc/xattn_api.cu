@@ -16,10 +16,10 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 int device_sms() {
     static int cache[64] = {};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 152;  // no device: plan as for a GB300
     if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
     int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
     if (dev >= 0 && dev < 64) cache[dev] = n;
     return n;
 }
@@ -200,6 +200,7 @@ int xattn_query_plan(const xattn_desc* desc, int32_t step, xattn_plan* out) {
     out->row_tiles = g.row_tiles;
     out->shared_ctas = k == 0 ? 0 : (k == 1 ? shared_tc_ctas_for(g) : g.R * g.Hkv * ((g.M + 3) / 4) * g.nsplit);
     out->fused = decode_is_fused(g, k, step) ? 1 : 0;
+    out->ns_tile = ns_tile_fits(g, k, step) ? 1 : 0;
     out->piece_stride = g.pieces;
     out->merge_ctas = out->fused ? 0 : merge_ctas_for(g);
     return XATTN_OK;
@@ -257,7 +258,8 @@ WsView ws_view(void* workspace, const Geometry& g) {
 int run_shared(const Geometry& g, int kernel, const void* q, const void* shared_k, const void* shared_v,
                const int32_t* shared_len, const WsView& ws, cudaStream_t st, bool fused = false,
                const void* ns_k_pool = nullptr, const void* ns_v_pool = nullptr,
-               const int32_t* beam_tok_idx = nullptr, void* out = nullptr, float* lse = nullptr) {
+               const int32_t* beam_tok_idx = nullptr, void* out = nullptr, float* lse = nullptr,
+               bool ns_tile = false) {
     cudaError_t e = cudaSuccess;
     if (kernel == 1) {
         auto qb = reinterpret_cast<const __nv_bfloat16*>(q);
@@ -266,8 +268,9 @@ int run_shared(const Geometry& g, int kernel, const void* q, const void* shared_
             return XATTN_ERR_CUDA;
         if (make_q_map(&mq, q, g) != CUDA_SUCCESS || make_ns_map(&mn, ws.part_o, g) != CUDA_SUCCESS)
             return XATTN_ERR_CUDA;
+        const NsTileArgs nst{ns_tile, ns_k_pool, ns_v_pool, beam_tok_idx};
         e = launch_shared_stage_tc(g, mk, mv, mq, mn, qb, shared_len, ws.part_o, ws.part_lse, ws.status, out, lse,
-                                   fused, st);
+                                   fused, nst, st);
     } else if (kernel == 2) {
         e = launch_shared_stage_simt(g, q, shared_k, shared_v, shared_len, ws.part_o, ws.part_lse, ws.status, st);
     }
@@ -285,22 +288,42 @@ int run_merge(const Geometry& g, const xattn_desc* desc, const void* q, const in
 
 }  // namespace
 
-extern "C" {
-
-int xattn_decode(const xattn_desc* desc, const void* q, const void* shared_k, const void* shared_v,
-                 const int32_t* shared_len, const void* ns_k_pool, const void* ns_v_pool,
-                 const int32_t* beam_tok_idx, int32_t step, void* out, float* lse, void* workspace,
-                 size_t workspace_bytes, xattn_stream_t stream) {
-    int rc = check_common(desc, q, workspace);
+// Every host-side check xattn_decode makes before it launches anything (descriptor, pointers,
+// alignment, step, workspace size); nothing is enqueued.
+int xattn::check_decode_args(const xattn_desc* desc, const void* q, const void* shared_k, const void* shared_v,
+                             const int32_t* shared_len, const void* ns_k_pool, const void* ns_v_pool,
+                             const int32_t* beam_tok_idx, int32_t step, const void* out, const float* lse,
+                             const void* workspace, size_t workspace_bytes) {
+    int rc = check_common(desc, q, const_cast<void*>(workspace));
     if (rc == XATTN_OK) rc = check_shared_args(desc, shared_k, shared_v, shared_len);
     if (rc == XATTN_OK) rc = check_merge_args(desc, ns_k_pool, ns_v_pool, beam_tok_idx, step, out, lse);
     if (rc != XATTN_OK) return rc;
     Geometry g;
     int kernel;
     plan(desc, step, &g, &kernel);
-    if (workspace_bytes < workspace_bytes_for(g)) return XATTN_ERR_WORKSPACE_TOO_SMALL;
+    return workspace_bytes < workspace_bytes_for(g) ? XATTN_ERR_WORKSPACE_TOO_SMALL : XATTN_OK;
+}
+
+extern "C" {
+
+int xattn_decode(const xattn_desc* desc, const void* q, const void* shared_k, const void* shared_v,
+                 const int32_t* shared_len, const void* ns_k_pool, const void* ns_v_pool,
+                 const int32_t* beam_tok_idx, int32_t step, void* out, float* lse, void* workspace,
+                 size_t workspace_bytes, xattn_stream_t stream) {
+    int rc = xattn::check_decode_args(desc, q, shared_k, shared_v, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx,
+                                      step, out, lse, workspace, workspace_bytes);
+    if (rc != XATTN_OK) return rc;
+    Geometry g;
+    int kernel;
+    plan(desc, step, &g, &kernel);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const WsView ws = ws_view(workspace, g);
+    if (ns_tile_fits(g, kernel, step)) {
+        // One launch: the Shared-stage kernel gathers the Non-Shared rows itself and attends to
+        // them as the first tile of each row tile; its online softmax merges the two parts.
+        return run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st, true, ns_k_pool, ns_v_pool,
+                          beam_tok_idx, out, lse, true);
+    }
     if (decode_is_fused(g, kernel, step)) {
         // Non-Shared part first, as one piece in the workspace; then the Shared stage, whose
         // epilogue merges it and writes out / lse.

@@ -50,12 +50,21 @@ inline size_t part_rows(const Geometry& g) { return (size_t)g.R * g.Hkv * g.piec
 // tmap_q: the Q tiles by TMA (box 64 x G x 128/G; G divides 128 since it is a power of two
 // up to 16); tmap_ns: part_o as {d, rows} fp32, box 32 x 128 (the fused epilogue stages the
 // Non-Shared piece through it).
+// ns_tile.enabled (with fused and g.step > 0): the kernel gathers the Non-Shared K/V rows
+// itself (pool_k / pool_v through the ancestry table idx) and attends to them as one more
+// 128-key tile per row tile; requires (128 / G) * step <= 128 (ns_tile_fits).
+struct NsTileArgs {
+    bool enabled;
+    const void* pool_k;
+    const void* pool_v;
+    const int32_t* idx;
+};
 cudaError_t launch_shared_stage_tc(const Geometry& g, const CUtensorMap& tmap_k,
                                    const CUtensorMap& tmap_v, const CUtensorMap& tmap_q,
                                    const CUtensorMap& tmap_ns, const __nv_bfloat16* q,
                                    const int32_t* shared_len, float* part_o, float* part_lse,
                                    int32_t* status, void* out, float* lse, bool fused,
-                                   cudaStream_t stream);
+                                   const NsTileArgs& ns_tile, cudaStream_t stream);
 // q, shared_k, shared_v: bf16, or fp32 when g.in_f32.
 cudaError_t launch_shared_stage_simt(const Geometry& g, const void* q, const void* shared_k, const void* shared_v,
                                      const int32_t* shared_len, float* part_o, float* part_lse,
@@ -76,10 +85,20 @@ cudaError_t launch_beam_update(int R, int BW, int Hkv, int d, int elem_bytes, in
                                void* pool_v, int32_t* idx, int32_t* status, cudaStream_t stream);
 
 int merge_ctas_for(const Geometry& g);
+// The host-side argument checks of xattn_decode, without launching anything.
+int check_decode_args(const xattn_desc* desc, const void* q, const void* shared_k, const void* shared_v,
+                      const int32_t* shared_len, const void* ns_k_pool, const void* ns_v_pool,
+                      const int32_t* beam_tok_idx, int32_t step, const void* out, const float* lse,
+                      const void* workspace, size_t workspace_bytes);
 // Whether xattn_decode runs the Shared stage and the Merge in one tensor-core kernel (after
 // a short Non-Shared kernel when step > 0): one prefix piece and a short Non-Shared part.
 inline bool decode_is_fused(const Geometry& g, int kernel, int step) {
     return kernel == 1 && g.nsplit == 1 && step <= kNsDirectMax;
+}
+// Whether the fused decode computes the Non-Shared part inside the Shared-stage kernel (one
+// launch): every row tile's beams' Non-Shared keys fit one 128-key tile.
+inline bool ns_tile_fits(const Geometry& g, int kernel, int step) {
+    return decode_is_fused(g, kernel, step) && step > 0 && (kTileRows / g.G) * step <= kTcTileKeys;
 }
 int shared_tc_ctas_for(const Geometry& g);
 

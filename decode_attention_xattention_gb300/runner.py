@@ -74,6 +74,16 @@ class DeviceBatch:
         self.workspace = torch.zeros((self.ws_bytes + 255) // 256 * 64, dtype=torch.int32, device=device)
         self.status = torch.zeros((1,), dtype=torch.int32, device=device)
 
+    def clone(self) -> "DeviceBatch":
+        """Another batch with the same values in buffers of its own (a device-to-device copy
+        of every tensor): distinct addresses, so that rotating through clones defeats the L2."""
+        c = object.__new__(DeviceBatch)
+        c.__dict__.update(self.__dict__)
+        for k, v in self.__dict__.items():
+            if isinstance(v, torch.Tensor):
+                setattr(c, k, v.clone())
+        return c
+
     # -- the method's calls --------------------------------------------------------------
     def beam_update(self, s: int) -> int:
         return xattn.xattn_beam_update(self.desc, self.parents[s] if s > 0 else None, self.new_k[s], self.new_v[s],

@@ -221,6 +221,19 @@ def sample_rows(w: Workload, n: int, seed: int = 1) -> np.ndarray:
     return np.asarray(sorted(rows), dtype=np.int64)
 
 
+def sample_rows_every_beam(w: Workload, extra: int, seed: int = 1) -> np.ndarray:
+    """Flat row ids (r*BW + b)*Hq + h: every beam's first and last query head, plus `extra`
+    more rows drawn at random (distinct, sorted)."""
+    beams = np.arange(w.num_requests * w.beam_width, dtype=np.int64)
+    forced = np.concatenate([beams * w.num_q_heads, beams * w.num_q_heads + w.num_q_heads - 1])
+    total = w.num_requests * w.beam_width * w.num_q_heads
+    rng = np.random.default_rng(seed)
+    pick = rng.choice(total, size=min(total, extra + len(forced)), replace=False)
+    rows = np.unique(forced)
+    rest = np.setdiff1d(pick, rows)[:extra]
+    return np.unique(np.concatenate([rows, rest]))
+
+
 # --------------------------------------------------------------------------------------
 # Beam-selection inputs (xGR section 2.2, xBeam): every beam's candidate list as a per-beam
 # top-K returns it, best first.

@@ -65,7 +65,7 @@ class xattn_plan(ctypes.Structure):
                 ("split_tokens", ctypes.c_int32), ("rows_per_unit", ctypes.c_int32),
                 ("row_tiles", ctypes.c_int32), ("shared_ctas", ctypes.c_int32),
                 ("merge_ctas", ctypes.c_int32), ("fused", ctypes.c_int32), ("piece_stride", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 2)]
+                ("ns_tile", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1)]
 
 
 _lib = None

@@ -202,12 +202,16 @@ XATTN_API int xattn_beam_select(int32_t num_requests, int32_t beam_width, int32_
  *   - Shapes whose xattn_decode_workspace_size exceeds that limit return
  *     XATTN_ERR_WORKSPACE_TOO_SMALL before anything is launched; an invalid descriptor
  *     returns XATTN_ERR_INVALID_ARG.
- *   - The first call on a device looks up the array's device address (with that device
- *     current); make that first call before any stream capture.
+ *   - The first call in each CUDA context looks up the array's device address (with that
+ *     context current) and caches it under the context's unique id; make that first call
+ *     before any stream capture.
+ *   - Every host-side check of xattn_decode runs before anything is enqueued: a rejected
+ *     call leaves the array untouched.
  *   - All calls share the array: calls whose GPU work overlaps (other streams or threads on
  *     the same device) race and must be serialised by the caller.
- *   - The status word is cleared at the start of each call; if `status_out` (a device
- *     int32, may be NULL) is given, the call's final status word is copied there on `stream`.
+ *   - The status word is cleared on `stream` at the start of each accepted call; if
+ *     `status_out` (a device int32, may be NULL) is given, the call's final status word is
+ *     copied there on `stream`.
  * No cudaMalloc, cudaFree or allocating library routine is called. Other arguments and
  * results are those of xattn_decode. */
 #define XATTN_NOALLOC_SCRATCH_BYTES (32u << 20)
@@ -235,7 +239,11 @@ typedef struct xattn_plan {
                                  prefix piece, step <= 32); 0: Shared stage, then the
                                  Non-Shared + Merge kernel(s)                              */
     int32_t piece_stride;     /* pieces per (request, KV head) in the workspace layout     */
-    int32_t reserved[2];
+    int32_t ns_tile;          /* 1: (fused only) the Shared-stage kernel gathers the Non-Shared
+                                 tokens itself and attends to them as one more 128-key tile
+                                 of each row tile (masked per beam), so xattn_decode is one
+                                 launch; 0: a Non-Shared kernel runs first                  */
+    int32_t reserved[1];
 } xattn_plan;
 
 XATTN_API int xattn_query_plan(const xattn_desc* desc, int32_t step, xattn_plan* plan);

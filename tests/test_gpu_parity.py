@@ -133,16 +133,60 @@ def test_medium_non_shared_parts_fused(T, d, Hq, Hkv):
     assert db.plan().fused == 1
 
 
-@pytest.mark.parametrize("shape", [(3, 8, 8, 1, 64, 8), (2, 5, 32, 2, 128, 7), (1, 4, 16, 16, 128, 8)],
-                         ids=["G8_d64_t8", "G16_d128_t7", "G1_Hkv16_t8_wide_rows"])
+@pytest.mark.parametrize("shape", [(3, 8, 8, 4, 64, 5), (2, 5, 8, 2, 128, 7), (1, 4, 16, 16, 128, 8)],
+                         ids=["G2_d64_t5", "G4_d128_t7", "G1_Hkv16_t8_wide_rows"])
 def test_short_non_shared_beam_kernel_shapes(shape):
-    """Short Non-Shared parts (step <= 8) go through the warp-per-beam kernel when the beam's
-    rows fit its shared memory, else through the per-head piece kernel (the last shape:
-    16 KV heads x 8 tokens x K and V rows exceed it)."""
+    """Short Non-Shared parts (step <= 8) whose keys do not fit one tile of the Shared-stage
+    kernel ((128 / G) * step > 128) go through the warp-per-beam kernel when the beam's rows
+    fit its shared memory, else through the per-head piece kernel (the last shape: 16 KV
+    heads x 8 tokens x K and V rows exceed it); the Shared stage merges the piece."""
     R, BW, Hq, Hkv, d, T = shape
     w = wl.custom(R=R, BW=BW, Hq=Hq, Hkv=Hkv, d=d, lens=(300,) * R, T=T, seed=50 + T)
     _, db, _ = run_and_check(w, split_tokens=4096)
-    assert db.plan().fused == 1
+    p = db.plan()
+    assert p.fused == 1 and p.ns_tile == 0
+
+
+NS_TILE = [
+    # (R, BW, Hq, Hkv, d, lens, T): (128 / G) * T <= 128 Non-Shared keys per row tile
+    (2, 40, 16, 4, 128, (1000, 129), 4),     # G 4: a full 128-key tile; M = 160 (ragged row tile)
+    (2, 5, 32, 2, 128, (300, 0), 16),        # G 16: 8 beams x 16 keys; request 1 Non-Shared only
+    (3, 24, 16, 2, 64, (517, 256, 1), 8),    # G 8, d 64: 16 beams x 8 keys
+    (1, 130, 2, 2, 128, (700,), 1),          # G 1: 128 beams x 1 key, two row tiles
+    (2, 64, 4, 2, 64, (384, 200), 2),        # G 2, d 64
+    (1, 3, 16, 2, 128, (2049,), 5),          # G 8: 3 of the tile's 16 beams exist
+    (2, 8, 8, 2, 128, (128, 255), 3),        # a prefix of exactly one tile; a ragged one
+]
+
+
+@pytest.mark.parametrize("shape", NS_TILE, ids=lambda s: f"R{s[0]}_BW{s[1]}_H{s[2]}x{s[3]}_d{s[4]}_t{s[6]}")
+def test_ns_tile_all_rows(shape):
+    """One launch: the Shared-stage kernel gathers every beam's Non-Shared rows through the
+    ancestry table into one more 128-key tile per row tile and attends to it (keys of other
+    beams masked) before the prefix tiles. Every row against the oracle."""
+    R, BW, Hq, Hkv, d, lens, T = shape
+    w = wl.custom(R=R, BW=BW, Hq=Hq, Hkv=Hkv, d=d, lens=lens, T=T, seed=90 + T)
+    _, db, _ = run_and_check(w, split_tokens=max(4096, w.max_shared_len))
+    p = db.plan()
+    assert p.fused == 1 and p.ns_tile == 1, (p.fused, p.ns_tile)
+
+
+def test_ns_tile_bad_slot_in_one_beam():
+    """A slot outside the pool in one beam's ancestry row on the one-launch path: status
+    BAD_SLOT, NaN output and LSE for that beam's rows only, the other beams exact."""
+    w = wl.custom(R=2, BW=16, Hq=8, Hkv=2, d=128, lens=(500, 300), T=3, seed=12)
+    db = DeviceBatch(wl.make_inputs(w), out_fp32=True, split_tokens=512)
+    db.build_cache()
+    assert db.plan().ns_tile == 1
+    db.idx[1, 9, 2] = 1 << 22
+    xattn.check(db.decode())
+    assert db.read_status() & xattn.XATTN_STATUS_BAD_SLOT
+    o = db.out.cpu()
+    l = db.lse.cpu()
+    assert torch.isnan(o[1, 9]).all() and torch.isnan(l[1, 9]).all()
+    good = torch.ones(w.num_requests, w.beam_width, dtype=torch.bool)
+    good[1, 9] = False
+    assert torch.isfinite(o[good]).all() and torch.isfinite(l[good]).all()
 
 
 def test_tiny_config_both_kernels():
@@ -250,25 +294,35 @@ def test_shared_stage_pieces_match_oracle_partials(kernel):
             compare(po[r, :, c], pl[r, :, c], ro[r], rl[r], f"piece {c} of request {r}")
 
 
-def test_equal_ancestry_equal_output_bitwise():
-    w = wl.custom(R=1, BW=8, Hq=8, Hkv=2, d=128, lens=(900,), T=3, seed=11)
+@pytest.mark.parametrize("Hkv,ns_tile", [(4, 0), (2, 1)], ids=["staged", "ns_tile"])
+def test_equal_ancestry_equal_output(Hkv, ns_tile):
+    """Beams with the same ancestry row and the same q rows get the same output. Bitwise
+    when the Non-Shared part is computed per beam (staged piece). With the Non-Shared part in
+    the Shared-stage tile, the two beams' keys sit in different columns of the tile, so the
+    tensor core may group their P.V terms differently: equal to fp32 rounding."""
+    w = wl.custom(R=1, BW=8, Hq=8, Hkv=Hkv, d=128, lens=(900,), T=3, seed=11)
     inp = wl.make_inputs(w)
     par = inp.parents.copy()
     par[1:, 0, :] = 3
     q = inp.q.copy()
     q[0, 5] = q[0, 2]
     inp = wl.Inputs(w, q, inp.shared_k, inp.shared_v, inp.shared_len, inp.new_k, inp.new_v, par)
-    db = DeviceBatch(inp)
+    db = DeviceBatch(inp, out_fp32=True, split_tokens=1024)
     db.build_cache()
+    assert db.plan().ns_tile == ns_tile
     idx = db.idx.clone()
     idx[0, 5] = idx[0, 2]
     db.idx.copy_(idx)
     xattn.check(db.decode())
     torch.cuda.synchronize()
-    o = db.out.float().cpu().numpy()
+    o = db.out.cpu().numpy()
     l = db.lse.cpu().numpy()
-    np.testing.assert_array_equal(o[0, 5], o[0, 2])
-    np.testing.assert_array_equal(l[0, 5], l[0, 2])
+    if ns_tile:
+        np.testing.assert_allclose(o[0, 5], o[0, 2], rtol=0, atol=2e-6)
+        np.testing.assert_allclose(l[0, 5], l[0, 2], rtol=0, atol=2e-6)
+    else:
+        np.testing.assert_array_equal(o[0, 5], o[0, 2])
+        np.testing.assert_array_equal(l[0, 5], l[0, 2])
 
 
 def test_repeated_calls_deterministic():
@@ -366,8 +420,19 @@ FULL = [wl.GR, wl.WIDE, wl.LONG, wl.FEATHER_1, wl.FEATHER_8, wl.FEATHER_64]
 
 @pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
 def test_full_size_sampled_rows(w):
-    rows = wl.sample_rows(w, 384, seed=2)
+    """Every beam's first and last query head plus 384 random rows against the oracle
+    (fp32 output: the computation itself); every output row and lse finite."""
+    rows = wl.sample_rows_every_beam(w, 384, seed=2)
     stats, db, _ = run_and_check(w, rows=rows)
-    # every output row is finite and every lse is finite
     assert torch.isfinite(db.out.float()).all()
     assert torch.isfinite(db.lse).all()
+
+
+@pytest.mark.parametrize("w", [wl.WIDE, wl.FEATHER_1], ids=lambda w: w.name)
+def test_full_size_bf16_output(w):
+    """The output the library returns by default (bf16) against the oracle at the stated
+    tolerances, at full size: every beam's first and last query head plus 384 random rows."""
+    rows = wl.sample_rows_every_beam(w, 384, seed=3)
+    stats, db, _ = run_and_check(w, rows=rows, out_fp32=False)
+    assert db.out.dtype == torch.bfloat16
+    assert torch.isfinite(db.out.float()).all()

@@ -1,7 +1,8 @@
 """xattn_decode_noalloc: the decode entry point for callers that cannot allocate device
 memory (a runtime that owns every allocation, a latency-critical thread that must not call
-cudaMalloc, a fixed memory budget). It must give what xattn_decode gives, call after call,
-using only the library's static scratch array. This file is collected last on purpose."""
+cudaMalloc, a fixed memory budget). Call after call, using only the library's static
+scratch array, it must match the fp64 oracle and give bit for bit what xattn_decode gives
+with a workspace of the caller's. This file is collected last on purpose."""
 
 import numpy as np
 import pytest
@@ -9,6 +10,7 @@ import torch
 
 from decode_attention_xattention_gb300 import build, workloads as wl, xattn
 from decode_attention_xattention_gb300.runner import DeviceBatch
+import oracle
 from gpu_helpers import compare
 
 pytestmark = pytest.mark.gpu
@@ -35,15 +37,22 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", CASES, ids=["fused", "split"])
-def test_noalloc_matches_workspace_entry_point(case):
+def test_noalloc_matches_oracle_and_workspace_entry_point(case):
+    """Two calls in a row on the shared scratch array: each matches the fp64 oracle within
+    the bf16 tolerances, and each is bit for bit what xattn_decode gives with a workspace of
+    the caller's (same plan, same kernels), so no stale scratch contents leak in."""
     w, split = case
     db = DeviceBatch(wl.make_inputs(w), split_tokens=split)
     db.build_cache()
     assert db.plan().fused == (1 if split >= w.max_shared_len else 0)
     xattn.check(db.decode())
     torch.cuda.synchronize()
-    ref_o = db.out.float().cpu().numpy().reshape(-1, w.head_dim)
-    ref_l = db.lse.cpu().numpy().reshape(-1)
+    ws_out, ws_lse = db.out.clone(), db.lse.clone()
+    orc = oracle.load()
+    inp = db.inputs
+    pk, pv, idx = oracle.build_cache(orc, inp)
+    ref_o, ref_l = orc.decode(oracle.dims_of(w), inp.q, inp.shared_k, inp.shared_v, inp.shared_len, pk, pv, idx,
+                              w.steps)
     status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
     for call in range(2):  # two calls in a row share the scratch array
         db.out.fill_(float("nan"))
@@ -51,9 +60,24 @@ def test_noalloc_matches_workspace_entry_point(case):
         xattn.check(_noalloc(db, status))
         torch.cuda.synchronize()
         assert int(status.item()) == 0, f"call {call}: status {int(status.item())}"
+        assert torch.equal(db.out, ws_out) and torch.equal(db.lse, ws_lse), f"call {call}: differs from xattn_decode"
         got_o = db.out.float().cpu().numpy().reshape(-1, w.head_dim)
         got_l = db.lse.cpu().numpy().reshape(-1)
         compare(got_o, got_l, ref_o, ref_l, f"noalloc call {call}")
+
+
+def test_noalloc_rejected_call_launches_nothing():
+    """A call that fails a host-side check (here a step past max_steps) returns its error and
+    enqueues nothing: the outputs keep their contents."""
+    w = wl.custom(R=1, BW=4, Hq=4, Hkv=2, d=128, lens=(200,), T=2, seed=34)
+    db = DeviceBatch(wl.make_inputs(w))
+    db.build_cache()
+    db.out.fill_(7.0)
+    rc = xattn.xattn_decode_noalloc(db.desc, db.q, db.shared_k, db.shared_v, db.shared_len, db.pool_k, db.pool_v,
+                                    db.idx, w.steps + 1, db.out, db.lse, None, db.stream)
+    assert rc == xattn.XATTN_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert bool((db.out.float() == 7.0).all())
 
 
 def test_noalloc_reports_device_status_per_call():
