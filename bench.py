@@ -208,14 +208,16 @@ def profile_traffic(kernel_file: str, workload: str):
 
 
 def launches_per_step(plan, step):
-    """Kernels of this library launched by one timed step: the beam update, then the
-    decode (the Shared-stage kernel alone when it gathers the Non-Shared part itself; the
-    Non-Shared kernel + Shared stage with merging epilogue when fused; else
+    """Kernels of this library launched by one timed step (xattn_decode_step): the beam update,
+    then the decode (the Shared-stage kernel alone when it takes the Non-Shared part in its own
+    tile; the Non-Shared kernel + Shared stage with merging epilogue when fused; else
     the Shared stage, if the prefix has storage, and the Non-Shared/Merge kernel, or the
     Non-Shared piece and row-merge kernels when the Non-Shared part is long)."""
+    if plan.ns_tile:  # the beam update, then the decode as its programmatic dependent
+        return 2
     n = 1
     if plan.fused:
-        n += (1 if (step > 0 and not plan.ns_tile) else 0) + 1
+        n += (1 if step > 0 else 0) + 1
     else:
         n += (1 if plan.shared_kernel != 0 else 0) + (2 if step > 32 else 1)
     return n
@@ -533,9 +535,8 @@ def measure_config(w, local, stream, peaks, peak_src, l2, cpu_budget_s, target_s
     plan = base.plan()
     flush_buf = torch.empty(int(2 * l2) // 4 + 1, dtype=torch.int32, device=f"cuda:{local}") if flush else None
 
-    def step(db):
-        xattn.check(db.beam_update(T - 1))
-        xattn.check(db.decode())
+    def step(db):  # token T-1's bookkeeping + the decode over tokens 0..T-1
+        xattn.check(db.decode_step(T - 1))
 
     with torch.cuda.stream(stream):
         for db in sets:
@@ -714,9 +715,8 @@ def main():
     nsets = len(sets)
     plan = sets[0].plan()
 
-    def step(db):
-        xattn.check(db.beam_update(T - 1))
-        xattn.check(db.decode())
+    def step(db):  # token T-1's bookkeeping + the decode over tokens 0..T-1
+        xattn.check(db.decode_step(T - 1))
 
     # eager warm-up of every call (also sets kernel attributes before capture)
     with torch.cuda.stream(stream):
@@ -800,8 +800,7 @@ def main():
         d_nk.copy_(h_nk, non_blocking=True)
         d_nv.copy_(h_nv, non_blocking=True)
         d_par.copy_(h_par, non_blocking=True)
-        xattn.check(db.beam_update(T - 1))
-        xattn.check(db.decode())
+        xattn.check(db.decode_step(T - 1))
         h_out.copy_(db.out, non_blocking=True)
         h_lse.copy_(db.lse, non_blocking=True)
 
@@ -883,11 +882,10 @@ def main():
                 for j in range(nd):
                     stream.wait_event(down_done[s][j])  # the slot's outputs were read back by step k-2
             with torch.cuda.stream(stream):
-                xattn.check(xattn.xattn_beam_update(db.desc, sl["par"], sl["nk"], sl["nv"], db.pool_k, db.pool_v,
-                                                    db.idx, T - 1, db.status, stream))
-                xattn.check(xattn.xattn_decode(db.desc, sl["q"], db.shared_k, db.shared_v, db.shared_len, db.pool_k,
-                                               db.pool_v, db.idx, T, sl["out"], sl["lse"], db.workspace, db.ws_bytes,
-                                               stream))
+                xattn.check(xattn.xattn_decode_step(db.desc, sl["par"] if T > 1 else None, sl["nk"], sl["nv"],
+                                                    sl["q"], db.shared_k, db.shared_v, db.shared_len, db.pool_k,
+                                                    db.pool_v, db.idx, T, sl["out"], sl["lse"], db.workspace,
+                                                    db.ws_bytes, stream))
                 comp_done[s].record(stream)
             ho, hl = collect[k] if collect is not None else (h_outs[s], h_lses[s])
             plan_dn = readback_plan(sl, ho, hl, nd, graph)

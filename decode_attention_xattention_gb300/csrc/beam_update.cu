@@ -17,7 +17,7 @@ namespace xattn {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTableInts = 8192;  // shared-memory band: 32 KB
+constexpr int kTableInts = 8192;  // largest shared-memory band: 32 KB (BW up to 8192, one column)
 
 // Table columns per table CTA: at most a 32 KB band, and about 2048 entries so that long
 // tables are spread over many CTAs.
@@ -30,6 +30,9 @@ __global__ void __launch_bounds__(kThreads) beam_update_kernel(
     int BW, int row16, int S, int Tmax, int step, int copy_ctas, const int32_t* __restrict__ parent,
     const uint4* __restrict__ new_k, const uint4* __restrict__ new_v, uint4* __restrict__ pool_k,
     uint4* __restrict__ pool_v, int32_t* __restrict__ idx, int32_t* status) {
+    // a decode launched after this kernel as its programmatic dependent may start now: it
+    // reads the pool and the table only after waiting for this grid to complete
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int r = blockIdx.x;
     if ((int)blockIdx.y < copy_ctas) {
         // 1. K/V of the new tokens: [BW, Hkv, d] of request r -> slots step*BW .. step*BW+BW-1
@@ -62,7 +65,7 @@ __global__ void __launch_bounds__(kThreads) beam_update_kernel(
     //    per table CTA (blockIdx.y - copy_ctas); each stages its range in shared memory (all
     //    reads, barrier, all writes). These CTAs copy nothing, so their dependent loads
     //    overlap the copies of the others.
-    __shared__ int32_t band[kTableInts];
+    extern __shared__ int32_t band[];  // BW x cols entries (dynamic: the copying CTAs hold none of it)
     const int tc = (int)blockIdx.y - copy_ctas;
     int32_t* tab = idx + (size_t)r * BW * Tmax;
     const int32_t* par = parent ? parent + (size_t)r * BW : nullptr;
@@ -106,7 +109,8 @@ cudaError_t launch_beam_update(int R, int BW, int Hkv, int d, int elem_bytes, in
     ybl = max(1, min(ybl, 1024));
     const int tcols = step > 0 ? (step + table_cols(BW, step) - 1) / table_cols(BW, step) : 1;
     dim3 grid(R, ybl + tcols);  // the last tcols CTAs of each request rewrite its ancestry table
-    beam_update_kernel<<<grid, kThreads, 0, stream>>>(
+    const size_t band_bytes = step > 0 ? (size_t)BW * table_cols(BW, step) * sizeof(int32_t) : 0;
+    beam_update_kernel<<<grid, kThreads, band_bytes, stream>>>(
         BW, row16, S, Tmax, step, ybl, parent, static_cast<const uint4*>(new_k), static_cast<const uint4*>(new_v),
         static_cast<uint4*>(pool_k), static_cast<uint4*>(pool_v), idx, status);
     return cudaGetLastError();

@@ -141,6 +141,7 @@ struct FusedArgs {
     const __nv_bfloat16* pool_k;
     const __nv_bfloat16* pool_v;
     const int32_t* idx;
+    int pdl;  // launched as the programmatic dependent of the beam update that writes the pool and table
 };
 
 // NST: the in-tile Non-Shared mode, compiled as its own instantiation so that the other
@@ -248,13 +249,18 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             constexpr int NSW = kTcTileKeys / KPS;
             const int ch = rloc % CH, kb0 = rloc / CH;
             const int b0 = mt * nb;
+            // (after a beam update launched just before this kernel, which wrote the pool and the
+            // table: wait for it; nothing read above is written by it)
+            if (fa.pdl) grid_dependency_wait();
             int sl[NSW];  // the slots first, every load in flight at once
 #pragma unroll
             for (int j = 0; j < NSW; ++j) {
                 const int cc = kb0 + KPS * j, bl = cc / g.step, bg = b0 + bl;
-                sl[j] = (cc < nk && bg < g.BW) ? __ldg(fa.idx + ((size_t)r * g.BW + bg) * g.Tmax + (cc - bl * g.step))
-                                               : -1;
-                if (ch == 0 && cc < nk && bg < g.BW && (sl[j] < 0 || sl[j] >= g.S)) {
+                const int v = (cc < nk && bg < g.BW)
+                                  ? __ldg(fa.idx + ((size_t)r * g.BW + bg) * g.Tmax + (cc - bl * g.step))
+                                  : -1;
+                sl[j] = v;
+                if (ch == 0 && cc < nk && bg < g.BW && (v < 0 || v >= g.S)) {
                     atomicOr(&bad_beam[wg][bl >> 5], 1u << (bl & 31));
                     set_status(status, XATTN_STATUS_BAD_SLOT);
                 }
@@ -269,10 +275,11 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                     const int cc = kb0 + KPS * j;
                     if (cc < nk) {
                         const uint32_t dst = dt + cc * 128 + (((ch & 7) ^ (cc & 7)) << 4);
-                        if (sl[j] >= 0 && sl[j] < g.S)
+                        if (sl[j] >= 0 && sl[j] < g.S) {
                             cp_async_16(dst, pool + (((size_t)r * g.S + sl[j]) * g.Hkv + h) * D + ch * 8);
-                        else
+                        } else {
                             st_shared_zero16(dst);
+                        }
                     } else if (pass == 1 && cc < ((nk + 15) & ~15)) {
                         // V rows past the last key, up to the end of its 16-key step: zero
                         st_shared_zero16(dt + cc * 128 + (((ch & 7) ^ (cc & 7)) << 4));
@@ -789,7 +796,7 @@ cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = (fa.enabled && g.step > 0 && !fa.ns_tile) ? 1 : 0;
+    cfg.numAttrs = ((fa.enabled && g.step > 0 && !fa.ns_tile) || fa.pdl) ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, shared_stage_tc_kernel<D, NST>, tk, tv, tq, tn, g, q, slen, po, pl, status, fa);
 }
 
@@ -801,9 +808,14 @@ cudaError_t launch_shared_stage_tc(const Geometry& g, const CUtensorMap& tmap_k,
                                    const CUtensorMap& tq, const CUtensorMap& tn, const __nv_bfloat16* q,
                                    const int32_t* shared_len, float* part_o, float* part_lse, int32_t* status, void* out,
                                    float* lse, bool fused, const NsTileArgs& nst_args, cudaStream_t stream) {
-    FusedArgs fa{out, lse, fused ? 1 : 0, nst_args.enabled ? 1 : 0,
+    FusedArgs fa{out,
+                 lse,
+                 fused ? 1 : 0,
+                 nst_args.enabled ? 1 : 0,
                  reinterpret_cast<const __nv_bfloat16*>(nst_args.pool_k),
-                 reinterpret_cast<const __nv_bfloat16*>(nst_args.pool_v), nst_args.idx};
+                 reinterpret_cast<const __nv_bfloat16*>(nst_args.pool_v),
+                 nst_args.idx,
+                 nst_args.pdl ? 1 : 0};
     const bool nst = fused && nst_args.enabled && g.step > 0;
     if (g.d == 128)
         return nst ? launch_d<128, true>(g, tmap_k, tmap_v, tq, tn, q, shared_len, part_o, part_lse, status, fa, stream)

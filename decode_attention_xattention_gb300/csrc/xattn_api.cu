@@ -259,7 +259,7 @@ int run_shared(const Geometry& g, int kernel, const void* q, const void* shared_
                const int32_t* shared_len, const WsView& ws, cudaStream_t st, bool fused = false,
                const void* ns_k_pool = nullptr, const void* ns_v_pool = nullptr,
                const int32_t* beam_tok_idx = nullptr, void* out = nullptr, float* lse = nullptr,
-               bool ns_tile = false) {
+               bool ns_tile = false, const NsTileArgs* ns_args = nullptr) {
     cudaError_t e = cudaSuccess;
     if (kernel == 1) {
         auto qb = reinterpret_cast<const __nv_bfloat16*>(q);
@@ -268,7 +268,8 @@ int run_shared(const Geometry& g, int kernel, const void* q, const void* shared_
             return XATTN_ERR_CUDA;
         if (make_q_map(&mq, q, g) != CUDA_SUCCESS || make_ns_map(&mn, ws.part_o, g) != CUDA_SUCCESS)
             return XATTN_ERR_CUDA;
-        const NsTileArgs nst{ns_tile, ns_k_pool, ns_v_pool, beam_tok_idx};
+        NsTileArgs nst{ns_tile, ns_k_pool, ns_v_pool, beam_tok_idx, false};
+        if (ns_args) nst = *ns_args;
         e = launch_shared_stage_tc(g, mk, mv, mq, mn, qb, shared_len, ws.part_o, ws.part_lse, ws.status, out, lse,
                                    fused, nst, st);
     } else if (kernel == 2) {
@@ -339,6 +340,36 @@ int xattn_decode(const xattn_desc* desc, const void* q, const void* shared_k, co
     rc = run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st);
     if (rc != XATTN_OK) return rc;
     return run_merge(g, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws, st);
+}
+
+int xattn_decode_step(const xattn_desc* desc, const int32_t* parent, const void* new_k, const void* new_v,
+                      const void* q, const void* shared_k, const void* shared_v, const int32_t* shared_len,
+                      void* ns_k_pool, void* ns_v_pool, int32_t* beam_tok_idx, int32_t step, void* out, float* lse,
+                      void* workspace, size_t workspace_bytes, xattn_stream_t stream) {
+    int rc = xattn::check_decode_args(desc, q, shared_k, shared_v, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx,
+                                      step, out, lse, workspace, workspace_bytes);
+    if (rc != XATTN_OK) return rc;
+    if (step < 1) return XATTN_ERR_INVALID_ARG;
+    if (desc->beam_width > 8192) return XATTN_ERR_UNSUPPORTED;
+    if (!new_k || !new_v || (step > 1 && !parent)) return XATTN_ERR_INVALID_ARG;
+    if (!aligned(new_k, 16) || !aligned(new_v, 16) || (parent && !aligned(parent, 4))) return XATTN_ERR_MISALIGNED;
+    Geometry g;
+    int kernel;
+    plan(desc, step, &g, &kernel);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const WsView ws = ws_view(workspace, g);
+    rc = xattn_beam_update(desc, parent, new_k, new_v, ns_k_pool, ns_v_pool, beam_tok_idx, step - 1, ws.status,
+                           stream);
+    if (rc != XATTN_OK) return rc;
+    if (ns_tile_fits(g, kernel, step)) {
+        // The decode as the beam update's programmatic dependent: its set-up, Q loads and prefix
+        // prefetches overlap the update; its gather waits for the update to complete.
+        const NsTileArgs pdl{true, ns_k_pool, ns_v_pool, beam_tok_idx, true};
+        return run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st, true, ns_k_pool, ns_v_pool,
+                          beam_tok_idx, out, lse, true, &pdl);
+    }
+    return xattn_decode(desc, q, shared_k, shared_v, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, step, out, lse,
+                        workspace, workspace_bytes, stream);
 }
 
 int xattn_decode_shared(const xattn_desc* desc, const void* q, const void* shared_k, const void* shared_v,

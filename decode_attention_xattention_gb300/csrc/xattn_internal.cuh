@@ -52,12 +52,14 @@ inline size_t part_rows(const Geometry& g) { return (size_t)g.R * g.Hkv * g.piec
 // Non-Shared piece through it).
 // ns_tile.enabled (with fused and g.step > 0): the kernel gathers the Non-Shared K/V rows
 // itself (pool_k / pool_v through the ancestry table idx) and attends to them as one more
-// 128-key tile per row tile; requires (128 / G) * step <= 128 (ns_tile_fits).
+// 128-key tile per row tile; requires (128 / G) * step <= 128 (ns_tile_fits). pdl: launched
+// as the programmatic dependent of the beam update just before it (its gather waits for it).
 struct NsTileArgs {
     bool enabled;
     const void* pool_k;
     const void* pool_v;
     const int32_t* idx;
+    bool pdl;
 };
 cudaError_t launch_shared_stage_tc(const Geometry& g, const CUtensorMap& tmap_k,
                                    const CUtensorMap& tmap_v, const CUtensorMap& tmap_q,

@@ -100,6 +100,14 @@ class DeviceBatch:
                                   self.out if out is None else out, self.lse if lse is None else lse,
                                   self.workspace, self.ws_bytes, self.stream)
 
+    def decode_step(self, s: int, out=None, lse=None) -> int:
+        """Token s's bookkeeping and the decode over tokens 0..s in one call
+        (xattn_decode_step with step = s + 1)."""
+        return xattn.xattn_decode_step(self.desc, self.parents[s] if s > 0 else None, self.new_k[s], self.new_v[s],
+                                       self.q, self.shared_k, self.shared_v, self.shared_len, self.pool_k,
+                                       self.pool_v, self.idx, s + 1, self.out if out is None else out,
+                                       self.lse if lse is None else lse, self.workspace, self.ws_bytes, self.stream)
+
     def decode_shared(self) -> int:
         return xattn.xattn_decode_shared(self.desc, self.q, self.shared_k, self.shared_v, self.shared_len,
                                          self.workspace, self.ws_bytes, self.stream)

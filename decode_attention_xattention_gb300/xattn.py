@@ -36,7 +36,7 @@ XATTN_DTYPE_F32 = 1
 
 # Every symbol include/xattn.h declares.
 EXPORTS = ("xattn_decode_workspace_size", "xattn_decode", "xattn_decode_shared", "xattn_decode_merge",
-           "xattn_beam_update", "xattn_read_status", "xattn_query_plan", "xattn_status_string",
+           "xattn_beam_update", "xattn_decode_step", "xattn_read_status", "xattn_query_plan", "xattn_status_string",
            "xattn_decode_noalloc", "xattn_beam_select",
            "xattn_cht_create", "xattn_cht_destroy", "xattn_cht_insert", "xattn_cht_best", "xattn_cht_admit",
            "xattn_cht_finish", "xattn_cht_cancel", "xattn_cht_missing", "xattn_cht_counts",
@@ -93,6 +93,8 @@ def load(path: str = LIB_PATH):
     lib.xattn_decode_noalloc.restype = ctypes.c_int
     lib.xattn_beam_update.argtypes = [pdesc, vp, vp, vp, vp, vp, vp, i32, vp, vp]
     lib.xattn_beam_update.restype = ctypes.c_int
+    lib.xattn_decode_step.argtypes = [pdesc, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+    lib.xattn_decode_step.restype = ctypes.c_int
     lib.xattn_beam_select.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
     lib.xattn_beam_select.restype = ctypes.c_int
     i64 = ctypes.c_int64
@@ -167,6 +169,14 @@ def xattn_decode_merge(desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, 
     return int(load().xattn_decode_merge(ctypes.byref(desc), _ptr(q), _ptr(shared_len), _ptr(ns_k_pool),
                                          _ptr(ns_v_pool), _ptr(beam_tok_idx), int(step), _ptr(out), _ptr(lse),
                                          _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def xattn_decode_step(desc, parent, new_k, new_v, q, shared_k, shared_v, shared_len, ns_k_pool, ns_v_pool,
+                      beam_tok_idx, step, out, lse, workspace, workspace_bytes, stream=None) -> int:
+    return int(load().xattn_decode_step(ctypes.byref(desc), _ptr(parent), _ptr(new_k), _ptr(new_v), _ptr(q),
+                                        _ptr(shared_k), _ptr(shared_v), _ptr(shared_len), _ptr(ns_k_pool),
+                                        _ptr(ns_v_pool), _ptr(beam_tok_idx), int(step), _ptr(out), _ptr(lse),
+                                        _ptr(workspace), int(workspace_bytes), _stream(stream)))
 
 
 def xattn_beam_update(desc, parent, new_k, new_v, ns_k_pool, ns_v_pool, beam_tok_idx, step, status=None,

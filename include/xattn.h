@@ -164,6 +164,22 @@ XATTN_API int xattn_beam_update(const xattn_desc* desc, const int32_t* parent, c
                       int32_t* beam_tok_idx, int32_t step, int32_t* status,
                       xattn_stream_t stream);
 
+/* One decode step with its bookkeeping: exactly xattn_beam_update(desc, parent, new_k, new_v,
+ * ns_k_pool, ns_v_pool, beam_tok_idx, step - 1, <workspace status word>) followed by
+ * xattn_decode(desc, q, ..., beam_tok_idx, step, out, lse, workspace, ...) on `stream`: the
+ * same output, LSE, pool contents, ancestry table and status bits, bit for bit (section 2.1:
+ * the Non-Shared cache is updated in place after each beam step). Requires
+ * 1 <= step <= Tmax and step*BW <= S; parent may be NULL when step == 1. When the
+ * Shared-stage kernel takes the Non-Shared part in its own tile (xattn_plan.ns_tile), it is
+ * launched as the beam update's programmatic dependent: its set-up, query loads and prefix
+ * prefetches overlap the update, and it reads the pool and the table only after the update
+ * has completed. */
+XATTN_API int xattn_decode_step(const xattn_desc* desc, const int32_t* parent, const void* new_k,
+                                const void* new_v, const void* q, const void* shared_k, const void* shared_v,
+                                const int32_t* shared_len, void* ns_k_pool, void* ns_v_pool,
+                                int32_t* beam_tok_idx, int32_t step, void* out, float* lse, void* workspace,
+                                size_t workspace_bytes, xattn_stream_t stream);
+
 /* Beam selection of one beam-search step (section 2.2, xBeam: early sort termination). For
  * each request r, candidate (b, k) with b < BW = beam_width and k < K = cand_per_beam scores
  *   beam_score[r, b] + cand_logp[r, b, k]          (one fp32 addition)
