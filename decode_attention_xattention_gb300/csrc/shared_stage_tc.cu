@@ -541,6 +541,9 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             for (int p = 0; p < npu; ++p) {
                 const int u = u0 + p, st = u % kU, use = u / kU;
                 if (use > 0 && !mbar_wait(&bars.u_empty[st], (use - 1) & 1, &abort_sh)) break;
+                if (!ns && p == kU)  // the first L2 prefetches once the first slot is free again: issued
+                    // with the first loads they competed with them for HBM across the whole grid
+                    for (int pp = kU; pp < min(npu, kU + kPrefetch); ++pp) prefetch_unit(pp);
                 if (ns ? (p + kPrefetch < npu) : (p >= kU && p + kPrefetch < npu)) prefetch_unit(p + kPrefetch);
                 uint8_t* slot = sU + st * C::kUnitBytes;
                 mbar_arrive_expect_tx(&bars.u_full[st], (p < ntiles ? C::kTileBytes : 0) + (p >= 1 ? C::kTileBytes : 0));
@@ -552,8 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                                     t0 + (p - 1) * kTcTileKeys, r);
                 }
                 issued = p + 1;
-                if (!ns && p == kU - 1)  // the first units' loads went out before any L2 prefetch
-                    for (int pp = kU; pp < min(npu, kU + kPrefetch); ++pp) prefetch_unit(pp);
+
             }
             // Staged Non-Shared piece: each row tile's piece (128 rows x d fp32, as 128-byte
             // swizzled boxes of 32 columns) for the epilogue: row tile 0 into the Q tiles once the
