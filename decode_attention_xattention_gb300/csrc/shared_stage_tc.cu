@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             // One tile: its S row in, P (bf16) back over it, running max and sum, O rescaled when
             // the max moved; valid columns [lo, lo + cnt), the rest get -inf.
             auto tile = [&](uint32_t parity, unsigned lo, unsigned cnt, bool first) -> bool {
-                if (!mbar_wait_warp(&bars.s_full[wg], parity, &abort_sh)) return false;
+                if (!mbar_wait(&bars.s_full[wg], parity, &abort_sh)) return false;
                 tc_fence_after();
                 // the whole 128-column row of S in registers with one wide load
                 uint32_t s[kTcTileKeys];
@@ -403,9 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         }
         bool beam_bad = false;
         if (have_o) {
-            if (ok && !mbar_wait_warp(&bars.o_full[wg], 0, &abort_sh)) ok = false;
-            if (ok && ns_staged && !mbar_wait_warp(&bars.ns_full[wg], 0, &abort_sh)) ok = false;
-            if (ok && ns && !mbar_wait_warp(&bars.ns_vfull[wg], 0, &abort_sh)) ok = false;  // bad_beam written
+            if (ok && !mbar_wait(&bars.o_full[wg], 0, &abort_sh)) ok = false;
+            if (ok && ns_staged && !mbar_wait(&bars.ns_full[wg], 0, &abort_sh)) ok = false;
+            if (ok && ns && !mbar_wait(&bars.ns_vfull[wg], 0, &abort_sh)) ok = false;  // bad_beam written
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
             if (!ok) {
@@ -587,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             }
         }
     } else if (warp == kWarpMma) {
-        // ============================================ MMA issuer
+        // ============================================ MMA issuer (lane 0: every MMA and commit)
         if (lane == 0 && nt > 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kTcTileKeys, 0, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
@@ -602,22 +602,52 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             const int lim_last = ntiles > 0 ? t1 - (t0 + (ntiles - 1) * kTcTileKeys) : 0;
             const int pv_steps_last = (lim_last + 15) / 16;
             const int ns_steps = (nk + 15) / 16;
-            // Descriptors are built once; an operand's descriptor for a byte offset only adds
-            // offset / 16 to the start-address field (addresses stay below 256 KB, so no carry
-            // leaves the field): few instructions per MMA for a thread that shares its issue
-            // slots with two busy softmax warps.
+            // Descriptors: an operand's descriptor for a byte offset only adds offset / 16 to the
+            // start-address field (addresses stay below 256 KB, so no carry leaves the field).
+            // Each tile's operand bases are formed once; every MMA then adds a constant.
             const uint64_t qdesc = smem_desc_sw128(smem_addr(sQ), 16, 1024);
             const uint64_t kdesc = smem_desc_sw128(smem_addr(sU), 16, 1024);
             const uint64_t vdesc = smem_desc_sw128(smem_addr(sU + C::kTileBytes), 16384, 1024);
-            auto issue_pv = [&](int i, int jt, int st) {
-                const uint32_t vo = st * C::kUnitBytes;
-                const int nk = jt == ntiles - 1 ? pv_steps_last : kTcTileKeys / 16;
+            // S_i = Q_i . K^T, the K tile at byte offset ko from the first slot's K tile.
+            auto issue_qk = [&](int i, uint32_t ko) {
+                const uint64_t qb = desc_at(qdesc, (uint32_t)i * C::kTileBytes), kb = desc_at(kdesc, ko);
+                const uint32_t d = tmem + i * 128;
 #pragma unroll
-                for (int kk = 0; kk < kTcTileKeys / 16; ++kk) {
-                    if (kk >= nk) break;
-                    mma_ts(tmem + kTmemO + i * 128, tmem + i * 128 + kk * 8, desc_at(vdesc, vo + kk * 2048), idesc_pv,
-                           (jt > 0 || ns || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_ss(d, desc_at(qb, off), desc_at(kb, off), idesc_qk, kk > 0 ? 1u : 0u);
                 }
+            };
+            // O_i (+)= P_i . V for `steps` 16-key steps, the V tile at byte offset vo from the
+            // first slot's V tile (a full tile's eight steps as one straight run of MMAs).
+            auto issue_pv = [&](int i, uint32_t vo, int steps, uint32_t acc0) {
+                const uint64_t vb = desc_at(vdesc, vo);
+                const uint32_t d = tmem + kTmemO + i * 128, a = tmem + i * 128;
+                if (steps == kTcTileKeys / 16) {
+#pragma unroll
+                    for (int kk = 0; kk < kTcTileKeys / 16; ++kk)
+                        mma_ts(d, a + kk * 8, desc_at(vb, kk * 2048), idesc_pv, kk > 0 ? 1u : acc0);
+                } else {
+                    for (int kk = 0; kk < steps; ++kk)
+                        mma_ts(d, a + kk * 8, desc_at(vb, kk * 2048), idesc_pv, kk > 0 ? 1u : acc0);
+                }
+            };
+            auto pv_tile = [&](int i, int jt, int st) {
+                issue_pv(i, (uint32_t)st * C::kUnitBytes, jt == ntiles - 1 ? pv_steps_last : kTcTileKeys / 16,
+                         (jt > 0 || ns) ? 1u : 0u);
+            };
+            // Zeroes the V rows lim_last .. end of their 16-token step in slot st (whole 128-byte
+            // rows, so the swizzle does not matter) and makes them visible to the tensor core
+            // before the last P.V.
+            auto zero_v_tail = [&](int st) {
+                uint8_t* vt = sU + st * C::kUnitBytes + C::kTileBytes;
+                for (int row = lim_last; row < pv_steps_last * 16; ++row)
+#pragma unroll
+                    for (int kb = 0; kb < C::KB; ++kb)
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch)
+                            *reinterpret_cast<uint4*>(vt + kb * 16384 + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+                fence_proxy_async_smem();
             };
             if constexpr (NST) {
                 // ---- in-tile mode. The Non-Shared tile: per row tile, Q.K^T against the gathered
@@ -625,13 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 for (int i = 0; i < ntile_m; ++i) {
                     if (!mbar_wait(&bars.ns_kfull[i], 0, &abort_sh)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t qo = i * C::kTileBytes, ko = i * C::kTileBytes;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_ss(tmem + i * 128, desc_at(qdesc, qo + off), desc_at(kdesc, ko + off), idesc_qk,
-                               kk > 0 ? 1u : 0u);
-                    }
+                    issue_qk(i, (uint32_t)i * C::kTileBytes);
                     mma_commit(&bars.s_full[i]);
                 }
                 if (ok) mma_commit(&bars.u_empty[0]);
@@ -640,26 +664,19 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 const int st0 = 2 % kU;
                 if (ok && ntiles > 0 && !mbar_wait(&bars.u_full[st0], 0, &abort_sh)) ok = false;
                 for (int i = 0; ok && i < ntile_m; ++i) {
-                    if (!mbar_wait(&bars.p_full[i], 0, &abort_sh) || !mbar_wait(&bars.ns_vfull[i], 0, &abort_sh)) {
+                    if (!mbar_wait(&bars.p_full[i], 0, &abort_sh) ||
+                        !mbar_wait(&bars.ns_vfull[i], 0, &abort_sh)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t vo = C::kUnitBytes + (i - 1) * C::kTileBytes;  // from sU + kTileBytes
-                    for (int kk = 0; kk < ns_steps; ++kk)
-                        mma_ts(tmem + kTmemO + i * 128, tmem + i * 128 + kk * 8, desc_at(vdesc, vo + kk * 2048),
-                               idesc_pv, kk > 0 ? 1u : 0u);
+                    // the gathered V tile of row tile i sits at slot 1's K position + i tiles
+                    issue_pv(i, (uint32_t)(C::kUnitBytes + (i - 1) * C::kTileBytes), ns_steps, 0u);
                     if (ntiles == 0) {
                         mma_commit(&bars.o_full[i]);  // O_i complete
                     } else {
                         tc_fence_after();
-                        const uint32_t qo = i * C::kTileBytes, ko = st0 * C::kUnitBytes;
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                            mma_ss(tmem + i * 128, desc_at(qdesc, qo + off), desc_at(kdesc, ko + off), idesc_qk,
-                                   kk > 0 ? 1u : 0u);
-                        }
+                        issue_qk(i, (uint32_t)st0 * C::kUnitBytes);
                         mma_commit(&bars.s_full[i]);
                     }
                 }
@@ -677,31 +694,15 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                         ok = false;
                         break;
                     }
-                    if (j == ntiles && (lim_last & 15) != 0) {
-                        uint8_t* vt = sU + st * C::kUnitBytes + C::kTileBytes;
-                        for (int row = lim_last; row < pv_steps_last * 16; ++row)
-#pragma unroll
-                            for (int kb = 0; kb < C::KB; ++kb)
-#pragma unroll
-                                for (int ch = 0; ch < 8; ++ch)
-                                    *reinterpret_cast<uint4*>(vt + kb * 16384 + row * 128 + ch * 16) =
-                                        make_uint4(0, 0, 0, 0);
-                        fence_proxy_async_smem();
-                    }
+                    if (j == ntiles && (lim_last & 15) != 0) zero_v_tail(st);
                     for (int i = 0; i < ntile_m; ++i) {
                         if (!mbar_wait(&bars.p_full[i], j & 1, &abort_sh)) { ok = false; break; }
                         tc_fence_after();
-                        issue_pv(i, j - 1, st);
+                        pv_tile(i, j - 1, st);
                         if (j == ntiles) mma_commit(&bars.o_full[i]);  // O_i complete
                         if (j < ntiles) {
                             tc_fence_after();
-                            const uint32_t qo = i * C::kTileBytes, ko = st * C::kUnitBytes;
-#pragma unroll
-                            for (int kk = 0; kk < D / 16; ++kk) {
-                                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                                mma_ss(tmem + i * 128, desc_at(qdesc, qo + off), desc_at(kdesc, ko + off), idesc_qk,
-                                       kk > 0 ? 1u : 0u);
-                            }
+                            issue_qk(i, (uint32_t)st * C::kUnitBytes);
                             mma_commit(&bars.s_full[i]);
                         }
                     }
@@ -719,34 +720,17 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                         ok = false;
                         break;
                     }
-                    if (j == ntiles && (lim_last & 15) != 0) {
-                        // zero V rows lim_last .. end of their 16-token step (whole 128-byte rows,
-                        // so the swizzle does not matter), then make them visible to the tensor core
-                        uint8_t* vt = sU + st * C::kUnitBytes + C::kTileBytes;
-                        for (int row = lim_last; row < pv_steps_last * 16; ++row)
-#pragma unroll
-                            for (int kb = 0; kb < C::KB; ++kb)
-#pragma unroll
-                                for (int ch = 0; ch < 8; ++ch)
-                                    *reinterpret_cast<uint4*>(vt + kb * 16384 + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
-                        fence_proxy_async_smem();
-                    }
+                    if (j == ntiles && (lim_last & 15) != 0) zero_v_tail(st);
                     for (int i = 0; i < ntile_m; ++i) {
                         if (j > 0) {
                             if (!mbar_wait(&bars.p_full[i], (j - 1) & 1, &abort_sh)) { ok = false; break; }
                             tc_fence_after();
-                            issue_pv(i, j - 1, st);
+                            pv_tile(i, j - 1, st);
                             if (j == ntiles) mma_commit(&bars.o_full[i]);  // O_i complete
                         }
                         if (j < ntiles) {
                             tc_fence_after();
-                            const uint32_t qo = i * C::kTileBytes, ko = st * C::kUnitBytes;
-#pragma unroll
-                            for (int kk = 0; kk < D / 16; ++kk) {
-                                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                                mma_ss(tmem + i * 128, desc_at(qdesc, qo + off), desc_at(kdesc, ko + off), idesc_qk,
-                                       kk > 0 ? 1u : 0u);
-                            }
+                            issue_qk(i, (uint32_t)st * C::kUnitBytes);
                             mma_commit(&bars.s_full[i]);
                         }
                     }
