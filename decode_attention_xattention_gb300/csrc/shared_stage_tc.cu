@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             // One tile: its S row in, P (bf16) back over it, running max and sum, O rescaled when
             // the max moved; valid columns [lo, lo + cnt), the rest get -inf.
             auto tile = [&](uint32_t parity, unsigned lo, unsigned cnt, bool first) -> bool {
-                if (!mbar_wait(&bars.s_full[wg], parity, &abort_sh)) return false;
+                if (!mbar_wait_all(&bars.s_full[wg], parity, &abort_sh)) return false;
                 tc_fence_after();
                 // the whole 128-column row of S in registers with one wide load
                 uint32_t s[kTcTileKeys];
@@ -403,9 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         }
         bool beam_bad = false;
         if (have_o) {
-            if (ok && !mbar_wait(&bars.o_full[wg], 0, &abort_sh)) ok = false;
-            if (ok && ns_staged && !mbar_wait(&bars.ns_full[wg], 0, &abort_sh)) ok = false;
-            if (ok && ns && !mbar_wait(&bars.ns_vfull[wg], 0, &abort_sh)) ok = false;  // bad_beam written
+            if (ok && !mbar_wait_all(&bars.o_full[wg], 0, &abort_sh)) ok = false;
+            if (ok && ns_staged && !mbar_wait_all(&bars.ns_full[wg], 0, &abort_sh)) ok = false;
+            if (ok && ns && !mbar_wait_all(&bars.ns_vfull[wg], 0, &abort_sh)) ok = false;  // bad_beam written
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
             if (!ok) {
