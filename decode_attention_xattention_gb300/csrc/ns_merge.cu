@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(32, piece_ctas_per_sm(D)) ns_piece_kernel(
 #pragma unroll 1
         for (int cb = 0; cb < nbk; ++cb) {
             const int buf = (int)(cseq % kRingBlocks);
-            if (!ptx::mbar_wait_warp(&full[buf], (cseq / kRingBlocks) & 1, abort_sh)) { ok = false; break; }
+            if (!ptx::mbar_wait_all(&full[buf], (cseq / kRingBlocks) & 1, abort_sh)) { ok = false; break; }
             bad = bad || buf_bad[buf] != 0;
             const bool last = cb == nbk - 1;
             if (!bad) {
