@@ -426,6 +426,7 @@ __global__ void __launch_bounds__(32, piece_ctas_per_sm(D)) ns_piece_kernel(
         for (int cb = 0; cb < nbk; ++cb) {
             const int buf = (int)(cseq % kRingBlocks);
             if (!ptx::mbar_wait_all(&full[buf], (cseq / kRingBlocks) & 1, abort_sh)) { ok = false; break; }
+            __syncwarp();  // the zero rows other lanes stored are visible to this lane's ldmatrix
             bad = bad || buf_bad[buf] != 0;
             const bool last = cb == nbk - 1;
             if (!bad) {
