@@ -267,9 +267,10 @@ __device__ __forceinline__ NsPiece ns_piece_of(const Geometry& g, unsigned npc, 
 // One warp per CTA, persistent: the grid is one wave of resident CTAs and CTA w takes the
 // pieces w, w + gridDim.x, ... in turn. A piece is cut into blocks of 16 positions; the
 // warp's blocks, across piece boundaries, stream through a ring of kRingBlocks buffers:
-// every pool row of a block (2d contiguous bytes of one head) is requested by one bulk copy
-// completing on the buffer's mbarrier, and a buffer is refilled with the block kRingBlocks
-// ahead as soon as its block is computed. The ring is kept short so that many warps fit on
+// the pool rows of a block (2d contiguous bytes of one head each) are copied 16 bytes per
+// lane with cp.async (half the warp K rows, half V rows), every lane's copies completing on
+// the buffer's mbarrier (one cp.async arrival per lane), and a buffer is refilled with the
+// block kRingBlocks ahead as soon as its block is computed. The ring is kept short so that many warps fit on
 // an SM: the warps' arithmetic is a chain of dependent steps, and it is the number of
 // warps, not the depth of one warp's ring, that keeps both the SM and HBM busy. The
 // ancestry slots of the next piece are loaded a piece ahead, its Q rows as soon as the
@@ -307,7 +308,7 @@ __global__ void __launch_bounds__(32, piece_ctas_per_sm(D)) ns_piece_kernel(
     const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
     const int stride = (int)gridDim.x;
     if (lane == 0) {
-        for (int j = 0; j < kRingBlocks; ++j) ptx::mbar_init(&full[j], 1);
+        for (int j = 0; j < kRingBlocks; ++j) ptx::mbar_init(&full[j], 32);  // one cp.async arrival per lane
         *abort_sh = 0;
         ptx::fence_barrier_init();
     }
@@ -358,17 +359,22 @@ __global__ void __launch_bounds__(32, piece_ctas_per_sm(D)) ns_piece_kernel(
         // zeroing below) are ordered before the copies that overwrite it
         ptx::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-            buf_bad[buf] = ibad ? 1 : 0;
-            ptx::mbar_arrive_expect_tx(&full[buf], ibad ? 0u : (uint32_t)(cnt * 2 * RB));
+        if (lane == 0) buf_bad[buf] = ibad ? 1 : 0;
+        // position k of the block: lanes 0..15 copy its K row, 16..31 its V row, 16 bytes each
+        if (!ibad) {
+            const int ch = lane & 15;
+            for (int k = 0; k < cnt; ++k) {
+                const int tk = t0 + k;
+                const int sv = __shfl_sync(0xffffffffu, tk < 32 ? is_a : is_b, tk & 31);
+                const size_t off = (((size_t)ip.r * g.S + sv) * g.Hkv + ip.h) * D;
+                const __nv_bfloat16* src = (lane < 16 ? pool_k : pool_v) + off;
+                uint8_t* dst = (lane < 16 ? k_sm : v_sm) + (buf * kPieceBlk + k) * RS;
+                if (ch < RB / 16) ptx::cp_async_16(ptx::smem_addr(dst + ch * 16), reinterpret_cast<const uint8_t*>(src) + ch * 16);
+                if (RB / 16 > 16) ptx::cp_async_16(ptx::smem_addr(dst + (ch + 16) * 16), reinterpret_cast<const uint8_t*>(src) + (ch + 16) * 16);
+            }
         }
-        const int tl = t0 + (lane & 15);  // lanes 0..15: K rows, 16..31: V rows of the block
-        const int sv = __shfl_sync(0xffffffffu, t0 < 32 ? is_a : is_b, tl & 31);
-        if (!ibad && (lane & 15) < cnt) {
-            const size_t off = (((size_t)ip.r * g.S + sv) * g.Hkv + ip.h) * D;
-            uint8_t* dst = (lane < 16 ? k_sm : v_sm) + (buf * kPieceBlk + (lane & 15)) * RS;
-            ptx::bulk_load(dst, (lane < 16 ? pool_k : pool_v) + off, RB, &full[buf]);
-        }
+        // each lane's arrival completes once its copies have landed
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(ptx::smem_addr(&full[buf])) : "memory");
         if (cnt < kPieceBlk) {
             // V rows past the piece are read by the MMA with weight 0: make them 0
             for (int e = lane; e < (kPieceBlk - cnt) * (RB / 16); e += 32)
