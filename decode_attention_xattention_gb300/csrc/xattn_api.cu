@@ -49,10 +49,9 @@ int check_desc(const xattn_desc* d) {
     if (d->split_tokens < 0 || d->split_tokens % kPieceGrain != 0) return XATTN_ERR_INVALID_ARG;
     if (d->shared_kernel < 0 || d->shared_kernel > 2) return XATTN_ERR_INVALID_ARG;
     if (d->dtype != XATTN_DTYPE_BF16 && d->dtype != XATTN_DTYPE_F32) return XATTN_ERR_UNSUPPORTED;
-    // fp32 inputs run on the CUDA-core kernels: the CUDA-core Shared stage and the direct
-    // walk of at most kNsDirectMax Non-Shared tokens
-    if (d->dtype == XATTN_DTYPE_F32 && (d->shared_kernel == 1 || d->max_steps > kNsDirectMax))
-        return XATTN_ERR_UNSUPPORTED;
+    // fp32 inputs: the Shared stage on CUDA cores or on the tf32 tensor-core kernel; the
+    // Non-Shared part by the direct walk of at most kNsDirectMax tokens
+    if (d->dtype == XATTN_DTYPE_F32 && d->max_steps > kNsDirectMax) return XATTN_ERR_UNSUPPORTED;
     if (d->out_dtype != XATTN_DTYPE_BF16 && d->out_dtype != XATTN_DTYPE_F32) return XATTN_ERR_UNSUPPORTED;
     if (d->head_dim != 64 && d->head_dim != 128) return XATTN_ERR_UNSUPPORTED;
     const int G = d->num_q_heads / d->num_kv_heads;
@@ -92,8 +91,10 @@ void plan(const xattn_desc* d, int step, Geometry* g, int* kernel) {
     // padding still streams the prefix at HBM speed (the MMA and exp work hide under the
     // loads), which the CUDA-core kernel does not reach. The CUDA-core kernel stays
     // selectable (shared_kernel = 2).
+    // fp32 storage: CUDA cores by default (fp32 arithmetic throughout), the tf32 tensor-core
+    // kernel (3) when asked for tensor cores.
     int k = 0;
-    if (g->Lmax > 0) k = g->in_f32 ? 2 : (d->shared_kernel ? d->shared_kernel : 1);
+    if (g->Lmax > 0) k = g->in_f32 ? (d->shared_kernel == 1 ? 3 : 2) : (d->shared_kernel ? d->shared_kernel : 1);
     *kernel = k;
     const int tiles = g->Lmax > 0 ? cdiv(g->Lmax, kPieceGrain) : 1;
     if (d->split_tokens > 0) {
@@ -101,9 +102,10 @@ void plan(const xattn_desc* d, int step, Geometry* g, int* kernel) {
     } else if (k == 0) {
         g->split_tokens = kPieceGrain;
     } else {
-        // tensor-core CTAs own two 128-row tiles; CUDA-core CTAs own four rows
-        const int64_t units = (int64_t)g->R * g->Hkv * (k == 1 ? cdiv(g->row_tiles, 2) : cdiv(g->M, 4));
-        const int64_t slots = (int64_t)device_sms() * (k == 1 ? 1 : 8);
+        // tensor-core CTAs own two 128-row tiles (tf32: one); CUDA-core CTAs own four rows
+        const int64_t units =
+            (int64_t)g->R * g->Hkv * (k == 1 ? cdiv(g->row_tiles, 2) : (k == 3 ? g->row_tiles : cdiv(g->M, 4)));
+        const int64_t slots = (int64_t)device_sms() * (k == 2 ? 8 : 1);
         int best_n = 1;
         double best = 1e30;
         for (int n = 1; n <= tiles; ++n) {
@@ -198,7 +200,10 @@ int xattn_query_plan(const xattn_desc* desc, int32_t step, xattn_plan* out) {
     out->split_tokens = g.split_tokens;
     out->rows_per_unit = g.M;
     out->row_tiles = g.row_tiles;
-    out->shared_ctas = k == 0 ? 0 : (k == 1 ? shared_tc_ctas_for(g) : g.R * g.Hkv * ((g.M + 3) / 4) * g.nsplit);
+    out->shared_ctas = k == 0   ? 0
+                       : k == 1 ? shared_tc_ctas_for(g)
+                       : k == 3 ? g.R * g.Hkv * g.row_tiles * g.nsplit
+                                : g.R * g.Hkv * ((g.M + 3) / 4) * g.nsplit;
     out->fused = decode_is_fused(g, k, step) ? 1 : 0;
     out->ns_tile = ns_tile_fits(g, k, step) ? 1 : 0;
     out->piece_stride = g.pieces;
@@ -274,6 +279,8 @@ int run_shared(const Geometry& g, int kernel, const void* q, const void* shared_
                                    fused, nst, st);
     } else if (kernel == 2) {
         e = launch_shared_stage_simt(g, q, shared_k, shared_v, shared_len, ws.part_o, ws.part_lse, ws.status, st);
+    } else if (kernel == 3) {
+        e = launch_shared_stage_tf32(g, q, shared_k, shared_v, shared_len, ws.part_o, ws.part_lse, ws.status, st);
     }
     return e == cudaSuccess ? XATTN_OK : XATTN_ERR_CUDA;
 }

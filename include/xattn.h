@@ -92,11 +92,13 @@ typedef struct xattn_desc {
     int32_t max_steps;      /* Tmax: row length of beam_tok_idx                            */
     float softmax_scale;    /* 0 selects 1/sqrt(d)                                         */
     int32_t dtype;          /* storage of q, K, V, the pools and new tokens: XATTN_DTYPE_BF16,
-                               or XATTN_DTYPE_F32 (used unrounded, on the CUDA-core kernels:
-                               shared_kernel must be 0 or 2 and max_steps <= 32, else
-                               XATTN_ERR_UNSUPPORTED)                                      */
-    int32_t shared_kernel;  /* Shared-stage kernel: 0 automatic (tensor cores), 1 tensor
-                               cores, 2 CUDA cores                                         */
+                               or XATTN_DTYPE_F32 (read without a bf16 step; max_steps <= 32,
+                               else XATTN_ERR_UNSUPPORTED). fp32 Shared stage: shared_kernel
+                               0 or 2 runs it on CUDA cores in fp32, 1 on the tensor cores
+                               with tcgen05 kind::tf32 (operands multiplied with 10 mantissa
+                               bits, fp32 accumulation); the Non-Shared part stays fp32.   */
+    int32_t shared_kernel;  /* Shared-stage kernel: 0 automatic (tensor cores for bf16, CUDA
+                               cores for fp32), 1 tensor cores, 2 CUDA cores               */
     int32_t split_tokens;   /* prefix tokens per Shared-stage piece: 0 automatic, else a
                                multiple of 128                                             */
     int32_t out_dtype;      /* dtype of `out`: XATTN_DTYPE_BF16 (0) or XATTN_DTYPE_F32      */
@@ -243,7 +245,9 @@ XATTN_API int xattn_read_status(void* workspace, int32_t* status_out, int32_t cl
 
 /* How xattn_decode will run these shapes (for tests and reports). */
 typedef struct xattn_plan {
-    int32_t shared_kernel;    /* 0 none (Lmax == 0), 1 tensor-core (tcgen05), 2 CUDA-core */
+    int32_t shared_kernel;    /* 0 none (Lmax == 0), 1 tensor-core (tcgen05 kind::f16),
+                                 2 CUDA-core, 3 tensor-core tf32 (tcgen05 kind::tf32, fp32
+                                 storage)                                                  */
     int32_t num_splits;       /* pieces the prefix is cut into                           */
     int32_t split_tokens;     /* tokens per piece (multiple of 128)                      */
     int32_t rows_per_unit;    /* M = BW * G stacked query rows per (request, KV head)    */

@@ -152,15 +152,21 @@ def test_plan_properties_over_shapes(lib):
 
 
 def test_fp32_inputs_plan_and_limits(lib):
-    """fp32 storage runs on the CUDA-core kernels: the planner picks the CUDA-core Shared
-    stage and the unfused path; the tensor-core kernel and Non-Shared parts longer than the
+    """fp32 storage: by default the planner picks the CUDA-core Shared stage (fp32 throughout)
+    and the unfused path; asking for tensor cores picks the tf32 kernel (3), one CTA per
+    (request, KV head, piece, 128-row tile), still unfused. Non-Shared parts longer than the
     direct walk (32 tokens) are rejected before any launch, as is an unknown dtype."""
     f32 = xattn.XATTN_DTYPE_F32
     d = xattn.make_desc(1, 4, 2, 1, 64, 256, 12, 3, 0.0, 0, 0, f32, f32)
     rc, p = xattn.xattn_query_plan(d, 3)
     assert rc == 0 and p.shared_kernel == 2 and p.fused == 0
     assert xattn.xattn_decode_workspace_size(d) > 0
-    for bad in (xattn.make_desc(1, 4, 2, 1, 64, 256, 12, 3, 0.0, 1, 0, f32, f32),
+    d = xattn.make_desc(2, 96, 16, 4, 128, 1000, 96 * 3, 3, 0.0, 1, 256, f32, f32)
+    rc, p = xattn.xattn_query_plan(d, 3)
+    assert rc == 0 and p.shared_kernel == 3 and p.fused == 0 and p.ns_tile == 0
+    assert p.row_tiles == 3 and p.num_splits == 4 and p.shared_ctas == 2 * 4 * 3 * 4
+    assert xattn.xattn_decode_workspace_size(d) > 0
+    for bad in (xattn.make_desc(1, 4, 2, 1, 64, 256, 4 * 33, 33, 0.0, 1, 0, f32, f32),
                 xattn.make_desc(1, 4, 2, 1, 64, 256, 4 * 33, 33, 0.0, 0, 0, f32, f32),
                 xattn.make_desc(1, 4, 2, 1, 64, 256, 12, 3, 0.0, 0, 0, f32, 7)):
         assert xattn.xattn_decode_workspace_size(bad) == 0

@@ -200,11 +200,85 @@ def test_tiny_config_both_kernels():
 TOL_F32 = (2e-5, 2e-6, 2e-5)
 
 
-@pytest.mark.parametrize("kernel", [0, 2])
+def check_tf32(w, split_tokens=0):
+    """fp32 storage with the Shared stage on the tensor cores (tcgen05 kind::tf32), against
+    the fp64 oracle within a bound derived from the tf32 operands, per row:
+      each prefix logit z = scale * q.k is off by at most eps = scale * 2^-9 * max_k sum|q_i k_i|
+      (both operands carry at most 2^-10 relative error; fp32 accumulation adds far less), so
+      every softmax weight moves by a factor within [e^-2eps, e^2eps] and their total
+      variation is at most e^2eps - 1; P and V enter the P.V product with 2^-10 relative
+      error each. Hence |dout| <= max|v| * ((e^2eps - 1) + 2^-9 e^2eps) and |dlse| <= eps,
+      plus a 1e-5 allowance for the fp32 arithmetic of the rest of the path (the Non-Shared
+      part and the merge are fp32)."""
+    orc = oracle.load()
+    db = DeviceBatch(wl.make_inputs(w), shared_kernel=1, split_tokens=split_tokens, out_fp32=True, input_f32=True)
+    assert db.plan().shared_kernel == 3 and db.input_f32 and db.pool_k.dtype == torch.float32
+    inp = db.inputs
+    db.build_cache()
+    xattn.check(db.decode())
+    torch.cuda.synchronize()
+    assert db.read_status() == 0
+    pk, pv, idx = oracle.build_cache(orc, inp)
+    ref_o, ref_l = orc.decode(oracle.dims_of(w), inp.q, inp.shared_k, inp.shared_v, inp.shared_len, pk, pv, idx,
+                              w.steps)
+    got_o = db.out.float().cpu().numpy().reshape(-1, w.head_dim).astype(np.float64)
+    got_l = db.lse.cpu().numpy().reshape(-1).astype(np.float64)
+    R, BW, Hq, Hkv, d = w.num_requests, w.beam_width, w.num_q_heads, w.num_kv_heads, w.head_dim
+    G = Hq // Hkv
+    scale = w.softmax_scale if w.softmax_scale > 0 else 1.0 / np.sqrt(d)
+    q = np.abs(np.asarray(inp.q, np.float64)).reshape(R, BW, Hkv, G, d)
+    eps = np.zeros((R, BW, Hkv, G))
+    vmax = np.zeros((R, Hkv))
+    for r in range(R):
+        L = int(inp.shared_len[r])
+        for h in range(Hkv):
+            vmax[r, h] = max(np.abs(np.asarray(pv[r, :, h], np.float64)).max(),
+                             np.abs(np.asarray(inp.shared_v[r, :L, h], np.float64)).max() if L else 0.0)
+            if L:
+                kabs = np.abs(np.asarray(inp.shared_k[r, :L, h], np.float64))
+                eps[r, :, h] = scale * 2.0 ** -9 * np.einsum("bgd,ld->bgl", q[r, :, h], kabs).max(axis=-1)
+    grow = np.exp(2 * eps)
+    bound_o = (vmax[:, None, :, None] * ((grow - 1) + 2.0 ** -9 * grow) + 1e-5).reshape(-1, 1)
+    bound_l = (eps + 1e-5).reshape(-1)
+    assert bound_o.max() < 0.5, bound_o.max()  # not vacuous for these inputs (|v| up to ~4)
+    err_o = np.abs(got_o - ref_o)
+    err_l = np.abs(got_l - ref_l)
+    assert np.isfinite(got_o).all() and np.isfinite(got_l).all()
+    assert (err_o <= bound_o).all(), (err_o.max(), float(bound_o.min()))
+    assert (err_l <= bound_l).all(), (err_l.max(), float(bound_l.min()))
+    # The bound is a worst case over operand errors of one sign; on these random inputs the
+    # errors average about 1e-4, while a key dropped or counted twice moves outputs by about
+    # 1/L: a regression guard on the mean.
+    assert err_o.mean() <= 1e-3, err_o.mean()
+    stats = dict(max=float(err_o.max()), mean=float(err_o.mean()), lse=float(err_l.max()),
+                 bound_min=float(bound_o.min()), bound_mean=float(bound_o.mean()),
+                 worst_ratio=float((err_o / bound_o).max()))
+    print(w.name, stats)
+    return stats
+
+
+@pytest.mark.parametrize("kernel", [0, 1, 2])
 def test_tiny_config_native_fp32(kernel):
-    """The Tiny configuration as specified: fp32 Q/K/V used unrounded (no bf16 step)."""
+    """The Tiny configuration as specified: fp32 Q/K/V used unrounded (no bf16 step): fp32
+    arithmetic on the CUDA cores (kernels 0 and 2), or the tensor cores in tf32 (kernel 1,
+    within the bound check_tf32 derives)."""
+    if kernel == 1:
+        check_tf32(wl.TINY)
+        return
     stats, db, _ = run_and_check(wl.TINY, shared_kernel=kernel, input_f32=True, tol=TOL_F32)
     assert db.input_f32 and db.plan().shared_kernel == 2 and db.pool_k.dtype == torch.float32
+
+
+@pytest.mark.parametrize("shape,split", [((2, 48, 8, 2, 128, (700, 0), 3), 256),
+                                         ((1, 64, 16, 1, 64, (300,), 5), 0),
+                                         ((2, 8, 4, 4, 128, (130, 129), 2), 128)],
+                         ids=["d128_2rowtiles_split_emptyprefix", "d64_G16_8rowtiles", "d128_G1_ragged"])
+def test_tf32_shapes(shape, split):
+    """The tf32 Shared stage on several row tiles, split and ragged prefixes (64-key tiles with
+    a ragged last tile), an empty prefix next to a full one, d = 64 and 128, G = 1 and 16."""
+    R, BW, Hq, Hkv, d, lens, T = shape
+    w = wl.custom(R=R, BW=BW, Hq=Hq, Hkv=Hkv, d=d, lens=lens, T=T, seed=60 + T, input_dtype="fp32")
+    check_tf32(w, split_tokens=split)
 
 
 @pytest.mark.parametrize("shape", [(2, 6, 8, 2, 128, (300, 129), 5), (1, 3, 16, 1, 64, (0,), 32),
