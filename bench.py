@@ -479,6 +479,7 @@ CONFIG_ORDER = ["gr_r8_bw128_h32x8_d128_L2048_t3", "tiny_r1_bw4_h2x1_d64_L256_t3
                 "long_r2_bw256_h32x8_d128_L32768+20000_t8", "feather_g1_seq64_h32x8_d128_L8192_s512",
                 "feather_g8_seq64_h32x8_d128_L8192_s512", "feather_g64_seq64_h32x8_d128_L8192_s512"]
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # 152 SMs x 128 fp32 FMA lanes x 2 flop x 2.07 GHz
+TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense tf32 / bf16 tensor rates (the measured peak is bf16)
 
 
 def ns_merge_bytes(w, plan, idx_np, elem):
@@ -503,7 +504,7 @@ def beam_update_bytes(w, elem):
     return 2 * R * BW * w.num_kv_heads * w.head_dim * 2 * elem + 2 * R * BW * T * 4 + R * BW * 4
 
 
-def measure_config(w, local, stream, peaks, peak_src, l2, cpu_budget_s, target_s=0.3):
+def measure_config(w, local, stream, peaks, peak_src, l2, cpu_budget_s, target_s=0.3, shared_kernel=0):
     """One workload measured the way the headline line is: CUDA-graph replays of one step
     (beam update + decode) on inputs resident in HBM, with either rotating copies of the
     inputs that together exceed twice the L2, or (small workloads) the L2 flushed before
@@ -521,7 +522,7 @@ def measure_config(w, local, stream, peaks, peak_src, l2, cpu_budget_s, target_s
     inp = wl.make_inputs(w)
     if not f32:
         inp = inp.as_bf16()
-    base = DeviceBatch(inp, device=f"cuda:{local}", stream=stream, input_f32=f32)
+    base = DeviceBatch(inp, device=f"cuda:{local}", stream=stream, input_f32=f32, shared_kernel=shared_kernel)
     with torch.cuda.stream(stream):
         base.build_cache(steps=T - 1)
     set_bytes = sum(t.numel() * t.element_size() for t in
@@ -608,35 +609,38 @@ def measure_config(w, local, stream, peaks, peak_src, l2, cpu_budget_s, target_s
             w.num_requests * w.beam_width * w.num_q_heads * w.head_dim * elem + \
             w.num_requests * w.num_kv_heads * plan.num_splits * M * (w.head_dim + 1) * 4
         kernels["shared_stage_alone"] = (
-            "shared_stage_tc" if plan.shared_kernel == 1 else "shared_stage_simt", flops, sbytes,
-            "tensor" if plan.shared_kernel == 1 else "alu")
+            {1: "shared_stage_tc", 2: "shared_stage_simt", 3: "shared_stage_tf32"}[plan.shared_kernel], flops, sbytes,
+            "tensor" if plan.shared_kernel in (1, 3) else "alu")
     if "merge_alone" in ms:
         kernels["merge_alone"] = ("ns_merge", 0.0, ns_merge_bytes(w, plan, idx_np, elem), None)
     kernels["beam_update"] = ("beam_update", 0.0, beam_update_bytes(w, elem), None)
     dom = max(kernels, key=lambda k: ms[k])
     kname, kflops, kbytes, compute_kind = kernels[dom]
     t_hbm = kbytes / (peaks["hbm_gbs"] * 1e9)
-    cpeak = peaks["bf16_tflops"] if compute_kind == "tensor" else FP32_ALU_TFLOPS
+    tf32 = plan.shared_kernel == 3
+    cpeak = (peaks["bf16_tflops"] * (TF32_OVER_BF16 if tf32 else 1.0)) if compute_kind == "tensor" else FP32_ALU_TFLOPS
     t_c = kflops / (cpeak * 1e12) if kflops > 0 else 0.0
     s_k = ms[dom] * 1e-3
     if t_c > t_hbm:
         roof = {"kernel": kname, "stage": dom, "bound": compute_kind, "achieved": kflops / s_k / 1e12,
                 "peak": cpeak, "unit": "TFLOP/s", "frac": kflops / s_k / 1e12 / cpeak,
                 "algorithmic_per_launch": kflops,
-                "peak_source": f"{peak_src} (burst; kernel timed alone)" if compute_kind == "tensor" else
+                "peak_source": (f"{peak_src} bf16 burst x 1.1/2.25 (nominal tf32/bf16)" if tf32 else
+                                f"{peak_src} (burst; kernel timed alone)") if compute_kind == "tensor" else
                 "fp32 FMA issue rate: 152 SMs x 128 lanes x 2 flop x 2.07 GHz"}
     else:
         roof = {"kernel": kname, "stage": dom, "bound": "hbm", "achieved": kbytes / s_k / 1e9,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": kbytes / s_k / 1e9 / peaks["hbm_gbs"],
                 "algorithmic_per_launch": kbytes, "peak_source": f"{peak_src} (copy bandwidth)"}
     src = {"shared_stage_tc": "shared_stage_tc.cu", "shared_stage_simt": "shared_stage_simt.cu",
-           "ns_merge": "ns_merge.cu", "beam_update": "beam_update.cu"}[kname]
+           "shared_stage_tf32": "shared_stage_tf32.cu", "ns_merge": "ns_merge.cu", "beam_update": "beam_update.cu"}[kname]
     roof["traffic"] = profile_traffic(src, w.name)
     step_s = ms["step"] * 1e-3
     t_bind = max(ub / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
     entry = {
         "config": config_of(w, {"shared_splits": plan.num_splits, "split_tokens": plan.split_tokens,
-                                "shared_kernel": {0: "none", 1: "tcgen05", 2: "cuda-core"}[plan.shared_kernel],
+                                "shared_kernel": {0: "none", 1: "tcgen05", 2: "cuda-core",
+                                                  3: "tcgen05-tf32"}[plan.shared_kernel],
                                 "fused_ns_merge": bool(plan.fused), "dtype": "f32" if f32 else "bf16"}),
         "l2": (f"L2 flushed (a {flush_buf.numel() * 4 / 1e6:.0f} MB write) before every timed step; per-step CUDA "
                f"events" if flush else f"{nsets} rotating copies of the {set_bytes / 1e6:.0f} MB input set "
@@ -1072,6 +1076,12 @@ def main():
             line["configs"][name] = measure_config(
                 wl.ALL[name], local, stream, peaks, peak_src, l2,
                 0.0 if (args.no_cpu_baseline or rank != 0) else args.config_cpu_seconds)
+            if wl.ALL[name].input_dtype == "fp32":
+                # fp32 storage runs on the CUDA cores by default; its tensor-core (tf32) Shared
+                # stage measured the same way beside it
+                e = measure_config(wl.ALL[name], local, stream, peaks, peak_src, l2, 0.0, shared_kernel=1)
+                line["configs"][name]["tensor_core_tf32"] = {
+                    k: e[k] for k in ("us_per_step", "beams_per_s", "stage_us", "roofline", "config")}
         line["configs_clocks"] = sampler.stop()
     if rank == 0:
         print(json.dumps(line), flush=True)
