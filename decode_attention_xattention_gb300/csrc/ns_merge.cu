@@ -705,6 +705,16 @@ __global__ void __launch_bounds__(256) ns_merge_kernel(
         if (lane == 0) set_status(status, XATTN_STATUS_EMPTY_ROW);
     }
 
+    // The pieces' LSEs of the G rows, lane l holding piece l (of the first 32), loaded before the
+    // Non-Shared walk so that their round trip overlaps it.
+    const size_t unit = (size_t)r * g.Hkv + h;
+    const int np = g.nsplit + g.ns_pieces;
+    const size_t prow_b = unit * g.pieces * g.M + (size_t)b * G;  // piece c row gg: + c*M + gg
+    float lc0[G];
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg)
+        lc0[gg] = (!bad && lane < np) ? __ldg(part_lse + prow_b + (size_t)lane * g.M + gg) : -INFINITY;
+
     RowState<E, G> st;
     st.init();
     bool slot_bad = false;
@@ -715,68 +725,87 @@ __global__ void __launch_bounds__(256) ns_merge_kernel(
 
     // Merge: fold every stored piece (prefix pieces, then Non-Shared pieces) into the
     // running state. A piece stores its normalised output o_c and natural-log lse_c; in
-    // base 2 it contributes weight 2^(lse_c * log2 e) times o_c. First pass: the pieces'
-    // LSEs, lane-parallel (lane l holds pieces c = l, l+32, ...), give each row's maximum
-    // and weights; second pass: weighted outputs, four pieces' loads in flight.
+    // base 2 it contributes weight 2^(lse_c * log2 e) times o_c. First pass, the G rows
+    // together: each lane keeps a running maximum and sum of its pieces' weights (pieces
+    // c = l, l + 32, ...), then the warp combines them. Second pass, row by row: the weighted
+    // outputs, eight pieces' rows in flight.
     if (!bad) {
-        const size_t unit = (size_t)r * g.Hkv + h;
-        const int np = g.nsplit + g.ns_pieces;
-        const size_t prow_b = unit * g.pieces * g.M + (size_t)b * G;  // piece c row gg: + c*M + gg
+        float pm[G], ps[G];
+        bool nan_seen = false;
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) {
-            float mx = st.m[gg];
-            bool nan_seen = false;
-            for (int c = lane; c < np; c += 32) {
-                const float lc = __ldg(part_lse + prow_b + (size_t)c * g.M + gg);
-                nan_seen |= (lc != lc);
-                mx = fmaxf(mx, lc * kLog2e);
+            pm[gg] = -INFINITY;
+            ps[gg] = 0.f;
+        }
+        for (int c = lane; c < np; c += 32) {
+            float lc[G];
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg)
+                lc[gg] = c < 32 ? lc0[gg] : __ldg(part_lse + prow_b + (size_t)c * g.M + gg);
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg) {
+                nan_seen |= (lc[gg] != lc[gg]);
+                const float sv = lc[gg] * kLog2e;
+                if (sv > pm[gg]) {
+                    ps[gg] = ps[gg] * ex2(pm[gg] - sv) + 1.f;
+                    pm[gg] = sv;
+                } else if (sv > -INFINITY) {
+                    ps[gg] += ex2(sv - pm[gg]);
+                }
             }
+        }
+        if (__any_sync(0xffffffffu, nan_seen)) bad = true;  // a failed piece poisons the row
+        if (!bad) {
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            if (__any_sync(0xffffffffu, nan_seen)) bad = true;  // a failed piece poisons the row
-            if (mx == -INFINITY) continue;                      // nothing at all for this row
-            const float alpha = ex2(st.m[gg] - mx);             // rescale the Non-Shared state
-            float lsum = 0.f;
-            for (int c = lane; c < np; c += 32) {
-                const float lc = __ldg(part_lse + prow_b + (size_t)c * g.M + gg);
-                lsum += (lc > -INFINITY) ? ex2(lc * kLog2e - mx) : 0.f;
-            }
-            lsum = warp_sum(lsum);
-            float acc[E];
+            for (int gg = 0; gg < G; ++gg) {
+                float mp = pm[gg];
 #pragma unroll
-            for (int e = 0; e < E; ++e) acc[e] = st.acc[gg][e] * alpha;
-            for (int c0 = 0; c0 < np; c0 += 4) {
-                float ov[4][E], wv[4];
+                for (int o = 16; o > 0; o >>= 1) mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
+                const float mx = fmaxf(st.m[gg], mp);
+                if (mx == -INFINITY) continue;  // nothing at all for this row
+                const float lsum = warp_sum(pm[gg] > -INFINITY ? ps[gg] * ex2(pm[gg] - mx) : 0.f);
+                const float alpha = ex2(st.m[gg] - mx);  // rescale the Non-Shared state
+                float acc[E];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int c = c0 + u;
-                    wv[u] = 0.f;
-                    if (c < np) {
-                        const size_t prow = prow_b + (size_t)c * g.M + gg;
-                        const float lc = __ldg(part_lse + prow);
-                        wv[u] = (lc > -INFINITY) ? ex2(lc * kLog2e - mx) : 0.f;
-                        const float* po = part_o + prow * D + lane * E;
-                        if constexpr (E == 4) {
-                            const float4 t = __ldg(reinterpret_cast<const float4*>(po));
-                            ov[u][0] = t.x; ov[u][1] = t.y; ov[u][2] = t.z; ov[u][3] = t.w;
-                        } else {
-                            const float2 t = __ldg(reinterpret_cast<const float2*>(po));
-                            ov[u][0] = t.x; ov[u][1] = t.y;
+                for (int e = 0; e < E; ++e) acc[e] = st.acc[gg][e] * alpha;
+                for (int c0 = 0; c0 < np; c0 += 32) {
+                    const int c = c0 + lane;
+                    const float lc = c0 == 0 ? lc0[gg]
+                                             : (c < np ? __ldg(part_lse + prow_b + (size_t)c * g.M + gg) : -INFINITY);
+                    const float wl = lc > -INFINITY ? ex2(lc * kLog2e - mx) : 0.f;
+                    const int nc = min(32, np - c0);
+                    for (int u0 = 0; u0 < nc; u0 += 8) {
+                        float ov[8][E], wv[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int cu = u0 + u;
+                            wv[u] = __shfl_sync(0xffffffffu, wl, cu & 31);
+                            if (cu < nc) {
+                                const float* po = part_o + (prow_b + (size_t)(c0 + cu) * g.M + gg) * D + lane * E;
+                                if constexpr (E == 4) {
+                                    const float4 t = __ldg(reinterpret_cast<const float4*>(po));
+                                    ov[u][0] = t.x; ov[u][1] = t.y; ov[u][2] = t.z; ov[u][3] = t.w;
+                                } else {
+                                    const float2 t = __ldg(reinterpret_cast<const float2*>(po));
+                                    ov[u][0] = t.x; ov[u][1] = t.y;
+                                }
+                            } else {
+                                wv[u] = 0.f;
+#pragma unroll
+                                for (int e = 0; e < E; ++e) ov[u][e] = 0.f;
+                            }
                         }
-                    } else {
 #pragma unroll
-                        for (int e = 0; e < E; ++e) ov[u][e] = 0.f;
+                        for (int u = 0; u < 8; ++u)
+#pragma unroll
+                            for (int e = 0; e < E; ++e) acc[e] = fmaf(wv[u], wv[u] != 0.f ? ov[u][e] : 0.f, acc[e]);
                     }
                 }
+                st.l[gg] = st.l[gg] * alpha + lsum;
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-#pragma unroll
-                    for (int e = 0; e < E; ++e) acc[e] = fmaf(wv[u], wv[u] != 0.f ? ov[u][e] : 0.f, acc[e]);
+                for (int e = 0; e < E; ++e) st.acc[gg][e] = acc[e];
+                st.m[gg] = mx;
             }
-            st.l[gg] = st.l[gg] * alpha + lsum;
-#pragma unroll
-            for (int e = 0; e < E; ++e) st.acc[gg][e] = acc[e];
-            st.m[gg] = mx;
         }
     }
 
