@@ -141,7 +141,11 @@ struct FusedArgs {
     const __nv_bfloat16* pool_k;
     const __nv_bfloat16* pool_v;
     const int32_t* idx;
-    int pdl;  // launched as the programmatic dependent of the beam update that writes the pool and table
+    // launched as the programmatic dependent of the beam update that writes the pool and table:
+    // in-tile mode the gather waits for it; otherwise nothing here reads what it writes, and
+    // thread 0 of every CTA waits for it at the end, so that the kernels queued after this one
+    // (the Non-Shared part) find the update complete
+    int pdl;
 };
 
 // NST: the in-tile Non-Shared mode, compiled as its own instantiation so that the other
@@ -754,6 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     __syncthreads();
     tc_fence_after();
     if (warp == kWarpMma && nt > 0) tmem_dealloc(tmem, kTmemCols);
+    if (!ns && fa.pdl && tid == 0) grid_dependency_wait();
 }
 
 template <int D, bool NST>

@@ -375,6 +375,16 @@ int xattn_decode_step(const xattn_desc* desc, const int32_t* parent, const void*
         return run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st, true, ns_k_pool, ns_v_pool,
                           beam_tok_idx, out, lse, true, &pdl);
     }
+    if (kernel == 1 && !decode_is_fused(g, kernel, step)) {
+        // Shared stage (prefix pieces) as the beam update's programmatic dependent: it reads
+        // nothing the update writes and runs beside it, waiting for it only at its end; then
+        // the Non-Shared + Merge kernel(s).
+        const NsTileArgs pdl{false, nullptr, nullptr, nullptr, true};
+        rc = run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st, false, nullptr, nullptr, nullptr,
+                        nullptr, nullptr, false, &pdl);
+        if (rc != XATTN_OK) return rc;
+        return run_merge(g, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws, st);
+    }
     return xattn_decode(desc, q, shared_k, shared_v, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, step, out, lse,
                         workspace, workspace_bytes, stream);
 }
