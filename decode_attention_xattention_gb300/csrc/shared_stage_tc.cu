@@ -705,8 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                         pv_tile(i, j - 1, st);
                         if (j == ntiles) mma_commit(&bars.o_full[i]);  // O_i complete
                         if (j < ntiles) {
-                            tc_fence_after();
-                            issue_qk(i, (uint32_t)st * C::kUnitBytes);
+                            issue_qk(i, (uint32_t)st * C::kUnitBytes);  // after the P wait's fence
                             mma_commit(&bars.s_full[i]);
                         }
                     }
@@ -733,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                             if (j == ntiles) mma_commit(&bars.o_full[i]);  // O_i complete
                         }
                         if (j < ntiles) {
-                            tc_fence_after();
+                            if (j == 0) tc_fence_after();  // later tiles: after the P wait's fence
                             issue_qk(i, (uint32_t)st * C::kUnitBytes);
                             mma_commit(&bars.s_full[i]);
                         }
