@@ -18,7 +18,11 @@ namespace {
 
 constexpr int kRB = 4;  // stacked rows per CTA
 constexpr int kWarps = 4;
-constexpr int kUnroll = 4;  // tokens in flight per warp
+// Tokens whose K/V rows a warp has in flight at once: the kernel serves few rows per unit, so
+// it is a chain of dependent memory round trips; more per trip, fewer trips (16 at d = 64
+// took the Tiny configuration's Shared stage from 19.2 to 15.0 us).
+template <int D>
+constexpr int kUnrollFor = D == 64 ? 16 : 8;
 constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ __forceinline__ float ex2(float x) {
@@ -57,6 +61,7 @@ __global__ void __launch_bounds__(kWarps * 32) shared_stage_simt_kernel(
     Geometry g, const T* __restrict__ q, const T* __restrict__ sk, const T* __restrict__ sv,
     const int32_t* __restrict__ shared_len, float* __restrict__ part_o, float* __restrict__ part_lse) {
     constexpr int E = D / 32;
+    constexpr int kUnroll = kUnrollFor<D>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nrb = (g.M + kRB - 1) / kRB;
     long t = blockIdx.x;
