@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kWarps * 32) shared_stage_simt_kernel(
     const size_t tok_stride = (size_t)g.Hkv * D;
     const T* kbase = sk + ((size_t)r * g.Lmax * g.Hkv + h) * D + lane * E;
     const T* vbase = sv + ((size_t)r * g.Lmax * g.Hkv + h) * D + lane * E;
-    // Warp w takes groups of kUnroll consecutive tokens (w*kUnroll, w*kUnroll + 16, ...);
+    // Warp w takes groups of kUnroll consecutive tokens (w*kUnroll, w*kUnroll + kWarps*kUnroll, ...);
     // the group's K and V rows are loaded before any is used.
     for (int j0 = t0 + warp * kUnroll; j0 < t1; j0 += kWarps * kUnroll) {
         float kv[kUnroll][E], vv[kUnroll][E];
