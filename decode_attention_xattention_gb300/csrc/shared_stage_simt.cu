@@ -59,7 +59,7 @@ __device__ __forceinline__ void load_in(const float* p, float (&x)[E]) {
 template <int D, typename T>
 __global__ void __launch_bounds__(kWarps * 32) shared_stage_simt_kernel(
     Geometry g, const T* __restrict__ q, const T* __restrict__ sk, const T* __restrict__ sv,
-    const int32_t* __restrict__ shared_len, float* __restrict__ part_o, float* __restrict__ part_lse) {
+    const int32_t* __restrict__ shared_len, float* __restrict__ part_o, float* __restrict__ part_lse, int pdl) {
     constexpr int E = D / 32;
     constexpr int kUnroll = kUnrollFor<D>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -164,29 +164,41 @@ __global__ void __launch_bounds__(kWarps * 32) shared_stage_simt_kernel(
             if (lane == 0) part_lse[prow] = (M + __log2f(wsum)) * kLn2;
         }
     }
+    // launched as the programmatic dependent of the beam update (it reads nothing the update
+    // writes): complete only after it, so that the kernels queued next find the update done
+    if (pdl && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace
 
 cudaError_t launch_shared_stage_simt(const Geometry& g, const void* q, const void* shared_k, const void* shared_v,
                                      const int32_t* shared_len, float* part_o, float* part_lse, int32_t* status,
-                                     cudaStream_t stream) {
+                                     cudaStream_t stream, bool pdl) {
     (void)status;
     const long nrb = (g.M + kRB - 1) / kRB;
     const long ctas = (long)g.R * g.Hkv * nrb * g.nsplit;
     if (ctas > 0x7fffffffL) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaError_t e = cudaSuccess;
     auto go = [&](auto kernel, auto tag) {
         using T = decltype(tag);
-        kernel<<<(unsigned)ctas, kWarps * 32, 0, stream>>>(g, static_cast<const T*>(q), static_cast<const T*>(shared_k),
-                                                           static_cast<const T*>(shared_v), shared_len, part_o,
-                                                           part_lse);
+        e = cudaLaunchKernelEx(&cfg, kernel, g, static_cast<const T*>(q), static_cast<const T*>(shared_k),
+                               static_cast<const T*>(shared_v), shared_len, part_o, part_lse, pdl ? 1 : 0);
     };
     if (g.d == 128 && g.in_f32) go(shared_stage_simt_kernel<128, float>, float{});
     else if (g.d == 128) go(shared_stage_simt_kernel<128, __nv_bfloat16>, __nv_bfloat16{});
     else if (g.d == 64 && g.in_f32) go(shared_stage_simt_kernel<64, float>, float{});
     else if (g.d == 64) go(shared_stage_simt_kernel<64, __nv_bfloat16>, __nv_bfloat16{});
     else return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace xattn

@@ -68,7 +68,7 @@ template <int D>
 __global__ void __launch_bounds__(kRows, 1) shared_stage_tf32_kernel(
     Geometry g, const float* __restrict__ q, const float* __restrict__ sk, const float* __restrict__ sv,
     const int32_t* __restrict__ shared_len, float* __restrict__ part_o, float* __restrict__ part_lse,
-    int32_t* status) {
+    int32_t* status, int pdl) {
     using C = Tf32Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -261,11 +261,14 @@ __global__ void __launch_bounds__(kRows, 1) shared_stage_tf32_kernel(
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+    // launched as the programmatic dependent of the beam update (it reads nothing the update
+    // writes): complete only after it, so that the kernels queued next find the update done
+    if (pdl && tid == 0) grid_dependency_wait();
 }
 
 template <int D>
 cudaError_t launch_d(const Geometry& g, const float* q, const float* sk, const float* sv, const int32_t* slen,
-                     float* po, float* pl, int32_t* status, cudaStream_t stream) {
+                     float* po, float* pl, int32_t* status, cudaStream_t stream, bool pdl) {
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -277,21 +280,31 @@ cudaError_t launch_d(const Geometry& g, const float* q, const float* sk, const f
     }
     const long ctas = (long)g.R * g.Hkv * g.nsplit * g.row_tiles;
     if (ctas <= 0 || ctas > 0x7fffffffL) return cudaErrorInvalidValue;
-    shared_stage_tf32_kernel<D><<<(unsigned)ctas, kRows, Tf32Cfg<D>::kSmemBytes, stream>>>(g, q, sk, sv, slen, po, pl,
-                                                                                         status);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(kRows);
+    cfg.dynamicSmemBytes = Tf32Cfg<D>::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, shared_stage_tf32_kernel<D>, g, q, sk, sv, slen, po, pl, status,
+                                             pdl ? 1 : 0);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_shared_stage_tf32(const Geometry& g, const void* q, const void* shared_k, const void* shared_v,
                                      const int32_t* shared_len, float* part_o, float* part_lse, int32_t* status,
-                                     cudaStream_t stream) {
+                                     cudaStream_t stream, bool pdl) {
     auto fq = static_cast<const float*>(q);
     auto fk = static_cast<const float*>(shared_k);
     auto fv = static_cast<const float*>(shared_v);
-    if (g.d == 64) return launch_d<64>(g, fq, fk, fv, shared_len, part_o, part_lse, status, stream);
-    if (g.d == 128) return launch_d<128>(g, fq, fk, fv, shared_len, part_o, part_lse, status, stream);
+    if (g.d == 64) return launch_d<64>(g, fq, fk, fv, shared_len, part_o, part_lse, status, stream, pdl);
+    if (g.d == 128) return launch_d<128>(g, fq, fk, fv, shared_len, part_o, part_lse, status, stream, pdl);
     return cudaErrorInvalidValue;
 }
 

@@ -278,9 +278,11 @@ int run_shared(const Geometry& g, int kernel, const void* q, const void* shared_
         e = launch_shared_stage_tc(g, mk, mv, mq, mn, qb, shared_len, ws.part_o, ws.part_lse, ws.status, out, lse,
                                    fused, nst, st);
     } else if (kernel == 2) {
-        e = launch_shared_stage_simt(g, q, shared_k, shared_v, shared_len, ws.part_o, ws.part_lse, ws.status, st);
+        e = launch_shared_stage_simt(g, q, shared_k, shared_v, shared_len, ws.part_o, ws.part_lse, ws.status, st,
+                                     ns_args && ns_args->pdl);
     } else if (kernel == 3) {
-        e = launch_shared_stage_tf32(g, q, shared_k, shared_v, shared_len, ws.part_o, ws.part_lse, ws.status, st);
+        e = launch_shared_stage_tf32(g, q, shared_k, shared_v, shared_len, ws.part_o, ws.part_lse, ws.status, st,
+                                     ns_args && ns_args->pdl);
     }
     return e == cudaSuccess ? XATTN_OK : XATTN_ERR_CUDA;
 }
@@ -375,7 +377,7 @@ int xattn_decode_step(const xattn_desc* desc, const int32_t* parent, const void*
         return run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st, true, ns_k_pool, ns_v_pool,
                           beam_tok_idx, out, lse, true, &pdl);
     }
-    if (kernel == 1 && !decode_is_fused(g, kernel, step)) {
+    if (kernel != 0 && !decode_is_fused(g, kernel, step)) {
         // Shared stage (prefix pieces) as the beam update's programmatic dependent: it reads
         // nothing the update writes and runs beside it, waiting for it only at its end; then
         // the Non-Shared + Merge kernel(s).

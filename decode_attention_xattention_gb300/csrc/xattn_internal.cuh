@@ -70,12 +70,13 @@ cudaError_t launch_shared_stage_tc(const Geometry& g, const CUtensorMap& tmap_k,
 // q, shared_k, shared_v: bf16, or fp32 when g.in_f32.
 cudaError_t launch_shared_stage_simt(const Geometry& g, const void* q, const void* shared_k, const void* shared_v,
                                      const int32_t* shared_len, float* part_o, float* part_lse,
-                                     int32_t* status, cudaStream_t stream);
+                                     int32_t* status, cudaStream_t stream, bool pdl = false);
 // Shared stage for fp32 storage on the tensor cores (tcgen05 kind::tf32), writing the same
-// per-piece partials as launch_shared_stage_simt.
+// per-piece partials as launch_shared_stage_simt. pdl (both): launched as the programmatic
+// dependent of the beam update just queued; the kernel completes only after it.
 cudaError_t launch_shared_stage_tf32(const Geometry& g, const void* q, const void* shared_k, const void* shared_v,
                                      const int32_t* shared_len, float* part_o, float* part_lse, int32_t* status,
-                                     cudaStream_t stream);
+                                     cudaStream_t stream, bool pdl = false);
 // q and the pools: bf16, or fp32 when g.in_f32 (then only the direct walk of at most
 // kNsDirectMax Non-Shared tokens, which the host checks).
 cudaError_t launch_ns_merge(const Geometry& g, const void* q, const void* pool_k, const void* pool_v,

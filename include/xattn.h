@@ -171,13 +171,13 @@ XATTN_API int xattn_beam_update(const xattn_desc* desc, const int32_t* parent, c
  * xattn_decode(desc, q, ..., beam_tok_idx, step, out, lse, workspace, ...) on `stream`: the
  * same output, LSE, pool contents, ancestry table and status bits, bit for bit (section 2.1:
  * the Non-Shared cache is updated in place after each beam step). Requires
- * 1 <= step <= Tmax and step*BW <= S; parent may be NULL when step == 1. The tensor-core
- * Shared-stage kernel is launched as the beam update's programmatic dependent: when it takes
- * the Non-Shared part in its own tile (xattn_plan.ns_tile), its set-up, query loads and prefix
- * prefetches overlap the update and it reads the pool and the table only after the update has
- * completed; when the decode is unfused (xattn_plan.fused == 0), it reads nothing the update
- * writes, runs beside it, and completes only after it, so that the Non-Shared + Merge
- * kernel(s) queued next find the update complete. */
+ * 1 <= step <= Tmax and step*BW <= S; parent may be NULL when step == 1. The Shared-stage
+ * kernel is launched as the beam update's programmatic dependent: when it takes the Non-Shared
+ * part in its own tile (xattn_plan.ns_tile), its set-up, query loads and prefix prefetches
+ * overlap the update and it reads the pool and the table only after the update has completed;
+ * when the decode is unfused (xattn_plan.fused == 0; every Shared-stage kernel, fp32 storage
+ * included), it reads nothing the update writes, runs beside it, and completes only after it,
+ * so that the Non-Shared + Merge kernel(s) queued next find the update complete. */
 XATTN_API int xattn_decode_step(const xattn_desc* desc, const int32_t* parent, const void* new_k,
                                 const void* new_v, const void* q, const void* shared_k, const void* shared_v,
                                 const int32_t* shared_len, void* ns_k_pool, void* ns_v_pool,

@@ -99,3 +99,23 @@ def test_decode_step_rejects_bad_arguments():
     assert xattn.xattn_decode_step(*args(0, None)) == xattn.XATTN_ERR_INVALID_ARG   # no token to add
     assert xattn.xattn_decode_step(*args(3, db.parents[1])) == xattn.XATTN_ERR_INVALID_ARG  # past max_steps
     assert xattn.xattn_decode_step(*args(2, None)) == xattn.XATTN_ERR_INVALID_ARG  # parents needed
+
+
+@pytest.mark.parametrize("kernel", [2, 1], ids=["cuda_core", "tf32"])
+def test_decode_step_fp32_storage(kernel):
+    """fp32 storage: the Shared stage (fp32 on the CUDA cores, or tf32 on the tensor cores)
+    launched beside the beam update gives, step after step, the same bits as the two calls."""
+    w = wl.custom(R=2, BW=6, Hq=8, Hkv=2, d=64, lens=(300, 129), T=4, seed=17, input_dtype="fp32")
+    inp = wl.make_inputs(w)
+    a = DeviceBatch(inp, shared_kernel=kernel, out_fp32=True, input_f32=True)
+    b = DeviceBatch(inp, shared_kernel=kernel, out_fp32=True, input_f32=True)
+    assert b.plan(w.steps).shared_kernel == (2 if kernel == 2 else 3) and b.plan(w.steps).fused == 0
+    for s in range(w.steps):
+        xattn.check(a.beam_update(s))
+        xattn.check(a.decode(s + 1))
+        xattn.check(b.decode_step(s))
+        torch.cuda.synchronize()
+        for x, y, what in ((a.out, b.out, "out"), (a.lse, b.lse, "lse"), (a.idx, b.idx, "table"),
+                           (a.pool_k, b.pool_k, "pool_k"), (a.pool_v, b.pool_v, "pool_v")):
+            assert torch.equal(bits(x), bits(y)), f"step {s}: {what} differs"
+    assert a.read_status() == 0 and b.read_status() == 0
