@@ -59,7 +59,6 @@ using namespace ptx;
 constexpr int kThreads = 320;
 constexpr int kWarpLoad = 8, kWarpMma = 9;
 constexpr int kMaxStages = 4;
-constexpr int kPrefetch = 4;  // K/V tiles prefetched into L2 ahead of their load
 constexpr uint32_t kTmemCols = 512;  // S0 | S1 | O0 | O1, 128 columns each
 constexpr uint32_t kTmemO = 256;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -516,8 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     } else if (warp == kWarpLoad) {
         // ============================================ TMA producer
         // Prefix unit p = {K(p) if p < ntiles, V(p-1) if p >= 1} (unit index u0 + p) goes into
-        // slot (u0 + p) % kU as soon as the unit kU before it has been consumed; L2 prefetch
-        // kPrefetch units ahead hides most of the HBM latency of the later load.
+        // slot (u0 + p) % kU as soon as the unit kU before it has been consumed. (L2 prefetches
+        // of later units, tried here, made the kernel 1-1.5 % slower and were taken out.)
         if (lane == 0 && nt > 0) {
             // the Q tiles first: per row tile one 64 d x G heads x 128/G beams box per 64 d
             // (128-byte swizzle, the K-major layout the MMA reads); beams past BW are zero-filled
@@ -531,24 +530,10 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
             const int npu = ntiles > 0 ? ntiles + 1 : 0;  // prefix units
-            auto prefetch_unit = [&](int p) {
-                for (int kb = 0; kb < C::KB; ++kb) {
-                    if (p < ntiles) tma_prefetch_4d(&tmap_k, kb * 64, h, t0 + p * kTcTileKeys, r);
-                    if (p >= 1) tma_prefetch_4d(&tmap_v, kb * 64, h, t0 + (p - 1) * kTcTileKeys, r);
-                }
-            };
-            // With the Non-Shared tile first, the first prefix loads wait for slots the gathered
-            // tile still holds: bring the first prefix units into L2 meanwhile.
-            if (ns)
-                for (int p = 0; p < min(npu, kPrefetch); ++p) prefetch_unit(p);
             int issued = 0;
             for (int p = 0; p < npu; ++p) {
                 const int u = u0 + p, st = u % kU, use = u / kU;
                 if (use > 0 && !mbar_wait(&bars.u_empty[st], (use - 1) & 1, &abort_sh)) break;
-                if (!ns && p == kU)  // the first L2 prefetches once the first slot is free again: issued
-                    // with the first loads they competed with them for HBM across the whole grid
-                    for (int pp = kU; pp < min(npu, kU + kPrefetch); ++pp) prefetch_unit(pp);
-                if (ns ? (p + kPrefetch < npu) : (p >= kU && p + kPrefetch < npu)) prefetch_unit(p + kPrefetch);
                 uint8_t* slot = sU + st * C::kUnitBytes;
                 mbar_arrive_expect_tx(&bars.u_full[st], (p < ntiles ? C::kTileBytes : 0) + (p >= 1 ? C::kTileBytes : 0));
                 for (int kb = 0; kb < C::KB; ++kb) {
