@@ -371,8 +371,8 @@ int xattn_decode_step(const xattn_desc* desc, const int32_t* parent, const void*
                            stream);
     if (rc != XATTN_OK) return rc;
     if (ns_tile_fits(g, kernel, step)) {
-        // The decode as the beam update's programmatic dependent: its set-up, Q loads and prefix
-        // prefetches overlap the update; its gather waits for the update to complete.
+        // The decode as the beam update's programmatic dependent: its set-up, Q loads and first K/V
+        // loads overlap the update; its gather waits for the update to complete.
         const NsTileArgs pdl{true, ns_k_pool, ns_v_pool, beam_tok_idx, true};
         return run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st, true, ns_k_pool, ns_v_pool,
                           beam_tok_idx, out, lse, true, &pdl);

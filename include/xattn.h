@@ -173,7 +173,7 @@ XATTN_API int xattn_beam_update(const xattn_desc* desc, const int32_t* parent, c
  * the Non-Shared cache is updated in place after each beam step). Requires
  * 1 <= step <= Tmax and step*BW <= S; parent may be NULL when step == 1. The Shared-stage
  * kernel is launched as the beam update's programmatic dependent: when it takes the Non-Shared
- * part in its own tile (xattn_plan.ns_tile), its set-up, query loads and prefix prefetches
+ * part in its own tile (xattn_plan.ns_tile), its set-up, query loads and first prefix loads
  * overlap the update and it reads the pool and the table only after the update has completed;
  * when the decode is unfused (xattn_plan.fused == 0; every Shared-stage kernel, fp32 storage
  * included), it reads nothing the update writes, runs beside it, and completes only after it,
