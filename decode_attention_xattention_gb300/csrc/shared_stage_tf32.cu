@@ -108,8 +108,9 @@ __global__ void __launch_bounds__(kRows, 1) shared_stage_tf32_kernel(
     }
     {  // this thread's Q row (zero past the unit's rows)
         const int b = row / g.G, gg = row - (row / g.G) * g.G;
-        const float4* qr =
-            reinterpret_cast<const float4*>(q + (((size_t)r * g.BW + b) * g.Hq + (size_t)h * g.G + gg) * D);
+        const float4* qr = row_ok ? reinterpret_cast<const float4*>(
+                                        q + (((size_t)r * g.BW + b) * g.Hq + (size_t)h * g.G + gg) * D)
+                                  : nullptr;
 #pragma unroll 4
         for (int k4 = 0; k4 < D / 4; ++k4) {
             const float4 v = row_ok ? __ldg(qr + k4) : make_float4(0.f, 0.f, 0.f, 0.f);
