@@ -995,7 +995,7 @@ cudaError_t launch_piece(const Geometry& g, int npc, cudaStream_t st, const __nv
 template <int D>
 cudaError_t launch_d(const Geometry& g, cudaStream_t st, const void* qv, const void* pkv, const void* pvv,
                      const int32_t* idx, const int32_t* slen, float* po, float* pl, void* out, float* lse,
-                     int32_t* status) {
+                     int32_t* status, cudaEvent_t join) {
     const dim3 grid((unsigned)(((long)g.R * g.BW * g.Hkv + 7) / 8)), block(256);
     if (g.in_f32) {
         // fp32 storage: the direct walk (step <= kNsDirectMax, checked on the host) and the merge
@@ -1030,6 +1030,10 @@ cudaError_t launch_d(const Geometry& g, cudaStream_t st, const void* qv, const v
         } else if (g.ns_to_piece || g.ns_pieces > 0) {                                                           \
             cudaError_t e = launch_piece<D, GV>(g, npc, st, q, pk, pv, idx, po, pl, status);                   \
             if (e != cudaSuccess) return e;                                                                      \
+            if (!g.ns_to_piece && join) {                                                                        \
+                e = cudaStreamWaitEvent(st, join, 0);                                                            \
+                if (e != cudaSuccess) return e;                                                                  \
+            }                                                                                                    \
             if (!g.ns_to_piece) merge_rows_kernel<D><<<rows_ctas, block, 0, st>>>(g, slen, po, pl, out, lse, status); \
         } else {                                                                                                 \
             ns_merge_kernel<D, GV, __nv_bfloat16><<<grid, block, 0, st>>>(g, q, pk, pv, idx, slen, po, pl, out, lse, status); \
@@ -1053,13 +1057,13 @@ int merge_ctas_for(const Geometry& g) {
 cudaError_t launch_ns_merge(const Geometry& g, const void* q, const void* pool_k,
                             const void* pool_v, const int32_t* beam_tok_idx, const int32_t* shared_len,
                             const float* part_o, const float* part_lse, void* out, float* lse, int32_t* status,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, cudaEvent_t join) {
     float* po = const_cast<float*>(part_o);
     float* pl = const_cast<float*>(part_lse);
     if (g.d == 128)
-        return launch_d<128>(g, stream, q, pool_k, pool_v, beam_tok_idx, shared_len, po, pl, out, lse, status);
+        return launch_d<128>(g, stream, q, pool_k, pool_v, beam_tok_idx, shared_len, po, pl, out, lse, status, join);
     if (g.d == 64)
-        return launch_d<64>(g, stream, q, pool_k, pool_v, beam_tok_idx, shared_len, po, pl, out, lse, status);
+        return launch_d<64>(g, stream, q, pool_k, pool_v, beam_tok_idx, shared_len, po, pl, out, lse, status, join);
     return cudaErrorInvalidValue;
 }
 

@@ -289,11 +289,71 @@ int run_shared(const Geometry& g, int kernel, const void* q, const void* shared_
 
 int run_merge(const Geometry& g, const xattn_desc* desc, const void* q, const int32_t* shared_len,
               const void* ns_k_pool, const void* ns_v_pool, const int32_t* beam_tok_idx, void* out, float* lse,
-              const WsView& ws, cudaStream_t st) {
+              const WsView& ws, cudaStream_t st, cudaEvent_t join = nullptr) {
     cudaError_t e = launch_ns_merge(g, q, ns_k_pool, ns_v_pool, beam_tok_idx,
                                     desc->max_shared_len > 0 ? shared_len : nullptr, ws.part_o, ws.part_lse,
-                                    out, lse, ws.status, st);
+                                    out, lse, ws.status, st, join);
     return e == cudaSuccess ? XATTN_OK : XATTN_ERR_CUDA;
+}
+
+// A second stream and two events per host thread and device, created on first use and kept
+// for the thread's lifetime: with a long Non-Shared part the Shared stage (prefix pieces) and
+// the Non-Shared piece kernel do not depend on each other, so the Shared stage runs on this
+// stream, forked from the caller's stream by one event and joined back by the other before
+// the row merge (graph capture follows the fork and the join). Per thread, so calls from
+// different host threads never share one.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    ~SideStream() {
+        if (join) cudaEventDestroy(join);
+        if (fork) cudaEventDestroy(fork);
+        if (s) cudaStreamDestroy(s);
+    }
+};
+SideStream* side_stream() {
+    static thread_local SideStream tbl[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    SideStream& x = tbl[dev];
+    if (!x.s) {
+        if (cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking) != cudaSuccess) {
+            x.s = nullptr;
+            return nullptr;
+        }
+        if (cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) != cudaSuccess)
+            return nullptr;
+    }
+    return (x.fork && x.join) ? &x : nullptr;
+}
+
+// Whether the decode takes the two-stream form: a prefix with storage, a long Non-Shared part
+// (its own piece kernel), no fusion.
+bool decode_two_streams(const Geometry& g, int kernel, int step) {
+    return kernel != 0 && !decode_is_fused(g, kernel, step) && g.ns_pieces > 0;
+}
+
+// The Shared stage forked onto the side stream; returns the event the row merge waits for, or
+// null when the fork could not be made (then nothing was enqueued).
+cudaEvent_t fork_shared(const Geometry& g, int kernel, const void* q, const void* shared_k, const void* shared_v,
+                        const int32_t* shared_len, const WsView& ws, cudaStream_t st, int* rc) {
+    *rc = XATTN_OK;
+    SideStream* ss = side_stream();
+    if (!ss) return nullptr;
+    if (cudaEventRecord(ss->fork, st) != cudaSuccess || cudaStreamWaitEvent(ss->s, ss->fork, 0) != cudaSuccess) {
+        *rc = XATTN_ERR_CUDA;
+        return nullptr;
+    }
+    *rc = run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, ss->s);
+    if (*rc == XATTN_OK && cudaEventRecord(ss->join, ss->s) != cudaSuccess) *rc = XATTN_ERR_CUDA;
+    if (*rc != XATTN_OK) {
+        // join whatever was enqueued before returning the error
+        cudaEventRecord(ss->join, ss->s);
+        cudaStreamWaitEvent(st, ss->join, 0);
+        return nullptr;
+    }
+    return ss->join;
 }
 
 }  // namespace
@@ -346,6 +406,12 @@ int xattn_decode(const xattn_desc* desc, const void* q, const void* shared_k, co
         return run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st, true, nullptr, nullptr, nullptr, out,
                           lse);
     }
+    if (decode_two_streams(g, kernel, step)) {
+        // the Shared stage beside the Non-Shared piece kernel; the row merge waits for both
+        cudaEvent_t join = fork_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st, &rc);
+        if (rc != XATTN_OK) return rc;
+        if (join) return run_merge(g, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws, st, join);
+    }
     rc = run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st);
     if (rc != XATTN_OK) return rc;
     return run_merge(g, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws, st);
@@ -367,6 +433,21 @@ int xattn_decode_step(const xattn_desc* desc, const int32_t* parent, const void*
     plan(desc, step, &g, &kernel);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const WsView ws = ws_view(workspace, g);
+    if (decode_two_streams(g, kernel, step)) {
+        // the Shared stage (which reads nothing the update writes) forked first, beside the
+        // update and the Non-Shared piece kernel; the row merge waits for both
+        cudaEvent_t join = fork_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st, &rc);
+        if (rc != XATTN_OK) return rc;
+        if (join) {
+            rc = xattn_beam_update(desc, parent, new_k, new_v, ns_k_pool, ns_v_pool, beam_tok_idx, step - 1,
+                                   ws.status, stream);
+            if (rc != XATTN_OK) {
+                cudaStreamWaitEvent(st, join, 0);  // leave nothing of this call unjoined
+                return rc;
+            }
+            return run_merge(g, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws, st, join);
+        }
+    }
     rc = xattn_beam_update(desc, parent, new_k, new_v, ns_k_pool, ns_v_pool, beam_tok_idx, step - 1, ws.status,
                            stream);
     if (rc != XATTN_OK) return rc;

@@ -78,11 +78,13 @@ cudaError_t launch_shared_stage_tf32(const Geometry& g, const void* q, const voi
                                      const int32_t* shared_len, float* part_o, float* part_lse, int32_t* status,
                                      cudaStream_t stream, bool pdl = false);
 // q and the pools: bf16, or fp32 when g.in_f32 (then only the direct walk of at most
-// kNsDirectMax Non-Shared tokens, which the host checks).
+// kNsDirectMax Non-Shared tokens, which the host checks). join: with a long Non-Shared part,
+// an event the row merge waits for after the piece kernel (the Shared stage's completion when
+// that runs on another stream); may be null.
 cudaError_t launch_ns_merge(const Geometry& g, const void* q, const void* pool_k, const void* pool_v,
                             const int32_t* beam_tok_idx, const int32_t* shared_len,
                             const float* part_o, const float* part_lse, void* out,
-                            float* lse, int32_t* status, cudaStream_t stream);
+                            float* lse, int32_t* status, cudaStream_t stream, cudaEvent_t join = nullptr);
 // One CTA per request; 1 <= BW, W <= 1024 (checked by the caller).
 cudaError_t launch_beam_select(int R, int BW, int K, int W, const float* beam_score, const float* cand_logp,
                                const int32_t* cand_token, int32_t* parent, int32_t* token, float* score,
