@@ -1067,4 +1067,21 @@ cudaError_t launch_ns_merge(const Geometry& g, const void* q, const void* pool_k
     return cudaErrorInvalidValue;
 }
 
+// The row merge alone over pieces 0 .. np-1 (the prefix pieces and the Non-Shared piece
+// `nsplit` the Non-Shared kernel wrote with ns_to_piece).
+cudaError_t launch_merge_rows(const Geometry& g, int np, const int32_t* shared_len, const float* part_o,
+                              const float* part_lse, void* out, float* lse, int32_t* status, cudaStream_t stream) {
+    Geometry gm = g;
+    gm.ns_to_piece = 0;
+    gm.ns_pieces = np - g.nsplit;  // the kernel folds nsplit + ns_pieces pieces
+    if (gm.ns_pieces < 0 || np > g.pieces) return cudaErrorInvalidValue;
+    const unsigned rows_ctas = (unsigned)(((long)g.R * g.BW * g.Hq + 7) / 8);
+    float* po = const_cast<float*>(part_o);
+    float* pl = const_cast<float*>(part_lse);
+    if (g.d == 128) merge_rows_kernel<128><<<rows_ctas, 256, 0, stream>>>(gm, shared_len, po, pl, out, lse, status);
+    else if (g.d == 64) merge_rows_kernel<64><<<rows_ctas, 256, 0, stream>>>(gm, shared_len, po, pl, out, lse, status);
+    else return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
 }  // namespace xattn

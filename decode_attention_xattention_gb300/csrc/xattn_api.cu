@@ -328,10 +328,29 @@ SideStream* side_stream() {
     return (x.fork && x.join) ? &x : nullptr;
 }
 
-// Whether the decode takes the two-stream form: a prefix with storage, a long Non-Shared part
-// (its own piece kernel), no fusion.
+// Whether the decode takes the two-stream form: a prefix with storage, no fusion, bf16, and
+// either a long Non-Shared part (its own piece kernel) or a short one next to a prefix cut in
+// pieces (the Non-Shared part then written as one more piece and folded by the row merge).
 bool decode_two_streams(const Geometry& g, int kernel, int step) {
-    return kernel != 0 && !decode_is_fused(g, kernel, step) && g.ns_pieces > 0;
+    if (kernel == 0 || decode_is_fused(g, kernel, step) || g.in_f32) return false;
+    return g.ns_pieces > 0 || (step > 0 && step <= kNsDirectMax && g.nsplit > 1);
+}
+
+// The Non-Shared part and the merge of the two-stream form, on `st`, the row merge after
+// `join` (the Shared stage's completion on the side stream).
+int run_ns_then_merge(const Geometry& g, const xattn_desc* desc, const void* q, const int32_t* shared_len,
+                      const void* ns_k_pool, const void* ns_v_pool, const int32_t* beam_tok_idx, void* out,
+                      float* lse, const WsView& ws, cudaStream_t st, cudaEvent_t join) {
+    if (g.ns_pieces > 0)  // the piece kernel, then (after the join) the row merge
+        return run_merge(g, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws, st, join);
+    Geometry gn = g;
+    gn.ns_to_piece = 1;  // the Non-Shared part as piece nsplit
+    int rc = run_merge(gn, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws, st);
+    if (cudaStreamWaitEvent(st, join, 0) != cudaSuccess && rc == XATTN_OK) rc = XATTN_ERR_CUDA;
+    if (rc != XATTN_OK) return rc;
+    const cudaError_t e = launch_merge_rows(g, g.nsplit + 1, desc->max_shared_len > 0 ? shared_len : nullptr,
+                                            ws.part_o, ws.part_lse, out, lse, ws.status, st);
+    return e == cudaSuccess ? XATTN_OK : XATTN_ERR_CUDA;
 }
 
 // The Shared stage forked onto the side stream; returns the event the row merge waits for, or
@@ -410,7 +429,9 @@ int xattn_decode(const xattn_desc* desc, const void* q, const void* shared_k, co
         // the Shared stage beside the Non-Shared piece kernel; the row merge waits for both
         cudaEvent_t join = fork_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st, &rc);
         if (rc != XATTN_OK) return rc;
-        if (join) return run_merge(g, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws, st, join);
+        if (join)
+            return run_ns_then_merge(g, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws, st,
+                                     join);
     }
     rc = run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st);
     if (rc != XATTN_OK) return rc;
@@ -445,7 +466,8 @@ int xattn_decode_step(const xattn_desc* desc, const int32_t* parent, const void*
                 cudaStreamWaitEvent(st, join, 0);  // leave nothing of this call unjoined
                 return rc;
             }
-            return run_merge(g, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws, st, join);
+            return run_ns_then_merge(g, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws, st,
+                                     join);
         }
     }
     rc = xattn_beam_update(desc, parent, new_k, new_v, ns_k_pool, ns_v_pool, beam_tok_idx, step - 1, ws.status,

@@ -85,6 +85,9 @@ cudaError_t launch_ns_merge(const Geometry& g, const void* q, const void* pool_k
                             const int32_t* beam_tok_idx, const int32_t* shared_len,
                             const float* part_o, const float* part_lse, void* out,
                             float* lse, int32_t* status, cudaStream_t stream, cudaEvent_t join = nullptr);
+// The row merge alone over pieces 0 .. np-1 of each row (np <= g.pieces).
+cudaError_t launch_merge_rows(const Geometry& g, int np, const int32_t* shared_len, const float* part_o,
+                              const float* part_lse, void* out, float* lse, int32_t* status, cudaStream_t stream);
 // One CTA per request; 1 <= BW, W <= 1024 (checked by the caller).
 cudaError_t launch_beam_select(int R, int BW, int K, int W, const float* beam_score, const float* cand_logp,
                                const int32_t* cand_token, int32_t* parent, int32_t* token, float* score,
