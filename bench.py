@@ -207,19 +207,21 @@ def profile_traffic(kernel_file: str, workload: str):
     return traffic if (traffic is not None and src_sha == sha) else None
 
 
-def launches_per_step(plan, step):
+def launches_per_step(plan, step, f32=False):
     """Kernels of this library launched by one timed step (xattn_decode_step): the beam update,
     then the decode (the Shared-stage kernel alone when it takes the Non-Shared part in its own
     tile; the Non-Shared kernel + Shared stage with merging epilogue when fused; else
-    the Shared stage, if the prefix has storage, and the Non-Shared/Merge kernel, or the
-    Non-Shared piece and row-merge kernels when the Non-Shared part is long)."""
+    the Shared stage, if the prefix has storage, and the Non-Shared/Merge kernel, or two
+    kernels, the Non-Shared part as pieces and the row merge, when the Non-Shared part is long
+    or, with bf16 storage, sits next to a prefix cut in pieces)."""
     if plan.ns_tile:  # the beam update, then the decode as its programmatic dependent
         return 2
     n = 1
     if plan.fused:
         n += (1 if step > 0 else 0) + 1
     else:
-        n += (1 if plan.shared_kernel != 0 else 0) + (2 if step > 32 else 1)
+        split_short = (not f32 and plan.shared_kernel != 0 and plan.num_splits > 1 and 0 < step <= 32)
+        n += (1 if plan.shared_kernel != 0 else 0) + (2 if (step > 32 or split_short) else 1)
     return n
 
 
@@ -658,7 +660,7 @@ def measure_config(w, local, stream, peaks, peak_src, l2, cpu_budget_s, target_s
                                     if "shared_stage_alone" in ms and plan.shared_kernel == 1 else None)},
         "binding_roofline_frac": t_bind / step_s,
         "roofline": roof,
-        "gpu_launches_per_step": launches_per_step(plan, T),
+        "gpu_launches_per_step": launches_per_step(plan, T, f32),
     }
     if cpu_budget_s > 0:
         v, cores, sample = cpu_oracle_sample(w, inp, cpu_budget_s)
@@ -1047,7 +1049,7 @@ def main():
                 "graph_pipelined_ms_per_step": ms_graph,
                 "pipeline_check": (f"bitwise equal to the serial schedule over 6 steps: eager {oks[0]}, graph {oks[1]}"
                                    if pipe_err is None else "error: " + pipe_err)},
-        "gpu_launches": launches_per_step(plan, T) * K,
+        "gpu_launches": launches_per_step(plan, T, w.input_dtype == "fp32") * K,
         "clocks": clocks,
     }
     line["beam_select"] = time_beam_select(f"cuda:{local}", stream, rank == 0 and not args.no_cpu_baseline)
