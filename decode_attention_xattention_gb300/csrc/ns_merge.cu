@@ -20,7 +20,8 @@
 //                      them), then folds in every prefix piece stored in the workspace and
 //                      writes out / lse (split prefixes).
 //   merge_rows_kernel  one warp per query row: folds every stored piece (prefix and
-//                      Non-Shared) and writes out / lse.
+//                      Non-Shared) and writes out / lse; merge_rows_few_kernel does the
+//                      same for rows of at most 8 pieces in one round trip.
 #include "xattn_internal.cuh"
 #include "sm100_ptx.cuh"
 
@@ -944,6 +945,90 @@ __global__ void __launch_bounds__(256) merge_rows_kernel(
     if (lane == 0) lse[row] = bad ? __uint_as_float(kNaN) : (mx + __log2f(lsum)) * kLn2;
 }
 
+// Row merge for rows of at most kMergeFew pieces (a prefix in a few pieces and a short
+// Non-Shared part): every piece's LSE and output vector requested at once, one round trip per
+// row, in few enough registers that four CTAs fit on an SM (twice the rows in flight of the
+// batched form, whose double buffer the long rows need).
+constexpr int kMergeFew = 8;
+template <int D>
+__global__ void __launch_bounds__(256, 4) merge_rows_few_kernel(
+    Geometry g, const int32_t* __restrict__ shared_len, const float* __restrict__ part_o,
+    const float* __restrict__ part_lse, void* __restrict__ out, float* __restrict__ lse, int32_t* status) {
+    constexpr int E = D / 32;
+    const int lane = threadIdx.x & 31;
+    const long row = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // (r*BW + b)*Hq + hq
+    if (row >= (long)g.R * g.BW * g.Hq) return;
+    const int hq = (int)(row % g.Hq);
+    const int b = (int)((row / g.Hq) % g.BW);
+    const int r = (int)(row / ((long)g.Hq * g.BW));
+    const int h = hq / g.G, gg = hq - h * g.G;
+    const int L = shared_len ? shared_len[r] : 0;
+    bool bad = (g.Lmax > 0) && (L < 0 || L > g.Lmax);
+    if (bad && lane == 0 && hq == 0 && b == 0) set_status(status, XATTN_STATUS_BAD_SHARED_LEN);
+    const int np = g.nsplit + g.ns_pieces;  // <= kMergeFew (checked on the host)
+    const size_t prow_b = ((size_t)r * g.Hkv + h) * g.pieces * g.M + (size_t)b * g.G + gg;  // + c*M
+    float ov[kMergeFew][E];
+#pragma unroll
+    for (int c = 0; c < kMergeFew; ++c) {
+        if (c < np) {
+            const float* po = part_o + (prow_b + (size_t)c * g.M) * D + lane * E;
+            if constexpr (E == 4) {
+                const float4 t = __ldg(reinterpret_cast<const float4*>(po));
+                ov[c][0] = t.x; ov[c][1] = t.y; ov[c][2] = t.z; ov[c][3] = t.w;
+            } else {
+                const float2 t = __ldg(reinterpret_cast<const float2*>(po));
+                ov[c][0] = t.x; ov[c][1] = t.y;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) ov[c][e] = 0.f;
+        }
+    }
+    const float lc = lane < np ? __ldg(part_lse + prow_b + (size_t)lane * g.M) : -INFINITY;
+    bad = bad || __any_sync(0xffffffffu, lc != lc);
+    float mx = lc * kLog2e;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float w = lc > -INFINITY ? ex2(lc * kLog2e - mx) : 0.f;  // piece `lane`'s weight
+    const float lsum = warp_sum(w);
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int c = 0; c < kMergeFew; ++c) {
+        const float wc = __shfl_sync(0xffffffffu, w, c);  // 0 past np
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = wc > 0.f ? fmaf(wc, ov[c][e], acc[e]) : acc[e];
+    }
+    bad = bad || !(lsum > 0.f);
+    const float inv = bad ? __uint_as_float(kNaN) : 1.f / lsum;
+    float o[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[e] = acc[e] * inv;
+    if (g.out_f32) {
+        float* dst = reinterpret_cast<float*>(out) + (size_t)row * D + lane * E;
+        if constexpr (E == 4) {
+            *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+            *reinterpret_cast<float2*>(dst) = make_float2(o[0], o[1]);
+        }
+    } else {
+        LaneVec<D>::store(reinterpret_cast<__nv_bfloat16*>(out) + (size_t)row * D + lane * E, o);
+    }
+    if (lane == 0) lse[row] = bad ? __uint_as_float(kNaN) : (mx + __log2f(lsum)) * kLn2;
+}
+
+// The row merge over nsplit + ns_pieces pieces per row, in the form that suits their number.
+template <int D>
+void launch_rows(const Geometry& g, cudaStream_t st, const int32_t* slen, const float* po, const float* pl,
+                 void* out, float* lse, int32_t* status) {
+    const unsigned rows_ctas = (unsigned)(((long)g.R * g.BW * g.Hq + 7) / 8);
+    if (g.nsplit + g.ns_pieces <= kMergeFew)
+        merge_rows_few_kernel<D><<<rows_ctas, 256, 0, st>>>(g, slen, po, pl, out, lse, status);
+    else
+        merge_rows_kernel<D><<<rows_ctas, 256, 0, st>>>(g, slen, po, pl, out, lse, status);
+}
+
 constexpr int kNsBeamMaxTok = 8;                 // tokens per beam for ns_beam_kernel
 constexpr size_t kNsBeamMaxWarpBytes = 48 * 1024;  // its shared memory per warp
 
@@ -1018,7 +1103,6 @@ cudaError_t launch_d(const Geometry& g, cudaStream_t st, const void* qv, const v
     const __nv_bfloat16* pk = static_cast<const __nv_bfloat16*>(pkv);
     const __nv_bfloat16* pv = static_cast<const __nv_bfloat16*>(pvv);
     const int npc = g.ns_to_piece ? 1 : g.ns_pieces;  // Non-Shared pieces per (r, b, h)
-    const unsigned rows_ctas = (unsigned)(((long)g.R * g.BW * g.Hq + 7) / 8);
     // short Non-Shared part ahead of the fused Shared stage: one warp per (request, beam)
     const bool beam_path = g.ns_to_piece && g.step <= kNsBeamMaxTok && ns_beam_warp_bytes(g) <= kNsBeamMaxWarpBytes;
     switch (g.G) {
@@ -1034,7 +1118,7 @@ cudaError_t launch_d(const Geometry& g, cudaStream_t st, const void* qv, const v
                 e = cudaStreamWaitEvent(st, join, 0);                                                            \
                 if (e != cudaSuccess) return e;                                                                  \
             }                                                                                                    \
-            if (!g.ns_to_piece) merge_rows_kernel<D><<<rows_ctas, block, 0, st>>>(g, slen, po, pl, out, lse, status); \
+            if (!g.ns_to_piece) launch_rows<D>(g, st, slen, po, pl, out, lse, status);                        \
         } else {                                                                                                 \
             ns_merge_kernel<D, GV, __nv_bfloat16><<<grid, block, 0, st>>>(g, q, pk, pv, idx, slen, po, pl, out, lse, status); \
         }                                                                                                        \
@@ -1075,11 +1159,8 @@ cudaError_t launch_merge_rows(const Geometry& g, int np, const int32_t* shared_l
     gm.ns_to_piece = 0;
     gm.ns_pieces = np - g.nsplit;  // the kernel folds nsplit + ns_pieces pieces
     if (gm.ns_pieces < 0 || np > g.pieces) return cudaErrorInvalidValue;
-    const unsigned rows_ctas = (unsigned)(((long)g.R * g.BW * g.Hq + 7) / 8);
-    float* po = const_cast<float*>(part_o);
-    float* pl = const_cast<float*>(part_lse);
-    if (g.d == 128) merge_rows_kernel<128><<<rows_ctas, 256, 0, stream>>>(gm, shared_len, po, pl, out, lse, status);
-    else if (g.d == 64) merge_rows_kernel<64><<<rows_ctas, 256, 0, stream>>>(gm, shared_len, po, pl, out, lse, status);
+    if (g.d == 128) launch_rows<128>(gm, stream, shared_len, part_o, part_lse, out, lse, status);
+    else if (g.d == 64) launch_rows<64>(gm, stream, shared_len, part_o, part_lse, out, lse, status);
     else return cudaErrorInvalidValue;
     return cudaGetLastError();
 }
