@@ -36,6 +36,8 @@ STEP_SHAPES = [
     (1, 130, 2, 2, 128, (700,), 1, 4096, True),         # G 1, one token: no parents yet
     (2, 6, 8, 4, 128, (300, 200), 5, 4096, False),      # G 2: 64 beams x 5 keys do not fit
     (2, 5, 8, 2, 128, (700, 300), 3, 256, False),       # prefix split in pieces
+    (2, 5, 8, 2, 128, (700, 300), 20, 256, False),      # ... 20 Non-Shared tokens: one piece by the piece kernel
+    (1, 6, 8, 1, 64, (600,), 12, 256, False),           # ... G 8, d 64
     (1, 4, 8, 2, 128, (300,), 40, 4096, False),         # 40 Non-Shared tokens: the piece kernels
 ]
 

@@ -445,9 +445,14 @@ def test_bounded_wait_gives_up_and_context_stays_usable():
     run_and_check(wl.custom(R=1, BW=4, Hq=4, Hkv=2, d=128, lens=(300,), T=3, seed=2))
 
 
-def test_bad_slot_sets_status_and_nan_row():
+# split 2048: one prefix piece (the decode in one kernel, the Non-Shared part in its tile);
+# 128: the prefix in two pieces, the short Non-Shared part written as one more piece beside
+# the Shared stage and the row merge after both
+@pytest.mark.parametrize("split", [2048, 128])
+def test_bad_slot_sets_status_and_nan_row(split):
     w = wl.custom(R=1, BW=4, Hq=4, Hkv=2, d=128, lens=(200,), T=2, seed=1)
-    db = DeviceBatch(wl.make_inputs(w))
+    db = DeviceBatch(wl.make_inputs(w), split_tokens=split)
+    assert (db.plan().num_splits > 1) == (split < 200)
     db.build_cache()
     db.idx[0, 1, 0] = 10_000
     xattn.check(db.decode())
@@ -458,9 +463,11 @@ def test_bad_slot_sets_status_and_nan_row():
     assert db.read_status() == 0  # cleared by the previous read
 
 
-def test_bad_shared_len_sets_status():
+@pytest.mark.parametrize("split", [2048, 128])
+def test_bad_shared_len_sets_status(split):
     w = wl.custom(R=2, BW=4, Hq=4, Hkv=2, d=128, lens=(200, 100), T=2, seed=1)
-    db = DeviceBatch(wl.make_inputs(w))
+    db = DeviceBatch(wl.make_inputs(w), split_tokens=split)
+    assert (db.plan().num_splits > 1) == (split < 200)
     db.build_cache()
     db.shared_len[1] = 5000
     xattn.check(db.decode())
