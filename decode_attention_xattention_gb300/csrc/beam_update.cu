@@ -100,12 +100,17 @@ __global__ void __launch_bounds__(kThreads) beam_update_kernel(
 
 cudaError_t launch_beam_update(int R, int BW, int Hkv, int d, int elem_bytes, int S, int Tmax, int step,
                                const int32_t* parent, const void* new_k, const void* new_v, void* pool_k,
-                               void* pool_v, int32_t* idx, int32_t* status, cudaStream_t stream) {
+                               void* pool_v, int32_t* idx, int32_t* status, cudaStream_t stream,
+                               int vectors_per_thread) {
     if (BW > kTableInts) return cudaErrorInvalidValue;
     if (((size_t)Hkv * d * elem_bytes) % 16 != 0) return cudaErrorInvalidValue;
     const int row16 = (int)((size_t)Hkv * d * elem_bytes / 16);  // 16-byte vectors per slot
     const size_t n16 = (size_t)BW * row16;
-    int ybl = (int)((n16 + kThreads - 1) / kThreads);  // about one vector of K and V per thread
+    // about vectors_per_thread 16-byte vectors of K and V per thread (all loads of a thread in
+    // flight at once): 4 keeps the grid near one CTA per SM, so that the update ends sooner; 1
+    // spreads it over more, smaller CTAs
+    const int vpt = vectors_per_thread > 0 ? vectors_per_thread : 1;
+    int ybl = (int)((n16 + (size_t)vpt * kThreads - 1) / ((size_t)vpt * kThreads));
     ybl = max(1, min(ybl, 1024));
     const int tcols = step > 0 ? (step + table_cols(BW, step) - 1) / table_cols(BW, step) : 1;
     dim3 grid(R, ybl + tcols);  // the last tcols CTAs of each request rewrite its ancestry table

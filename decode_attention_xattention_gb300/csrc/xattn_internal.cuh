@@ -95,7 +95,12 @@ cudaError_t launch_beam_select(int R, int BW, int K, int W, const float* beam_sc
 // elem_bytes: bytes per K/V element (2: bf16, 4: fp32).
 cudaError_t launch_beam_update(int R, int BW, int Hkv, int d, int elem_bytes, int S, int Tmax, int step,
                                const int32_t* parent, const void* new_k, const void* new_v, void* pool_k,
-                               void* pool_v, int32_t* idx, int32_t* status, cudaStream_t stream);
+                               void* pool_v, int32_t* idx, int32_t* status, cudaStream_t stream,
+                               int vectors_per_thread = 4);
+// xattn_beam_update with the copy's vectors per thread (launch_beam_update).
+int beam_update(const xattn_desc* desc, const int32_t* parent, const void* new_k, const void* new_v,
+                void* ns_k_pool, void* ns_v_pool, int32_t* beam_tok_idx, int32_t step, int32_t* status,
+                cudaStream_t stream, int vectors_per_thread);
 
 int merge_ctas_for(const Geometry& g);
 // The host-side argument checks of xattn_decode, without launching anything.
