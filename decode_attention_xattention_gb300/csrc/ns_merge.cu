@@ -1054,7 +1054,8 @@ cudaError_t launch_beam(const Geometry& g, cudaStream_t st, const __nv_bfloat16*
 // One wave of resident one-warp CTAs (fewer when there are fewer pieces).
 template <int D, int G>
 cudaError_t launch_piece(const Geometry& g, int npc, cudaStream_t st, const __nv_bfloat16* q, const __nv_bfloat16* pk,
-                         const __nv_bfloat16* pv, const int32_t* idx, float* po, float* pl, int32_t* status) {
+                         const __nv_bfloat16* pv, const int32_t* idx, float* po, float* pl, int32_t* status,
+                         bool equal_split) {
     const long ntasks = (long)g.R * g.BW * g.Hkv * npc;
     if (ntasks <= 0) return cudaSuccess;
     if (ntasks > 0x7fffffffL) return cudaErrorInvalidValue;
@@ -1072,7 +1073,13 @@ cudaError_t launch_piece(const Geometry& g, int npc, cudaStream_t st, const __nv
         if (e != cudaSuccess) return e;
         resident[dev] = (per_sm > 0 ? per_sm : 1) * (sms > 0 ? sms : 1);
     }
-    const int grid = (int)(ntasks < resident[dev] ? ntasks : resident[dev]);
+    // One wave of warps; with equal_split only as many as give every warp the same number of
+    // pieces (no last round run by a few warps), which is faster when the warps start together;
+    // when they start one after another behind a long kernel on another stream, the full wave
+    // with the smaller last round is.
+    const long per = (ntasks + resident[dev] - 1) / resident[dev];
+    const int grid = equal_split ? (int)((ntasks + per - 1) / per)
+                                 : (int)(ntasks < resident[dev] ? ntasks : resident[dev]);
     ns_piece_kernel<D, G><<<grid, 32, smem, st>>>(g, npc, (int)ntasks, q, pk, pv, idx, po, pl, status);
     return cudaSuccess;
 }
@@ -1080,7 +1087,7 @@ cudaError_t launch_piece(const Geometry& g, int npc, cudaStream_t st, const __nv
 template <int D>
 cudaError_t launch_d(const Geometry& g, cudaStream_t st, const void* qv, const void* pkv, const void* pvv,
                      const int32_t* idx, const int32_t* slen, float* po, float* pl, void* out, float* lse,
-                     int32_t* status, cudaEvent_t join) {
+                     int32_t* status, cudaEvent_t join, bool equal_split) {
     const dim3 grid((unsigned)(((long)g.R * g.BW * g.Hkv + 7) / 8)), block(256);
     if (g.in_f32) {
         // fp32 storage: the direct walk (step <= kNsDirectMax, checked on the host) and the merge
@@ -1112,7 +1119,7 @@ cudaError_t launch_d(const Geometry& g, cudaStream_t st, const void* qv, const v
             cudaError_t e = launch_beam<D, GV>(g, st, q, pk, pv, idx, po, pl, status);                          \
             if (e != cudaSuccess) return e;                                                                      \
         } else if (g.ns_to_piece || g.ns_pieces > 0) {                                                           \
-            cudaError_t e = launch_piece<D, GV>(g, npc, st, q, pk, pv, idx, po, pl, status);                   \
+            cudaError_t e = launch_piece<D, GV>(g, npc, st, q, pk, pv, idx, po, pl, status, equal_split);      \
             if (e != cudaSuccess) return e;                                                                      \
             if (!g.ns_to_piece && join) {                                                                        \
                 e = cudaStreamWaitEvent(st, join, 0);                                                            \
@@ -1141,13 +1148,13 @@ int merge_ctas_for(const Geometry& g) {
 cudaError_t launch_ns_merge(const Geometry& g, const void* q, const void* pool_k,
                             const void* pool_v, const int32_t* beam_tok_idx, const int32_t* shared_len,
                             const float* part_o, const float* part_lse, void* out, float* lse, int32_t* status,
-                            cudaStream_t stream, cudaEvent_t join) {
+                            cudaStream_t stream, cudaEvent_t join, bool equal_split) {
     float* po = const_cast<float*>(part_o);
     float* pl = const_cast<float*>(part_lse);
     if (g.d == 128)
-        return launch_d<128>(g, stream, q, pool_k, pool_v, beam_tok_idx, shared_len, po, pl, out, lse, status, join);
+        return launch_d<128>(g, stream, q, pool_k, pool_v, beam_tok_idx, shared_len, po, pl, out, lse, status, join, equal_split);
     if (g.d == 64)
-        return launch_d<64>(g, stream, q, pool_k, pool_v, beam_tok_idx, shared_len, po, pl, out, lse, status, join);
+        return launch_d<64>(g, stream, q, pool_k, pool_v, beam_tok_idx, shared_len, po, pl, out, lse, status, join, equal_split);
     return cudaErrorInvalidValue;
 }
 

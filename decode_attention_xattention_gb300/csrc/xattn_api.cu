@@ -289,10 +289,10 @@ int run_shared(const Geometry& g, int kernel, const void* q, const void* shared_
 
 int run_merge(const Geometry& g, const xattn_desc* desc, const void* q, const int32_t* shared_len,
               const void* ns_k_pool, const void* ns_v_pool, const int32_t* beam_tok_idx, void* out, float* lse,
-              const WsView& ws, cudaStream_t st, cudaEvent_t join = nullptr) {
+              const WsView& ws, cudaStream_t st, cudaEvent_t join = nullptr, bool equal_split = true) {
     cudaError_t e = launch_ns_merge(g, q, ns_k_pool, ns_v_pool, beam_tok_idx,
                                     desc->max_shared_len > 0 ? shared_len : nullptr, ws.part_o, ws.part_lse,
-                                    out, lse, ws.status, st, join);
+                                    out, lse, ws.status, st, join, equal_split);
     return e == cudaSuccess ? XATTN_OK : XATTN_ERR_CUDA;
 }
 
@@ -338,11 +338,22 @@ bool decode_two_streams(const Geometry& g, int kernel, int step) {
 
 // The Non-Shared part and the merge of the two-stream form, on `st`, the row merge after
 // `join` (the Shared stage's completion on the side stream).
-int run_ns_then_merge(const Geometry& g, const xattn_desc* desc, const void* q, const int32_t* shared_len,
-                      const void* ns_k_pool, const void* ns_v_pool, const int32_t* beam_tok_idx, void* out,
-                      float* lse, const WsView& ws, cudaStream_t st, cudaEvent_t join) {
-    if (g.ns_pieces > 0)  // the piece kernel, then (after the join) the row merge
-        return run_merge(g, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws, st, join);
+int run_ns_then_merge(const Geometry& g, int kernel, const xattn_desc* desc, const void* q,
+                      const int32_t* shared_len, const void* ns_k_pool, const void* ns_v_pool,
+                      const int32_t* beam_tok_idx, void* out, float* lse, const WsView& ws, cudaStream_t st,
+                      cudaEvent_t join) {
+    if (g.ns_pieces > 0) {
+        // the piece kernel, then (after the join) the row merge. The piece kernel's warps take an
+        // equal number of pieces when the Shared stage beside it is short (one wave of at most 8
+        // tiles per CTA): they then start together; behind a longer one they start one after
+        // another as its CTAs end, and the full wave finishes sooner.
+        const int sms = device_sms();
+        const long ctas = kernel == 1 ? shared_tc_ctas_for(g) : 0;
+        const long tiles = (g.split_tokens + kTcTileKeys - 1) / kTcTileKeys;
+        const bool short_shared = kernel == 1 && tiles * ((ctas + sms - 1) / sms) <= 8;
+        return run_merge(g, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws, st, join,
+                         short_shared);
+    }
     Geometry gn = g;
     gn.ns_to_piece = 1;  // the Non-Shared part as piece nsplit
     int rc = run_merge(gn, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws, st);
@@ -430,8 +441,8 @@ int xattn_decode(const xattn_desc* desc, const void* q, const void* shared_k, co
         cudaEvent_t join = fork_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st, &rc);
         if (rc != XATTN_OK) return rc;
         if (join)
-            return run_ns_then_merge(g, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws, st,
-                                     join);
+            return run_ns_then_merge(g, kernel, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse,
+                                     ws, st, join);
     }
     rc = run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st);
     if (rc != XATTN_OK) return rc;
@@ -466,8 +477,8 @@ int xattn_decode_step(const xattn_desc* desc, const int32_t* parent, const void*
                 cudaStreamWaitEvent(st, join, 0);  // leave nothing of this call unjoined
                 return rc;
             }
-            return run_ns_then_merge(g, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws, st,
-                                     join);
+            return run_ns_then_merge(g, kernel, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse,
+                                     ws, st, join);
         }
     }
     // ahead of a decode that is its programmatic dependent and gathers what it writes, the

@@ -84,7 +84,8 @@ cudaError_t launch_shared_stage_tf32(const Geometry& g, const void* q, const voi
 cudaError_t launch_ns_merge(const Geometry& g, const void* q, const void* pool_k, const void* pool_v,
                             const int32_t* beam_tok_idx, const int32_t* shared_len,
                             const float* part_o, const float* part_lse, void* out,
-                            float* lse, int32_t* status, cudaStream_t stream, cudaEvent_t join = nullptr);
+                            float* lse, int32_t* status, cudaStream_t stream, cudaEvent_t join = nullptr,
+                            bool equal_split = true);
 // The row merge alone over pieces 0 .. np-1 of each row (np <= g.pieces).
 cudaError_t launch_merge_rows(const Geometry& g, int np, const int32_t* shared_len, const float* part_o,
                               const float* part_lse, void* out, float* lse, int32_t* status, cudaStream_t stream);
