@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(kWarps * 32) shared_stage_simt_kernel(
 
 cudaError_t launch_shared_stage_simt(const Geometry& g, const void* q, const void* shared_k, const void* shared_v,
                                      const int32_t* shared_len, float* part_o, float* part_lse, int32_t* status,
-                                     cudaStream_t stream, bool pdl) {
+                                     cudaStream_t stream, bool pdl, cudaEvent_t started) {
     (void)status;
     const long nrb = (g.M + kRB - 1) / kRB;
     const long ctas = (long)g.R * g.Hkv * nrb * g.nsplit;
@@ -182,11 +182,19 @@ cudaError_t launch_shared_stage_simt(const Geometry& g, const void* q, const voi
     cfg.gridDim = dim3((unsigned)ctas);
     cfg.blockDim = dim3(kWarps * 32);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na++].val.programmaticStreamSerializationAllowed = 1;
+    }
+    if (started) {
+        attr[na].id = cudaLaunchAttributeLaunchCompletionEvent;
+        attr[na].val.launchCompletionEvent.event = started;
+        attr[na++].val.launchCompletionEvent.flags = 0;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = na;
     cudaError_t e = cudaSuccess;
     auto go = [&](auto kernel, auto tag) {
         using T = decltype(tag);

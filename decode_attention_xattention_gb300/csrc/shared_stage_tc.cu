@@ -748,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
 template <int D, bool NST>
 cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
                      const CUtensorMap& tn, const __nv_bfloat16* q, const int32_t* slen, float* po, float* pl, int32_t* status,
-                     const FusedArgs& fa, cudaStream_t stream) {
+                     const FusedArgs& fa, cudaStream_t stream, cudaEvent_t started) {
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -767,11 +767,21 @@ cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    // `started` (optional) is recorded once every CTA has begun: a launch on another stream
+    // that waits for it finds this kernel's CTAs already placed.
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if ((fa.enabled && g.step > 0 && !fa.ns_tile) || fa.pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na++].val.programmaticStreamSerializationAllowed = 1;
+    }
+    if (started) {
+        attr[na].id = cudaLaunchAttributeLaunchCompletionEvent;
+        attr[na].val.launchCompletionEvent.event = started;
+        attr[na++].val.launchCompletionEvent.flags = 0;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = ((fa.enabled && g.step > 0 && !fa.ns_tile) || fa.pdl) ? 1 : 0;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, shared_stage_tc_kernel<D, NST>, tk, tv, tq, tn, g, q, slen, po, pl, status, fa);
 }
 
@@ -792,12 +802,14 @@ cudaError_t launch_shared_stage_tc(const Geometry& g, const CUtensorMap& tmap_k,
                  nst_args.idx,
                  nst_args.pdl ? 1 : 0};
     const bool nst = fused && nst_args.enabled && g.step > 0;
+    const cudaEvent_t ev = nst_args.started;
     if (g.d == 128)
-        return nst ? launch_d<128, true>(g, tmap_k, tmap_v, tq, tn, q, shared_len, part_o, part_lse, status, fa, stream)
-                   : launch_d<128, false>(g, tmap_k, tmap_v, tq, tn, q, shared_len, part_o, part_lse, status, fa, stream);
+        return nst ? launch_d<128, true>(g, tmap_k, tmap_v, tq, tn, q, shared_len, part_o, part_lse, status, fa, stream, ev)
+                   : launch_d<128, false>(g, tmap_k, tmap_v, tq, tn, q, shared_len, part_o, part_lse, status, fa, stream,
+                                          ev);
     if (g.d == 64)
-        return nst ? launch_d<64, true>(g, tmap_k, tmap_v, tq, tn, q, shared_len, part_o, part_lse, status, fa, stream)
-                   : launch_d<64, false>(g, tmap_k, tmap_v, tq, tn, q, shared_len, part_o, part_lse, status, fa, stream);
+        return nst ? launch_d<64, true>(g, tmap_k, tmap_v, tq, tn, q, shared_len, part_o, part_lse, status, fa, stream, ev)
+                   : launch_d<64, false>(g, tmap_k, tmap_v, tq, tn, q, shared_len, part_o, part_lse, status, fa, stream, ev);
     return cudaErrorInvalidValue;
 }
 

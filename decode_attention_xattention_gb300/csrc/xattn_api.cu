@@ -68,8 +68,11 @@ int cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
 // Split plan of the Shared stage. A piece is a run of whole 128-token tiles. The automatic
 // choice minimises (waves of CTAs) x (tiles per CTA + one tile of fixed cost per CTA), so
-// that short units are split until they fill the GPU but not beyond.
-void plan(const xattn_desc* d, int step, Geometry* g, int* kernel) {
+// that short units are split until they fill the GPU but not beyond. with_ns: the plan of a
+// whole decode (xattn_decode, xattn_decode_step), which also weighs a long Non-Shared part
+// run beside the Shared stage; without it (xattn_decode_shared and xattn_decode_merge, whose
+// pieces must agree whatever the step) the split does not depend on the step.
+void plan(const xattn_desc* d, int step, Geometry* g, int* kernel, bool with_ns = true) {
     g->R = d->num_requests;
     g->BW = d->beam_width;
     g->Hq = d->num_q_heads;
@@ -114,6 +117,29 @@ void plan(const xattn_desc* d, int step, Geometry* g, int* kernel) {
             const double waves = (double)cdiv(units * n, slots);
             const double cost = waves * (per + 1.0) + 0.02 * n;  // small charge for merge traffic
             if (cost < best) { best = cost; best_n = n; }
+        }
+        // A long Non-Shared part (its own piece kernel, bf16) runs beside the tensor-core Shared
+        // stage on the SMs that stage leaves free. In units of one 128-key tile of a Shared-stage
+        // CTA (about 1.75 us): the Shared stage takes its waves x (tiles per CTA + about 5 for
+        // the prologue and epilogue); the piece kernel's work is its pool bytes at about
+        // 4.4 TB/s, done at the free SMs' share of that rate while the Shared stage runs and at
+        // the full rate after it. The step ends with the later of the two. Never more pieces
+        // than without the Non-Shared part (the workspace is sized by the plan of step 0).
+        if (with_ns && k == 1 && !g->in_f32 && step > kNsDirectMax) {
+            const double ns_units = (double)g->R * g->BW * step * g->Hkv * g->d * 2 * 2 / 4.4e12 / 1.75e-6;
+            const int base_n = best_n;
+            best = 1e30;
+            for (int n = 1; n <= base_n; ++n) {
+                const int per = cdiv(tiles, n);
+                if (n > 1 && cdiv(tiles, per) != n) continue;
+                const double waves = (double)cdiv(units * n, slots);
+                const double t_sh = waves * (per + 5.0);
+                const double free_frac = waves > 1.0 ? 0.0 : 1.0 - (double)(units * n) / (double)slots;
+                const double during = t_sh * free_frac;
+                const double t_ns = ns_units <= during ? ns_units / free_frac : t_sh + (ns_units - during);
+                const double cost = (t_sh > t_ns ? t_sh : t_ns) + 0.02 * n;
+                if (cost < best) { best = cost; best_n = n; }
+            }
         }
         g->split_tokens = cdiv(tiles, best_n) * kPieceGrain;
     }
@@ -279,7 +305,7 @@ int run_shared(const Geometry& g, int kernel, const void* q, const void* shared_
                                    fused, nst, st);
     } else if (kernel == 2) {
         e = launch_shared_stage_simt(g, q, shared_k, shared_v, shared_len, ws.part_o, ws.part_lse, ws.status, st,
-                                     ns_args && ns_args->pdl);
+                                     ns_args && ns_args->pdl, ns_args ? ns_args->started : nullptr);
     } else if (kernel == 3) {
         e = launch_shared_stage_tf32(g, q, shared_k, shared_v, shared_len, ws.part_o, ws.part_lse, ws.status, st,
                                      ns_args && ns_args->pdl);
@@ -296,16 +322,18 @@ int run_merge(const Geometry& g, const xattn_desc* desc, const void* q, const in
     return e == cudaSuccess ? XATTN_OK : XATTN_ERR_CUDA;
 }
 
-// A second stream and two events per host thread and device, created on first use and kept
-// for the thread's lifetime: with a long Non-Shared part the Shared stage (prefix pieces) and
-// the Non-Shared piece kernel do not depend on each other, so the Shared stage runs on this
-// stream, forked from the caller's stream by one event and joined back by the other before
-// the row merge (graph capture follows the fork and the join). Per thread, so calls from
-// different host threads never share one.
+// A second stream and three events per host thread and device, created on first use and
+// kept for the thread's lifetime: with a long Non-Shared part the Shared stage (prefix
+// pieces) and the Non-Shared piece kernel do not depend on each other, so the Shared stage
+// runs on this stream, forked from the caller's stream by one event and joined back by
+// another before the row merge (graph capture follows the fork and the join). The third is
+// recorded once every CTA of the Shared stage has begun. Per thread, so calls from different
+// host threads never share one.
 struct SideStream {
     cudaStream_t s = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr, started = nullptr;
     ~SideStream() {
+        if (started) cudaEventDestroy(started);
         if (join) cudaEventDestroy(join);
         if (fork) cudaEventDestroy(fork);
         if (s) cudaStreamDestroy(s);
@@ -322,10 +350,11 @@ SideStream* side_stream() {
             return nullptr;
         }
         if (cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) != cudaSuccess)
+            cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&x.started, cudaEventDisableTiming) != cudaSuccess)
             return nullptr;
     }
-    return (x.fork && x.join) ? &x : nullptr;
+    return (x.fork && x.join && x.started) ? &x : nullptr;
 }
 
 // Whether the decode takes the two-stream form: a prefix with storage, no fusion, bf16, and
@@ -338,11 +367,20 @@ bool decode_two_streams(const Geometry& g, int kernel, int step) {
 
 // The Non-Shared part and the merge of the two-stream form, on `st`, the row merge after
 // `join` (the Shared stage's completion on the side stream).
+// started: when not null, the piece kernel waits for it (every CTA of the Shared stage has
+// begun), so that its many small CTAs cannot take the SMs first and hold the Shared stage's
+// one-per-SM CTAs back until they are done. xattn_decode uses it; in xattn_decode_step the
+// beam update ahead of the piece kernel gives the Shared stage that head start, and a second
+// dependency there made the wait last until the Shared stage's end.
 int run_ns_then_merge(const Geometry& g, int kernel, const xattn_desc* desc, const void* q,
                       const int32_t* shared_len, const void* ns_k_pool, const void* ns_v_pool,
                       const int32_t* beam_tok_idx, void* out, float* lse, const WsView& ws, cudaStream_t st,
-                      cudaEvent_t join) {
+                      cudaEvent_t join, cudaEvent_t started) {
     if (g.ns_pieces > 0) {
+        if (started && cudaStreamWaitEvent(st, started, 0) != cudaSuccess) {
+            cudaStreamWaitEvent(st, join, 0);  // leave nothing of this call unjoined
+            return XATTN_ERR_CUDA;
+        }
         // the piece kernel, then (after the join) the row merge. The piece kernel's warps take an
         // equal number of pieces when the Shared stage beside it is short (one wave of at most 8
         // tiles per CTA): they then start together; behind a longer one they start one after
@@ -365,9 +403,11 @@ int run_ns_then_merge(const Geometry& g, int kernel, const xattn_desc* desc, con
 }
 
 // The Shared stage forked onto the side stream; returns the event the row merge waits for, or
-// null when the fork could not be made (then nothing was enqueued).
+// null when the fork could not be made (then nothing was enqueued). *started: the event
+// recorded once every CTA of the Shared stage has begun.
 cudaEvent_t fork_shared(const Geometry& g, int kernel, const void* q, const void* shared_k, const void* shared_v,
-                        const int32_t* shared_len, const WsView& ws, cudaStream_t st, int* rc) {
+                        const int32_t* shared_len, const WsView& ws, cudaStream_t st, int* rc,
+                        cudaEvent_t* started) {
     *rc = XATTN_OK;
     SideStream* ss = side_stream();
     if (!ss) return nullptr;
@@ -375,7 +415,10 @@ cudaEvent_t fork_shared(const Geometry& g, int kernel, const void* q, const void
         *rc = XATTN_ERR_CUDA;
         return nullptr;
     }
-    *rc = run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, ss->s);
+    NsTileArgs launch{false, nullptr, nullptr, nullptr, false, ss->started};
+    *rc = run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, ss->s, false, nullptr, nullptr, nullptr,
+                     nullptr, nullptr, false, &launch);
+    *started = ss->started;
     if (*rc == XATTN_OK && cudaEventRecord(ss->join, ss->s) != cudaSuccess) *rc = XATTN_ERR_CUDA;
     if (*rc != XATTN_OK) {
         // join whatever was enqueued before returning the error
@@ -438,11 +481,12 @@ int xattn_decode(const xattn_desc* desc, const void* q, const void* shared_k, co
     }
     if (decode_two_streams(g, kernel, step)) {
         // the Shared stage beside the Non-Shared piece kernel; the row merge waits for both
-        cudaEvent_t join = fork_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st, &rc);
+        cudaEvent_t started = nullptr;
+        cudaEvent_t join = fork_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st, &rc, &started);
         if (rc != XATTN_OK) return rc;
         if (join)
             return run_ns_then_merge(g, kernel, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse,
-                                     ws, st, join);
+                                     ws, st, join, started);
     }
     rc = run_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st);
     if (rc != XATTN_OK) return rc;
@@ -468,7 +512,8 @@ int xattn_decode_step(const xattn_desc* desc, const int32_t* parent, const void*
     if (decode_two_streams(g, kernel, step)) {
         // the Shared stage (which reads nothing the update writes) forked first, beside the
         // update and the Non-Shared piece kernel; the row merge waits for both
-        cudaEvent_t join = fork_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st, &rc);
+        cudaEvent_t started = nullptr;
+        cudaEvent_t join = fork_shared(g, kernel, q, shared_k, shared_v, shared_len, ws, st, &rc, &started);
         if (rc != XATTN_OK) return rc;
         if (join) {
             rc = xattn_beam_update(desc, parent, new_k, new_v, ns_k_pool, ns_v_pool, beam_tok_idx, step - 1,
@@ -478,7 +523,7 @@ int xattn_decode_step(const xattn_desc* desc, const int32_t* parent, const void*
                 return rc;
             }
             return run_ns_then_merge(g, kernel, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse,
-                                     ws, st, join);
+                                     ws, st, join, nullptr);
         }
     }
     // ahead of a decode that is its programmatic dependent and gathers what it writes, the
@@ -532,7 +577,7 @@ int xattn_decode_merge(const xattn_desc* desc, const void* q, const int32_t* sha
     if (rc != XATTN_OK) return rc;
     Geometry g;
     int kernel;
-    plan(desc, step, &g, &kernel);
+    plan(desc, step, &g, &kernel, false);
     if (workspace_bytes < workspace_bytes_for(g)) return XATTN_ERR_WORKSPACE_TOO_SMALL;
     return run_merge(g, desc, q, shared_len, ns_k_pool, ns_v_pool, beam_tok_idx, out, lse, ws_view(workspace, g),
                      reinterpret_cast<cudaStream_t>(stream));

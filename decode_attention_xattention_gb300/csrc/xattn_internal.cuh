@@ -60,6 +60,7 @@ struct NsTileArgs {
     const void* pool_v;
     const int32_t* idx;
     bool pdl;
+    cudaEvent_t started = nullptr;  // recorded once every CTA of the launch has begun (optional)
 };
 cudaError_t launch_shared_stage_tc(const Geometry& g, const CUtensorMap& tmap_k,
                                    const CUtensorMap& tmap_v, const CUtensorMap& tmap_q,
@@ -70,7 +71,8 @@ cudaError_t launch_shared_stage_tc(const Geometry& g, const CUtensorMap& tmap_k,
 // q, shared_k, shared_v: bf16, or fp32 when g.in_f32.
 cudaError_t launch_shared_stage_simt(const Geometry& g, const void* q, const void* shared_k, const void* shared_v,
                                      const int32_t* shared_len, float* part_o, float* part_lse,
-                                     int32_t* status, cudaStream_t stream, bool pdl = false);
+                                     int32_t* status, cudaStream_t stream, bool pdl = false,
+                                     cudaEvent_t started = nullptr);
 // Shared stage for fp32 storage on the tensor cores (tcgen05 kind::tf32), writing the same
 // per-piece partials as launch_shared_stage_simt. pdl (both): launched as the programmatic
 // dependent of the beam update just queued; the kernel completes only after it.

@@ -137,8 +137,12 @@ XATTN_API int xattn_decode(const xattn_desc* desc, const void* q, const void* sh
                  float* lse, void* workspace, size_t workspace_bytes, xattn_stream_t stream);
 
 /* The two halves of xattn_decode, for callers that schedule the stages themselves (and
- * for measuring them apart). xattn_decode(...) is exactly xattn_decode_shared(...)
- * followed by xattn_decode_merge(...) on the same stream and workspace.
+ * for measuring them apart). xattn_decode_shared(...) followed by xattn_decode_merge(...) on
+ * the same stream and workspace computes what xattn_decode(...) computes. The two halves cut
+ * the prefix as xattn_query_plan(desc, 0, ...) reports, whatever the step; xattn_decode with a
+ * long Non-Shared part (step > 32, bf16 storage, tensor-core Shared stage) may cut it into
+ * fewer pieces (xattn_query_plan(desc, step, ...)), leaving SMs to the Non-Shared kernel that
+ * runs beside the Shared stage, and then agrees with the halves to rounding.
  *
  * xattn_decode_shared: the Shared stage alone. For every (request r, KV head h) it stacks
  * the BW*G query rows of that KV head (row m = b*G + g) against the prefix, cut into
