@@ -151,6 +151,38 @@ def test_plan_properties_over_shapes(lib):
             assert ws >= 256 + rows * d * 4 + rows * 4
 
 
+def test_plan_with_long_non_shared_part(lib):
+    """A decode whose long Non-Shared part runs beside the tensor-core Shared stage is planned
+    with fewer, longer prefix pieces where that leaves the Non-Shared kernel SMs (one prefix
+    group of 64 sequences, 8192-token prefix, 512-token suffixes: 16 pieces at step 0, 4 at
+    step 512), never with more pieces than at step 0 (the workspace is sized by that plan),
+    and only for bf16 storage on the tensor cores with more than 32 Non-Shared tokens."""
+    import itertools
+    d = xattn.make_desc(1, 64, 32, 8, 128, 8192, 512 * 64, 512)
+    _, p0 = xattn.xattn_query_plan(d, 0)
+    _, p32 = xattn.xattn_query_plan(d, 32)
+    _, p512 = xattn.xattn_query_plan(d, 512)
+    assert (p0.num_splits, p32.num_splits, p512.num_splits) == (16, 16, 4)
+    assert p512.shared_ctas == 32 and p512.fused == 0
+    ws = xattn.xattn_decode_workspace_size(d)
+    for step in (0, 33, 100, 512):
+        _, p = xattn.xattn_query_plan(d, step)
+        rows = 1 * 8 * p.piece_stride * 64 * 4
+        assert ws >= 256 + rows * 128 * 4 + rows * 4
+    # the CUDA-core kernel and fp32 storage keep the step's split
+    for kernel, dtype in ((2, xattn.XATTN_DTYPE_BF16), (2, xattn.XATTN_DTYPE_F32)):
+        dk = xattn.make_desc(1, 64, 32, 8, 128, 8192, 512 * 64, 512, shared_kernel=kernel, dtype=dtype)
+        assert xattn.xattn_query_plan(dk, 512)[1].num_splits == xattn.xattn_query_plan(dk, 0)[1].num_splits
+    # never more pieces than at step 0, over a grid of shapes
+    for (R, BW, Hq, Hkv), Lmax, T in itertools.product(
+            [(1, 64, 32, 8), (8, 8, 32, 8), (64, 1, 32, 8), (4, 128, 16, 4), (2, 256, 32, 8)],
+            [1024, 8192, 32768], [33, 100, 512]):
+        dg = xattn.make_desc(R, BW, Hq, Hkv, 128, Lmax, BW * T, T)
+        n0 = xattn.xattn_query_plan(dg, 0)[1].num_splits
+        nT = xattn.xattn_query_plan(dg, T)[1].num_splits
+        assert 1 <= nT <= n0, (R, BW, Hq, Hkv, Lmax, T, n0, nT)
+
+
 def test_fp32_inputs_plan_and_limits(lib):
     """fp32 storage: by default the planner picks the CUDA-core Shared stage (fp32 throughout)
     and the unfused path; asking for tensor cores picks the tf32 kernel (3), one CTA per
