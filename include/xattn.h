@@ -27,14 +27,15 @@
  *   - Every pointer except `desc`, `status_out` (xattn_read_status) is a DEVICE pointer
  *     on the current device. The caller owns every buffer; the library allocates no device
  *     buffers and keeps no data between calls. Its only CUDA objects of its own: per host
- *     thread and device, one stream and two events, created at the first bf16 decode that
+ *     thread and device, one stream and three events, created at the first bf16 decode that
  *     does not fuse its Non-Shared part into the Shared stage and has either a Non-Shared
  *     part long enough for its own piece kernel (more than 32 tokens) or a short one next
  *     to a prefix cut in several pieces: the Shared stage of such a decode runs on that
  *     stream, forked from `stream` by one event at the start of the call and joined back by
- *     the other before the row merge, so it overlaps the Non-Shared kernel (and, in
- *     xattn_decode_step, the beam update). The fork and the join follow graph capture of
- *     `stream`.
+ *     another before the row merge, so it overlaps the Non-Shared kernel (and, in
+ *     xattn_decode_step, the beam update). In xattn_decode the piece kernel of a long
+ *     Non-Shared part also waits for the third, recorded once every CTA of the Shared stage
+ *     has begun. The fork and the joins follow graph capture of `stream`.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream) and never
  *     synchronise, except xattn_read_status.
  *   - Tensors are dense, row-major (innermost dimension last), 16-byte aligned.
