@@ -73,14 +73,16 @@ constexpr uint32_t kNaN = 0x7fc00000u;
 // units 0 and 1 are the gathered Non-Shared K tiles (both row tiles) and V tiles (their own
 // barriers, one per row tile), and the prefix units follow as units 2, 3, ...; the full
 // barrier of slot 0 or 1 then sees its first TMA unit as phase 0.
-template <int D>
+template <int D, int U = (D == 64 ? 4 : 2)>
 struct Cfg {
-    static constexpr int kUnits = D == 64 ? 4 : 2;
+    static constexpr int kUnits = U;
+    // query tiles held: two row tiles, or one when a third unit slot takes the second's place
+    static constexpr int kQTiles = (D == 128 && U == 3) ? 1 : 2;
     static constexpr int KB = D / 64;              // 128-byte swizzle blocks along d
     static constexpr int kTileBytes = KB * 16384;  // 128 rows (or tokens) x d bf16
     static constexpr int kUnitBytes = 2 * kTileBytes;  // K tile, then V tile
-    static constexpr int kOffQ = 0;                // two row tiles
-    static constexpr int kOffU = kOffQ + 2 * kTileBytes;
+    static constexpr int kOffQ = 0;                // kQTiles row tiles
+    static constexpr int kOffU = kOffQ + kQTiles * kTileBytes;
     static constexpr int kSmemBytes = kOffU + kUnits * kUnitBytes + 1024;
 };
 
@@ -150,13 +152,15 @@ struct FusedArgs {
 // NST: the in-tile Non-Shared mode, compiled as its own instantiation so that the other
 // modes' loops carry none of its branches (the MMA-issuing thread shares its issue slots
 // with two softmax warps, and every instruction in its loop shows in the tile period).
-template <int D, bool NST>
+// U: unit slots (default 2 at d = 128; 3 with a single row tile per CTA, whose query tile
+// leaves room for a third).
+template <int D, bool NST, int U = (D == 64 ? 4 : 2)>
 __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_ns, Geometry g,
     const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ shared_len, float* __restrict__ part_o,
     float* __restrict__ part_lse, int32_t* status, FusedArgs fa) {
-    using C = Cfg<D>;
+    using C = Cfg<D, U>;
     constexpr int kU = C::kUnits;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -394,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         // Staged Non-Shared piece of this row (Non-Shared kernel ran first). With prefix tiles it
         // is staged in shared memory by the producer (tile 0 over the Q tiles, tile 1 over the
         // last unit's slot); its LSE is loaded before the wait for the last P.V.
-        const bool staged = fa.enabled && g.step > 0 && !ns;
+        const bool staged = fa.enabled && g.step > 0 && !ns && C::kQTiles == 2;
         const bool fused_ns = staged && row_ok;
         const bool ns_staged = staged && have_o;  // warp-uniform
         const size_t nsrow = ((size_t)unit * g.pieces + g.nsplit) * g.M + row;
@@ -550,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             // swizzled boxes of 32 columns) for the epilogue: row tile 0 into the Q tiles once the
             // last Q.K^T is done, row tile 1 into the slot of unit ntiles - 1 once it is consumed.
             bool ns_issued[2] = {false, false};
-            if (fa.enabled && g.step > 0 && !ns && issued == npu) {
+            if (fa.enabled && g.step > 0 && !ns && C::kQTiles == 2 && issued == npu) {
                 grid_dependency_wait();  // the Non-Shared kernel launched before this one has finished
                 for (int i = 0; i < ntile_m; ++i) {
                     const int jl = ntiles - 1, st = jl % kU;
@@ -745,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     if (!ns && fa.pdl && tid == 0) grid_dependency_wait();
 }
 
-template <int D, bool NST>
+template <int D, bool NST, int U = (D == 64 ? 4 : 2)>
 cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
                      const CUtensorMap& tn, const __nv_bfloat16* q, const int32_t* slen, float* po, float* pl, int32_t* status,
                      const FusedArgs& fa, cudaStream_t stream, cudaEvent_t started) {
@@ -753,8 +757,8 @@ cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(shared_stage_tc_kernel<D, NST>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(shared_stage_tc_kernel<D, NST, U>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, U>::kSmemBytes);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
@@ -765,7 +769,7 @@ cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ctas);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
+    cfg.dynamicSmemBytes = Cfg<D, U>::kSmemBytes;
     cfg.stream = stream;
     // `started` (optional) is recorded once every CTA has begun: a launch on another stream
     // that waits for it finds this kernel's CTAs already placed.
@@ -782,7 +786,7 @@ cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, shared_stage_tc_kernel<D, NST>, tk, tv, tq, tn, g, q, slen, po, pl, status, fa);
+    return cudaLaunchKernelEx(&cfg, shared_stage_tc_kernel<D, NST, U>, tk, tv, tq, tn, g, q, slen, po, pl, status, fa);
 }
 
 }  // namespace
@@ -803,6 +807,10 @@ cudaError_t launch_shared_stage_tc(const Geometry& g, const CUtensorMap& tmap_k,
                  nst_args.pdl ? 1 : 0};
     const bool nst = fused && nst_args.enabled && g.step > 0;
     const cudaEvent_t ev = nst_args.started;
+    // one row tile per CTA and partials only: a third K/V unit slot in place of the second
+    // query tile (more loads in flight for the prefix stream)
+    if (g.d == 128 && !fused && !nst && g.row_tiles == 1)
+        return launch_d<128, false, 3>(g, tmap_k, tmap_v, tq, tn, q, shared_len, part_o, part_lse, status, fa, stream, ev);
     if (g.d == 128)
         return nst ? launch_d<128, true>(g, tmap_k, tmap_v, tq, tn, q, shared_len, part_o, part_lse, status, fa, stream, ev)
                    : launch_d<128, false>(g, tmap_k, tmap_v, tq, tn, q, shared_len, part_o, part_lse, status, fa, stream,
