@@ -509,6 +509,34 @@ def test_full_size_sampled_rows(w):
     assert torch.isfinite(db.lse).all()
 
 
+@pytest.mark.parametrize("w", [wl.GR, wl.LONG, wl.FEATHER_1, wl.FEATHER_8], ids=lambda w: w.name)
+def test_full_size_decode_step_sampled_rows(w):
+    """The bench's timed call, xattn_decode_step for the last token (beam update + decode in
+    one call: the in-tile decode as the update's dependent at GR; the Shared stage on the side
+    stream beside the update and the Non-Shared kernels for Long and Feather), at full size:
+    the pool and table bit-equal to the oracle's, and every beam's first and last query head
+    plus 384 random rows against the oracle."""
+    orc = oracle.load()
+    inp = wl.make_inputs(w)
+    db = DeviceBatch(inp, out_fp32=True)
+    db.build_cache(steps=w.steps - 1)
+    xattn.check(db.decode_step(w.steps - 1))
+    torch.cuda.synchronize()
+    assert db.read_status() == 0
+    dev_in = db.inputs
+    pk, pv, idx = oracle.build_cache(orc, dev_in)
+    np.testing.assert_array_equal(db.idx.cpu().numpy(), idx)
+    np.testing.assert_array_equal(bf16_tensor_to_f32(db.pool_k), pk)
+    np.testing.assert_array_equal(bf16_tensor_to_f32(db.pool_v), pv)
+    rows = wl.sample_rows_every_beam(w, 384, seed=4)
+    ref_o, ref_l = orc.decode(oracle.dims_of(w), dev_in.q, dev_in.shared_k, dev_in.shared_v, dev_in.shared_len, pk,
+                              pv, idx, w.steps, rows=rows)
+    got_o = db.out.float().cpu().numpy().reshape(-1, w.head_dim)[rows]
+    got_l = db.lse.cpu().numpy().reshape(-1)[rows]
+    compare(got_o, got_l, ref_o, ref_l, w.name)
+    assert torch.isfinite(db.out.float()).all() and torch.isfinite(db.lse).all()
+
+
 @pytest.mark.parametrize("w", [wl.WIDE, wl.FEATHER_1], ids=lambda w: w.name)
 def test_full_size_bf16_output(w):
     """The output the library returns by default (bf16) against the oracle at the stated
