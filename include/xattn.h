@@ -226,7 +226,7 @@ XATTN_API int xattn_beam_select(int32_t num_requests, int32_t beam_width, int32_
                                 const int32_t* cand_token, int32_t* parent, int32_t* token, float* score,
                                 xattn_stream_t stream);
 
-/* Allocation-free decode. The paper has no counterpart to this call; it exists for callers
+/* Allocation-free decode. xAttention as published has no counterpart to this call; it exists for callers
  * that cannot allocate device memory or hand the library a workspace (a runtime that owns
  * every allocation, a latency-critical thread that must not trigger cudaMalloc, a fixed
  * memory budget). It does exactly what xattn_decode does, with its workspace taken from a
