@@ -226,10 +226,11 @@ XATTN_API int xattn_beam_select(int32_t num_requests, int32_t beam_width, int32_
                                 const int32_t* cand_token, int32_t* parent, int32_t* token, float* score,
                                 xattn_stream_t stream);
 
-/* Allocation-free decode. xAttention as published has no counterpart to this call; it exists for callers
- * that cannot allocate device memory or hand the library a workspace (a runtime that owns
- * every allocation, a latency-critical thread that must not trigger cudaMalloc, a fixed
- * memory budget). It does exactly what xattn_decode does, with its workspace taken from a
+/* Allocation-free decode. xAttention as published has no counterpart to this call; it
+ * exists for callers that cannot allocate device memory or hand the library a workspace (a
+ * runtime that owns every allocation, a latency-critical thread that must not trigger
+ * cudaMalloc, a fixed memory budget). It does exactly what xattn_decode does, with its
+ * workspace taken from a
  * static device array of XATTN_NOALLOC_SCRATCH_BYTES (32 MiB) inside the library; every
  * device that loads the library holds that array until the process exits.
  *   - Shapes whose xattn_decode_workspace_size exceeds that limit return
