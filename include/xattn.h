@@ -230,9 +230,9 @@ XATTN_API int xattn_beam_select(int32_t num_requests, int32_t beam_width, int32_
  * exists for callers that cannot allocate device memory or hand the library a workspace (a
  * runtime that owns every allocation, a latency-critical thread that must not trigger
  * cudaMalloc, a fixed memory budget). It does exactly what xattn_decode does, with its
- * workspace taken from a
- * static device array of XATTN_NOALLOC_SCRATCH_BYTES (32 MiB) inside the library; every
- * device that loads the library holds that array until the process exits.
+ * workspace taken from a static device array of XATTN_NOALLOC_SCRATCH_BYTES (32 MiB) inside
+ * the library; every device that loads the library holds that array until the process
+ * exits.
  *   - Shapes whose xattn_decode_workspace_size exceeds that limit return
  *     XATTN_ERR_WORKSPACE_TOO_SMALL before anything is launched; an invalid descriptor
  *     returns XATTN_ERR_INVALID_ARG.
