@@ -526,10 +526,7 @@ int xattn_decode_step(const xattn_desc* desc, const int32_t* parent, const void*
                                      ws, st, join, nullptr);
         }
     }
-    // ahead of a decode that is its programmatic dependent and gathers what it writes, the
-    // update spread over more, smaller CTAs measured a little faster
-    rc = beam_update(desc, parent, new_k, new_v, ns_k_pool, ns_v_pool, beam_tok_idx, step - 1, ws.status, st,
-                     ns_tile_fits(g, kernel, step) ? 1 : 4);
+    rc = beam_update(desc, parent, new_k, new_v, ns_k_pool, ns_v_pool, beam_tok_idx, step - 1, ws.status, st, 4);
     if (rc != XATTN_OK) return rc;
     if (ns_tile_fits(g, kernel, step)) {
         // The decode as the beam update's programmatic dependent: its set-up, Q loads and first K/V
