@@ -84,6 +84,10 @@ struct Cfg {
     static constexpr int kOffQ = 0;                // kQTiles row tiles
     static constexpr int kOffU = kOffQ + kQTiles * kTileBytes;
     static constexpr int kSmemBytes = kOffU + kUnits * kUnitBytes + 1024;
+    // in-tile mode: one more K tile after the unit slots (prefix tile 0, loaded at the start
+    // while the gathered Non-Shared tiles hold the slots)
+    static constexpr int kOffX = kOffU + kUnits * kUnitBytes;
+    static constexpr int kSmemBytesNst = kSmemBytes + kTileBytes;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -131,6 +135,7 @@ struct Bars {
     uint64_t o_full[2], final_mma;
     uint64_t q_free, ns_full[2];  // last Q.K^T done; staged Non-Shared piece of row tile i in place
     uint64_t ns_kfull[2], ns_vfull[2];  // in-tile mode: row tile i's gathered K / V rows (and flags) in place
+    uint64_t x_full;  // in-tile mode: prefix tile 0's K tile in its own region
 };
 
 // Epilogue mode and the Non-Shared inputs of the fused decode.
@@ -195,7 +200,10 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
     const int nb = kTileRows / g.G;
     const int nk = ns ? nb * g.step : 0;
     const int nt = ntiles + (ns ? 1 : 0);  // tiles every row tile attends to (tile 0: Non-Shared)
-    const int u0 = ns ? 2 : 0;             // unit index of prefix unit 0
+    // unit index of prefix unit p = u0 + p. In-tile mode: units 0 and 1 are the gathered
+    // Non-Shared K and V tiles, prefix unit 0 (K(0) alone) sits in region X, and prefix units
+    // p >= 1 follow as units 2, 3, ...
+    const int u0 = ns ? 1 : 0;
 
     if (tid == 0) {
         for (int s = 0; s < kU; ++s) {
@@ -210,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
         mbar_init(&bars.o_full[0], 1);
         mbar_init(&bars.o_full[1], 1);
         mbar_init(&bars.final_mma, 1);
+        mbar_init(&bars.x_full, 1);
         mbar_init(&bars.q_free, 1);
         mbar_init(&bars.ns_full[0], 1);
         mbar_init(&bars.ns_full[1], 1);
@@ -535,7 +544,13 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             prefetch_tmap(&tmap_v);
             const int npu = ntiles > 0 ? ntiles + 1 : 0;  // prefix units
             int issued = 0;
-            for (int p = 0; p < npu; ++p) {
+            if (ns && ntiles > 0) {  // prefix tile 0's K tile into region X at once
+                mbar_arrive_expect_tx(&bars.x_full, C::kTileBytes);
+                for (int kb = 0; kb < C::KB; ++kb)
+                    tma_load_4d(smem + C::kOffX + kb * 16384, &tmap_k, &bars.x_full, kb * 64, h, t0, r);
+                issued = 1;
+            }
+            for (int p = ns ? 1 : 0; p < npu; ++p) {
                 const int u = u0 + p, st = u % kU, use = u / kU;
                 if (use > 0 && !mbar_wait(&bars.u_empty[st], (use - 1) & 1, &abort_sh)) break;
                 uint8_t* slot = sU + st * C::kUnitBytes;
@@ -570,10 +585,11 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             }
             if (abort_sh) {  // let the copies still in flight land before the CTA exits
                 volatile int never = 0;
-                for (int p = max(0, issued - kU); p < issued; ++p) {
+                for (int p = max(ns ? 1 : 0, issued - kU); p < issued; ++p) {
                     const int u = u0 + p;
                     mbar_wait(&bars.u_full[u % kU], (u / kU - ((ns && u % kU < 2) ? 1 : 0)) & 1, &never);
                 }
+                if (ns && issued > 0) mbar_wait(&bars.x_full, 0, &never);
                 for (int i = 0; i < ntile_m; ++i) mbar_wait(&bars.q_ready[i], 0, &never);
                 for (int i = 0; i < 2; ++i)
                     if (ns_issued[i]) mbar_wait(&bars.ns_full[i], 0, &never);
@@ -653,9 +669,8 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 }
                 if (ok) mma_commit(&bars.u_empty[0]);
                 // Iteration 0: per row tile, P.V of the Non-Shared tile (gathered V tile, slot 1),
-                // then Q.K^T of prefix tile 0 (unit 2, slot 2 % kU, the first phase of its barrier).
-                const int st0 = 2 % kU;
-                if (ok && ntiles > 0 && !mbar_wait(&bars.u_full[st0], 0, &abort_sh)) ok = false;
+                // then Q.K^T of prefix tile 0 (its K tile in region X, loaded at the start).
+                if (ok && ntiles > 0 && !mbar_wait(&bars.x_full, 0, &abort_sh)) ok = false;
                 for (int i = 0; ok && i < ntile_m; ++i) {
                     if (!mbar_wait(&bars.p_full[i], 0, &abort_sh) ||
                         !mbar_wait(&bars.ns_vfull[i], 0, &abort_sh)) {
@@ -669,20 +684,19 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                         mma_commit(&bars.o_full[i]);  // O_i complete
                     } else {
                         tc_fence_after();
-                        issue_qk(i, (uint32_t)st0 * C::kUnitBytes);
+                        issue_qk(i, (uint32_t)(C::kOffX - C::kOffU));
                         mma_commit(&bars.s_full[i]);
                     }
                 }
                 if (ok) {
                     if (ntiles == 1) mma_commit(&bars.q_free);
                     mma_commit(&bars.u_empty[1]);
-                    if (ntiles > 0) mma_commit(&bars.u_empty[st0]);
                 }
-                // Prefix iterations j >= 1 read unit j + 2 = {K(j), V(j-1)}; its full barrier phase
+                // Prefix iterations j >= 1 read unit j + 1 = {K(j), V(j-1)}; its full barrier phase
                 // is one less in slots 0 and 1 (the gathered tiles held them first), and the P
                 // phases are one on (the Non-Shared tile took the first).
                 for (int j = 1; ok && j <= ntiles; ++j) {
-                    const int u = j + 2, st = u % kU;
+                    const int u = j + 1, st = u % kU;
                     if (!mbar_wait(&bars.u_full[st], (u / kU - (st < 2 ? 1 : 0)) & 1, &abort_sh)) {
                         ok = false;
                         break;
@@ -757,8 +771,8 @@ cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(shared_stage_tc_kernel<D, NST, U>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, U>::kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(shared_stage_tc_kernel<D, NST, U>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             NST ? Cfg<D, U>::kSmemBytesNst : Cfg<D, U>::kSmemBytes);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
@@ -769,7 +783,7 @@ cudaError_t launch_d(const Geometry& g, const CUtensorMap& tk, const CUtensorMap
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ctas);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Cfg<D, U>::kSmemBytes;
+    cfg.dynamicSmemBytes = NST ? Cfg<D, U>::kSmemBytesNst : Cfg<D, U>::kSmemBytes;
     cfg.stream = stream;
     // `started` (optional) is recorded once every CTA has begun: a launch on another stream
     // that waits for it finds this kernel's CTAs already placed.
