@@ -308,6 +308,11 @@ __global__ void __launch_bounds__(32, piece_ctas_per_sm(D)) ns_piece_kernel(
     uint8_t* v_sm = k_sm + kRingBlocks * kPieceBlk * RS;
     const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
     const int stride = (int)gridDim.x;
+    // The pool rows are read once: marked first out of L2, so that they do not push out what
+    // is read again soon (the pieces' partial results, which the row merge reads next, and the
+    // Shared stage's partials and K/V tiles beside it).
+    uint64_t l2_first;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(l2_first));
     if (lane == 0) {
         for (int j = 0; j < kRingBlocks; ++j) ptx::mbar_init(&full[j], 32);  // one cp.async arrival per lane
         *abort_sh = 0;
@@ -370,8 +375,12 @@ __global__ void __launch_bounds__(32, piece_ctas_per_sm(D)) ns_piece_kernel(
                 const size_t off = (((size_t)ip.r * g.S + sv) * g.Hkv + ip.h) * D;
                 const __nv_bfloat16* src = (lane < 16 ? pool_k : pool_v) + off;
                 uint8_t* dst = (lane < 16 ? k_sm : v_sm) + (buf * kPieceBlk + k) * RS;
-                if (ch < RB / 16) ptx::cp_async_16(ptx::smem_addr(dst + ch * 16), reinterpret_cast<const uint8_t*>(src) + ch * 16);
-                if (RB / 16 > 16) ptx::cp_async_16(ptx::smem_addr(dst + (ch + 16) * 16), reinterpret_cast<const uint8_t*>(src) + (ch + 16) * 16);
+                if (ch < RB / 16)
+                    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(ptx::smem_addr(dst + ch * 16)),
+                                 "l"(reinterpret_cast<const uint8_t*>(src) + ch * 16), "l"(l2_first) : "memory");
+                if (RB / 16 > 16)
+                    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(ptx::smem_addr(dst + (ch + 16) * 16)),
+                                 "l"(reinterpret_cast<const uint8_t*>(src) + (ch + 16) * 16), "l"(l2_first) : "memory");
             }
         }
         // each lane's arrival completes once its copies have landed
