@@ -544,9 +544,8 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
             prefetch_tmap(&tmap_v);
             const int npu = ntiles > 0 ? ntiles + 1 : 0;  // prefix units
             int issued = 0;
-            // writing partials for a later merge: the prefix tiles first out of L2, so that the
-            // partials stay there for the merge
-            const bool stream_hint = !fa.enabled;
+            // the prefix tiles first out of L2 (each is read by the CTAs of its unit about at once,
+            // then never again): the partials, the Non-Shared rows and the queries stay there
             uint64_t l2_first;
             asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(l2_first));
             if (ns && ntiles > 0) {  // prefix tile 0's K tile into region X at once
@@ -561,20 +560,12 @@ __global__ void __launch_bounds__(kThreads, 1) shared_stage_tc_kernel(
                 uint8_t* slot = sU + st * C::kUnitBytes;
                 mbar_arrive_expect_tx(&bars.u_full[st], (p < ntiles ? C::kTileBytes : 0) + (p >= 1 ? C::kTileBytes : 0));
                 for (int kb = 0; kb < C::KB; ++kb) {
-                    if (stream_hint) {
-                        if (p < ntiles)
-                            tma_load_4d_hint(slot + kb * 16384, &tmap_k, &bars.u_full[st], kb * 64, h,
-                                             t0 + p * kTcTileKeys, r, l2_first);
-                        if (p >= 1)
-                            tma_load_4d_hint(slot + C::kTileBytes + kb * 16384, &tmap_v, &bars.u_full[st], kb * 64, h,
-                                             t0 + (p - 1) * kTcTileKeys, r, l2_first);
-                    } else {
-                        if (p < ntiles)
-                            tma_load_4d(slot + kb * 16384, &tmap_k, &bars.u_full[st], kb * 64, h, t0 + p * kTcTileKeys, r);
-                        if (p >= 1)
-                            tma_load_4d(slot + C::kTileBytes + kb * 16384, &tmap_v, &bars.u_full[st], kb * 64, h,
-                                        t0 + (p - 1) * kTcTileKeys, r);
-                    }
+                    if (p < ntiles)
+                        tma_load_4d_hint(slot + kb * 16384, &tmap_k, &bars.u_full[st], kb * 64, h,
+                                         t0 + p * kTcTileKeys, r, l2_first);
+                    if (p >= 1)
+                        tma_load_4d_hint(slot + C::kTileBytes + kb * 16384, &tmap_v, &bars.u_full[st], kb * 64, h,
+                                         t0 + (p - 1) * kTcTileKeys, r, l2_first);
                 }
                 issued = p + 1;
 
